@@ -1,0 +1,194 @@
+"""CPU oracle for MQA/GQA incremental decode attention (fp64, plain C behind ctypes).
+
+TEST INFRASTRUCTURE, NOT THE PRODUCT. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package. It shares no code with the
+CUDA library and never imports it; the library never imports this.
+
+What each function computes, and the passage it follows:
+
+* :func:`kv_cache_bytes` -- ``2 x layers x kv_heads x seq_len x head_dim x dtype_bytes``
+  ("GQA与MQA深度实战", ybb.press, §一 and §七).
+* :func:`kv_append` -- write the new token's K/V row of every KV head at position ``pos[b]``
+  (same page, §八; nanhubrain.csdn.net MQA article §2.2, concatenation along the sequence axis).
+* :func:`decode_attention` -- for every sequence ``b`` and query head ``i`` with
+  ``j = i // (h/g)``: ``softmax_t(scale * q_i . K_{j,t}) . V_{j,t}`` over ``t < seq_lens[b]``
+  (ybb.press page §五).
+* :func:`attention_partial` / :func:`lse_merge` -- per-range softmax states and their
+  log-sum-exp combination (not on the pages; the identity that makes splitting a sequence exact).
+* :func:`bf16_to_f64` / :func:`f64_to_bf16` -- bfloat16 conversions from the bit layout
+  (round to nearest, ties to even).
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms, the pages' printed
+numbers, invariants and library routines.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_BOUNDS = 4
+
+_lib = None
+
+
+def _configure(lib):
+    u64, i32, dbl, vp = ctypes.c_uint64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+    lib.oracle_kv_cache_bytes.restype = u64
+    lib.oracle_kv_cache_bytes.argtypes = [u64] * 5
+    lib.oracle_bf16_to_double.restype = dbl
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_double_to_bf16.argtypes = [dbl]
+    lib.oracle_kv_append.restype = i32
+    lib.oracle_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32]
+    for name in ("oracle_decode_attention_bf16", "oracle_decode_attention_f64"):
+        fn = getattr(lib, name)
+        fn.restype = i32
+        fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dbl, i32]
+    lib.oracle_attention_partial_f64.restype = i32
+    lib.oracle_attention_partial_f64.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, dbl,
+                                                 i32, i32, vp, vp, vp]
+    lib.oracle_lse_merge.restype = i32
+    lib.oracle_lse_merge.argtypes = [vp, vp, vp, i32, i32, vp]
+    lib.oracle_num_threads.restype = i32
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _configure(ctypes.CDLL(_build.build()))
+    return _lib
+
+
+def _swap_library(path):
+    """Load another build of the oracle source (used by the mutation tests, which compile a
+    deliberately broken copy to show that the pins catch it). Returns the previous handle."""
+    global _lib
+    prev = _load()
+    _lib = _configure(ctypes.CDLL(path)) if path is not None else None
+    return prev
+
+
+def _restore_library(handle):
+    global _lib
+    _lib = handle
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses by default (the host's logical cores)."""
+    return int(_load().oracle_num_threads())
+
+
+def kv_cache_bytes(num_layers: int, num_kv_heads: int, seq_len: int, head_dim: int,
+                   dtype_bytes: int) -> int:
+    return int(_load().oracle_kv_cache_bytes(num_layers, num_kv_heads, seq_len, head_dim,
+                                             dtype_bytes))
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Widen bfloat16 bit patterns (uint16) to float64, exactly."""
+    lib = _load()
+    b = _c(bits, np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    flat_in, flat_out = b.reshape(-1), out.reshape(-1)
+    for k in range(flat_in.size):
+        flat_out[k] = lib.oracle_bf16_to_double(int(flat_in[k]))
+    return out
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """Round float64 values to bfloat16 bit patterns (nearest, ties to even)."""
+    lib = _load()
+    a = _c(x, np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    flat_in, flat_out = a.reshape(-1), out.reshape(-1)
+    for k in range(flat_in.size):
+        flat_out[k] = lib.oracle_double_to_bf16(float(flat_in[k]))
+    return out
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, pos, n_max: int | None = None) -> int:
+    """Append in place. ``k_new``/``v_new``: uint16 [b, g, d_h]; caches: uint16
+    [b, g, n_max, d_h] (modified in place, must be C-contiguous uint16 arrays); ``pos``: int32 [b].
+    Returns the oracle status (0 ok, 4 if some ``pos`` is outside ``[0, n_max)``)."""
+    lib = _load()
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint16 and c.flags.c_contiguous):
+            raise TypeError("caches must be C-contiguous uint16 numpy arrays (updated in place)")
+    b, g, nm, d_h = k_cache.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    p = _c(pos, np.int32)
+    return int(lib.oracle_kv_append(_ptr(kn), _ptr(vn), _ptr(k_cache), _ptr(v_cache), _ptr(p),
+                                    b, g, d_h, nm))
+
+
+def decode_attention(q, k_cache, v_cache, seq_lens, scale: float, threads: int = 0,
+                     return_status: bool = False):
+    """fp64 grouped decode attention.
+
+    ``q`` [b, h, d_h]; caches [b, g, n_max, d_h]; either all uint16 (bfloat16 bit patterns,
+    widened exactly) or all float64. ``seq_lens`` int32 [b]. Returns float64 [b, h, d_h].
+    """
+    lib = _load()
+    q = np.asarray(q)
+    if q.dtype == np.uint16:
+        fn, dt = lib.oracle_decode_attention_bf16, np.uint16
+    else:
+        fn, dt = lib.oracle_decode_attention_f64, np.float64
+    qq, kk, vv = _c(q, dt), _c(k_cache, dt), _c(v_cache, dt)
+    lens = _c(seq_lens, np.int32)
+    b, h, d_h = qq.shape
+    _, g, n_max, d_k = kk.shape
+    if d_k != d_h or vv.shape != kk.shape or lens.shape != (b,):
+        raise ValueError("shape mismatch")
+    out = np.empty((b, h, d_h), dtype=np.float64)
+    st = int(fn(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(lens), _ptr(out), b, h, g, d_h, n_max,
+                float(scale), int(threads)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return (out, st) if return_status else out
+
+
+def attention_partial(q, k_cache, v_cache, scale: float, t_begin: int, t_end: int):
+    """Per-range softmax state over rows ``[t_begin, t_end)`` (float64 inputs).
+    Returns ``(m [b,h], l [b,h], o [b,h,d_h])`` with ``o`` un-normalised."""
+    lib = _load()
+    qq = _c(q, np.float64)
+    kk, vv = _c(k_cache, np.float64), _c(v_cache, np.float64)
+    b, h, d_h = qq.shape
+    _, g, n_max, _ = kk.shape
+    m = np.empty((b, h)); l = np.empty((b, h)); o = np.empty((b, h, d_h))
+    st = int(lib.oracle_attention_partial_f64(_ptr(qq), _ptr(kk), _ptr(vv), b, h, g, d_h, n_max,
+                                              float(scale), t_begin, t_end, _ptr(m), _ptr(l),
+                                              _ptr(o)))
+    if st:
+        raise ValueError(f"oracle partial failed with status {st}")
+    return m, l, o
+
+
+def lse_merge(m, l, o) -> np.ndarray:
+    """Merge S partial states of one row: ``m`` [S], ``l`` [S], ``o`` [S, d_h] -> [d_h]."""
+    lib = _load()
+    mm, ll, oo = _c(m, np.float64), _c(l, np.float64), _c(o, np.float64)
+    S, d_h = oo.shape
+    out = np.empty(d_h)
+    st = int(lib.oracle_lse_merge(_ptr(mm), _ptr(ll), _ptr(oo), S, d_h, _ptr(out)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("bad merge arguments")
+    return out

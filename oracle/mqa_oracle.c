@@ -1,0 +1,294 @@
+/*
+ * mqa_oracle.c -- plain, slow, fp64 CPU oracle for the incremental decode step of
+ * Multi-Query / Grouped-Query Attention (KV-cache append + grouped attention).
+ *
+ * THIS IS TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT. Only the test suite, the package's
+ * smoke check and the benchmark's CPU-baseline leg may load it. It shares no code, header,
+ * table or helper with the CUDA library: it is written directly from the definitions on the
+ * source pages, with no blocking, fusion or reordering beyond what those definitions state.
+ *
+ * Sources (web pages on MQA/GQA; cited by page title and section):
+ *   [GQA-MQA] "分组查询注意力（GQA）与多查询注意力（MQA）深度实战" (ybb.press)
+ *       §一  KV_bytes = 2 x num_layers x num_kv_heads x seq_len x head_dim x dtype_bytes
+ *       §四  g = num_kv_heads, the h query heads split evenly into g groups
+ *       §五  j = i // (h/g);  score_{i,t} = Q_i . K_{j,t} / sqrt(d_h);
+ *            alpha_{i,t} = softmax_t(score_{i,t});  O_i = sum_t alpha_{i,t} V_{j,t}
+ *       §八  the reference module writes the new token's K/V rows into the cache at the
+ *            current position, then attends over every cached row up to and including it
+ *   [MQA-CSDN] nanhubrain.csdn.net MQA decoding article, §2.2: the decode step concatenates the
+ *            new K/V row onto the cache along the sequence axis, then takes logits of every
+ *            query head against the (shared) keys.
+ *   [MQA-ENC] "多查詢注意力" (compassingai.com), section "KV Cache 結構與視訊記憶體佔用對比".
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - attention covers rows 0 .. L_b-1 of sequence b, where L_b (seq_lens[b]) already counts the
+ *     token appended in this step;
+ *   - heads of one group are contiguous: query head i uses KV head i / (h/g);
+ *   - the caller passes the scale (the pages use 1/sqrt(d_h));
+ *   - a length outside 1..n_max is an error: that sequence's output is all zeros and the call
+ *     returns ORACLE_ERR_BOUNDS;
+ *   - the "scores minus their maximum" form of softmax is the definition written out; the
+ *     maximum cancels exactly in exact arithmetic.
+ *
+ * Storage conventions (chosen to match the library's memory layout so that the same buffers can
+ * be handed to both, never to share code):
+ *   q        [b][h][d_h]            bf16 bit patterns (uint16_t) or double
+ *   k_cache  [b][g][n_max][d_h]     idem
+ *   v_cache  [b][g][n_max][d_h]     idem
+ *   out      [b][h][d_h]            double
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_INVALID_ARG 1
+#define ORACLE_ERR_BOUNDS 4
+
+/* ------------------------------------------------------------------------------------------ */
+/* KV-cache size: [GQA-MQA] §一 and §七; [MQA-ENC] KV Cache section.                          */
+/* ------------------------------------------------------------------------------------------ */
+uint64_t oracle_kv_cache_bytes(uint64_t num_layers, uint64_t num_kv_heads, uint64_t seq_len,
+                               uint64_t head_dim, uint64_t dtype_bytes) {
+  /* factor 2: one K and one V tensor per layer */
+  return 2u * num_layers * num_kv_heads * seq_len * head_dim * dtype_bytes;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* bfloat16 <-> double, written from the bfloat16 bit layout: 1 sign bit, 8 exponent bits     */
+/* (bias 127), 7 fraction bits.                                                               */
+/* ------------------------------------------------------------------------------------------ */
+double oracle_bf16_to_double(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int expo = (bits >> 7) & 0xFF;
+  int frac = bits & 0x7F;
+  double mag;
+  if (expo == 0xFF) {
+    mag = frac ? NAN : INFINITY;
+  } else if (expo == 0) {
+    /* subnormal: frac * 2^(1 - 127 - 7) */
+    mag = ldexp((double)frac, -133);
+  } else {
+    /* normal: (1 + frac/128) * 2^(expo - 127) = (128 + frac) * 2^(expo - 134) */
+    mag = ldexp((double)(128 + frac), expo - 134);
+  }
+  return sign ? -mag : mag;
+}
+
+/* Round a double to the nearest bfloat16, ties to even. Returns the bit pattern. */
+uint16_t oracle_double_to_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isinf(a)) return sign | 0x7F80;
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);           /* a = m * 2^e2, m in [0.5, 1)  =>  a in [2^(e2-1), 2^e2) */
+  int E = e2 - 1;          /* a in [2^E, 2^(E+1)) */
+  /* spacing of the bf16 grid around a: 2^(E-7) for normals, 2^-133 below 2^-126 */
+  int spacing_exp = (E < -126) ? -133 : (E - 7);
+  double units = ldexp(a, -spacing_exp);   /* exact: scaling by a power of two */
+  double r = floor(units);
+  double rem = units - r;
+  if (rem > 0.5 || (rem == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  double v = ldexp(r, spacing_exp);
+  /* largest finite bf16 is (2 - 2^-7) * 2^127; anything that rounds past it is infinite */
+  if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+  if (v < ldexp(1.0, -126)) {
+    /* subnormal (or rounded up to the smallest normal, which the same formula encodes) */
+    return sign | (uint16_t)ldexp(v, 133);
+  }
+  int ev;
+  frexp(v, &ev);
+  int Ev = ev - 1;         /* v in [2^Ev, 2^(Ev+1)) */
+  uint16_t frac = (uint16_t)(ldexp(v, 7 - Ev) - 128.0);
+  return sign | (uint16_t)((Ev + 127) << 7) | frac;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* KV append: [GQA-MQA] §八 (cache_k[:, start:start+T] = k with T = 1);                      */
+/* [MQA-CSDN] §2.2 (concat along the sequence axis). Bit copy of one row per (b, KV head).    */
+/* ------------------------------------------------------------------------------------------ */
+int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
+                     uint16_t* v_cache, const int32_t* pos, int b, int g, int d_h, int n_max) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    int p = pos[bi];
+    if (p < 0 || p >= n_max) { status = ORACLE_ERR_BOUNDS; continue; }
+    for (int j = 0; j < g; ++j) {
+      size_t src = ((size_t)bi * g + j) * (size_t)d_h;
+      size_t dst = (((size_t)bi * g + j) * (size_t)n_max + (size_t)p) * (size_t)d_h;
+      memcpy(k_cache + dst, k_new + src, (size_t)d_h * sizeof(uint16_t));
+      memcpy(v_cache + dst, v_new + src, (size_t)d_h * sizeof(uint16_t));
+    }
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Grouped decode attention: [GQA-MQA] §五.                                                   */
+/* ------------------------------------------------------------------------------------------ */
+enum { KIND_BF16 = 0, KIND_F64 = 1 };
+
+static inline double load_elem(const void* base, size_t idx, int kind) {
+  if (kind == KIND_F64) return ((const double*)base)[idx];
+  return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+}
+
+/* Softmax-weighted sum over rows t in [t_begin, t_end) for one (sequence, query head).
+ * Writes m = max score, l = sum_t exp(score_t - m), o[d] = sum_t exp(score_t - m) V[t][d].
+ * An empty range gives m = -inf, l = 0, o = 0. */
+static void attend_range(const void* q, const void* k_cache, const void* v_cache, int kind,
+                         int bi, int i, int h, int g, int d_h, int n_max, double scale,
+                         int t_begin, int t_end, double* scores, double* m_out, double* l_out,
+                         double* o_out) {
+  int group_size = h / g;
+  int j = i / group_size;                      /* §五: j = i // (h/g) */
+  size_t q_off = ((size_t)bi * h + i) * (size_t)d_h;
+  size_t kv_off = ((size_t)bi * g + j) * (size_t)n_max * (size_t)d_h;
+
+  for (int d = 0; d < d_h; ++d) o_out[d] = 0.0;
+  if (t_end <= t_begin) { *m_out = -INFINITY; *l_out = 0.0; return; }
+
+  /* score_{i,t} = scale * sum_d Q_i[d] K_{j,t}[d] */
+  double m = -INFINITY;
+  for (int t = t_begin; t < t_end; ++t) {
+    double s = 0.0;
+    for (int d = 0; d < d_h; ++d)
+      s += load_elem(q, q_off + d, kind) * load_elem(k_cache, kv_off + (size_t)t * d_h + d, kind);
+    s *= scale;
+    scores[t - t_begin] = s;
+    if (s > m) m = s;
+  }
+  /* weights exp(s - m), their sum, and the weighted sum of value rows */
+  double l = 0.0;
+  for (int t = t_begin; t < t_end; ++t) {
+    double w = exp(scores[t - t_begin] - m);
+    l += w;
+    for (int d = 0; d < d_h; ++d)
+      o_out[d] += w * load_elem(v_cache, kv_off + (size_t)t * d_h + d, kind);
+  }
+  *m_out = m;
+  *l_out = l;
+}
+
+static int check_attention_args(const void* q, const void* k, const void* v, const int32_t* lens,
+                                 const double* out, int b, int h, int g, int d_h, int n_max) {
+  if (!q || !k || !v || !lens || !out) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return ORACLE_ERR_INVALID_ARG;
+  if (h % g != 0) return ORACLE_ERR_INVALID_ARG;  /* §十 item 1: heads split evenly */
+  return ORACLE_OK;
+}
+
+static int attention_full(const void* q, const void* k_cache, const void* v_cache, int kind,
+                          const int32_t* seq_lens, double* out, int b, int h, int g, int d_h,
+                          int n_max, double scale, int threads) {
+  int st = check_attention_args(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max);
+  if (st) return st;
+  int bad = 0;
+  for (int bi = 0; bi < b; ++bi)
+    if (seq_lens[bi] < 1 || seq_lens[bi] > n_max) bad = 1;
+#ifdef _OPENMP
+  if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel num_threads(threads)
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)n_max);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d_h);
+#ifdef _OPENMP
+#pragma omp for collapse(2) schedule(dynamic, 1)
+#endif
+    for (int bi = 0; bi < b; ++bi) {
+      for (int i = 0; i < h; ++i) {
+        double* o = out + ((size_t)bi * h + i) * (size_t)d_h;
+        int L = seq_lens[bi];
+        if (L < 1 || L > n_max) {
+          for (int d = 0; d < d_h; ++d) o[d] = 0.0;
+          continue;
+        }
+        double m, l;
+        attend_range(q, k_cache, v_cache, kind, bi, i, h, g, d_h, n_max, scale, 0, L, scores,
+                     &m, &l, acc);
+        /* O_i = sum_t alpha_{i,t} V_{j,t},  alpha = exp(s - m) / l */
+        for (int d = 0; d < d_h; ++d) o[d] = acc[d] / l;
+      }
+    }
+    free(scores);
+    free(acc);
+  }
+  return bad ? ORACLE_ERR_BOUNDS : ORACLE_OK;
+}
+
+int oracle_decode_attention_bf16(const uint16_t* q, const uint16_t* k_cache,
+                                 const uint16_t* v_cache, const int32_t* seq_lens, double* out,
+                                 int b, int h, int g, int d_h, int n_max, double scale,
+                                 int threads) {
+  return attention_full(q, k_cache, v_cache, KIND_BF16, seq_lens, out, b, h, g, d_h, n_max,
+                        scale, threads);
+}
+
+int oracle_decode_attention_f64(const double* q, const double* k_cache, const double* v_cache,
+                                const int32_t* seq_lens, double* out, int b, int h, int g,
+                                int d_h, int n_max, double scale, int threads) {
+  return attention_full(q, k_cache, v_cache, KIND_F64, seq_lens, out, b, h, g, d_h, n_max,
+                        scale, threads);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Split-sequence partials and their log-sum-exp merge. The pages do not describe splitting;  */
+/* this is the identity  softmax over a union of ranges = exp-weighted combination of the     */
+/* per-range softmax states, used to check that splitting a sequence changes nothing.         */
+/* ------------------------------------------------------------------------------------------ */
+int oracle_attention_partial_f64(const double* q, const double* k_cache, const double* v_cache,
+                                 int b, int h, int g, int d_h, int n_max, double scale,
+                                 int t_begin, int t_end, double* m_out, double* l_out,
+                                 double* o_out) {
+  if (!q || !k_cache || !v_cache || !m_out || !l_out || !o_out) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0 || h % g) return ORACLE_ERR_INVALID_ARG;
+  if (t_begin < 0 || t_end > n_max) return ORACLE_ERR_BOUNDS;
+  double* scores = (double*)malloc(sizeof(double) * (size_t)n_max);
+  for (int bi = 0; bi < b; ++bi)
+    for (int i = 0; i < h; ++i) {
+      size_t r = (size_t)bi * h + i;
+      attend_range(q, k_cache, v_cache, KIND_F64, bi, i, h, g, d_h, n_max, scale, t_begin, t_end,
+                   scores, &m_out[r], &l_out[r], &o_out[r * (size_t)d_h]);
+    }
+  free(scores);
+  return ORACLE_OK;
+}
+
+/* Merge S partial states (m_s, l_s, o_s[d]) of one row:
+ *   M = max_s m_s,  out[d] = sum_s exp(m_s - M) o_s[d] / sum_s exp(m_s - M) l_s.
+ * Empty partials (m = -inf) carry zero weight. */
+int oracle_lse_merge(const double* m, const double* l, const double* o, int S, int d_h,
+                     double* out) {
+  if (!m || !l || !o || !out || S <= 0 || d_h <= 0) return ORACLE_ERR_INVALID_ARG;
+  double M = -INFINITY;
+  for (int s = 0; s < S; ++s)
+    if (m[s] > M) M = m[s];
+  for (int d = 0; d < d_h; ++d) out[d] = 0.0;
+  if (M == -INFINITY) return ORACLE_ERR_BOUNDS;   /* every range empty: no softmax exists */
+  double denom = 0.0;
+  for (int s = 0; s < S; ++s) {
+    if (m[s] == -INFINITY) continue;
+    double w = exp(m[s] - M);
+    denom += w * l[s];
+    for (int d = 0; d < d_h; ++d) out[d] += w * o[(size_t)s * d_h + d];
+  }
+  for (int d = 0; d < d_h; ++d) out[d] /= denom;
+  return ORACLE_OK;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

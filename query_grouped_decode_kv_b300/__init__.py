@@ -1,0 +1,20 @@
+"""MQA / GQA incremental decode attention for NVIDIA B300 (sm_103a).
+
+The compute lives in ``libmqa.so`` (hand-written CUDA behind a C ABI, declared in
+``include/mqa.h``). :mod:`query_grouped_decode_kv_b300.binding` marshals torch tensors into that ABI;
+it computes nothing itself. Importing a binding name loads the library and fails loudly if it has
+not been built.
+"""
+from __future__ import annotations
+
+_BINDING_NAMES = {
+    "kv_append", "decode_attention", "get_device_status", "status_string", "MqaError",
+    "library_path", "kernel_launch_count",
+}
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)

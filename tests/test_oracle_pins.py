@@ -1,0 +1,401 @@
+"""Pins for the CPU oracle: each test fixes an oracle function to something other than itself --
+numbers printed on the pages, closed forms, invariants of the definition, special cases that reduce
+to a library routine, and brute force on tiny inputs. A plausible slip in the oracle (a dropped
+scale, a wrong sign, a transposed operand, a strided instead of contiguous head->group map, an
+off-by-one length, a missing normalisation) fails at least one of these.
+
+CPU only (no GPU marker).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------------------------
+# KV-cache size formula: the pages' printed figures
+# --------------------------------------------------------------------------------------------
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden("kv_cache_bytes.json")["cases"], ids=lambda c: c["id"])
+def test_kv_bytes_matches_page_figures(case):
+    got = oracle.kv_cache_bytes(**case["args"])
+    assert got == math.prod(case["printed_factors"])
+    if case.get("printed_value_is_wrong"):
+        # the page's decimal point slipped by one place: the product is ten times the print
+        assert got == pytest.approx(10 * case["printed_value"], rel=0.01)
+        assert got != pytest.approx(case["printed_value"], rel=0.5)
+    else:
+        assert got == pytest.approx(case["printed_value"], rel=case["printed_rel_tol"])
+
+
+@pytest.mark.parametrize("ratio", _golden("kv_cache_bytes.json")["ratios"], ids=lambda r: r["id"])
+def test_kv_bytes_group_ratio(ratio):
+    full = oracle.kv_cache_bytes(1, ratio["h"], 4096, 128, 2)
+    grouped = oracle.kv_cache_bytes(1, ratio["g"], 4096, 128, 2)
+    if "mha_over_gqa" in ratio:
+        assert full / grouped == ratio["mha_over_gqa"]
+    else:
+        assert 100.0 * grouped / full == pytest.approx(ratio["percent_of_mha"],
+                                                       abs=ratio["printed_abs_tol"])
+
+
+def test_kv_bytes_80_layer_workload_allocation():
+    # 80 layers, g=8, 32769 rows (32768 context + the appended token), d_h=128, bf16, 8 sequences:
+    # the 70B-class decode workload holds about 86 GB of cache.
+    per_seq = oracle.kv_cache_bytes(80, 8, 32769, 128, 2)
+    assert 8 * per_seq == 85_901_967_360
+
+
+# --------------------------------------------------------------------------------------------
+# bfloat16 conversions: against IEEE float32 reinterpretation and torch's rounding
+# --------------------------------------------------------------------------------------------
+def test_bf16_widening_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.bf16_to_f64(bits)
+    # library route: a bf16 pattern is the upper half of an IEEE binary32
+    with np.errstate(invalid="ignore"):
+        ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_bf16_rounding_ties_and_edges():
+    one_ulp = 2.0 ** -7
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + one_ulp / 2, 0x3F80),           # tie -> even (down)
+        (1.0 + 3 * one_ulp / 2, 0x3F82),       # tie -> even (up)
+        (1.0 + one_ulp / 2 + 2.0 ** -30, 0x3F81),  # just above the tie
+        (-2.0, 0xC000),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (2.0 ** -133, 0x0001),                 # smallest subnormal
+        (2.0 ** -134, 0x0000),                 # tie between 0 and the smallest subnormal -> even
+        (3 * 2.0 ** -134, 0x0002),             # tie between 1 and 2 subnormal units -> even
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),   # largest finite
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),   # tie at the top rounds to infinity
+        (math.inf, 0x7F80),
+        (-math.inf, 0xFF80),
+    ]
+    got = oracle.f64_to_bf16([x for x, _ in cases])
+    assert [int(x) for x in got] == [bits for _, bits in cases]
+    assert int(oracle.f64_to_bf16([math.nan])[0]) & 0x7F80 == 0x7F80
+
+
+def test_bf16_rounding_matches_torch_on_float32_values():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000),
+                        rng.standard_normal(1000)]).astype(np.float32)
+    ours = oracle.f64_to_bf16(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# --------------------------------------------------------------------------------------------
+# KV append
+# --------------------------------------------------------------------------------------------
+def test_append_writes_exactly_one_row_per_kv_head():
+    rng = np.random.default_rng(1)
+    b, g, n_max, d_h = 3, 2, 9, 64
+    kc = rng.integers(0, 65536, (b, g, n_max, d_h), dtype=np.uint16)
+    vc = rng.integers(0, 65536, (b, g, n_max, d_h), dtype=np.uint16)
+    kn = rng.integers(0, 65536, (b, g, d_h), dtype=np.uint16)
+    vn = rng.integers(0, 65536, (b, g, d_h), dtype=np.uint16)
+    pos = np.array([0, 8, 4], dtype=np.int32)
+    k0, v0 = kc.copy(), vc.copy()
+    assert oracle.kv_append(kn, vn, kc, vc, pos) == oracle.OK
+    for bi in range(b):
+        assert np.array_equal(kc[bi, :, pos[bi]], kn[bi])
+        assert np.array_equal(vc[bi, :, pos[bi]], vn[bi])
+    mask = np.ones((b, g, n_max), dtype=bool)
+    for bi in range(b):
+        mask[bi, :, pos[bi]] = False
+    assert np.array_equal(kc[mask], k0[mask]) and np.array_equal(vc[mask], v0[mask])
+
+
+def test_append_rejects_out_of_range_positions_without_writing():
+    rng = np.random.default_rng(2)
+    b, g, n_max, d_h = 2, 1, 4, 64
+    kc = rng.integers(0, 65536, (b, g, n_max, d_h), dtype=np.uint16)
+    vc = kc.copy()
+    kn = rng.integers(0, 65536, (b, g, d_h), dtype=np.uint16)
+    k0 = kc.copy()
+    st = oracle.kv_append(kn, kn, kc, vc, np.array([4, -1], dtype=np.int32))
+    assert st == oracle.ERR_BOUNDS
+    assert np.array_equal(kc, k0)
+
+
+# --------------------------------------------------------------------------------------------
+# Attention: closed forms
+# --------------------------------------------------------------------------------------------
+def _f64_case(b, h, g, d_h, n_max, seed=0):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((b, h, d_h))
+    k = rng.standard_normal((b, g, n_max, d_h))
+    v = rng.standard_normal((b, g, n_max, d_h))
+    return q, k, v
+
+
+def test_closed_form_two_keys():
+    # q = (1, 0); keys (0, 0) and (ln 3, 0), scale 1 -> weights 1/4, 3/4;
+    # values (1, 0) and (0, 1) -> output (1/4, 3/4).
+    q = np.array([[[1.0, 0.0]]])
+    k = np.array([[[[0.0, 0.0], [math.log(3.0), 0.0]]]])
+    v = np.array([[[[1.0, 0.0], [0.0, 1.0]]]])
+    out = oracle.decode_attention(q, k, v, np.array([2], np.int32), scale=1.0)
+    assert out[0, 0] == pytest.approx([0.25, 0.75], abs=1e-15)
+    # the scale multiplies the logit: scale 2 -> weights 1/10, 9/10
+    out2 = oracle.decode_attention(q, k, v, np.array([2], np.int32), scale=2.0)
+    assert out2[0, 0] == pytest.approx([0.1, 0.9], abs=1e-15)
+    # a negative query flips the preference: weights 3/4, 1/4
+    out3 = oracle.decode_attention(-q, k, v, np.array([2], np.int32), scale=1.0)
+    assert out3[0, 0] == pytest.approx([0.75, 0.25], abs=1e-15)
+
+
+def test_closed_form_with_huge_logits():
+    # logits 1000 and 1000 + ln 3: exp() of either overflows a double, the softmax does not --
+    # weights are still 1/4 and 3/4
+    q = np.array([[[1.0, 0.0]]])
+    k = np.array([[[[1000.0, 0.0], [1000.0 + math.log(3.0), 0.0]]]])
+    v = np.array([[[[1.0, 0.0], [0.0, 1.0]]]])
+    out = oracle.decode_attention(q, k, v, np.array([2], np.int32), scale=1.0)
+    assert out[0, 0] == pytest.approx([0.25, 0.75], abs=1e-12)
+
+
+def test_closed_form_head_to_group_map_is_contiguous():
+    # h=4, g=2: heads 0,1 read KV head 0 and heads 2,3 read KV head 1 (j = i // (h/g)).
+    # KV head 0 values are all (1, 0); KV head 1 values are all (0, 1).
+    b, h, g, d_h, n = 1, 4, 2, 2, 3
+    q = np.random.default_rng(3).standard_normal((b, h, d_h))
+    k = np.random.default_rng(4).standard_normal((b, g, n, d_h))
+    v = np.zeros((b, g, n, d_h))
+    v[0, 0, :, 0] = 1.0
+    v[0, 1, :, 1] = 1.0
+    out = oracle.decode_attention(q, k, v, np.array([n], np.int32), scale=0.7)
+    expect = np.array([[1, 0], [1, 0], [0, 1], [0, 1]], dtype=float)
+    assert np.allclose(out[0], expect, atol=1e-15)
+
+
+def test_weights_sum_to_one():
+    q, k, _ = _f64_case(2, 8, 2, 64, 37, seed=7)
+    v = np.ones_like(k)
+    out = oracle.decode_attention(q, k, v, np.array([37, 5], np.int32), scale=0.3)
+    assert np.allclose(out, 1.0, atol=1e-14)
+
+
+def test_identical_keys_give_mean_of_values():
+    q, _, v = _f64_case(1, 4, 1, 64, 20, seed=8)
+    k = np.broadcast_to(np.random.default_rng(9).standard_normal(64), (1, 1, 20, 64)).copy()
+    L = 13
+    out = oracle.decode_attention(q, k, v, np.array([L], np.int32), scale=0.125)
+    assert np.allclose(out[0], v[0, 0, :L].mean(axis=0), atol=1e-14)
+
+
+def test_zero_scale_gives_mean_of_values():
+    q, k, v = _f64_case(2, 4, 2, 64, 11, seed=10)
+    out = oracle.decode_attention(q, k, v, np.array([11, 3], np.int32), scale=0.0)
+    for bi, L in enumerate((11, 3)):
+        for i in range(4):
+            assert np.allclose(out[bi, i], v[bi, i // 2, :L].mean(axis=0), atol=1e-14)
+
+
+def test_one_dominant_key_selects_its_value():
+    q, k, v = _f64_case(1, 2, 1, 64, 16, seed=11)
+    t_star = 9
+    k[0, 0, t_star] = 40.0 * q[0, 0] / np.linalg.norm(q[0, 0])  # logit ~ 40|q| above the rest
+    out = oracle.decode_attention(q, k, v, np.array([16], np.int32), scale=1.0)
+    assert np.allclose(out[0, 0], v[0, 0, t_star], atol=1e-9)
+
+
+def test_single_row_returns_that_value_exactly():
+    rng = np.random.default_rng(12)
+    b, h, g, d_h, n_max = 2, 8, 2, 128, 4
+    q = rng.integers(0, 65536, (b, h, d_h), dtype=np.uint16) & 0xBFFF  # finite values
+    k = rng.integers(0, 65536, (b, g, n_max, d_h), dtype=np.uint16) & 0xBFFF
+    v = rng.integers(0, 65536, (b, g, n_max, d_h), dtype=np.uint16) & 0xBFFF
+    out = oracle.decode_attention(q, k, v, np.array([1, 1], np.int32), scale=0.088)
+    for bi in range(b):
+        for i in range(h):
+            assert np.array_equal(out[bi, i], oracle.bf16_to_f64(v[bi, i // 4, 0]))
+
+
+def test_rows_beyond_length_are_never_read():
+    q, k, v = _f64_case(2, 4, 1, 64, 12, seed=13)
+    lens = np.array([7, 12], np.int32)
+    ref = oracle.decode_attention(q, k, v, lens, scale=0.2)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, :, 7:] = np.nan
+    v2[0, :, 7:] = np.inf
+    out = oracle.decode_attention(q, k2, v2, lens, scale=0.2)
+    assert np.array_equal(out, ref)
+
+
+def test_shifting_every_key_by_one_vector_changes_nothing():
+    # q.(K_t + c) = q.K_t + q.c: a per-row constant added to every logit cancels in softmax
+    q, k, v = _f64_case(1, 4, 2, 64, 25, seed=14)
+    c = np.random.default_rng(15).standard_normal(64) * 3.0
+    a = oracle.decode_attention(q, k, v, np.array([25], np.int32), scale=0.5)
+    bshift = oracle.decode_attention(q, k + c, v, np.array([25], np.int32), scale=0.5)
+    assert np.allclose(a, bshift, atol=1e-12)
+
+
+def test_length_out_of_range_is_an_error_with_zero_output():
+    q, k, v = _f64_case(2, 2, 1, 64, 5, seed=16)
+    out, st = oracle.decode_attention(q, k, v, np.array([0, 6], np.int32), scale=1.0,
+                                      return_status=True)
+    assert st == oracle.ERR_BOUNDS
+    assert np.all(out == 0.0)
+
+
+def test_uneven_grouping_is_rejected():
+    q, k, v = _f64_case(1, 6, 4, 64, 3)
+    with pytest.raises(ValueError):
+        oracle.decode_attention(q, k, v, np.array([3], np.int32), scale=1.0)
+
+
+# --------------------------------------------------------------------------------------------
+# Attention: reductions to MHA / MQA, and library routines
+# --------------------------------------------------------------------------------------------
+def test_g_equals_h_is_independent_single_head_attention():
+    b, h, d_h, n = 2, 4, 64, 10
+    q, k, v = _f64_case(b, h, h, d_h, n, seed=17)
+    lens = np.array([10, 6], np.int32)
+    full = oracle.decode_attention(q, k, v, lens, scale=0.125)
+    for i in range(h):
+        single = oracle.decode_attention(q[:, i:i + 1], k[:, i:i + 1], v[:, i:i + 1], lens,
+                                         scale=0.125)
+        assert np.array_equal(full[:, i:i + 1], single)
+
+
+def test_g_equals_one_shares_kv_across_every_head():
+    b, h, d_h, n = 1, 8, 64, 10
+    q, k, v = _f64_case(b, h, 1, d_h, n, seed=18)
+    q[:, 5] = q[:, 2]                                 # two heads ask the same question
+    out = oracle.decode_attention(q, k, v, np.array([n], np.int32), scale=0.125)
+    assert np.array_equal(out[0, 5], out[0, 2])
+    for i in range(h):
+        single = oracle.decode_attention(q[:, i:i + 1], k, v, np.array([n], np.int32),
+                                         scale=0.125)
+        assert np.array_equal(out[:, i:i + 1], single)
+
+
+@pytest.mark.parametrize("h,g,d_h", [(8, 1, 64), (8, 2, 64), (8, 8, 128), (4, 2, 128),
+                                     (6, 3, 64)])
+def test_matches_torch_sdpa_with_grouped_kv(h, g, d_h):
+    # library route: torch's scaled_dot_product_attention in float64 with enable_gqa, whose
+    # KV-head expansion is repeat_interleave over contiguous head groups (the ybb.press page's
+    # reference module, §八)
+    b, n_max = 2, 17
+    q, k, v = _f64_case(b, h, g, d_h, n_max, seed=h * 100 + g * 10 + d_h)
+    lens = np.array([17, 9], np.int32)
+    scale = 1.0 / math.sqrt(d_h)
+    out = oracle.decode_attention(q, k, v, lens, scale=scale)
+    for bi in range(b):
+        L = int(lens[bi])
+        qt = torch.from_numpy(q[bi][:, None, :])          # [h, 1, d]
+        kt = torch.from_numpy(k[bi][:, :L])               # [g, L, d]
+        vt = torch.from_numpy(v[bi][:, :L])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt[None], kt[None], vt[None], scale=scale, enable_gqa=True)[0, :, 0]
+        assert np.allclose(out[bi], ref.numpy(), atol=1e-12, rtol=0)
+
+
+def test_matches_repeat_interleave_einsum_formulation():
+    # the ybb.press page's §八 module expands the g KV heads to h with repeat_interleave, then
+    # takes einsum logits, softmax and an einsum with the values; restated here in float64
+    b, h, g, d_h, n = 1, 8, 2, 64, 13
+    q, k, v = _f64_case(b, h, g, d_h, n, seed=19)
+    scale = 1.0 / math.sqrt(d_h)
+    out = oracle.decode_attention(q, k, v, np.array([n], np.int32), scale=scale)
+    qt = torch.from_numpy(q)[:, None]                    # [B, T=1, h, d]
+    krep = torch.from_numpy(k[0]).repeat_interleave(h // g, dim=0)   # [h, L, d]
+    vrep = torch.from_numpy(v[0]).repeat_interleave(h // g, dim=0)
+    scores = torch.einsum("bthd,hld->bhtl", qt, krep) * scale
+    attn = torch.softmax(scores, dim=-1)
+    ref = torch.einsum("bhtl,hld->bthd", attn, vrep)[:, 0]
+    assert np.allclose(out, ref.numpy(), atol=1e-12, rtol=0)
+
+
+def test_bf16_inputs_are_widened_exactly():
+    rng = np.random.default_rng(20)
+    b, h, g, d_h, n = 1, 4, 2, 64, 9
+    q = oracle.f64_to_bf16(rng.standard_normal((b, h, d_h)))
+    k = oracle.f64_to_bf16(rng.standard_normal((b, g, n, d_h)))
+    v = oracle.f64_to_bf16(rng.standard_normal((b, g, n, d_h)))
+    lens = np.array([n], np.int32)
+    a = oracle.decode_attention(q, k, v, lens, scale=0.125)
+    wide = [(x.astype(np.uint32) << 16).view(np.float32).astype(np.float64) for x in (q, k, v)]
+    bref = oracle.decode_attention(*wide, lens, scale=0.125)
+    assert np.array_equal(a, bref)
+
+
+def test_brute_force_tiny_shapes_against_python_loops():
+    # pure-Python loops, straight from the definition, on very small shapes
+    for (b, h, g, d_h, n_max, seed) in [(1, 2, 1, 64, 3, 21), (2, 4, 2, 64, 5, 22),
+                                        (2, 2, 2, 128, 4, 23)]:
+        q, k, v = _f64_case(b, h, g, d_h, n_max, seed=seed)
+        lens = np.array([n_max - bi for bi in range(b)], np.int32)
+        out = oracle.decode_attention(q, k, v, lens, scale=0.3)
+        for bi in range(b):
+            for i in range(h):
+                j = i // (h // g)
+                L = int(lens[bi])
+                logits = [0.3 * sum(q[bi, i, d] * k[bi, j, t, d] for d in range(d_h))
+                          for t in range(L)]
+                z = sum(math.exp(x) for x in logits)
+                for d in range(0, d_h, 17):
+                    o = sum(math.exp(logits[t]) / z * v[bi, j, t, d] for t in range(L))
+                    assert out[bi, i, d] == pytest.approx(o, abs=1e-12)
+
+
+# --------------------------------------------------------------------------------------------
+# Split-sequence partials and the log-sum-exp merge
+# --------------------------------------------------------------------------------------------
+def test_merge_of_partials_equals_whole_range():
+    b, h, g, d_h, n = 2, 8, 2, 64, 40
+    q, k, v = _f64_case(b, h, g, d_h, n, seed=24)
+    scale = 0.125
+    full = oracle.decode_attention(q, k, v, np.array([n, n], np.int32), scale=scale)
+    for cuts in ([0, 40], [0, 1, 40], [0, 13, 14, 27, 40], [0, 0, 20, 20, 40]):
+        parts = [oracle.attention_partial(q, k, v, scale, lo, hi)
+                 for lo, hi in zip(cuts[:-1], cuts[1:])]
+        m = np.stack([p[0] for p in parts]); l = np.stack([p[1] for p in parts])
+        o = np.stack([p[2] for p in parts])
+        for bi in range(b):
+            for i in range(h):
+                merged = oracle.lse_merge(m[:, bi, i], l[:, bi, i], o[:, bi, i])
+                assert np.allclose(merged, full[bi, i], atol=1e-13)
+
+
+def test_merge_closed_form_with_huge_logits():
+    # partial maxima 1000 and 1000 + ln 3 with unit sums: combination weights 1/3 and 1
+    m = np.array([1000.0, 1000.0 + math.log(3.0)])
+    l = np.array([1.0, 1.0])
+    o = np.array([[1.0, 0.0], [0.0, 1.0]])
+    assert oracle.lse_merge(m, l, o) == pytest.approx([0.25, 0.75], abs=1e-12)
+
+
+def test_single_partial_normalises_and_empty_partials_carry_no_weight():
+    q, k, v = _f64_case(1, 1, 1, 64, 6, seed=25)
+    m, l, o = oracle.attention_partial(q, k, v, 0.5, 0, 6)
+    me, le, oe = oracle.attention_partial(q, k, v, 0.5, 3, 3)
+    assert me[0, 0] == -math.inf and le[0, 0] == 0.0 and not oe.any()
+    one = oracle.lse_merge(m[0], l[0], o[0])
+    assert np.allclose(one, o[0, 0] / l[0, 0], atol=1e-15)
+    two = oracle.lse_merge(np.concatenate([m[0], me[0]]), np.concatenate([l[0], le[0]]),
+                           np.concatenate([o[0], oe[0]]))
+    assert np.array_equal(one, two)
