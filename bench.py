@@ -1,0 +1,403 @@
+"""Benchmark: the MQA/GQA decode step (KV append + grouped attention) on B300.
+
+Default workload: the 80-layer GQA decode step of a 70B-class model (b=8 sequences, h=64 query
+heads, g=8 KV heads, d_h=128, contexts uniform in [1024, 32768], about 86 GB of bf16 cache): one
+step appends one token's K/V and runs attention in all 80 layers back to back.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
+with inputs resident in HBM (lower is better); ``e2e`` is the same step driven from pinned host
+buffers with the host->device copy of the step's inputs (q, k_new, v_new of every layer) and the
+device->host read of its outputs inside the timed region. ``roofline`` reports the attention
+call's HBM throughput on algorithmic bytes (K/V rows read + q read + out written) against the
+measured copy bandwidth. ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the
+same workload. The reference arm (``--impl reference``) times that oracle as the reference.
+
+Every layer reads about 0.55 GB of cache (above the 126 MB L2) and a step reads about 44 GB, so
+no L2 flush is needed between timed steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from query_grouped_decode_kv_b300 import inputs  # noqa: E402
+
+METRIC = "decode-attention µs/step and KV-cache GB/s as % of B300 HBM peak"
+UNIT = "us/step"
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
+                  "query_grouped_decode_kv_b300/csrc/ptx.cuh",
+                  "query_grouped_decode_kv_b300/csrc/mqa_abi.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+
+
+# ------------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    per = rec.get("per_workload", {}).get(workload)
+    return None if per is None else per.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = f"/tmp/mqa_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        try:
+            self.fh.close()
+        except Exception:
+            pass
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for ln in f:
+                    parts = [p.strip() for p in ln.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def kv_bytes(w, lens) -> int:
+    """Algorithmic bytes of one attention call: K and V rows read (2 * g * L_b * d_h * 2 over the
+    batch), q read and out written (b * h * d_h * 2 each)."""
+    total_rows = int(lens.sum())
+    return 2 * w.g * total_rows * w.d_h * 2 + 2 * w.b * w.h * w.d_h * 2
+
+
+def attention_flops(w, lens) -> int:
+    return 4 * w.h * int(lens.sum()) * w.d_h
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (our arm's cpu_baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0):
+    """Time the fp64 oracle on whole sequences of this workload's shape (one layer), adding
+    sequences until about ``target_s`` seconds of CPU work; return (us_per_step, details)."""
+    import numpy as np
+
+    import oracle
+    _, lens = inputs.positions_and_lengths(w)
+    threads = oracle.num_threads()
+    # sample sequences: one per length quantile, longest first, generated on the host
+    order = sorted(range(w.b), key=lambda i: -int(lens[i]))
+    spent, rows_done, seqs = 0.0, 0, []
+    for bi in order:
+        L = int(lens[bi])
+        sw = inputs.custom("oracle_sample", 1, w.h, w.g, w.d_h, L - 1, L - 1, kv_std=w.kv_std,
+                           wid=500 + bi)
+        q, _, _ = inputs.step_inputs(sw, 0, "cpu")
+        k, v = inputs.cache(sw, 0, "cpu")
+        qb = q.view(torch.int16).numpy().view(np.uint16)
+        kb = k.view(torch.int16).numpy().view(np.uint16)
+        vb = v.view(torch.int16).numpy().view(np.uint16)
+        lb = np.array([L], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode_attention(qb, kb, vb, lb, sw.scale, threads=threads)
+        spent += time.perf_counter() - t0
+        rows_done += L
+        seqs.append(L)
+        if spent >= target_s or spent >= max_s:
+            break
+    total_rows = int(lens.sum()) * w.layers
+    us_per_step = spent / rows_done * total_rows * 1e6
+    detail = (f"{len(seqs)} whole sequence(s) of one layer (lengths {seqs}, all {w.h} heads), "
+              f"{spent:.1f} s of oracle time, scaled by attended rows to {w.layers} layer(s) x "
+              f"{w.b} sequences")
+    return us_per_step, threads, detail, spent
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = inputs.WORKLOADS[args.workload]
+    times = []
+    for it in range(args.warmup + args.steps):
+        us, threads, detail, _ = oracle_sample_timing(w, target_s=2.0, max_s=10.0)
+        if it >= args.warmup:
+            times.append(us)
+    us = statistics.median(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": detail},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def step_kv_bytes(w) -> int:
+    _, lens = inputs.positions_and_lengths(w)
+    return kv_bytes(w, lens) * w.layers
+
+
+def needs_l2_flush(w) -> bool:
+    """A step that reads less than twice the L2 could be served from it on the next step."""
+    return step_kv_bytes(w) < 2 * L2_BYTES
+
+
+def workload_config(w):
+    return {"workload": w.name, "b": w.b, "h": w.h, "g": w.g, "d_h": w.d_h, "layers": w.layers,
+            "context": [w.ctx_lo, w.ctx_hi], "n_max": w.n_max, "kv_dtype": "bf16",
+            "l2": ("L2 flushed between steps (256 MB write)" if needs_l2_flush(w)
+                   else "inputs larger than L2 (no flush)")}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import query_grouped_decode_kv_b300 as mqa
+    from query_grouped_decode_kv_b300.decode_step import LayerState, StepInputs, decode_step
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = inputs.WORKLOADS[args.workload]
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    pos, lens = inputs.positions_and_lengths(w)
+    pos_d, lens_d = pos.to(dev), lens.to(dev)
+    layers, xs, outs = [], [], []
+    for li in range(w.layers):
+        k, v = inputs.cache(w, li, dev, tail="random")
+        layers.append(LayerState(k, v))
+        xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
+        outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
+    # small workloads fit in L2: flush it between steps by writing a buffer twice its size
+    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if needs_l2_flush(w)
+             else None)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        if flush is not None:
+            flush.fill_(1)
+        decode_step(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream, attn_events=events)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
+
+    # ---- device-timed region ----
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(w.layers)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = mqa.kernel_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    launches = mqa.kernel_launch_count() - launches0
+    assert mqa.get_device_status() == 0, "device status latched an error in the timed region"
+    ms_total = t_start.elapsed_time(t_end)
+    attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
+    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1000.0
+
+    # ---- end to end through host buffers ----
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hq = [pin(x.q) for x in xs]
+    hk = [pin(x.k_new) for x in xs]
+    hv = [pin(x.v_new) for x in xs]
+    ho = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
+    d2h = sum(t.numel() * t.element_size() for t in ho)
+
+    def e2e_step():
+        for li in range(w.layers):
+            xs[li].q.copy_(hq[li], non_blocking=True)
+            xs[li].k_new.copy_(hk[li], non_blocking=True)
+            xs[li].v_new.copy_(hv[li], non_blocking=True)
+        step()
+        for li in range(w.layers):
+            ho[li].copy_(outs[li], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---- max over ranks ----
+    ms_per_step = ms_total / args.steps
+    e2e_per_step = e2e_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_per_step, e2e_per_step, attn_avg_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, e2e_per_step, attn_avg_s = (float(x) for x in t.tolist())
+
+    if rank == 0:
+        peak, peak_kind = measured_peak_hbm()
+        nbytes = kv_bytes(w, lens)
+        achieved = nbytes / attn_avg_s / 1e9
+        traffic = recorded_traffic(w.name)
+        # weak scaling: every rank runs its own full step; N steps finish in ms_per_step
+        value_us = ms_per_step * 1000.0 / world
+        cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w)
+        line = {
+            "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w),
+            "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
+            "attention_us_per_layer": attn_avg_s * 1e6,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "kernel": "mqa_decode_attention call (split kernel + merge kernel)",
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "flops_per_launch": attention_flops(w, lens)},
+            "e2e": {"value": e2e_per_step * 1000.0 / world, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(launches),
+            "clocks": clocks.summary(),
+            "cpu_baseline": {"value": cb_us, "unit": UNIT, "cores": cb_threads, "kind": "oracle",
+                             "sample": cb_detail},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa_70b_80l", choices=sorted(inputs.WORKLOADS))
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

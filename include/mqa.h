@@ -1,0 +1,146 @@
+/*
+ * mqa.h -- C ABI of libmqa.so: the incremental decode step of Multi-Query / Grouped-Query
+ * Attention on NVIDIA B300 (sm_103a).
+ *
+ * Notation (from "分组查询注意力（GQA）与多查询注意力（MQA）深度实战", ybb.press, §四/§五):
+ *   b     sequences in the batch
+ *   h     query heads;  g = num_kv_heads  (g = h is MHA, g = 1 is MQA), h % g == 0
+ *   G     = h / g, the query heads that share one K/V head; query head i reads KV head
+ *           j = i / G, so the heads of one group are contiguous
+ *   d_h   head dimension (64 or 128)
+ *   n_max rows allocated per (sequence, KV head) in the cache
+ *
+ * Memory layout (all row-major, no padding, every tensor on the current CUDA device):
+ *   q, out           [b][h][d_h]            bfloat16
+ *   k_new, v_new     [b][g][d_h]            bfloat16
+ *   k_cache, v_cache [b][g][n_max][d_h]     bfloat16
+ *   pos, seq_lens    [b]                    int32
+ * bfloat16 values travel as their 16-bit patterns (mqa_bf16).
+ *
+ * Ownership: the caller allocates and owns every buffer; the library keeps no pointer to them
+ * after a call returns. The library owns one internal workspace per (device, stream) for the
+ * split-sequence partial results of mqa_decode_attention; it grows on demand (cudaMalloc, so
+ * the first call at a new, larger shape must happen outside CUDA-graph capture) and lives until
+ * the process exits.
+ *
+ * Ordering and errors: both compute calls only enqueue work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and return before the GPU has finished. Call mqa_kv_append
+ * before mqa_decode_attention on the same stream so that attention sees the new row. Arguments
+ * are checked on the host before anything is enqueued; a failed check returns an error code and
+ * enqueues nothing. Problems only the GPU can see (a position or length out of range, an
+ * internal wait that timed out) are latched in a per-device status word that
+ * mqa_get_device_status() reads; such a sequence's output is written as zeros and its cache is
+ * left untouched -- nothing is truncated silently. No C++ exception crosses this boundary.
+ */
+#ifndef MQA_H_
+#define MQA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MQA_API __attribute__((visibility("default")))
+#else
+#define MQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mqa_bf16;
+
+typedef enum mqa_status {
+  MQA_OK = 0,
+  MQA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, non-positive size, h % g != 0, ... */
+  MQA_ERR_UNSUPPORTED = 2,    /* a valid request outside what the kernels implement */
+  MQA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
+  MQA_ERR_DEVICE_BOUNDS = 4,  /* (latched) a pos or seq_lens entry was out of range */
+  MQA_ERR_TIMEOUT = 5         /* (latched) an in-kernel wait exceeded its time limit */
+} mqa_status;
+
+/*
+ * mqa_kv_append -- write this step's K and V rows into the cache.
+ *
+ * Defined by the decode step of "GQA与MQA深度实战" (ybb.press) §八, which stores the new token's
+ * K/V for the g KV heads at the current position before attending, and by the
+ * nanhubrain.csdn.net MQA article §2.2, which concatenates the new row onto the cached K/V
+ * along the sequence axis.
+ *
+ * For every sequence bi < b and KV head j < g:
+ *     k_cache[bi][j][pos[bi]][:] = k_new[bi][j][:]      (and the same for V)
+ * The copy is bit-exact; every other byte of both caches is left unchanged.
+ *
+ *   k_new, v_new     device, [b][g][d_h] bf16, 16-byte aligned, read only
+ *   k_cache, v_cache device, [b][g][n_max][d_h] bf16, 16-byte aligned, updated in place
+ *   pos              device, [b] int32, the row to write, 0 <= pos[bi] < n_max
+ *   b, g, d_h, n_max sizes (> 0; d_h in {64, 128})
+ *   stream           cudaStream_t to enqueue on
+ *
+ * Returns MQA_OK, MQA_ERR_INVALID_ARG, MQA_ERR_UNSUPPORTED or MQA_ERR_CUDA. A pos entry outside
+ * [0, n_max) skips that sequence and latches MQA_ERR_DEVICE_BOUNDS.
+ */
+MQA_API int mqa_kv_append(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
+                  mqa_bf16* v_cache, const int32_t* pos, int b, int g, int d_h, int n_max,
+                  void* stream);
+
+/*
+ * mqa_decode_attention -- grouped scaled-dot-product attention of one new query token per
+ * sequence against its cached keys and values.
+ *
+ * Defined by "GQA与MQA深度实战" (ybb.press) §五: with j = i / (h/g),
+ *     score_{i,t} = scale * q_i . K_{j,t},   alpha_{i,t} = softmax_t(score_{i,t}),
+ *     O_i = sum_t alpha_{i,t} V_{j,t};
+ * the page's scale is 1/sqrt(d_h). The sum runs over the rows t < seq_lens[bi] of sequence bi,
+ * which include the row appended this step (the page's §八 module attends over every cached
+ * position up to and including the new one). Rows at or beyond seq_lens[bi] are never read into
+ * the result, whatever they hold.
+ *
+ * Inputs are bf16, products and sums are fp32, `out` is rounded to bf16 (nearest-even). The
+ * result matches the fp64 definition within the tolerances stated by the tests.
+ *
+ *   q                device, [b][h][d_h] bf16, 16-byte aligned, read only
+ *   k_cache, v_cache device, [b][g][n_max][d_h] bf16, 16-byte aligned, read only
+ *   seq_lens         device, [b] int32, 1 <= seq_lens[bi] <= n_max
+ *   out              device, [b][h][d_h] bf16, 16-byte aligned, written
+ *   b, h, g          sizes (> 0, h % g == 0, h / g <= 64, b <= 8192)
+ *   d_h              64 or 128
+ *   n_max            cache rows per (sequence, KV head), > 0
+ *   scale            finite logit scale (normally 1/sqrt(d_h))
+ *   stream           cudaStream_t to enqueue on
+ *
+ * Returns MQA_OK, MQA_ERR_INVALID_ARG, MQA_ERR_UNSUPPORTED or MQA_ERR_CUDA. A seq_lens entry
+ * outside [1, n_max] writes zeros for that sequence and latches MQA_ERR_DEVICE_BOUNDS. Two calls
+ * that share a stream share that stream's workspace and are ordered by the stream; calls on
+ * different streams use different workspaces.
+ */
+MQA_API int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
+                         const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
+                         int n_max, float scale, void* stream);
+
+/* A static, human-readable name for a status code. Never returns NULL. */
+MQA_API const char* mqa_status_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear the status word latched by kernels on the current
+ * device. *status_out receives MQA_OK or the first latched error. Returns MQA_OK, or
+ * MQA_ERR_CUDA if the synchronisation or the read failed (for instance after a kernel fault),
+ * or MQA_ERR_INVALID_ARG if status_out is NULL.
+ */
+MQA_API int mqa_get_device_status(void* stream, int* status_out);
+
+/* Number of kernels this library has launched in this process (all devices, all streams). */
+MQA_API uint64_t mqa_kernel_launch_count(void);
+
+/*
+ * Testing hook: force the number of CTAs that split the attention work (0 = automatic choice)
+ * and the inner-product path (0 = automatic: tensor cores when h/g >= 8, CUDA cores otherwise;
+ * 1 = CUDA cores; 2 = tensor cores). Process-wide; returns MQA_ERR_INVALID_ARG for a negative
+ * CTA count or an unknown path. Results must not depend on either setting beyond rounding.
+ */
+MQA_API int mqa_debug_override(int num_ctas, int path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_H_ */

@@ -1,0 +1,141 @@
+"""ctypes binding over ``libmqa.so`` (declared in ``include/mqa.h``).
+
+Argument marshalling only: shapes are read off the torch tensors, pointers and the current CUDA
+stream are handed to the C ABI, and a non-zero status becomes :class:`MqaError`. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback path. Importing this module
+raises ``ImportError`` if the library has not been built (``python -m
+query_grouped_decode_kv_b300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libmqa.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libmqa.so is not built ({_LIB_PATH}); run "
+                      "`python -m query_grouped_decode_kv_b300.build`")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+_vp, _i32, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+
+_lib.mqa_kv_append.restype = _i32
+_lib.mqa_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp]
+_lib.mqa_decode_attention.restype = _i32
+_lib.mqa_decode_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                      _f32, _vp]
+_lib.mqa_status_string.restype = ctypes.c_char_p
+_lib.mqa_status_string.argtypes = [_i32]
+_lib.mqa_get_device_status.restype = _i32
+_lib.mqa_get_device_status.argtypes = [_vp, ctypes.POINTER(_i32)]
+_lib.mqa_kernel_launch_count.restype = ctypes.c_uint64
+_lib.mqa_kernel_launch_count.argtypes = []
+_lib.mqa_debug_override.restype = _i32
+_lib.mqa_debug_override.argtypes = [_i32, _i32]
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_TIMEOUT = range(6)
+
+
+class MqaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def raw() -> ctypes.CDLL:
+    """The loaded library, for callers that pass raw pointers themselves."""
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.mqa_status_string(int(status)).decode()
+
+
+def kernel_launch_count() -> int:
+    return int(_lib.mqa_kernel_launch_count())
+
+
+def debug_override(num_ctas: int = 0, path: int = 0) -> None:
+    st = _lib.mqa_debug_override(int(num_ctas), int(path))
+    if st:
+        raise MqaError(st, "mqa_debug_override")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor with {ndim} dims, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the latched device status (0 = ok)."""
+    out = _i32(0)
+    st = _lib.mqa_get_device_status(_vp(_stream_handle(stream)), ctypes.byref(out))
+    if st:
+        raise MqaError(st, "mqa_get_device_status")
+    return int(out.value)
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, pos: torch.Tensor, stream=None) -> None:
+    """``k_cache[b, j, pos[b]] = k_new[b, j]`` (and V) for every sequence b and KV head j."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    b, g, n_max, d_h = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h) \
+            or pos.shape != (b,):
+        raise ValueError("kv_append: inconsistent shapes")
+    st = _lib.mqa_kv_append(k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                            v_cache.data_ptr(), pos.data_ptr(), b, g, d_h, n_max,
+                            _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append")
+
+
+def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     seq_lens: torch.Tensor, out: torch.Tensor | None = None,
+                     scale: float | None = None, stream=None) -> torch.Tensor:
+    """Grouped decode attention: ``out[b, i] = softmax(scale q[b,i] K_j^T) V_j``, j = i // (h/g),
+    over the first ``seq_lens[b]`` cache rows. ``scale`` defaults to ``1/sqrt(d_h)``."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,):
+        raise ValueError("decode_attention: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_attention: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   seq_lens.data_ptr(), out.data_ptr(), b, h, g, d_h, n_max,
+                                   float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention")
+    return out

@@ -1,0 +1,742 @@
+// decode_attention.cuh -- grouped decode attention for sm_103a.
+//
+// Definition ("分组查询注意力（GQA）与多查询注意力（MQA）深度实战", ybb.press, §五): for query head i
+// of sequence bi, with j = i / G and G = h / g,
+//     O_i = sum_{t < L} softmax_t(scale * q_i . K_{j,t}) V_{j,t},   L = seq_lens[bi].
+//
+// Work decomposition. The unit of work is a tile of kTileKeys consecutive cache rows of one
+// "segment" (sequence bi, KV head j). Segments are laid end to end in (bi, j) order, forming
+// W = g * sum_bi ceil(L_bi / kTileKeys) tiles, and CTA c of P takes the contiguous tile range
+// [c*W/P, (c+1)*W/P). Lengths live on the device, so every CTA derives W and its range from
+// seq_lens itself: the split is balanced to within one tile whatever the length mix, and the host
+// never synchronises to read lengths. A segment that lies entirely inside one CTA's range is
+// finished by that CTA; otherwise each CTA writes a partial softmax state (m, l, o) into slot
+// c + segment, and a second kernel merges the slots with the log-sum-exp identity.
+//
+// Inside a CTA: one producer warp streams each tile's K and V rows from HBM into a ring of
+// shared-memory stages with bulk tensor copies (TMA, 128-byte swizzle); four consumer warps read
+// every stage once, so the K/V bytes of a KV head are fetched exactly once and reused by all G
+// query heads that share them. Each consumer warp keeps an online softmax (running max m and
+// sum l in fp32, log2 domain) for its slice of the tile's keys; at a segment's end the warps'
+// states are combined through shared memory.
+//
+// Inner products: for G >= 8 the grouped heads form a real dense contraction and run on tensor
+// cores (bf16 mma.sync m16n8k16, fp32 accumulate; S = Q K^T with the heads as M, then O += P V).
+// For G < 8 (MHA-like grouping) CUDA cores do fp32 FMAs.
+//
+// Every wait is bounded in time: on expiry the kernel latches MQA_ERR_TIMEOUT and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "status.cuh"
+
+namespace mqa {
+
+constexpr int kTileKeys = 64;       // cache rows per pipeline stage
+constexpr int kStages = 4;          // stages in the shared-memory ring
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
+constexpr int kMaxBatch = 8192;
+constexpr int kMaxGroup = 64;       // largest G = h / g served
+constexpr int kCombRows = 16;       // rows per warp in the combine scratch
+constexpr int kSwizzleRowBytes = 128;
+
+struct DecodeParams {
+  const __nv_bfloat16* q;     // [b][h][D]
+  const int32_t* seq_lens;    // [b]
+  __nv_bfloat16* out;         // [b][h][D]
+  float* part_o;              // [slots][G][D]   un-normalised partial outputs
+  float2* part_ml;            // [slots][G]      (running max in log2 units, running sum)
+  int b, h, g, G, n_max;
+  int num_ctas;               // P
+  float scale_log2;           // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
+__host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
+
+// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort][prefix(b+1)]
+__host__ __device__ constexpr int smem_fixed_bytes(int D) {
+  return kStages * stage_bytes(D) + kConsumerWarps * kCombRows * comb_row_floats(D) * 4 +
+         kConsumerWarps * kCombRows * 8 + (2 * kStages + 1) * 8 + 16;
+}
+__host__ __device__ constexpr size_t smem_bytes(int D, int b) {
+  return 1024 + static_cast<size_t>(smem_fixed_bytes(D)) + static_cast<size_t>(b + 1) * 4;
+}
+
+__device__ __forceinline__ int tiles_of_length(int L, int n_max) {
+  return (L >= 1 && L <= n_max) ? (L + kTileKeys - 1) / kTileKeys : 0;
+}
+
+// Byte offset of (key row, column d) inside one K or V stage: the row is split into 64-column
+// halves of 128 bytes (one TMA box each); inside a half the 16-byte chunk index is XORed with
+// (row % 8), the 128-byte swizzle the TMA applies. `d` must be a multiple of 8 here.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int key, int d) {
+  const int half = d >> 6;
+  const int chunk = (d >> 3) & 7;
+  return base + static_cast<uint32_t>(half * (kTileKeys * kSwizzleRowBytes) +
+                                      key * kSwizzleRowBytes + ((chunk ^ (key & 7)) << 4));
+}
+
+// Walks the tiles of one CTA's range in segment order.
+struct TileCursor {
+  int bi, j, tile, nt;
+  __device__ __forceinline__ void start(unsigned long long x, const uint32_t* pre, int B, int g) {
+    // largest bi with g * pre[bi] <= x (that sequence then has at least one tile)
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<unsigned long long>(g) * pre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    bi = lo;
+    nt = static_cast<int>(pre[bi + 1] - pre[bi]);
+    const unsigned long long rem = x - static_cast<unsigned long long>(g) * pre[bi];
+    j = static_cast<int>(rem / nt);
+    tile = static_cast<int>(rem % nt);
+  }
+  __device__ __forceinline__ void advance(const uint32_t* pre, int B, int g) {
+    if (++tile < nt) return;
+    tile = 0;
+    if (++j < g) return;
+    j = 0;
+    do { ++bi; } while (bi < B && pre[bi + 1] == pre[bi]);
+    nt = bi < B ? static_cast<int>(pre[bi + 1] - pre[bi]) : 0;
+  }
+};
+
+struct SharedLayout {
+  uint8_t* stages;      // kStages x stage_bytes(D), 1024-aligned
+  float* comb_o;        // [kConsumerWarps][kCombRows][comb_row_floats(D)]
+  float2* comb_ml;      // [kConsumerWarps][kCombRows]
+  uint64_t* full;       // [kStages]
+  uint64_t* empty;      // [kStages]
+  uint64_t* cbar;       // consumer-wide barrier
+  volatile int* abort;  // set when any warp gives up
+  uint32_t* pre;        // [b + 1] tiles before each sequence
+};
+
+template <int D>
+__device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
+  SharedLayout s;
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  s.stages = p;
+  p += kStages * stage_bytes(D);
+  s.comb_o = reinterpret_cast<float*>(p);
+  p += kConsumerWarps * kCombRows * comb_row_floats(D) * 4;
+  s.comb_ml = reinterpret_cast<float2*>(p);
+  p += kConsumerWarps * kCombRows * 8;
+  s.full = reinterpret_cast<uint64_t*>(p);
+  s.empty = s.full + kStages;
+  s.cbar = s.empty + kStages;
+  p += (2 * kStages + 1) * 8;
+  s.abort = reinterpret_cast<volatile int*>(p);
+  p += 16;
+  s.pre = reinterpret_cast<uint32_t*>(p);
+  return s;
+}
+
+// Consumer-wide barrier on an mbarrier (all 128 consumer threads arrive), bounded in time.
+__device__ __forceinline__ bool consumer_sync(const SharedLayout& sh, uint32_t& phase,
+                                              unsigned long long limit) {
+  mbar_arrive(sh.cbar);
+  const bool ok = mbar_wait_bounded(sh.cbar, phase, limit, sh.abort);
+  phase ^= 1u;
+  return ok;
+}
+
+__device__ __forceinline__ void give_up(const SharedLayout& sh) {
+  latch_status(kStatusTimeout);
+  *sh.abort = 1;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Combine the consumer warps' states for one segment and write the result: the final bf16 output
+// when the whole segment lies in this CTA, else a partial state in workspace slot `slot`.
+// Row `hr` (a head of the group) has contributions at comb[(w, r)] for the pairs rows_of() gives.
+// ---------------------------------------------------------------------------------------------
+template <int D, class RowMap>
+__device__ __forceinline__ void combine_and_store(const DecodeParams& P, const SharedLayout& sh,
+                                                  int bi, int j, bool complete, int slot,
+                                                  RowMap rows_of) {
+  const int tid = threadIdx.x;  // 0 .. 127 (consumer threads)
+  const int G = P.G;
+  for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+    const int hr = idx / D;
+    const int d = idx - hr * D;
+    int ws[kConsumerWarps], rs[kConsumerWarps];
+    const int n = rows_of(hr, ws, rs);
+    float M = -INFINITY;
+    for (int c = 0; c < n; ++c) M = fmaxf(M, sh.comb_ml[ws[c] * kCombRows + rs[c]].x);
+    float acc = 0.f, den = 0.f;
+    for (int c = 0; c < n; ++c) {
+      const float2 ml = sh.comb_ml[ws[c] * kCombRows + rs[c]];
+      const float wgt = fast_exp2(ml.x - M);
+      den += wgt * ml.y;
+      acc += wgt * sh.comb_o[(ws[c] * kCombRows + rs[c]) * comb_row_floats(D) + d];
+    }
+    if (complete) {
+      const size_t o = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d;
+      P.out[o] = __float2bfloat16_rn(acc / den);
+    } else {
+      const size_t r = static_cast<size_t>(slot) * G + hr;
+      P.part_o[r * D + d] = acc;
+      if (d == 0) P.part_ml[r] = make_float2(M, den);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Tensor-core consumer (G >= 8). WM warps (one per 16 heads) form a group; kConsumerWarps / WM
+// groups split each tile's keys.
+// ---------------------------------------------------------------------------------------------
+template <int D, int WM>
+struct MmaConsumer {
+  static constexpr int NGRP = kConsumerWarps / WM;
+  static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
+  static constexpr int NT_S = KPW / 8;          // score tiles (n = 8 keys)
+  static constexpr int KS_QK = D / 16;          // k-steps over the head dimension
+  static constexpr int NT_O = D / 8;            // output tiles (n = 8 columns)
+  static constexpr int KS_PV = KPW / 16;        // k-steps over keys
+  static_assert(NT_S % 2 == 0 && KS_PV >= 1, "tile split");
+
+  uint32_t qa[KS_QK][4];
+  float o[NT_O][4];
+  float m[2], l[2];
+
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
+                                                int lane) {
+    const int r0 = mi * 16 + (lane >> 2), r1 = r0 + 8;
+    const __nv_bfloat16* qb = P.q + (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * P.G) * D;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + static_cast<size_t>(r0) * D);
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + static_cast<size_t>(r1) * D);
+    const bool v0 = r0 < P.G, v1 = r1 < P.G;
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ++ks) {
+      const int c = (ks * 16 + (lane & 3) * 2) >> 1;  // in bf16 pairs
+      qa[ks][0] = v0 ? __ldg(q0 + c) : 0u;
+      qa[ks][1] = v1 ? __ldg(q1 + c) : 0u;
+      qa[ks][2] = v0 ? __ldg(q0 + c + 4) : 0u;
+      qa[ks][3] = v1 ? __ldg(q1 + c + 4) : 0u;
+    }
+#pragma unroll
+    for (int n = 0; n < NT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // One tile. `valid` = number of the tile's rows that lie below the sequence length.
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
+                                       int valid, float scale_log2) {
+    float s[NT_S][4];
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    const int mat = lane >> 3, rr = lane & 7;
+    // S = Q K^T
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ++ks) {
+#pragma unroll
+      for (int np = 0; np < NT_S / 2; ++np) {
+        const int key = grp * KPW + np * 16 + rr + ((mat & 2) ? 8 : 0);
+        const int d = ks * 16 + ((mat & 1) ? 8 : 0);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz(kbase, key, d), b0, b1, b2, b3);
+        mma_16816(s[2 * np], qa[ks], b0, b1);
+        mma_16816(s[2 * np + 1], qa[ks], b2, b3);
+      }
+    }
+    // scale (log2 domain), mask rows at or beyond the length, running max per head row
+    const int c2 = (lane & 3) * 2;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      const int key = grp * KPW + n * 8 + c2;
+      const bool ok0 = key < valid, ok1 = key + 1 < valid;
+      s[n][0] = ok0 ? s[n][0] * scale_log2 : -INFINITY;
+      s[n][1] = ok1 ? s[n][1] * scale_log2 : -INFINITY;
+      s[n][2] = ok0 ? s[n][2] * scale_log2 : -INFINITY;
+      s[n][3] = ok1 ? s[n][3] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = fast_exp2(m[0] - ref0), al1 = fast_exp2(m[1] - ref1);
+    m[0] = mn0;
+    m[1] = mn1;
+    // weights, rounded to bf16 once: the same rounded values feed P V and the running sum, so
+    // the normalised weights still add up to one
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] = round_bf16(fast_exp2(s[n][0] - ref0));
+      s[n][1] = round_bf16(fast_exp2(s[n][1] - ref0));
+      s[n][2] = round_bf16(fast_exp2(s[n][2] - ref1));
+      s[n][3] = round_bf16(fast_exp2(s[n][3] - ref1));
+      ps0 += s[n][0] + s[n][1];
+      ps1 += s[n][2] + s[n][3];
+    }
+    l[0] = l[0] * al0 + ps0;
+    l[1] = l[1] * al1 + ps1;
+#pragma unroll
+    for (int n = 0; n < NT_O; ++n) {
+      o[n][0] *= al0; o[n][1] *= al0;
+      o[n][2] *= al1; o[n][3] *= al1;
+    }
+    // O += P V  (the packing below is exact: the weights are already bf16 values)
+#pragma unroll
+    for (int kk = 0; kk < KS_PV; ++kk) {
+      uint32_t a[4];
+      a[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < NT_O / 2; ++dp) {
+        const int key = grp * KPW + kk * 16 + rr + ((mat & 1) ? 8 : 0);
+        const int d = dp * 16 + ((mat & 2) ? 8 : 0);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(swz(vbase, key, d), b0, b1, b2, b3);
+        mma_16816(o[2 * dp], a, b0, b1);
+        mma_16816(o[2 * dp + 1], a, b2, b3);
+      }
+    }
+  }
+
+  // Publish this warp's state (rows mi*16 .. mi*16+15 of the group) to the combine scratch.
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+    float l0 = l[0], l1 = l[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int r = lane >> 2, c2 = (lane & 3) * 2;
+    float* row0 = sh.comb_o + (warp * kCombRows + r) * comb_row_floats(D);
+    float* row1 = sh.comb_o + (warp * kCombRows + r + 8) * comb_row_floats(D);
+#pragma unroll
+    for (int n = 0; n < NT_O; ++n) {
+      *reinterpret_cast<float2*>(row0 + n * 8 + c2) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(row1 + n * 8 + c2) = make_float2(o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+      sh.comb_ml[warp * kCombRows + r] = make_float2(m[0], l0);
+      sh.comb_ml[warp * kCombRows + r + 8] = make_float2(m[1], l1);
+    }
+  }
+
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int grp = 0; grp < NGRP; ++grp) {
+        ws[grp] = grp * WM + (hr >> 4);
+        rs[grp] = hr & 15;
+      }
+      return NGRP;
+    }
+  };
+};
+
+// ---------------------------------------------------------------------------------------------
+// CUDA-core consumer (G < 8). Warp w takes keys [16w, 16w + 16) of every tile; lane owns
+// DPL = D/32 consecutive columns of q, K, V and the output.
+// ---------------------------------------------------------------------------------------------
+template <int D, int G>
+struct CcConsumer {
+  static constexpr int DPL = D / 32;
+  static constexpr int KPW = kTileKeys / kConsumerWarps;  // 16
+  static_assert(KPW == 16, "the reduce-scatter below is written for 16 keys per warp");
+
+  float qf[G][DPL];
+  float o[G][DPL];
+  float m[G], l[G];
+
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int lane) {
+    const __nv_bfloat16* qb = P.q + (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G) * D;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        qf[hh][e] = __bfloat162float(qb[hh * D + lane * DPL + e]);
+        o[hh][e] = 0.f;
+      }
+      m[hh] = -INFINITY;
+      l[hh] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void load_row(uint32_t base, int key, int lane, float (&f)[DPL]) const {
+    const int d0 = lane * DPL;
+    const uint32_t addr = swz(base, key, d0 & ~7) + (d0 & 7) * 2;
+    if constexpr (DPL == 4) {
+      uint32_t x, y;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
+      const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);
+      const __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162*>(&y);
+      f[0] = __low2float(a); f[1] = __high2float(a);
+      f[2] = __low2float(c); f[3] = __high2float(c);
+    } else {
+      uint32_t x;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+      const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);
+      f[0] = __low2float(a); f[1] = __high2float(a);
+    }
+  }
+
+  // Sum v[0..15] (one partial per key) over the 32 lanes; lane l ends with the full sum for
+  // key l >> 1 (lanes 2k and 2k+1 hold the same value). 16 shuffles instead of 16 x 5.
+  __device__ __forceinline__ static float reduce_scatter16(float (&v)[16], int lane) {
+    float a[8];
+    const bool up16 = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float send = up16 ? v[i] : v[i + 8];
+      const float keep = up16 ? v[i + 8] : v[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float b4[4];
+    const bool up8 = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = up8 ? a[i] : a[i + 4];
+      const float keep = up8 ? a[i + 4] : a[i];
+      b4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float c2[2];
+    const bool up4 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = up4 ? b4[i] : b4[i + 2];
+      const float keep = up4 ? b4[i + 2] : b4[i];
+      c2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    const bool up2 = lane & 2;
+    const float send = up2 ? c2[0] : c2[1];
+    const float keep = up2 ? c2[1] : c2[0];
+    float r = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    return r;
+  }
+
+  // `nvalid` = rows of this warp's 16 keys below the sequence length (warp-uniform, 0..16).
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int warp, int lane,
+                                       int nvalid, float scale_log2) {
+    const int key0 = warp * KPW;
+    float kf[KPW][DPL];
+#pragma unroll
+    for (int kk = 0; kk < KPW; ++kk) {
+      if (kk < nvalid) {
+        load_row(kbase, key0 + kk, lane, kf[kk]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) kf[kk][e] = 0.f;
+      }
+    }
+    const bool mine_valid = (lane >> 1) < nvalid;
+    float p[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float part[KPW];
+#pragma unroll
+      for (int kk = 0; kk < KPW; ++kk) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc = fmaf(qf[hh][e], kf[kk][e], acc);
+        part[kk] = acc;
+      }
+      const float dot = reduce_scatter16(part, lane);
+      const float s = mine_valid ? dot * scale_log2 : -INFINITY;
+      float mx = s;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(m[hh], mx);
+      const float ref = (mn == -INFINITY) ? 0.f : mn;
+      const float al = fast_exp2(m[hh] - ref);
+      m[hh] = mn;
+      p[hh] = fast_exp2(s - ref);
+      l[hh] = l[hh] * al + ((lane & 1) ? 0.f : p[hh]);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[hh][e] *= al;
+    }
+    // O += P V over the valid keys (p for key kk sits in lanes 2kk and 2kk+1)
+#pragma unroll
+    for (int kk = 0; kk < KPW; ++kk) {
+      if (kk < nvalid) {
+        float vf[DPL];
+        load_row(vbase, key0 + kk, lane, vf);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float pk = __shfl_sync(0xffffffffu, p[hh], 2 * kk);
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float lsum = l[hh];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      float* row = sh.comb_o + (warp * kCombRows + hh) * comb_row_floats(D);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) row[lane * DPL + e] = o[hh][e];
+      if (lane == 0) sh.comb_ml[warp * kCombRows + hh] = make_float2(m[hh], lsum);
+    }
+  }
+
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) { ws[w] = w; rs[w] = hr; }
+      return kConsumerWarps;
+    }
+  };
+};
+
+// ---------------------------------------------------------------------------------------------
+// The kernel. `Consumer` is MmaConsumer<D, WM> or CcConsumer<D, G>.
+// ---------------------------------------------------------------------------------------------
+template <int D, class Consumer, bool kTensorCores, int WM>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const SharedLayout sh = carve_shared<D>(smem_raw);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int B = P.b;
+
+  // ---- tiles per sequence and their exclusive prefix (every CTA computes the same) ----------
+  __shared__ uint32_t part_sums[kThreads];
+  {
+    const int chunk = (B + kThreads - 1) / kThreads;
+    const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
+    uint32_t s = 0;
+    for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+    part_sums[tid] = s;
+    if (tid == 0) {
+      *sh.abort = 0;
+      for (int st = 0; st < kStages; ++st) {
+        mbar_init(&sh.full[st], 1);
+        mbar_init(&sh.empty[st], kConsumerWarps);
+      }
+      mbar_init(sh.cbar, kConsumerWarps * 32);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t run = 0;
+      for (int t = 0; t < kThreads; ++t) { const uint32_t v = part_sums[t]; part_sums[t] = run; run += v; }
+      sh.pre[B] = run;
+    }
+    __syncthreads();
+    uint32_t run = part_sums[tid];
+    for (int i = lo; i < hi; ++i) {
+      sh.pre[i] = run;
+      run += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+    }
+    __syncthreads();
+  }
+
+  // ---- sequences with an out-of-range length: zero output, latch the error ------------------
+  for (int bi = blockIdx.x; bi < B; bi += P.num_ctas) {
+    const int L = __ldg(P.seq_lens + bi);
+    if (L >= 1 && L <= P.n_max) continue;
+    if (tid == 0) latch_status(kStatusDeviceBounds);
+    __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.h * D;
+    for (int e = tid; e < P.h * D; e += kThreads) ob[e] = __float2bfloat16_rn(0.f);
+  }
+
+  const unsigned long long W = static_cast<unsigned long long>(P.g) * sh.pre[B];
+  const unsigned long long x0 = W * blockIdx.x / P.num_ctas;
+  const unsigned long long x1 = W * (blockIdx.x + 1) / P.num_ctas;
+  if (x0 >= x1) return;
+  const int ntiles = static_cast<int>(x1 - x0);
+  const uint32_t stages_base = smem_addr(sh.stages);
+  constexpr uint32_t kStageBytes = stage_bytes(D);
+  constexpr uint32_t kKvBytes = kStageBytes / 2;
+
+  if (warp == kConsumerWarps) {
+    // ================================ producer ================================================
+    if (lane != 0) return;
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+    const uint64_t policy = l2_policy_evict_first();
+    TileCursor cur;
+    cur.start(x0, sh.pre, B, P.g);
+    int issued = 0;
+    for (int k = 0; k < ntiles; ++k) {
+      const int st = k % kStages;
+      const uint32_t par = ((k / kStages) & 1) ^ 1;
+      if (!mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort)) {
+        if (!*sh.abort) give_up(sh);
+        break;
+      }
+      mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
+      const int z = cur.bi * P.g + cur.j;
+      const int y = cur.tile * kTileKeys;
+      uint8_t* kdst = sh.stages + st * kStageBytes;
+      uint8_t* vdst = kdst + kKvBytes;
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, &tm_k, &sh.full[st], half * 64, y,
+                    z, policy);
+        tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, &tm_v, &sh.full[st], half * 64, y,
+                    z, policy);
+      }
+      ++issued;
+      cur.advance(sh.pre, B, P.g);
+    }
+    // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
+    const volatile int never = 0;
+    for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
+      mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.timeout_ns, &never);
+    return;
+  }
+
+  // ================================== consumers ================================================
+  Consumer cons;
+  const int grp = kTensorCores ? warp / WM : warp;
+  const int mi = kTensorCores ? warp % WM : 0;
+  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / kConsumerWarps : kTileKeys / kConsumerWarps;
+  uint32_t cphase = 0;
+  TileCursor cur;
+  cur.start(x0, sh.pre, B, P.g);
+  int L = 0;
+  bool began_at_zero = false;
+  for (int k = 0; k < ntiles; ++k) {
+    const int st = k % kStages;
+    if (!mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
+      if (!*sh.abort) give_up(sh);
+      return;
+    }
+    if (k == 0 || cur.tile == 0) {
+      L = __ldg(P.seq_lens + cur.bi);
+      began_at_zero = (cur.tile == 0);
+      if constexpr (kTensorCores) cons.begin_segment(P, cur.bi, cur.j, mi, lane);
+      else cons.begin_segment(P, cur.bi, cur.j, lane);
+    }
+    const int tile_start = cur.tile * kTileKeys;
+    const int valid = min(L - tile_start, kTileKeys);  // >= 1
+    const uint32_t kbase = stages_base + st * kStageBytes;
+    const uint32_t vbase = kbase + kKvBytes;
+    if constexpr (kTensorCores) {
+      // V rows at or beyond the length may hold anything (NaN included) and 0 * NaN = NaN on
+      // the tensor cores: zero this group's invalid V rows before P V reads them.
+      const int g0 = grp * kGroupKeys;
+      if (valid < g0 + kGroupKeys) {
+        uint8_t* vst = sh.stages + st * kStageBytes + kKvBytes;
+        const int first = max(valid, g0);
+        const int rows = g0 + kGroupKeys - first;
+        const int chunks_per_row = D * 2 / 16;
+        for (int c = lane; c < rows * chunks_per_row; c += 32) {
+          const int key = first + c / chunks_per_row;
+          const int ch = c % chunks_per_row;
+          const int half = ch >> 3, sub = ch & 7;
+          *reinterpret_cast<uint4*>(vst + half * kTileKeys * kSwizzleRowBytes +
+                                    key * kSwizzleRowBytes + sub * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      cons.tile(kbase, vbase, grp, lane, valid, P.scale_log2);
+    } else {
+      const int nvalid = max(0, min(valid - warp * kGroupKeys, kGroupKeys));
+      cons.tile(kbase, vbase, warp, lane, nvalid, P.scale_log2);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[st]);
+
+    const bool seg_end = (cur.tile == cur.nt - 1);
+    if (seg_end || k == ntiles - 1) {
+      const bool complete = began_at_zero && seg_end;
+      const int seg = cur.bi * P.g + cur.j;
+      cons.publish(sh, warp, lane);
+      if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
+      combine_and_store<D>(P, sh, cur.bi, cur.j, complete, static_cast<int>(blockIdx.x) + seg,
+                           typename Consumer::Rows{});
+      if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
+    }
+    cur.advance(sh.pre, B, P.g);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Merge the partial states of segments that were split across CTAs:
+//   M = max_c m_c,  o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c.
+// One block per segment (bi, j); a segment finished by one CTA is skipped.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) merge_partials_kernel(const DecodeParams P) {
+  const int seg = blockIdx.x;
+  const int bi = seg / P.g, j = seg - (seg / P.g) * P.g;
+  const int L = __ldg(P.seq_lens + bi);
+  const int nt = tiles_of_length(L, P.n_max);
+  if (nt == 0) return;
+  // tiles before sequence bi, and all tiles
+  __shared__ unsigned long long red[2][128];
+  unsigned long long before = 0, total = 0;
+  for (int i = threadIdx.x; i < P.b; i += blockDim.x) {
+    const unsigned long long t = tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+    total += t;
+    if (i < bi) before += t;
+  }
+  red[0][threadIdx.x] = before;
+  red[1][threadIdx.x] = total;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) {
+      red[0][threadIdx.x] += red[0][threadIdx.x + s];
+      red[1][threadIdx.x] += red[1][threadIdx.x + s];
+    }
+    __syncthreads();
+  }
+  const unsigned long long Pn = static_cast<unsigned long long>(P.num_ctas);
+  const unsigned long long W = static_cast<unsigned long long>(P.g) * red[1][0];
+  const unsigned long long s0 = static_cast<unsigned long long>(P.g) * red[0][0] +
+                                static_cast<unsigned long long>(j) * nt;
+  const unsigned long long s1 = s0 + nt - 1;
+  // CTA owning tile x: the largest c with c*W/P <= x
+  const int c_first = static_cast<int>(((s0 + 1) * Pn - 1) / W);
+  const int c_last = static_cast<int>(((s1 + 1) * Pn - 1) / W);
+  if (c_first == c_last) return;
+  // CTAs with an empty range (possible when P > W) wrote nothing: skip them
+  auto owns_tiles = [&](int c) {
+    return W * static_cast<unsigned long long>(c) / Pn <
+           W * static_cast<unsigned long long>(c + 1) / Pn;
+  };
+  const int G = P.G;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int hr = idx / D, d = idx - (idx / D) * D;
+    float M = -INFINITY;
+    for (int c = c_first; c <= c_last; ++c)
+      if (owns_tiles(c)) M = fmaxf(M, P.part_ml[static_cast<size_t>(c + seg) * G + hr].x);
+    float acc = 0.f, den = 0.f;
+    for (int c = c_first; c <= c_last; ++c) {
+      if (!owns_tiles(c)) continue;
+      const size_t r = static_cast<size_t>(c + seg) * G + hr;
+      const float2 ml = P.part_ml[r];
+      const float w = fast_exp2(ml.x - M);
+      den += w * ml.y;
+      acc += w * P.part_o[r * D + d];
+    }
+    P.out[(static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d] =
+        __float2bfloat16_rn(acc / den);
+  }
+}
+
+}  // namespace mqa

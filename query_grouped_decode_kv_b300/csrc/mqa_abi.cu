@@ -1,0 +1,323 @@
+// mqa_abi.cu -- the extern "C" entry points declared in include/mqa.h: host-side argument
+// checks, the per-(device, stream) workspace, TMA descriptors, and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cmath>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/mqa.h"
+#include "decode_attention.cuh"
+#include "kv_append.cuh"
+#include "status.cuh"
+
+namespace {
+
+using mqa::DecodeParams;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_force_ctas{0};
+std::atomic<int> g_force_path{0};
+
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+// ------------------------------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Cache [b][g][n_max][d_h] bf16 seen as a 3-D tensor (d_h, n_max, b*g); box = 64 columns x
+// kTileKeys rows, 128-byte swizzle. Rows past n_max read as zeros.
+bool make_cache_map(CUtensorMap* map, const void* base, int bg, int n_max, int d_h) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_h), static_cast<cuuint64_t>(n_max),
+                              static_cast<cuuint64_t>(bg)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * 2,
+                                 static_cast<cuuint64_t>(n_max) * d_h * 2};
+  const cuuint32_t box[3] = {64, mqa::kTileKeys, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Workspace for split-sequence partial states, one per (device, stream); grows on demand.
+// ------------------------------------------------------------------------------------------------
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+int get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& ws = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+  if (ws.bytes < bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MQA_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return MQA_ERR_UNSUPPORTED;  // cannot grow in capture
+    if (ws.ptr) {
+      // the old buffer may still be read by earlier work on this stream
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return MQA_ERR_CUDA;
+      cudaFree(ws.ptr);
+      ws.ptr = nullptr;
+      ws.bytes = 0;
+    }
+    const size_t grow = bytes + bytes / 4;
+    if (cudaMalloc(&ws.ptr, grow) != cudaSuccess) {
+      ws.ptr = nullptr;
+      return MQA_ERR_CUDA;
+    }
+    ws.bytes = grow;
+  }
+  *out = ws.ptr;
+  return MQA_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+};
+std::mutex g_dev_mutex;
+std::map<int, DeviceInfo> g_dev;
+
+int device_info(int dev, DeviceInfo* info) {
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MQA_ERR_CUDA;
+    it = g_dev.emplace(dev, d).first;
+  }
+  *info = it->second;
+  return MQA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Kernel selection
+// ------------------------------------------------------------------------------------------------
+using AttnKernel = void (*)(const CUtensorMap, const CUtensorMap, const DecodeParams);
+
+template <int D, int WM>
+AttnKernel mma_kernel() {
+  return mqa::decode_attention_kernel<D, mqa::MmaConsumer<D, WM>, true, WM>;
+}
+template <int D, int G>
+AttnKernel cc_kernel() {
+  return mqa::decode_attention_kernel<D, mqa::CcConsumer<D, G>, false, 1>;
+}
+
+template <int D>
+AttnKernel pick_kernel(bool tensor_cores, int G) {
+  if (tensor_cores) {
+    if (G <= 16) return mma_kernel<D, 1>();
+    if (G <= 32) return mma_kernel<D, 2>();
+    return mma_kernel<D, 4>();
+  }
+  switch (G) {
+    case 1: return cc_kernel<D, 1>();
+    case 2: return cc_kernel<D, 2>();
+    case 3: return cc_kernel<D, 3>();
+    case 4: return cc_kernel<D, 4>();
+    case 5: return cc_kernel<D, 5>();
+    case 6: return cc_kernel<D, 6>();
+    case 7: return cc_kernel<D, 7>();
+    default: return nullptr;
+  }
+}
+
+std::mutex g_attr_mutex;
+std::map<std::pair<int, const void*>, size_t> g_smem_set;  // (device, kernel) -> bytes allowed
+
+int ensure_smem(int dev, const void* kernel, size_t bytes) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  size_t& cur = g_smem_set[{dev, kernel}];
+  if (cur >= bytes) return MQA_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  cur = bytes;
+  return MQA_OK;
+}
+
+int launch_error() { return cudaGetLastError() == cudaSuccess ? MQA_OK : MQA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mqa_status_string(int status) {
+  switch (status) {
+    case MQA_OK: return "MQA_OK";
+    case MQA_ERR_INVALID_ARG: return "MQA_ERR_INVALID_ARG: invalid argument";
+    case MQA_ERR_UNSUPPORTED: return "MQA_ERR_UNSUPPORTED: shape or setting not supported";
+    case MQA_ERR_CUDA: return "MQA_ERR_CUDA: CUDA runtime error";
+    case MQA_ERR_DEVICE_BOUNDS: return "MQA_ERR_DEVICE_BOUNDS: pos or seq_lens out of range";
+    case MQA_ERR_TIMEOUT: return "MQA_ERR_TIMEOUT: an in-kernel wait timed out";
+    default: return "unknown mqa status";
+  }
+}
+
+uint64_t mqa_kernel_launch_count(void) { return g_launches.load(); }
+
+int mqa_debug_override(int num_ctas, int path) {
+  if (num_ctas < 0 || path < 0 || path > 2) return MQA_ERR_INVALID_ARG;
+  g_force_ctas.store(num_ctas);
+  g_force_path.store(path);
+  return MQA_OK;
+}
+
+int mqa_get_device_status(void* stream, int* status_out) {
+  if (!status_out) return MQA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MQA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, mqa::g_device_status, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(mqa::g_device_status, &zero, sizeof(int), 0,
+                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MQA_ERR_CUDA;
+  *status_out = v;
+  return MQA_OK;
+}
+
+int mqa_kv_append(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
+                  mqa_bf16* v_cache, const int32_t* pos, int b, int g, int d_h, int n_max,
+                  void* stream) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(b) * g;
+  if (rows > (1ll << 31) || static_cast<double>(rows) * n_max * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+
+  const int chunks = d_h / 8;
+  const long long total = rows * chunks;
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  mqa::kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, g, chunks,
+      n_max);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
+                         const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
+                         int n_max, float scale, void* stream) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
+  if (h % g != 0) return MQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const int G = h / g;
+  if (G > mqa::kMaxGroup || b > mqa::kMaxBatch) return MQA_ERR_UNSUPPORTED;
+  const long long bg = static_cast<long long>(b) * g;
+  const long long tiles_per_seg = (static_cast<long long>(n_max) + mqa::kTileKeys - 1) / mqa::kTileKeys;
+  if (bg > (1ll << 24) || static_cast<long long>(b) * tiles_per_seg >= (1ll << 31) ||
+      static_cast<double>(bg) * n_max * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+  const int force_path = g_force_path.load();
+  const bool tensor_cores = force_path == 0 ? (G >= 8) : (force_path == 2);
+  if (!tensor_cores && G > 7) return MQA_ERR_UNSUPPORTED;
+
+  // ---- device side ----
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MQA_ERR_CUDA;
+  DeviceInfo info;
+  if (int st = device_info(dev, &info)) return st;
+
+  // CTAs: one per SM, but no more than a quarter of the (upper bound on the) tile count, so that
+  // tiny problems are not scattered into many partial states.
+  const long long w_max = bg * tiles_per_seg;
+  long long ctas = (w_max + 3) / 4;
+  if (ctas > info.sms) ctas = info.sms;
+  if (ctas < 1) ctas = 1;
+  if (const int f = g_force_ctas.load()) ctas = f;
+
+  const long long slots = ctas + bg;
+  const size_t part_o_bytes = static_cast<size_t>(slots) * G * d_h * sizeof(float);
+  const size_t part_ml_bytes = static_cast<size_t>(slots) * G * sizeof(float2);
+  void* ws = nullptr;
+  if (ctas > 1) {
+    if (int st = get_workspace(dev, s, part_o_bytes + part_ml_bytes, &ws)) return st;
+  }
+
+  CUtensorMap tmk, tmv;
+  if (!make_cache_map(&tmk, k_cache, static_cast<int>(bg), n_max, d_h) ||
+      !make_cache_map(&tmv, v_cache, static_cast<int>(bg), n_max, d_h))
+    return MQA_ERR_CUDA;
+
+  DecodeParams P;
+  P.q = reinterpret_cast<const __nv_bfloat16*>(q);
+  P.seq_lens = seq_lens;
+  P.out = reinterpret_cast<__nv_bfloat16*>(out);
+  P.part_o = static_cast<float*>(ws);
+  P.part_ml = ws ? reinterpret_cast<float2*>(static_cast<char*>(ws) + part_o_bytes) : nullptr;
+  P.b = b;
+  P.h = h;
+  P.g = g;
+  P.G = G;
+  P.n_max = n_max;
+  P.num_ctas = static_cast<int>(ctas);
+  P.scale_log2 = scale * 1.4426950408889634f;
+  P.timeout_ns = kWaitLimitNs;
+
+  AttnKernel kern = d_h == 128 ? pick_kernel<128>(tensor_cores, G) : pick_kernel<64>(tensor_cores, G);
+  if (!kern) return MQA_ERR_UNSUPPORTED;
+  const size_t smem = mqa::smem_bytes(d_h, b);
+  if (int st = ensure_smem(dev, reinterpret_cast<const void*>(kern), smem)) return st;
+  kern<<<static_cast<unsigned>(ctas), mqa::kThreads, smem, s>>>(tmk, tmv, P);
+  g_launches.fetch_add(1);
+  if (int st = launch_error()) return st;
+  if (ctas > 1) {
+    if (d_h == 128)
+      mqa::merge_partials_kernel<128><<<static_cast<unsigned>(bg), 128, 0, s>>>(P);
+    else
+      mqa::merge_partials_kernel<64><<<static_cast<unsigned>(bg), 128, 0, s>>>(P);
+    g_launches.fetch_add(1);
+    if (int st = launch_error()) return st;
+  }
+  return MQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+"""The C ABI on the host, without a GPU: libmqa.so loads, exports every function include/mqa.h
+declares, and rejects bad arguments with the documented status before any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from query_grouped_decode_kv_b300 import build as mqa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mqa.h")
+
+OK, INVALID, UNSUPPORTED, CUDA_ERR, BOUNDS, TIMEOUT = range(6)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = mqa_build.build()
+    L = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    L.mqa_kv_append.restype = i32
+    L.mqa_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    L.mqa_decode_attention.restype = i32
+    L.mqa_decode_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                       ctypes.c_float, vp]
+    L.mqa_status_string.restype = ctypes.c_char_p
+    L.mqa_get_device_status.restype = i32
+    L.mqa_get_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+    L.mqa_debug_override.restype = i32
+    L.mqa_debug_override.argtypes = [i32, i32]
+    L.mqa_kernel_launch_count.restype = ctypes.c_uint64
+    return L
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mqa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mqa_kv_append", "mqa_decode_attention", "mqa_status_string",
+                     "mqa_get_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in mqa.h but not exported"
+
+
+def test_library_exports_nothing_undeclared():
+    # the .so is built with hidden visibility: only the extern "C" ABI is exported
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", mqa_build.build()], check=True,
+                         capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    mqa = {s for s in exported if s.startswith("mqa_")}
+    assert mqa == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.mqa_status_string(code).decode().startswith("MQA_")
+    assert lib.mqa_status_string(42) == b"unknown mqa status"
+
+
+# fake, well-aligned device addresses: these calls must fail in the host checks, before CUDA
+A = 0x7f0000000000
+
+
+def _attn(lib, q=A, k=A + 0x1000, v=A + 0x2000, lens=A + 0x3000, out=A + 0x4000, b=2, h=8, g=2,
+          d_h=128, n_max=100, scale=0.088):
+    return lib.mqa_decode_attention(q, k, v, lens, out, b, h, g, d_h, n_max, scale, None)
+
+
+def _append(lib, kn=A, vn=A + 0x1000, kc=A + 0x2000, vc=A + 0x3000, pos=A + 0x4000, b=2, g=2,
+            d_h=128, n_max=100):
+    return lib.mqa_kv_append(kn, vn, kc, vc, pos, b, g, d_h, n_max, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID), (dict(lens=0), INVALID),
+    (dict(out=0), INVALID),
+    (dict(b=0), INVALID), (dict(h=-1), INVALID), (dict(g=0), INVALID), (dict(n_max=0), INVALID),
+    (dict(h=8, g=3), INVALID),                    # heads must split evenly into groups
+    (dict(scale=math.inf), INVALID), (dict(scale=math.nan), INVALID),
+    (dict(q=A + 8), INVALID), (dict(k=A + 2), INVALID), (dict(out=A + 4), INVALID),
+    (dict(lens=A + 2), INVALID),
+    (dict(d_h=96), UNSUPPORTED), (dict(d_h=256), UNSUPPORTED),
+    (dict(h=128, g=1), UNSUPPORTED),              # h/g above 64
+    (dict(b=8193), UNSUPPORTED),
+])
+def test_attention_host_checks(lib, kw, code):
+    assert _attn(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(kn=0), INVALID), (dict(vn=0), INVALID), (dict(kc=0), INVALID), (dict(vc=0), INVALID),
+    (dict(pos=0), INVALID), (dict(b=0), INVALID), (dict(g=-2), INVALID), (dict(n_max=0), INVALID),
+    (dict(kc=A + 8), INVALID), (dict(pos=A + 1), INVALID),
+    (dict(d_h=80), UNSUPPORTED),
+])
+def test_append_host_checks(lib, kw, code):
+    assert _append(lib, **kw) == code
+
+
+def test_debug_override_validation(lib):
+    assert lib.mqa_debug_override(-1, 0) == INVALID
+    assert lib.mqa_debug_override(0, 3) == INVALID
+    assert lib.mqa_debug_override(0, 0) == OK
+
+
+def test_forced_cuda_core_path_rejects_large_groups(lib):
+    assert lib.mqa_debug_override(0, 1) == OK
+    try:
+        assert _attn(lib, h=8, g=1) == UNSUPPORTED   # G = 8 has no CUDA-core kernel
+    finally:
+        lib.mqa_debug_override(0, 0)
+
+
+def test_device_status_needs_an_output(lib):
+    assert lib.mqa_get_device_status(None, None) == INVALID
