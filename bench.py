@@ -8,9 +8,11 @@ step appends one token's K/V and runs attention in all 80 layers back to back.
                     [--workload NAME]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
-with inputs resident in HBM (lower is better); ``e2e`` is the same step driven from pinned host
-buffers with the host->device copy of the step's inputs (q, k_new, v_new of every layer) and the
-device->host read of its outputs inside the timed region. ``roofline`` reports the attention
+with inputs resident in HBM (lower is better): each timed step is one CUDA-graph replay of the
+whole step (every layer's append and attention). ``e2e`` is the same step driven eagerly through
+the public Python API from pinned host buffers, with the host->device copy of the step's inputs
+(q, k_new, v_new of every layer) and the device->host read of its outputs inside the timed
+region. ``roofline`` reports the attention
 call's HBM throughput on algorithmic bytes (K/V rows read + q read + out written) against the
 measured copy bandwidth. ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the
 same workload. The reference arm (``--impl reference``) times that oracle as the reference.
@@ -269,7 +271,7 @@ def run_ours(args, world, rank, local):
     # small workloads fit in L2: flush it between steps by writing a buffer twice its size
     flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if needs_l2_flush(w)
              else None)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
 
     def step(events=None):
@@ -282,26 +284,43 @@ def run_ours(args, world, rank, local):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(args.warmup):
-        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
     torch.cuda.synchronize()
     assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
 
-    # ---- device-timed region ----
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(w.layers)] for _ in range(args.steps)]
+    # ---- the step as CUDA graphs: one graph per timed step, each with its own timing events
+    # (external event nodes around every attention call), replayed back to back ----
+    graphs, ev = [], []
+    launches_per_step = None
+    for s_i in range(args.steps):
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(w.layers)]
+        g = torch.cuda.CUDAGraph()
+        n0 = mqa.kernel_launch_count()
+        with torch.cuda.graph(g, stream=stream):
+            step(evs)
+        if launches_per_step is None:
+            launches_per_step = mqa.kernel_launch_count() - n0
+        graphs.append(g)
+        ev.append(evs)
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+    torch.cuda.synchronize()
+
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = mqa.kernel_launch_count()
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
-        t_start.record(stream)
-        for s in range(args.steps):
-            step(ev[s])
-        t_end.record(stream)
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for g in graphs:
+                g.replay()
+            t_end.record(stream)
         torch.cuda.synchronize()
         barrier()
-    launches = mqa.kernel_launch_count() - launches0
+    launches = launches_per_step * args.steps
     assert mqa.get_device_status() == 0, "device status latched an error in the timed region"
     ms_total = t_start.elapsed_time(t_end)
     attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
@@ -317,6 +336,7 @@ def run_ours(args, world, rank, local):
     d2h = sum(t.numel() * t.element_size() for t in ho)
 
     def e2e_step():
+        # eager, through the public API: copy in, append + attention per layer, copy out
         for li in range(w.layers):
             xs[li].q.copy_(hq[li], non_blocking=True)
             xs[li].k_new.copy_(hk[li], non_blocking=True)
@@ -325,16 +345,18 @@ def run_ours(args, world, rank, local):
         for li in range(w.layers):
             ho[li].copy_(outs[li], non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1)

@@ -12,6 +12,7 @@ tokens cached before this step's token is appended, so the attended length is ``
 * ``mqa_long``     b=64, h=32, g=1,  d_h=128, context 8192
 * ``mha_ref``      b=8,  h=32, g=32, d_h=128, context 8192
 * ``gqa_70b_80l``  b=8,  h=64, g=8,  d_h=128, context ~ U{1024..32768}, 80 layers, caches ~ N(0, 0.5)
+* ``gqa_70b_1l``   the first layer of ``gqa_70b_80l`` alone (same seeds and lengths)
 
 Every tensor is bfloat16 rounded (nearest-even) from a float32 normal draw. Seeds are fixed per
 (workload, layer, tensor) so any single layer can be regenerated on its own, on any device.
@@ -61,6 +62,9 @@ WORKLOADS = {
         Workload("mha_ref", 4, b=8, h=32, g=32, d_h=128, ctx_lo=8192, ctx_hi=8192),
         Workload("gqa_70b_80l", 5, b=8, h=64, g=8, d_h=128, ctx_lo=1024, ctx_hi=32768,
                  layers=80, kv_std=0.5),
+        # one layer of the 80-layer workload (same kernel configuration; for profiling)
+        Workload("gqa_70b_1l", 5, b=8, h=64, g=8, d_h=128, ctx_lo=1024, ctx_hi=32768,
+                 layers=1, kv_std=0.5),
     )
 }
 
