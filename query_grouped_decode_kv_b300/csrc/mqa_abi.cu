@@ -167,6 +167,118 @@ int ensure_smem(int dev, const void* kernel, size_t bytes) {
 
 int launch_error() { return cudaGetLastError() == cudaSuccess ? MQA_OK : MQA_ERR_CUDA; }
 
+// ------------------------------------------------------------------------------------------------
+// Decode attention: host checks and launch plan, then the launch itself with a given scratch area
+// (the split partial states: part_o [slots][G][d_h] fp32 followed by part_ml [slots][G] float2).
+// ------------------------------------------------------------------------------------------------
+struct DecodePlan {
+  const mqa_bf16 *q, *k_cache, *v_cache;
+  const int32_t* seq_lens;
+  mqa_bf16* out;
+  int b, h, g, d_h, n_max, G;
+  float scale;
+  bool tensor_cores;
+  cudaStream_t stream;
+  int dev;
+  long long bg, ctas;
+  size_t part_o_bytes, scratch_bytes;  // scratch_bytes = 0 when one CTA does all the work
+};
+
+int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
+                const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h, int n_max,
+                float scale, void* stream, DecodePlan* plan) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
+  if (h % g != 0) return MQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const int G = h / g;
+  if (G > mqa::kMaxGroup || b > mqa::kMaxBatch) return MQA_ERR_UNSUPPORTED;
+  const long long bg = static_cast<long long>(b) * g;
+  const long long tiles_per_seg =
+      (static_cast<long long>(n_max) + mqa::kTileKeys - 1) / mqa::kTileKeys;
+  if (bg > (1ll << 24) || static_cast<long long>(b) * tiles_per_seg >= (1ll << 31) ||
+      static_cast<double>(bg) * n_max * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+  const int force_path = g_force_path.load();
+  const bool tensor_cores = force_path == 0 ? (G >= 8) : (force_path == 2);
+  if (!tensor_cores && G > 7) return MQA_ERR_UNSUPPORTED;
+
+  // ---- device facts ----
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MQA_ERR_CUDA;
+  DeviceInfo info;
+  if (int st = device_info(dev, &info)) return st;
+
+  // CTAs: one per SM, but no more than a quarter of the (upper bound on the) tile count, so that
+  // tiny problems are not scattered into many partial states.
+  const long long w_max = bg * tiles_per_seg;
+  long long ctas = (w_max + 3) / 4;
+  if (ctas > info.sms) ctas = info.sms;
+  if (ctas < 1) ctas = 1;
+  if (const int f = g_force_ctas.load()) ctas = f;
+
+  const long long slots = ctas + bg;
+  DecodePlan& p = *plan;
+  p.q = q; p.k_cache = k_cache; p.v_cache = v_cache; p.seq_lens = seq_lens; p.out = out;
+  p.b = b; p.h = h; p.g = g; p.d_h = d_h; p.n_max = n_max; p.G = G;
+  p.scale = scale;
+  p.tensor_cores = tensor_cores;
+  p.stream = static_cast<cudaStream_t>(stream);
+  p.dev = dev;
+  p.bg = bg;
+  p.ctas = ctas;
+  p.part_o_bytes = static_cast<size_t>(slots) * G * d_h * sizeof(float);
+  p.scratch_bytes =
+      ctas > 1 ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
+  return MQA_OK;
+}
+
+int launch_decode(const DecodePlan& p, void* scratch) {
+  CUtensorMap tmk, tmv;
+  if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h) ||
+      !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h))
+    return MQA_ERR_CUDA;
+
+  DecodeParams P;
+  P.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  P.seq_lens = p.seq_lens;
+  P.out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  P.part_o = static_cast<float*>(scratch);
+  P.part_ml = scratch ? reinterpret_cast<float2*>(static_cast<char*>(scratch) + p.part_o_bytes)
+                      : nullptr;
+  P.b = p.b;
+  P.h = p.h;
+  P.g = p.g;
+  P.G = p.G;
+  P.n_max = p.n_max;
+  P.num_ctas = static_cast<int>(p.ctas);
+  P.scale_log2 = p.scale * 1.4426950408889634f;
+  P.timeout_ns = kWaitLimitNs;
+
+  AttnKernel kern = p.d_h == 128 ? pick_kernel<128>(p.tensor_cores, p.G)
+                                 : pick_kernel<64>(p.tensor_cores, p.G);
+  if (!kern) return MQA_ERR_UNSUPPORTED;
+  const size_t smem = mqa::smem_bytes(p.d_h, p.b);
+  if (int st = ensure_smem(p.dev, reinterpret_cast<const void*>(kern), smem)) return st;
+  kern<<<static_cast<unsigned>(p.ctas), mqa::kThreads, smem, p.stream>>>(tmk, tmv, P);
+  g_launches.fetch_add(1);
+  if (int st = launch_error()) return st;
+  if (p.ctas > 1) {
+    if (p.d_h == 128)
+      mqa::merge_partials_kernel<128><<<static_cast<unsigned>(p.bg), 128, 0, p.stream>>>(P);
+    else
+      mqa::merge_partials_kernel<64><<<static_cast<unsigned>(p.bg), 128, 0, p.stream>>>(P);
+    g_launches.fetch_add(1);
+    if (int st = launch_error()) return st;
+  }
+  return MQA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,85 +351,15 @@ int mqa_kv_append(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cach
 int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
                          const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
                          int n_max, float scale, void* stream) {
-  // ---- host checks (no CUDA call before this block is done) ----
-  if (!q || !k_cache || !v_cache || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
-  if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
-  if (h % g != 0) return MQA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-    return MQA_ERR_INVALID_ARG;
-  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
-  const int G = h / g;
-  if (G > mqa::kMaxGroup || b > mqa::kMaxBatch) return MQA_ERR_UNSUPPORTED;
-  const long long bg = static_cast<long long>(b) * g;
-  const long long tiles_per_seg = (static_cast<long long>(n_max) + mqa::kTileKeys - 1) / mqa::kTileKeys;
-  if (bg > (1ll << 24) || static_cast<long long>(b) * tiles_per_seg >= (1ll << 31) ||
-      static_cast<double>(bg) * n_max * d_h > 9.0e18)
-    return MQA_ERR_UNSUPPORTED;
-  const int force_path = g_force_path.load();
-  const bool tensor_cores = force_path == 0 ? (G >= 8) : (force_path == 2);
-  if (!tensor_cores && G > 7) return MQA_ERR_UNSUPPORTED;
-
-  // ---- device side ----
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MQA_ERR_CUDA;
-  DeviceInfo info;
-  if (int st = device_info(dev, &info)) return st;
-
-  // CTAs: one per SM, but no more than a quarter of the (upper bound on the) tile count, so that
-  // tiny problems are not scattered into many partial states.
-  const long long w_max = bg * tiles_per_seg;
-  long long ctas = (w_max + 3) / 4;
-  if (ctas > info.sms) ctas = info.sms;
-  if (ctas < 1) ctas = 1;
-  if (const int f = g_force_ctas.load()) ctas = f;
-
-  const long long slots = ctas + bg;
-  const size_t part_o_bytes = static_cast<size_t>(slots) * G * d_h * sizeof(float);
-  const size_t part_ml_bytes = static_cast<size_t>(slots) * G * sizeof(float2);
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan))
+    return st;
   void* ws = nullptr;
-  if (ctas > 1) {
-    if (int st = get_workspace(dev, s, part_o_bytes + part_ml_bytes, &ws)) return st;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.scratch_bytes, &ws)) return st;
   }
-
-  CUtensorMap tmk, tmv;
-  if (!make_cache_map(&tmk, k_cache, static_cast<int>(bg), n_max, d_h) ||
-      !make_cache_map(&tmv, v_cache, static_cast<int>(bg), n_max, d_h))
-    return MQA_ERR_CUDA;
-
-  DecodeParams P;
-  P.q = reinterpret_cast<const __nv_bfloat16*>(q);
-  P.seq_lens = seq_lens;
-  P.out = reinterpret_cast<__nv_bfloat16*>(out);
-  P.part_o = static_cast<float*>(ws);
-  P.part_ml = ws ? reinterpret_cast<float2*>(static_cast<char*>(ws) + part_o_bytes) : nullptr;
-  P.b = b;
-  P.h = h;
-  P.g = g;
-  P.G = G;
-  P.n_max = n_max;
-  P.num_ctas = static_cast<int>(ctas);
-  P.scale_log2 = scale * 1.4426950408889634f;
-  P.timeout_ns = kWaitLimitNs;
-
-  AttnKernel kern = d_h == 128 ? pick_kernel<128>(tensor_cores, G) : pick_kernel<64>(tensor_cores, G);
-  if (!kern) return MQA_ERR_UNSUPPORTED;
-  const size_t smem = mqa::smem_bytes(d_h, b);
-  if (int st = ensure_smem(dev, reinterpret_cast<const void*>(kern), smem)) return st;
-  kern<<<static_cast<unsigned>(ctas), mqa::kThreads, smem, s>>>(tmk, tmv, P);
-  g_launches.fetch_add(1);
-  if (int st = launch_error()) return st;
-  if (ctas > 1) {
-    if (d_h == 128)
-      mqa::merge_partials_kernel<128><<<static_cast<unsigned>(bg), 128, 0, s>>>(P);
-    else
-      mqa::merge_partials_kernel<64><<<static_cast<unsigned>(bg), 128, 0, s>>>(P);
-    g_launches.fetch_add(1);
-    if (int st = launch_error()) return st;
-  }
-  return MQA_OK;
+  return launch_decode(plan, ws);
 }
 
 }  // extern "C"
