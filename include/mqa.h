@@ -117,6 +117,36 @@ MQA_API int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, con
                          const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
                          int n_max, float scale, void* stream);
 
+/*
+ * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
+ * memory. The source pages have no counterpart to this call; it exists for users of the library.
+ *
+ * mqa_decode_attention may call cudaMalloc the first time a stream needs a larger workspace. Some
+ * callers cannot allow that. One example is a host framework that has already reserved the
+ * device's memory for its own pool, where cudaMalloc fails or fragments that pool. Another is a
+ * latency-critical loop that cannot take cudaMalloc's implicit device synchronisation. This
+ * variant runs the same kernels and computes the same result. It keeps its scratch (the split
+ * partial states) in a fixed array of MQA_NOALLOC_SCRATCH_BYTES inside the library's device
+ * memory, which every GPU that loads the library holds until the process exits. The call itself
+ * allocates nothing: it calls no cudaMalloc, no cudaFree and no allocating library routine.
+ *
+ * Arguments, layout, ownership, ordering and errors are those of mqa_decode_attention, plus:
+ *   - a problem whose scratch does not fit returns MQA_ERR_UNSUPPORTED and enqueues nothing. The
+ *     scratch needed is (P + b*g) * (h/g) * (d_h + 2) * 4 bytes, where
+ *     P = min(number of SMs, ceil(b*g*ceil(n_max/64) / 4)); it is 0 when P is 1;
+ *   - the first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current, so make that first call before any stream capture;
+ *   - all calls share the one array, which keeps the last call's contents. Each call writes every
+ *     scratch word before it reads it, so nothing needs clearing between calls. Calls that overlap
+ *     on the GPU (for instance on two streams at once) race on the array; the caller must order
+ *     them.
+ */
+#define MQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+MQA_API int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
+                                         const mqa_bf16* v_cache, const int32_t* seq_lens,
+                                         mqa_bf16* out, int b, int h, int g, int d_h, int n_max,
+                                         float scale, void* stream);
+
 /* A static, human-readable name for a status code. Never returns NULL. */
 MQA_API const char* mqa_status_string(int status);
 

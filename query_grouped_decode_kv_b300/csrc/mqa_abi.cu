@@ -279,6 +279,29 @@ int launch_decode(const DecodePlan& p, void* scratch) {
   return MQA_OK;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Scratch for mqa_decode_attention_noalloc: a fixed array in this module's device memory, so the
+// call itself allocates nothing. In host code the array's name is only a host-side stand-in, so
+// its device address is looked up once per device (with that device current) and cached.
+// ------------------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MQA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+std::map<int, void*> g_noalloc_addr;  // device ordinal -> device address of g_noalloc_scratch
+
+int noalloc_scratch_address(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  auto it = g_noalloc_addr.find(dev);
+  if (it == g_noalloc_addr.end()) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return MQA_ERR_CUDA;
+    it = g_noalloc_addr.emplace(dev, ptr).first;
+  }
+  *out = it->second;
+  return MQA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -360,6 +383,22 @@ int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_b
     if (int st = get_workspace(plan.dev, plan.stream, plan.scratch_bytes, &ws)) return st;
   }
   return launch_decode(plan, ws);
+}
+
+int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
+                                 const mqa_bf16* v_cache, const int32_t* seq_lens, mqa_bf16* out,
+                                 int b, int h, int g, int d_h, int n_max, float scale,
+                                 void* stream) {
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan))
+    return st;
+  if (plan.scratch_bytes > MQA_NOALLOC_SCRATCH_BYTES) return MQA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (plan.scratch_bytes > 0) {
+    if (int st = noalloc_scratch_address(plan.dev, &scratch)) return st;
+  }
+  return launch_decode(plan, scratch);
 }
 
 }  // extern "C"
