@@ -131,17 +131,23 @@ MQA_API int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, con
  * allocates nothing: it calls no cudaMalloc, no cudaFree and no allocating library routine.
  *
  * Arguments, layout, ownership, ordering and errors are those of mqa_decode_attention, plus:
- *   - a problem whose scratch does not fit returns MQA_ERR_UNSUPPORTED and enqueues nothing. The
- *     scratch needed is (P + b*g) * (h/g) * (d_h + 2) * 4 bytes, where
- *     P = min(number of SMs, ceil(b*g*ceil(n_max/64) / 4)); it is 0 when P is 1;
+ *   - the array holds MQA_NOALLOC_MAX_SEGMENTS arrival counters (one per sequence and KV head)
+ *     followed by the split partial states. A problem with more than MQA_NOALLOC_MAX_SEGMENTS
+ *     values of b*g, or whose partial states need more than the rest of the array, returns
+ *     MQA_ERR_UNSUPPORTED and enqueues nothing. The partial states need
+ *     (P + b*g) * (h/g) * (d_h + 2) * 4 bytes, where
+ *     P = min(number of SMs, ceil(b*g*ceil(n_max/64) / 4)); nothing is needed when P is 1;
  *   - the first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *     with that device current, so make that first call before any stream capture;
- *   - all calls share the one array, which keeps the last call's contents. Each call writes every
- *     scratch word before it reads it, so nothing needs clearing between calls. Calls that overlap
- *     on the GPU (for instance on two streams at once) race on the array; the caller must order
- *     them.
+ *   - all calls share the one array, which keeps the last call's contents. The only words that
+ *     must start at zero are the per-segment arrival counters: the array is zero when the library
+ *     loads, every call that finishes leaves them at zero, and after mqa_get_device_status has
+ *     reported MQA_ERR_TIMEOUT the next call clears them first (cudaMemsetAsync, which allocates
+ *     nothing). Everything else is written before it is read. Calls that overlap on the GPU (for
+ *     instance on two streams at once) race on the array; the caller must order them.
  */
 #define MQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+#define MQA_NOALLOC_MAX_SEGMENTS 16384u
 MQA_API int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
                                          const mqa_bf16* v_cache, const int32_t* seq_lens,
                                          mqa_bf16* out, int b, int h, int g, int d_h, int n_max,

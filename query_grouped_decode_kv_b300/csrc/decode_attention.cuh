@@ -11,7 +11,8 @@
 // seq_lens itself: the split is balanced to within one tile whatever the length mix, and the host
 // never synchronises to read lengths. A segment that lies entirely inside one CTA's range is
 // finished by that CTA; otherwise each CTA writes a partial softmax state (m, l, o) into slot
-// c + segment, and a second kernel merges the slots with the log-sum-exp identity.
+// c + segment and counts its arrival on the segment's counter, and the last CTA to arrive merges
+// the slots with the log-sum-exp identity (then resets the counter to zero for the next call).
 //
 // Inside a CTA: one producer warp streams each tile's K and V rows from HBM into a ring of
 // shared-memory stages with bulk tensor copies (TMA, 128-byte swizzle); four consumer warps read
@@ -51,6 +52,7 @@ struct DecodeParams {
   __nv_bfloat16* out;         // [b][h][D]
   float* part_o;              // [slots][G][D]   un-normalised partial outputs
   float2* part_ml;            // [slots][G]      (running max in log2 units, running sum)
+  unsigned int* seg_arrivals; // [b*g] CTAs that have stored a partial; zero between calls
   int b, h, g, G, n_max;
   int num_ctas;               // P
   float scale_log2;           // scale * log2(e)
@@ -63,7 +65,7 @@ __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 // Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort][prefix(b+1)]
 __host__ __device__ constexpr int smem_fixed_bytes(int D) {
   return kStages * stage_bytes(D) + kConsumerWarps * kCombRows * comb_row_floats(D) * 4 +
-         kConsumerWarps * kCombRows * 8 + (2 * kStages + 1) * 8 + 16;
+         kConsumerWarps * kCombRows * 8 + (2 * kStages + 1) * 8 + 16;  // + abort, merge flag
 }
 __host__ __device__ constexpr size_t smem_bytes(int D, int b) {
   return 1024 + static_cast<size_t>(smem_fixed_bytes(D)) + static_cast<size_t>(b + 1) * 4;
@@ -117,6 +119,7 @@ struct SharedLayout {
   uint64_t* empty;      // [kStages]
   uint64_t* cbar;       // consumer-wide barrier
   volatile int* abort;  // set when any warp gives up
+  volatile int* merge;  // this CTA is the last to arrive at the segment being finished
   uint32_t* pre;        // [b + 1] tiles before each sequence
 };
 
@@ -136,6 +139,7 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.cbar = s.empty + kStages;
   p += (2 * kStages + 1) * 8;
   s.abort = reinterpret_cast<volatile int*>(p);
+  s.merge = s.abort + 1;
   p += 16;
   s.pre = reinterpret_cast<uint32_t*>(p);
   return s;
@@ -189,6 +193,106 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& P, const S
       if (d == 0) P.part_ml[r] = make_float2(M, den);
     }
   }
+}
+
+// ---------------------------------------------------------------------------------------------
+// The CTAs whose tile ranges cover a segment's tiles [s0, s1]: c_first .. c_last, skipping CTAs
+// whose range is empty (only possible when W < P). CTA owning tile x: the largest c with
+// c*W/P <= x, i.e. ((x+1)*P - 1) / W.
+// ---------------------------------------------------------------------------------------------
+struct SegmentPieces {
+  int c_first, c_last;
+  bool all_own;            // W >= P: every CTA owns at least one tile
+  unsigned long long W, Pn;
+  __device__ __forceinline__ SegmentPieces(unsigned long long s0, unsigned long long s1,
+                                           unsigned long long W_, int P_)
+      : W(W_), Pn(static_cast<unsigned long long>(P_)) {
+    c_first = static_cast<int>(((s0 + 1) * Pn - 1) / W);
+    c_last = static_cast<int>(((s1 + 1) * Pn - 1) / W);
+    all_own = W >= Pn;
+  }
+  __device__ __forceinline__ bool owns(int c) const {
+    return all_own || (W * static_cast<unsigned long long>(c) / Pn <
+                       W * static_cast<unsigned long long>(c + 1) / Pn);
+  }
+  __device__ __forceinline__ unsigned int count() const {
+    if (all_own) return static_cast<unsigned int>(c_last - c_first + 1);
+    unsigned int n = 0;
+    for (int c = c_first; c <= c_last; ++c) n += owns(c) ? 1u : 0u;
+    return n;
+  }
+};
+
+// Merge the partial states of a segment split across CTAs (run by the 128 consumer threads of
+// the last CTA to arrive):  M = max_c m_c,  o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c.
+// Partials written by other SMs are read from L2 (ld.global.cg), never from a stale L1 line.
+//
+// This usually runs at the very end of the kernel (the CTA whose range ends inside a long segment
+// arrives last), so it is written for latency: the pieces' (m, l) are staged in shared memory with
+// independent loads, the per-head weights 2^(m_c - M) / l are computed once, and each output
+// element then issues the loads of all pieces at once. Returns false if a barrier timed out.
+template <int D>
+__device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const SharedLayout& sh,
+                                                    uint32_t& cphase, int bi, int j, int seg,
+                                                    const SegmentPieces& pc) {
+  const int G = P.G;
+  const int tid = threadIdx.x;
+  const size_t out0 = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G) * D;
+  const int np = pc.c_last - pc.c_first + 1;
+  constexpr int kScratchFloats = kConsumerWarps * kCombRows * comb_row_floats(D);
+  if (!pc.all_own || 3 * np * G > kScratchFloats) {
+    // general case (some CTAs own no tiles, or too many pieces to stage): plain loops
+    for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+      const int hr = idx / D;
+      const int d = idx - hr * D;
+      float M = -INFINITY;
+      for (int c = pc.c_first; c <= pc.c_last; ++c)
+        if (pc.owns(c)) M = fmaxf(M, __ldcg(P.part_ml + static_cast<size_t>(c + seg) * G + hr).x);
+      float acc = 0.f, den = 0.f;
+      for (int c = pc.c_first; c <= pc.c_last; ++c) {
+        if (!pc.owns(c)) continue;
+        const size_t r = static_cast<size_t>(c + seg) * G + hr;
+        const float2 ml = __ldcg(P.part_ml + r);
+        const float w = fast_exp2(ml.x - M);
+        den += w * ml.y;
+        acc += w * __ldcg(P.part_o + r * D + d);
+      }
+      P.out[out0 + idx] = __float2bfloat16_rn(acc / den);
+    }
+    return true;
+  }
+  // the combine scratch is free here: stage (m, l) of every piece, then the weights
+  float2* ml = reinterpret_cast<float2*>(sh.comb_o);  // [np][G]
+  float* wgt = sh.comb_o + 2 * np * G;                  // [np][G]
+  const size_t slot0 = static_cast<size_t>(pc.c_first + seg);
+  for (int e = tid; e < np * G; e += kConsumerWarps * 32) ml[e] = __ldcg(P.part_ml + slot0 * G + e);
+  if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
+  for (int hr = tid; hr < G; hr += kConsumerWarps * 32) {
+    float M = -INFINITY;
+    for (int pi = 0; pi < np; ++pi) M = fmaxf(M, ml[pi * G + hr].x);
+    float den = 0.f;
+    for (int pi = 0; pi < np; ++pi) den += fast_exp2(ml[pi * G + hr].x - M) * ml[pi * G + hr].y;
+    const float inv = 1.f / den;
+    for (int pi = 0; pi < np; ++pi) wgt[pi * G + hr] = fast_exp2(ml[pi * G + hr].x - M) * inv;
+  }
+  if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
+  // outputs, four consecutive columns per thread
+  const float4* po = reinterpret_cast<const float4*>(P.part_o);
+  for (int idx = tid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+    const int hr = idx / (D / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int pi = 0; pi < np; ++pi) {
+      const float w = wgt[pi * G + hr];
+      const float4 o = __ldcg(po + (slot0 + pi) * G * (D / 4) + idx);
+      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    }
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(P.out + out0) + 2 * idx;
+    dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  // the scratch is written again by the next segment's combine
+  return consumer_sync(sh, cphase, P.timeout_ns);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -530,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     part_sums[tid] = s;
     if (tid == 0) {
       *sh.abort = 0;
+      *sh.merge = 0;
       for (int st = 0; st < kStages; ++st) {
         mbar_init(&sh.full[st], 1);
         mbar_init(&sh.empty[st], kConsumerWarps);
@@ -669,73 +774,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
       combine_and_store<D>(P, sh, cur.bi, cur.j, complete, static_cast<int>(blockIdx.x) + seg,
                            typename Consumer::Rows{});
+      if (!complete) __threadfence();  // this CTA's partial is visible before it is counted
       if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
+      if (!complete) {
+        const unsigned long long s0 = static_cast<unsigned long long>(P.g) * sh.pre[cur.bi] +
+                                      static_cast<unsigned long long>(cur.j) * cur.nt;
+        const SegmentPieces pc(s0, s0 + cur.nt - 1, W, P.num_ctas);
+        if (tid == 0) {
+          const unsigned int before = atomicAdd(P.seg_arrivals + seg, 1u);
+          *sh.merge = (before + 1u == pc.count()) ? 1 : 0;
+        }
+        if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
+        if (*sh.merge) {
+          __threadfence();
+          if (!merge_split_segment<D>(P, sh, cphase, cur.bi, cur.j, seg, pc)) {
+            if (!*sh.abort) give_up(sh);
+            return;
+          }
+          if (tid == 0) P.seg_arrivals[seg] = 0u;  // ready for the next call
+        }
+      }
     }
     cur.advance(sh.pre, B, P.g);
-  }
-}
-
-// ---------------------------------------------------------------------------------------------
-// Merge the partial states of segments that were split across CTAs:
-//   M = max_c m_c,  o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c.
-// One block per segment (bi, j); a segment finished by one CTA is skipped.
-// ---------------------------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(128) merge_partials_kernel(const DecodeParams P) {
-  const int seg = blockIdx.x;
-  const int bi = seg / P.g, j = seg - (seg / P.g) * P.g;
-  const int L = __ldg(P.seq_lens + bi);
-  const int nt = tiles_of_length(L, P.n_max);
-  if (nt == 0) return;
-  // tiles before sequence bi, and all tiles
-  __shared__ unsigned long long red[2][128];
-  unsigned long long before = 0, total = 0;
-  for (int i = threadIdx.x; i < P.b; i += blockDim.x) {
-    const unsigned long long t = tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
-    total += t;
-    if (i < bi) before += t;
-  }
-  red[0][threadIdx.x] = before;
-  red[1][threadIdx.x] = total;
-  __syncthreads();
-  for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) {
-      red[0][threadIdx.x] += red[0][threadIdx.x + s];
-      red[1][threadIdx.x] += red[1][threadIdx.x + s];
-    }
-    __syncthreads();
-  }
-  const unsigned long long Pn = static_cast<unsigned long long>(P.num_ctas);
-  const unsigned long long W = static_cast<unsigned long long>(P.g) * red[1][0];
-  const unsigned long long s0 = static_cast<unsigned long long>(P.g) * red[0][0] +
-                                static_cast<unsigned long long>(j) * nt;
-  const unsigned long long s1 = s0 + nt - 1;
-  // CTA owning tile x: the largest c with c*W/P <= x
-  const int c_first = static_cast<int>(((s0 + 1) * Pn - 1) / W);
-  const int c_last = static_cast<int>(((s1 + 1) * Pn - 1) / W);
-  if (c_first == c_last) return;
-  // CTAs with an empty range (possible when P > W) wrote nothing: skip them
-  auto owns_tiles = [&](int c) {
-    return W * static_cast<unsigned long long>(c) / Pn <
-           W * static_cast<unsigned long long>(c + 1) / Pn;
-  };
-  const int G = P.G;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int hr = idx / D, d = idx - (idx / D) * D;
-    float M = -INFINITY;
-    for (int c = c_first; c <= c_last; ++c)
-      if (owns_tiles(c)) M = fmaxf(M, P.part_ml[static_cast<size_t>(c + seg) * G + hr].x);
-    float acc = 0.f, den = 0.f;
-    for (int c = c_first; c <= c_last; ++c) {
-      if (!owns_tiles(c)) continue;
-      const size_t r = static_cast<size_t>(c + seg) * G + hr;
-      const float2 ml = P.part_ml[r];
-      const float w = fast_exp2(ml.x - M);
-      den += w * ml.y;
-      acc += w * P.part_o[r * D + d];
-    }
-    P.out[(static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d] =
-        __float2bfloat16_rn(acc / den);
   }
 }
 

@@ -20,6 +20,9 @@ namespace {
 using mqa::DecodeParams;
 
 std::atomic<uint64_t> g_launches{0};
+// Bumped each time mqa_get_device_status reports MQA_ERR_TIMEOUT: a kernel that gave up may have
+// left arrival counters non-zero, so every scratch area clears them once more before its next use.
+std::atomic<uint64_t> g_timeout_epoch{0};
 std::atomic<int> g_force_ctas{0};
 std::atomic<int> g_force_path{0};
 
@@ -65,37 +68,59 @@ bool make_cache_map(CUtensorMap* map, const void* base, int bg, int n_max, int d
 }
 
 // ------------------------------------------------------------------------------------------------
-// Workspace for split-sequence partial states, one per (device, stream); grows on demand.
+// Workspace, one per (device, stream), growing on demand. Two separate buffers: the split partial
+// states (written before they are read in every call), and one arrival counter per segment. The
+// counters must read zero when a call starts: a new counter buffer is zeroed, every call that
+// finishes leaves its counters at zero, and nothing else ever writes there.
 // ------------------------------------------------------------------------------------------------
-struct Workspace {
+struct DeviceBuffer {
   void* ptr = nullptr;
   size_t bytes = 0;
+};
+struct Workspace {
+  DeviceBuffer partials, counters;
+  uint64_t clean_epoch = 0;  // g_timeout_epoch when its counters were last known to be zero
 };
 std::mutex g_ws_mutex;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 
-int get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+// Grow `buf` to at least `bytes` (with 25% headroom); zero the new buffer when `zero`.
+int grow_buffer(DeviceBuffer& buf, size_t bytes, cudaStream_t stream, bool zero) {
+  if (buf.bytes >= bytes) return MQA_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MQA_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return MQA_ERR_UNSUPPORTED;  // cannot grow in capture
+  if (buf.ptr) {
+    // the old buffer may still be used by earlier work on this stream
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MQA_ERR_CUDA;
+    cudaFree(buf.ptr);
+    buf.ptr = nullptr;
+    buf.bytes = 0;
+  }
+  const size_t grow = bytes + bytes / 4;
+  if (cudaMalloc(&buf.ptr, grow) != cudaSuccess) {
+    buf.ptr = nullptr;
+    return MQA_ERR_CUDA;
+  }
+  if (zero && cudaMemsetAsync(buf.ptr, 0, grow, stream) != cudaSuccess) return MQA_ERR_CUDA;
+  buf.bytes = grow;
+  return MQA_OK;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t counter_bytes,
+                  void** partials, unsigned int** counters, bool* clear) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   Workspace& ws = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
-  if (ws.bytes < bytes) {
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MQA_ERR_CUDA;
-    if (cap != cudaStreamCaptureStatusNone) return MQA_ERR_UNSUPPORTED;  // cannot grow in capture
-    if (ws.ptr) {
-      // the old buffer may still be read by earlier work on this stream
-      if (cudaStreamSynchronize(stream) != cudaSuccess) return MQA_ERR_CUDA;
-      cudaFree(ws.ptr);
-      ws.ptr = nullptr;
-      ws.bytes = 0;
-    }
-    const size_t grow = bytes + bytes / 4;
-    if (cudaMalloc(&ws.ptr, grow) != cudaSuccess) {
-      ws.ptr = nullptr;
-      return MQA_ERR_CUDA;
-    }
-    ws.bytes = grow;
+  if (int st = grow_buffer(ws.partials, partial_bytes, stream, false)) return st;
+  const uint64_t epoch = g_timeout_epoch.load();
+  if (ws.counters.bytes < counter_bytes) {
+    if (int st = grow_buffer(ws.counters, counter_bytes, stream, true)) return st;
+    ws.clean_epoch = epoch;
   }
-  *out = ws.ptr;
+  *clear = ws.clean_epoch != epoch;
+  ws.clean_epoch = epoch;
+  *partials = ws.partials.ptr;
+  *counters = static_cast<unsigned int*>(ws.counters.ptr);
   return MQA_OK;
 }
 
@@ -181,7 +206,9 @@ struct DecodePlan {
   cudaStream_t stream;
   int dev;
   long long bg, ctas;
-  size_t part_o_bytes, scratch_bytes;  // scratch_bytes = 0 when one CTA does all the work
+  // scratch, needed only with more than one CTA: partial states (part_o then part_ml) and one
+  // arrival counter per segment, kept in a region of its own
+  size_t part_o_bytes, partial_bytes, counter_bytes;
 };
 
 int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
@@ -233,12 +260,16 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   p.bg = bg;
   p.ctas = ctas;
   p.part_o_bytes = static_cast<size_t>(slots) * G * d_h * sizeof(float);
-  p.scratch_bytes =
-      ctas > 1 ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
+  p.partial_bytes = ctas > 1 ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
+  p.counter_bytes = ctas > 1 ? static_cast<size_t>(bg) * sizeof(unsigned int) : 0;
   return MQA_OK;
 }
 
-int launch_decode(const DecodePlan& p, void* scratch) {
+// `clear_counters`: zero the per-segment arrival counters first. They are zero whenever the
+// scratch is fresh and every finished call leaves them at zero; only a call that gave up
+// (MQA_ERR_TIMEOUT) can leave them dirty.
+int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
+                  bool clear_counters) {
   CUtensorMap tmk, tmv;
   if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h) ||
       !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h))
@@ -248,9 +279,13 @@ int launch_decode(const DecodePlan& p, void* scratch) {
   P.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
   P.seq_lens = p.seq_lens;
   P.out = reinterpret_cast<__nv_bfloat16*>(p.out);
-  P.part_o = static_cast<float*>(scratch);
-  P.part_ml = scratch ? reinterpret_cast<float2*>(static_cast<char*>(scratch) + p.part_o_bytes)
-                      : nullptr;
+  P.part_o = static_cast<float*>(partials);
+  P.part_ml = partials ? reinterpret_cast<float2*>(static_cast<char*>(partials) + p.part_o_bytes)
+                       : nullptr;
+  P.seg_arrivals = counters;
+  if (counters && clear_counters &&
+      cudaMemsetAsync(counters, 0, p.counter_bytes, p.stream) != cudaSuccess)
+    return MQA_ERR_CUDA;
   P.b = p.b;
   P.h = p.h;
   P.g = p.g;
@@ -267,16 +302,7 @@ int launch_decode(const DecodePlan& p, void* scratch) {
   if (int st = ensure_smem(p.dev, reinterpret_cast<const void*>(kern), smem)) return st;
   kern<<<static_cast<unsigned>(p.ctas), mqa::kThreads, smem, p.stream>>>(tmk, tmv, P);
   g_launches.fetch_add(1);
-  if (int st = launch_error()) return st;
-  if (p.ctas > 1) {
-    if (p.d_h == 128)
-      mqa::merge_partials_kernel<128><<<static_cast<unsigned>(p.bg), 128, 0, p.stream>>>(P);
-    else
-      mqa::merge_partials_kernel<64><<<static_cast<unsigned>(p.bg), 128, 0, p.stream>>>(P);
-    g_launches.fetch_add(1);
-    if (int st = launch_error()) return st;
-  }
-  return MQA_OK;
+  return launch_error();
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -285,20 +311,31 @@ int launch_decode(const DecodePlan& p, void* scratch) {
 // its device address is looked up once per device (with that device current) and cached.
 // ------------------------------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MQA_NOALLOC_SCRATCH_BYTES];
+// Its first kNoallocCounterBytes hold the per-segment arrival counters (MQA_NOALLOC_MAX_SEGMENTS
+// of them); the split partial states follow.
+constexpr size_t kNoallocCounterBytes = MQA_NOALLOC_MAX_SEGMENTS * sizeof(unsigned int);
 
+struct NoallocScratch {
+  void* ptr = nullptr;       // device address of g_noalloc_scratch on this device
+  uint64_t clean_epoch = 0;  // the array starts zeroed, so its counters start clean
+};
 std::mutex g_noalloc_mutex;
-std::map<int, void*> g_noalloc_addr;  // device ordinal -> device address of g_noalloc_scratch
+std::map<int, NoallocScratch> g_noalloc_addr;  // device ordinal -> its copy of the array
 
-int noalloc_scratch_address(int dev, void** out) {
+int noalloc_scratch_address(int dev, void** out, bool* clear) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   auto it = g_noalloc_addr.find(dev);
   if (it == g_noalloc_addr.end()) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+    NoallocScratch sc;
+    if (cudaGetSymbolAddress(&sc.ptr, g_noalloc_scratch) != cudaSuccess || sc.ptr == nullptr)
       return MQA_ERR_CUDA;
-    it = g_noalloc_addr.emplace(dev, ptr).first;
+    sc.clean_epoch = g_timeout_epoch.load();
+    it = g_noalloc_addr.emplace(dev, sc).first;
   }
-  *out = it->second;
+  const uint64_t epoch = g_timeout_epoch.load();
+  *clear = it->second.clean_epoch != epoch;
+  it->second.clean_epoch = epoch;
+  *out = it->second.ptr;
   return MQA_OK;
 }
 
@@ -340,6 +377,7 @@ int mqa_get_device_status(void* stream, int* status_out) {
                               cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MQA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MQA_ERR_CUDA;
+  if (v == MQA_ERR_TIMEOUT) g_timeout_epoch.fetch_add(1);
   *status_out = v;
   return MQA_OK;
 }
@@ -378,11 +416,15 @@ int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_b
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan))
     return st;
-  void* ws = nullptr;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.scratch_bytes, &ws)) return st;
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
   }
-  return launch_decode(plan, ws);
+  return launch_decode(plan, partials, counters, clear);
 }
 
 int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
@@ -393,12 +435,19 @@ int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan))
     return st;
-  if (plan.scratch_bytes > MQA_NOALLOC_SCRATCH_BYTES) return MQA_ERR_UNSUPPORTED;
+  if (plan.counter_bytes > kNoallocCounterBytes ||
+      plan.partial_bytes > MQA_NOALLOC_SCRATCH_BYTES - kNoallocCounterBytes)
+    return MQA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  if (plan.scratch_bytes > 0) {
-    if (int st = noalloc_scratch_address(plan.dev, &scratch)) return st;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = noalloc_scratch_address(plan.dev, &scratch, &clear)) return st;
   }
-  return launch_decode(plan, scratch);
+  // the counters keep a fixed leading region of the array, so no other call's partial states
+  // ever land on them
+  unsigned int* counters = static_cast<unsigned int*>(scratch);
+  void* partials = scratch ? static_cast<char*>(scratch) + kNoallocCounterBytes : nullptr;
+  return launch_decode(plan, partials, counters, clear);
 }
 
 }  // extern "C"
