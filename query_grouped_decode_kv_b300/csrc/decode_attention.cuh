@@ -39,11 +39,22 @@ namespace mqa {
 
 constexpr int kTileKeys = 64;       // cache rows per pipeline stage
 constexpr int kStages = 4;          // stages in the shared-memory ring
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
+// NW (a template parameter below) is the number of consumer warps: 4 or 8.
+//  - NW = 4: one producer warp comes on top (160 threads, one warp per SM sub-partition each).
+//  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
+//    every thread kLaunchRegsWide registers (the most 384 threads can have on one SM); the
+//    producer warpgroup then hands registers back (setmaxnreg.dec to kProducerRegs) and the
+//    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Only one producer lane works.
+__host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 1); }
+constexpr int kLaunchRegsWide = 168;
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 216;
+static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= 384 * kLaunchRegsWide,
+              "the register split must fit in what the launch allocated");
+static_assert(2 * 32 * kConsumerRegs + 32 * kProducerRegs <= 16384,
+              "two consumer warps and one producer warp share a sub-partition's registers");
 constexpr int kMaxBatch = 8192;
 constexpr int kMaxGroup = 64;       // largest G = h / g served
-constexpr int kCombRows = 16;       // rows per warp in the combine scratch
 constexpr int kSwizzleRowBytes = 128;
 
 struct DecodeParams {
@@ -62,13 +73,14 @@ struct DecodeParams {
 __host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
 __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 
-// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort][prefix(b+1)]
-__host__ __device__ constexpr int smem_fixed_bytes(int D) {
-  return kStages * stage_bytes(D) + kConsumerWarps * kCombRows * comb_row_floats(D) * 4 +
-         kConsumerWarps * kCombRows * 8 + (2 * kStages + 1) * 8 + 16;  // + abort, merge flag
+// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort][prefix(b+1)].
+// CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
+__host__ __device__ constexpr int smem_fixed_bytes(int D, int NW, int CR) {
+  return kStages * stage_bytes(D) + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
+         (2 * kStages + 1) * 8 + 16;  // + abort, merge flag
 }
-__host__ __device__ constexpr size_t smem_bytes(int D, int b) {
-  return 1024 + static_cast<size_t>(smem_fixed_bytes(D)) + static_cast<size_t>(b + 1) * 4;
+__host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR, int b) {
+  return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR)) + static_cast<size_t>(b + 1) * 4;
 }
 
 __device__ __forceinline__ int tiles_of_length(int L, int n_max) {
@@ -113,8 +125,8 @@ struct TileCursor {
 
 struct SharedLayout {
   uint8_t* stages;      // kStages x stage_bytes(D), 1024-aligned
-  float* comb_o;        // [kConsumerWarps][kCombRows][comb_row_floats(D)]
-  float2* comb_ml;      // [kConsumerWarps][kCombRows]
+  float* comb_o;        // [NW][CR][comb_row_floats(D)]
+  float2* comb_ml;      // [NW][CR]
   uint64_t* full;       // [kStages]
   uint64_t* empty;      // [kStages]
   uint64_t* cbar;       // consumer-wide barrier
@@ -123,7 +135,7 @@ struct SharedLayout {
   uint32_t* pre;        // [b + 1] tiles before each sequence
 };
 
-template <int D>
+template <int D, int NW, int CR>
 __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   SharedLayout s;
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
@@ -131,9 +143,9 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.stages = p;
   p += kStages * stage_bytes(D);
   s.comb_o = reinterpret_cast<float*>(p);
-  p += kConsumerWarps * kCombRows * comb_row_floats(D) * 4;
+  p += NW * CR * comb_row_floats(D) * 4;
   s.comb_ml = reinterpret_cast<float2*>(p);
-  p += kConsumerWarps * kCombRows * 8;
+  p += NW * CR * 8;
   s.full = reinterpret_cast<uint64_t*>(p);
   s.empty = s.full + kStages;
   s.cbar = s.empty + kStages;
@@ -145,7 +157,7 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   return s;
 }
 
-// Consumer-wide barrier on an mbarrier (all 128 consumer threads arrive), bounded in time.
+// Consumer-wide barrier on an mbarrier (all 32 * NW consumer threads arrive), bounded in time.
 __device__ __forceinline__ bool consumer_sync(const SharedLayout& sh, uint32_t& phase,
                                               unsigned long long limit) {
   mbar_arrive(sh.cbar);
@@ -164,25 +176,25 @@ __device__ __forceinline__ void give_up(const SharedLayout& sh) {
 // when the whole segment lies in this CTA, else a partial state in workspace slot `slot`.
 // Row `hr` (a head of the group) has contributions at comb[(w, r)] for the pairs rows_of() gives.
 // ---------------------------------------------------------------------------------------------
-template <int D, class RowMap>
+template <int D, int NW, int CR, class RowMap>
 __device__ __forceinline__ void combine_and_store(const DecodeParams& P, const SharedLayout& sh,
                                                   int bi, int j, bool complete, int slot,
                                                   RowMap rows_of) {
-  const int tid = threadIdx.x;  // 0 .. 127 (consumer threads)
+  const int tid = threadIdx.x;  // 0 .. 32 * NW - 1 (consumer threads)
   const int G = P.G;
-  for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+  for (int idx = tid; idx < G * D; idx += NW * 32) {
     const int hr = idx / D;
     const int d = idx - hr * D;
-    int ws[kConsumerWarps], rs[kConsumerWarps];
+    int ws[NW], rs[NW];
     const int n = rows_of(hr, ws, rs);
     float M = -INFINITY;
-    for (int c = 0; c < n; ++c) M = fmaxf(M, sh.comb_ml[ws[c] * kCombRows + rs[c]].x);
+    for (int c = 0; c < n; ++c) M = fmaxf(M, sh.comb_ml[ws[c] * CR + rs[c]].x);
     float acc = 0.f, den = 0.f;
     for (int c = 0; c < n; ++c) {
-      const float2 ml = sh.comb_ml[ws[c] * kCombRows + rs[c]];
+      const float2 ml = sh.comb_ml[ws[c] * CR + rs[c]];
       const float wgt = fast_exp2(ml.x - M);
       den += wgt * ml.y;
-      acc += wgt * sh.comb_o[(ws[c] * kCombRows + rs[c]) * comb_row_floats(D) + d];
+      acc += wgt * sh.comb_o[(ws[c] * CR + rs[c]) * comb_row_floats(D) + d];
     }
     if (complete) {
       const size_t o = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d;
@@ -231,7 +243,7 @@ struct SegmentPieces {
 // arrives last), so it is written for latency: the pieces' (m, l) are staged in shared memory with
 // independent loads, the per-head weights 2^(m_c - M) / l are computed once, and each output
 // element then issues the loads of all pieces at once. Returns false if a barrier timed out.
-template <int D>
+template <int D, int NW, int CR>
 __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const SharedLayout& sh,
                                                     uint32_t& cphase, int bi, int j, int seg,
                                                     const SegmentPieces& pc) {
@@ -239,10 +251,10 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
   const int tid = threadIdx.x;
   const size_t out0 = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G) * D;
   const int np = pc.c_last - pc.c_first + 1;
-  constexpr int kScratchFloats = kConsumerWarps * kCombRows * comb_row_floats(D);
+  constexpr int kScratchFloats = NW * CR * comb_row_floats(D);
   if (!pc.all_own || 3 * np * G > kScratchFloats) {
     // general case (some CTAs own no tiles, or too many pieces to stage): plain loops
-    for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
       const int hr = idx / D;
       const int d = idx - hr * D;
       float M = -INFINITY;
@@ -265,9 +277,9 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
   float2* ml = reinterpret_cast<float2*>(sh.comb_o);  // [np][G]
   float* wgt = sh.comb_o + 2 * np * G;                  // [np][G]
   const size_t slot0 = static_cast<size_t>(pc.c_first + seg);
-  for (int e = tid; e < np * G; e += kConsumerWarps * 32) ml[e] = __ldcg(P.part_ml + slot0 * G + e);
+  for (int e = tid; e < np * G; e += NW * 32) ml[e] = __ldcg(P.part_ml + slot0 * G + e);
   if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
-  for (int hr = tid; hr < G; hr += kConsumerWarps * 32) {
+  for (int hr = tid; hr < G; hr += NW * 32) {
     float M = -INFINITY;
     for (int pi = 0; pi < np; ++pi) M = fmaxf(M, ml[pi * G + hr].x);
     float den = 0.f;
@@ -278,7 +290,7 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
   if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
   // outputs, four consecutive columns per thread
   const float4* po = reinterpret_cast<const float4*>(P.part_o);
-  for (int idx = tid; idx < G * D / 4; idx += kConsumerWarps * 32) {
+  for (int idx = tid; idx < G * D / 4; idx += NW * 32) {
     const int hr = idx / (D / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
@@ -296,12 +308,14 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
 }
 
 // ---------------------------------------------------------------------------------------------
-// Tensor-core consumer (G >= 8). WM warps (one per 16 heads) form a group; kConsumerWarps / WM
-// groups split each tile's keys.
+// Tensor-core consumer (G >= 8). WM warps (one per 16 heads) form a group; NW / WM groups split
+// each tile's keys.
 // ---------------------------------------------------------------------------------------------
-template <int D, int WM>
+template <int D, int WM, int NW>
 struct MmaConsumer {
-  static constexpr int NGRP = kConsumerWarps / WM;
+  static constexpr int kWarps = NW;
+  static constexpr int kCombRows = 16;  // head rows per warp
+  static constexpr int NGRP = NW / WM;
   static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
   static constexpr int NT_S = KPW / 8;          // score tiles (n = 8 keys)
   static constexpr int KS_QK = D / 16;          // k-steps over the head dimension
@@ -451,14 +465,19 @@ struct MmaConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer (G < 8). Warp w takes keys [16w, 16w + 16) of every tile; lane owns
-// DPL = D/32 consecutive columns of q, K, V and the output.
+// CUDA-core consumer (G < 8). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
+// 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output.
 // ---------------------------------------------------------------------------------------------
-template <int D, int G>
+template <int D, int G, int NW>
 struct CcConsumer {
+  static constexpr int kWarps = NW;
+  static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
   static constexpr int DPL = D / 32;
-  static constexpr int KPW = kTileKeys / kConsumerWarps;  // 16
-  static_assert(KPW == 16, "the reduce-scatter below is written for 16 keys per warp");
+  static constexpr int KPW = kTileKeys / NW;
+  static_assert(KPW == 16 || KPW == 8, "the reduce-scatter below handles 8 or 16 keys per warp");
+  // after the reduce-scatter, lane l holds the dot product of key l >> kLaneShift
+  static constexpr int kLaneShift = KPW == 16 ? 1 : 2;
+  static constexpr int kSame = 1 << kLaneShift;  // lanes holding the same key
 
   float qf[G][DPL];
   float o[G][DPL];
@@ -496,38 +515,28 @@ struct CcConsumer {
     }
   }
 
-  // Sum v[0..15] (one partial per key) over the 32 lanes; lane l ends with the full sum for
-  // key l >> 1 (lanes 2k and 2k+1 hold the same value). 16 shuffles instead of 16 x 5.
-  __device__ __forceinline__ static float reduce_scatter16(float (&v)[16], int lane) {
-    float a[8];
-    const bool up16 = lane & 16;
+  // Sum v[0..KPW-1] (one partial per key) over the 32 lanes; lane l ends with the full sum for
+  // key l >> kLaneShift (the kSame lanes of a key hold the same value). Each exchange level halves
+  // the values a lane keeps, so KPW keys cost KPW - 1 + kLaneShift shuffles instead of 5 KPW.
+  __device__ __forceinline__ static float reduce_scatter(float (&v)[KPW], int lane) {
+    float cur[KPW];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float send = up16 ? v[i] : v[i + 8];
-      const float keep = up16 ? v[i + 8] : v[i];
-      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-    float b4[4];
-    const bool up8 = lane & 8;
+    for (int i = 0; i < KPW; ++i) cur[i] = v[i];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float send = up8 ? a[i] : a[i + 4];
-      const float keep = up8 ? a[i + 4] : a[i];
-      b4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float c2[2];
-    const bool up4 = lane & 4;
+    for (int lvl = 0; (KPW >> lvl) > 1; ++lvl) {
+      const int half = (KPW >> lvl) / 2;
+      const int off = 16 >> lvl;
+      const bool up = lane & off;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float send = up4 ? b4[i] : b4[i + 2];
-      const float keep = up4 ? b4[i + 2] : b4[i];
-      c2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      for (int i = 0; i < half; ++i) {
+        const float send = up ? cur[i] : cur[i + half];
+        const float keep = up ? cur[i + half] : cur[i];
+        cur[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
     }
-    const bool up2 = lane & 2;
-    const float send = up2 ? c2[0] : c2[1];
-    const float keep = up2 ? c2[1] : c2[0];
-    float r = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    float r = cur[0];
+#pragma unroll
+    for (int off = kSame / 2; off >= 1; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
     return r;
   }
 
@@ -545,7 +554,7 @@ struct CcConsumer {
         for (int e = 0; e < DPL; ++e) kf[kk][e] = 0.f;
       }
     }
-    const bool mine_valid = (lane >> 1) < nvalid;
+    const bool mine_valid = (lane >> kLaneShift) < nvalid;
     float p[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -557,23 +566,21 @@ struct CcConsumer {
         for (int e = 0; e < DPL; ++e) acc = fmaf(qf[hh][e], kf[kk][e], acc);
         part[kk] = acc;
       }
-      const float dot = reduce_scatter16(part, lane);
+      const float dot = reduce_scatter(part, lane);
       const float s = mine_valid ? dot * scale_log2 : -INFINITY;
       float mx = s;
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+#pragma unroll
+      for (int off = kSame; off <= 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float mn = fmaxf(m[hh], mx);
       const float ref = (mn == -INFINITY) ? 0.f : mn;
       const float al = fast_exp2(m[hh] - ref);
       m[hh] = mn;
       p[hh] = fast_exp2(s - ref);
-      l[hh] = l[hh] * al + ((lane & 1) ? 0.f : p[hh]);
+      l[hh] = l[hh] * al + ((lane & (kSame - 1)) ? 0.f : p[hh]);
 #pragma unroll
       for (int e = 0; e < DPL; ++e) o[hh][e] *= al;
     }
-    // O += P V over the valid keys (p for key kk sits in lanes 2kk and 2kk+1)
+    // O += P V over the valid keys (p for key kk sits in lanes kk * kSame .. kk * kSame + kSame - 1)
 #pragma unroll
     for (int kk = 0; kk < KPW; ++kk) {
       if (kk < nvalid) {
@@ -581,7 +588,7 @@ struct CcConsumer {
         load_row(vbase, key0 + kk, lane, vf);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const float pk = __shfl_sync(0xffffffffu, p[hh], 2 * kk);
+          const float pk = __shfl_sync(0xffffffffu, p[hh], kk * kSame);
 #pragma unroll
           for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
         }
@@ -605,21 +612,24 @@ struct CcConsumer {
   struct Rows {
     __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) { ws[w] = w; rs[w] = hr; }
-      return kConsumerWarps;
+      for (int w = 0; w < NW; ++w) { ws[w] = w; rs[w] = hr; }
+      return NW;
     }
   };
 };
 
 // ---------------------------------------------------------------------------------------------
-// The kernel. `Consumer` is MmaConsumer<D, WM> or CcConsumer<D, G>.
+// The kernel. `Consumer` is MmaConsumer<D, WM, NW> or CcConsumer<D, G, NW>.
 // ---------------------------------------------------------------------------------------------
 template <int D, class Consumer, bool kTensorCores, int WM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
+  constexpr int NW = Consumer::kWarps;
+  constexpr int CR = Consumer::kCombRows;
+  constexpr int kThreads = threads_of(NW);
   extern __shared__ uint8_t smem_raw[];
-  const SharedLayout sh = carve_shared<D>(smem_raw);
+  const SharedLayout sh = carve_shared<D, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int B = P.b;
@@ -637,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *sh.merge = 0;
       for (int st = 0; st < kStages; ++st) {
         mbar_init(&sh.full[st], 1);
-        mbar_init(&sh.empty[st], kConsumerWarps);
+        mbar_init(&sh.empty[st], NW);
       }
-      mbar_init(sh.cbar, kConsumerWarps * 32);
+      mbar_init(sh.cbar, NW * 32);
       fence_barrier_init();
     }
     __syncthreads();
@@ -675,9 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kStageBytes = stage_bytes(D);
   constexpr uint32_t kKvBytes = kStageBytes / 2;
 
-  if (warp == kConsumerWarps) {
+  if constexpr (NW == 8) {
+    if (warp >= NW) setmaxnreg_dec<kProducerRegs>();
+    else setmaxnreg_inc<kConsumerRegs>();
+  }
+  if (warp >= NW) {
     // ================================ producer ================================================
-    if (lane != 0) return;
+    if (warp != NW || lane != 0) return;
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
     const uint64_t policy = l2_policy_evict_first();
@@ -717,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Consumer cons;
   const int grp = kTensorCores ? warp / WM : warp;
   const int mi = kTensorCores ? warp % WM : 0;
-  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / kConsumerWarps : kTileKeys / kConsumerWarps;
+  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / NW : kTileKeys / NW;
   uint32_t cphase = 0;
   TileCursor cur;
   cur.start(x0, sh.pre, B, P.g);
@@ -772,8 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int seg = cur.bi * P.g + cur.j;
       cons.publish(sh, warp, lane);
       if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
-      combine_and_store<D>(P, sh, cur.bi, cur.j, complete, static_cast<int>(blockIdx.x) + seg,
-                           typename Consumer::Rows{});
+      combine_and_store<D, NW, CR>(P, sh, cur.bi, cur.j, complete, static_cast<int>(blockIdx.x) + seg,
+                               typename Consumer::Rows{});
       if (!complete) __threadfence();  // this CTA's partial is visible before it is counted
       if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
       if (!complete) {
@@ -787,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
         if (*sh.merge) {
           __threadfence();
-          if (!merge_split_segment<D>(P, sh, cphase, cur.bi, cur.j, seg, pc)) {
+          if (!merge_split_segment<D, NW, CR>(P, sh, cphase, cur.bi, cur.j, seg, pc)) {
             if (!*sh.abort) give_up(sh);
             return;
           }

@@ -148,45 +148,66 @@ int device_info(int dev, DeviceInfo* info) {
 // ------------------------------------------------------------------------------------------------
 using AttnKernel = void (*)(const CUtensorMap, const CUtensorMap, const DecodeParams);
 
-template <int D, int WM>
-AttnKernel mma_kernel() {
-  return mqa::decode_attention_kernel<D, mqa::MmaConsumer<D, WM>, true, WM>;
-}
-template <int D, int G>
-AttnKernel cc_kernel() {
-  return mqa::decode_attention_kernel<D, mqa::CcConsumer<D, G>, false, 1>;
+// A kernel instance with the launch facts the host needs: consumer warps and combine rows.
+struct AttnKernelChoice {
+  AttnKernel fn = nullptr;
+  int nw = 0, cr = 0;
+};
+
+template <class Consumer, int D, bool TC, int WM>
+AttnKernelChoice choice() {
+  return {mqa::decode_attention_kernel<D, Consumer, TC, WM>, Consumer::kWarps, Consumer::kCombRows};
 }
 
+// Eight consumer warps (two per SM sub-partition) hide the latency of the per-tile dependency
+// chains of the CUDA-core path, where one warp per sub-partition leaves most issue slots idle. The
+// tensor-core path keeps four: its cost per tile is the mma.sync throughput itself, which a
+// second warp per sub-partition does not raise.
 template <int D>
-AttnKernel pick_kernel(bool tensor_cores, int G) {
+AttnKernelChoice pick_kernel(bool tensor_cores, int G) {
+  using mqa::CcConsumer;
+  using mqa::MmaConsumer;
   if (tensor_cores) {
-    if (G <= 16) return mma_kernel<D, 1>();
-    if (G <= 32) return mma_kernel<D, 2>();
-    return mma_kernel<D, 4>();
+    if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, true, 1>();
+    if (G <= 32) return choice<MmaConsumer<D, 2, 4>, D, true, 2>();
+    return choice<MmaConsumer<D, 4, 4>, D, true, 4>();
   }
   switch (G) {
-    case 1: return cc_kernel<D, 1>();
-    case 2: return cc_kernel<D, 2>();
-    case 3: return cc_kernel<D, 3>();
-    case 4: return cc_kernel<D, 4>();
-    case 5: return cc_kernel<D, 5>();
-    case 6: return cc_kernel<D, 6>();
-    case 7: return cc_kernel<D, 7>();
-    default: return nullptr;
+    case 1: return choice<CcConsumer<D, 1, 8>, D, false, 1>();
+    case 2: return choice<CcConsumer<D, 2, 8>, D, false, 1>();
+    case 3: return choice<CcConsumer<D, 3, 8>, D, false, 1>();
+    case 4: return choice<CcConsumer<D, 4, 8>, D, false, 1>();
+    case 5: return choice<CcConsumer<D, 5, 8>, D, false, 1>();
+    case 6: return choice<CcConsumer<D, 6, 8>, D, false, 1>();
+    case 7: return choice<CcConsumer<D, 7, 8>, D, false, 1>();
+    default: return {};
   }
 }
 
 std::mutex g_attr_mutex;
 std::map<std::pair<int, const void*>, size_t> g_smem_set;  // (device, kernel) -> bytes allowed
 
-int ensure_smem(int dev, const void* kernel, size_t bytes) {
+// Allow the kernel `bytes` of dynamic shared memory, and on first use check its register count:
+// the eight-consumer-warp kernels move registers between warpgroups (setmaxnreg), which only
+// completes if the launch allocated what the split assumes. A kernel built otherwise is refused
+// rather than launched.
+int prepare_kernel(int dev, const AttnKernelChoice& kc, size_t bytes) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
-  size_t& cur = g_smem_set[{dev, kernel}];
-  if (cur >= bytes) return MQA_OK;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const void* fn = reinterpret_cast<const void*>(kc.fn);
+  auto it = g_smem_set.find({dev, fn});
+  if (it == g_smem_set.end()) {
+    if (kc.nw == 8) {
+      cudaFuncAttributes attr{};
+      if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) return MQA_ERR_CUDA;
+      if (attr.numRegs != mqa::kLaunchRegsWide) return MQA_ERR_UNSUPPORTED;
+    }
+    it = g_smem_set.emplace(std::make_pair(dev, fn), size_t{0}).first;
+  }
+  if (it->second >= bytes) return MQA_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes)) != cudaSuccess)
     return MQA_ERR_CUDA;
-  cur = bytes;
+  it->second = bytes;
   return MQA_OK;
 }
 
@@ -295,12 +316,12 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.scale_log2 = p.scale * 1.4426950408889634f;
   P.timeout_ns = kWaitLimitNs;
 
-  AttnKernel kern = p.d_h == 128 ? pick_kernel<128>(p.tensor_cores, p.G)
-                                 : pick_kernel<64>(p.tensor_cores, p.G);
-  if (!kern) return MQA_ERR_UNSUPPORTED;
-  const size_t smem = mqa::smem_bytes(p.d_h, p.b);
-  if (int st = ensure_smem(p.dev, reinterpret_cast<const void*>(kern), smem)) return st;
-  kern<<<static_cast<unsigned>(p.ctas), mqa::kThreads, smem, p.stream>>>(tmk, tmv, P);
+  const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.tensor_cores, p.G)
+                                           : pick_kernel<64>(p.tensor_cores, p.G);
+  if (!kc.fn) return MQA_ERR_UNSUPPORTED;
+  const size_t smem = mqa::smem_bytes(p.d_h, kc.nw, kc.cr, p.b);
+  if (int st = prepare_kernel(p.dev, kc, smem)) return st;
+  kc.fn<<<static_cast<unsigned>(p.ctas), mqa::threads_of(kc.nw), smem, p.stream>>>(tmk, tmv, P);
   g_launches.fetch_add(1);
   return launch_error();
 }

@@ -75,6 +75,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------------------------
+// Warpgroup register reallocation (all 128 threads of a warpgroup execute the same one).
+// ---------------------------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------------------------
 // Bulk tensor copy global -> shared (TMA), completion signalled on an mbarrier.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
