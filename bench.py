@@ -2,23 +2,27 @@
 
 Default workload: the 80-layer GQA decode step of a 70B-class model (b=8 sequences, h=64 query
 heads, g=8 KV heads, d_h=128, contexts uniform in [1024, 32768], about 86 GB of bf16 cache): one
-step appends one token's K/V and runs attention in all 80 layers back to back.
+step appends one token's K/V and runs attention in all 80 layers back to back, one fused launch
+(mqa_decode_step) per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
-with inputs resident in HBM (lower is better): each timed step is one CUDA-graph replay of the
-whole step (every layer's append and attention), K replays back to back. ``e2e`` is the same step driven eagerly through
-the public Python API from pinned host buffers, with the host->device copy of the step's inputs
-(q, k_new, v_new of every layer) and the device->host read of its outputs inside the timed
-region. ``roofline`` reports the attention kernel's HBM throughput on algorithmic bytes (K/V rows
-read + q read + out written) against the measured copy bandwidth; its launch durations come from
-a second timed pass of K steps whose graphs carry CUDA event nodes around every attention call. ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the
-same workload. The reference arm (``--impl reference``) times that oracle as the reference.
+with inputs resident in HBM (lower is better), from CUDA-graph replays of the whole step (every
+layer's append and attention): K replays back to back between two events, or, for workloads small
+enough to sit in L2, one graph per step that flushes L2 (a 252 MB write) and then times the step
+between its own event nodes. ``e2e`` is the same step driven eagerly through the public Python
+API from pinned host buffers, with the host->device copy of the step's inputs (q, k_new, v_new of
+every layer) and the device->host read of its outputs inside the timed region. ``roofline``
+reports the decode kernel's HBM throughput on algorithmic bytes (K/V rows read, q read, out
+written, new rows read and written) against the measured copy bandwidth; its launch durations
+come from a second timed pass of K steps whose graphs carry CUDA event nodes around every launch.
+``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same workload. The reference
+arm (``--impl reference``) times that oracle as the reference.
 
-Every layer reads about 0.55 GB of cache (above the 126 MB L2) and a step reads about 44 GB, so
-no L2 flush is needed between timed steps.
+Every layer of the default workload reads about 0.7 GB of cache (above the 126 MB L2) and a step
+reads about 57 GB, so no L2 flush is needed between its timed steps.
 """
 from __future__ import annotations
 
@@ -154,10 +158,12 @@ class ClockSampler:
 
 
 def kv_bytes(w, lens) -> int:
-    """Algorithmic bytes of one attention call: K and V rows read (2 * g * L_b * d_h * 2 over the
-    batch), q read and out written (b * h * d_h * 2 each)."""
+    """Algorithmic bytes of one fused decode-step launch (one layer): K and V rows read
+    (2 * g * L_b * d_h * 2 over the batch), q read and out written (b * h * d_h * 2 each), and the
+    append's new rows read and written (2 * b * g * d_h * 2 each)."""
     total_rows = int(lens.sum())
-    return 2 * w.g * total_rows * w.d_h * 2 + 2 * w.b * w.h * w.d_h * 2
+    return (2 * w.g * total_rows * w.d_h * 2 + 2 * w.b * w.h * w.d_h * 2
+            + 2 * 2 * w.b * w.g * w.d_h * 2)
 
 
 def attention_flops(w, lens) -> int:
@@ -251,7 +257,7 @@ def workload_config(w):
 # ------------------------------------------------------------------------------------------------
 def run_ours(args, world, rank, local):
     import query_grouped_decode_kv_b300 as mqa
-    from query_grouped_decode_kv_b300.decode_step import LayerState, StepInputs, decode_step
+    from query_grouped_decode_kv_b300.layers import LayerState, StepInputs, decode_layers
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -274,15 +280,22 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
 
-    def step(events=None):
+    def step(events=None, step_events=None):
         if flush is not None:
             flush.fill_(1)
-        decode_step(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream, attn_events=events)
+        if step_events is not None:
+            step_events[0].record(stream)
+        decode_layers(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream, attn_events=events)
+        if step_events is not None:
+            step_events[1].record(stream)
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
+
+    def timing_event():
+        return torch.cuda.Event(enable_timing=True, external=True)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -290,25 +303,37 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
 
-    # ---- the step as a CUDA graph, replayed back to back: this gives `value` ----
-    step_graph = torch.cuda.CUDAGraph()
+    # ---- `value`: the step as CUDA-graph replays. Without an L2 flush, one graph replayed K
+    # times back to back between two events. With a flush, one graph per step whose event nodes
+    # bracket the step but not the flush before it, so the flush's time is not counted. ----
     n0 = mqa.kernel_launch_count()
-    with torch.cuda.graph(step_graph, stream=stream):
-        step()
-    launches_per_step = mqa.kernel_launch_count() - n0
+    if flush is None:
+        step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(step_graph, stream=stream):
+            step()
+        value_graphs, value_events = [step_graph] * args.steps, None
+    else:
+        value_graphs, value_events = [], []
+        for _ in range(args.steps):
+            pair = (timing_event(), timing_event())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(step_events=pair)
+            value_graphs.append(g)
+            value_events.append(pair)
+    launches_per_step = (mqa.kernel_launch_count() - n0) // (1 if flush is None else args.steps)
     # ---- per-launch attention durations: the same step with external event nodes around every
-    # attention call, one graph per timed step so each launch keeps its own events ----
+    # attention launch, one graph per timed step so each launch keeps its own events ----
     timed_graphs, ev = [], []
     for _ in range(args.steps):
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(w.layers)]
+        evs = [(timing_event(), timing_event()) for _ in range(w.layers)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(evs)
         timed_graphs.append(g)
         ev.append(evs)
     with torch.cuda.stream(stream):
-        step_graph.replay()
+        value_graphs[0].replay()
         timed_graphs[0].replay()
     torch.cuda.synchronize()
 
@@ -318,8 +343,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             t_start.record(stream)
-            for _ in range(args.steps):
-                step_graph.replay()
+            for g in value_graphs:
+                g.replay()
             t_end.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -332,7 +357,8 @@ def run_ours(args, world, rank, local):
         barrier()
     launches = launches_per_step * args.steps
     assert mqa.get_device_status() == 0, "device status latched an error in the timed region"
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = (t_start.elapsed_time(t_end) if value_events is None
+                else sum(a.elapsed_time(b) for a, b in value_events))
     attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
     attn_avg_s = sum(attn_ms) / len(attn_ms) / 1000.0
 
@@ -345,31 +371,37 @@ def run_ours(args, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
     d2h = sum(t.numel() * t.element_size() for t in ho)
 
-    def e2e_step():
-        # eager, through the public API: copy in, append + attention per layer, copy out
+    def e2e_step(pair=None):
+        # eager, through the public API: copy in, append + attention per layer, copy out; an L2
+        # flush (small workloads only) runs before the step's start event
+        if flush is not None:
+            flush.fill_(1)
+        if pair is not None:
+            pair[0].record(stream)
         for li in range(w.layers):
             xs[li].q.copy_(hq[li], non_blocking=True)
             xs[li].k_new.copy_(hk[li], non_blocking=True)
             xs[li].v_new.copy_(hv[li], non_blocking=True)
-        step()
+        decode_layers(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream)
         for li in range(w.layers):
             ho[li].copy_(outs[li], non_blocking=True)
+        if pair is not None:
+            pair[1].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(2):
             e2e_step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        for pair in e2e_events:
+            e2e_step(pair)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_events)
 
     # ---- max over ranks ----
     ms_per_step = ms_total / args.steps
@@ -398,7 +430,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_kind": f"{peak_kind} copy bandwidth",
-                         "kernel": "decode_attention_kernel (one launch per attention call)",
+                         "kernel": "decode_attention_kernel (one fused append + attention launch per layer)",
                          "algorithmic_bytes_per_launch": nbytes,
                          "flops_per_launch": attention_flops(w, lens)},
             "e2e": {"value": e2e_per_step * 1000.0 / world, "unit": UNIT,

@@ -118,6 +118,38 @@ MQA_API int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, con
                          int n_max, float scale, void* stream);
 
 /*
+ * mqa_decode_step -- one whole decode step of one layer in a single launch: the append of
+ * mqa_kv_append followed by the attention of mqa_decode_attention, with the same result as
+ * calling the two in that order on one stream (the cache rows bit for bit, `out` within the
+ * same tolerances).
+ *
+ * Defined by the decode step of "GQA与MQA深度实战" (ybb.press) §八 (store the new token's K/V at
+ * the current position, then attend over every cached row up to and including it) and §五 (the
+ * grouped attention, see mqa_decode_attention); the nanhubrain.csdn.net MQA article §2.2 orders
+ * the append before the attention in the same way.
+ *
+ * The new rows are written by the CTA that loads the tile holding them, immediately before that
+ * tile is copied into shared memory, so the step reads each cache row once and launches once.
+ *
+ *   q, out           as for mqa_decode_attention
+ *   k_new, v_new     device, [b][g][d_h] bf16, 16-byte aligned, read only
+ *   k_cache, v_cache device, [b][g][n_max][d_h] bf16, 16-byte aligned; row pos[bi] of every
+ *                    (bi, j) is written, every other row only read
+ *   pos              device, [b] int32, 0 <= pos[bi] < n_max
+ *   seq_lens         device, [b] int32, 1 <= seq_lens[bi] <= n_max; normally pos[bi] + 1
+ *   b, h, g, d_h, n_max, scale, stream   as for mqa_decode_attention
+ *
+ * Returns MQA_OK, MQA_ERR_INVALID_ARG, MQA_ERR_UNSUPPORTED or MQA_ERR_CUDA. A pos entry out of
+ * range skips that sequence's append; a seq_lens entry out of range writes zeros for that
+ * sequence's output; both latch MQA_ERR_DEVICE_BOUNDS. The workspace is that of
+ * mqa_decode_attention (shared per stream).
+ */
+MQA_API int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                            mqa_bf16* k_cache, mqa_bf16* v_cache, const int32_t* pos,
+                            const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
+                            int n_max, float scale, void* stream);
+
+/*
  * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
  * memory. The source pages have no counterpart to this call; it exists for users of the library.
  *

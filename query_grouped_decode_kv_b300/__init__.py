@@ -8,7 +8,7 @@ not been built.
 from __future__ import annotations
 
 _BINDING_NAMES = {
-    "kv_append", "decode_attention", "get_device_status", "status_string", "MqaError",
+    "kv_append", "decode_attention", "decode_step", "get_device_status", "status_string", "MqaError",
     "library_path", "kernel_launch_count", "debug_override", "raw",
 }
 

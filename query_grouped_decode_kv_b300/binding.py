@@ -29,6 +29,9 @@ _lib.mqa_kv_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, 
 _lib.mqa_decode_attention.restype = _i32
 _lib.mqa_decode_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                       _f32, _vp]
+_lib.mqa_decode_step.restype = _i32
+_lib.mqa_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                 _i32, _f32, _vp]
 _lib.mqa_status_string.restype = ctypes.c_char_p
 _lib.mqa_status_string.argtypes = [_i32]
 _lib.mqa_get_device_status.restype = _i32
@@ -138,4 +141,39 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                                    float(scale), _vp(_stream_handle(stream)))
     if st:
         raise MqaError(st, "mqa_decode_attention")
+    return out
+
+
+def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, pos: torch.Tensor, seq_lens: torch.Tensor,
+                out: torch.Tensor | None = None, scale: float | None = None,
+                stream=None) -> torch.Tensor:
+    """One launch doing :func:`kv_append` then :func:`decode_attention`: writes ``k_new``/``v_new``
+    at row ``pos[b]`` of the caches and attends over the first ``seq_lens[b]`` rows."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,) \
+            or pos.shape != (b,) or k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h):
+        raise ValueError("decode_step: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_step: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                              k_cache.data_ptr(), v_cache.data_ptr(), pos.data_ptr(),
+                              seq_lens.data_ptr(), out.data_ptr(), b, h, g, d_h, n_max,
+                              float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step")
     return out

@@ -68,6 +68,13 @@ struct DecodeParams {
   int num_ctas;               // P
   float scale_log2;           // scale * log2(e)
   unsigned long long timeout_ns;
+  // Fused append (mqa_decode_step): this step's K/V rows, written at row pos[bi] of the caches
+  // before any tile holding that row is loaded. All null when the call only attends.
+  const int32_t* pos;         // [b]
+  const uint4* k_new;         // [b][g][D/8] 16-byte chunks
+  const uint4* v_new;
+  uint4* k_rows;              // the caches as 16-byte chunks, [b][g][n_max][D/8]
+  uint4* v_rows;
 };
 
 __host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
@@ -95,6 +102,49 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int key, int d) {
   const int chunk = (d >> 3) & 7;
   return base + static_cast<uint32_t>(half * (kTileKeys * kSwizzleRowBytes) +
                                       key * kSwizzleRowBytes + ((chunk ^ (key & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Fused append. Row pos[bi] of segment (bi, j) receives k_new[bi][j] and v_new[bi][j]. When a
+// tile of the segment holds that row (pos < tiles * kTileKeys), the CTA that loads the tile writes
+// the row first (write_new_row, from its producer warp, ordered before the tile's bulk copy by a
+// generic-to-async proxy fence), so attention sees the new row. Every other valid row is written
+// by append_uncovered_rows, spread over all CTAs; no tile of this launch reads it.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ bool row_is_loaded(int p, int L, int n_max) {
+  return static_cast<long long>(p) < static_cast<long long>(tiles_of_length(L, n_max)) * kTileKeys;
+}
+
+template <int D>
+__device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int nthreads) {
+  constexpr int CH = D / 8;  // 16-byte chunks per row
+  const long long total = static_cast<long long>(P.b) * P.g * CH;
+  const long long stride = static_cast<long long>(P.num_ctas) * nthreads;
+  for (long long idx = static_cast<long long>(blockIdx.x) * nthreads + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long row = idx / CH;  // = bi * g + j
+    const int c = static_cast<int>(idx - row * CH);
+    const int bi = static_cast<int>(row / P.g);
+    const int p = __ldg(P.pos + bi);
+    if (p < 0 || p >= P.n_max) {
+      if (c == 0 && row == static_cast<long long>(bi) * P.g) latch_status(kStatusDeviceBounds);
+      continue;
+    }
+    if (row_is_loaded(p, __ldg(P.seq_lens + bi), P.n_max)) continue;
+    const long long dst = (row * P.n_max + p) * CH + c;
+    P.k_rows[dst] = __ldg(P.k_new + idx);
+    P.v_rows[dst] = __ldg(P.v_new + idx);
+  }
+}
+
+// One warp writes the K and V row of segment `seg` at cache row `p` (lane = 16-byte chunk).
+template <int D>
+__device__ __forceinline__ void write_new_row(const DecodeParams& P, int seg, int p, int lane) {
+  constexpr int CH = D / 8;
+  const long long src = static_cast<long long>(seg) * CH;
+  const long long dst = (static_cast<long long>(seg) * P.n_max + p) * CH;
+  if (lane < CH) P.k_rows[dst + lane] = __ldg(P.k_new + src + lane);
+  else if (lane < 2 * CH) P.v_rows[dst + lane - CH] = __ldg(P.v_new + src + lane - CH);
 }
 
 // Walks the tiles of one CTA's range in segment order.
@@ -653,10 +703,24 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       fence_barrier_init();
     }
     __syncthreads();
-    if (tid == 0) {
-      uint32_t run = 0;
-      for (int t = 0; t < kThreads; ++t) { const uint32_t v = part_sums[t]; part_sums[t] = run; run += v; }
-      sh.pre[B] = run;
+    if (warp == 0) {
+      // exclusive scan of the kThreads chunk sums: each lane takes kPer consecutive ones, the
+      // lanes' totals are scanned with shuffles
+      constexpr int kPer = kThreads / 32;
+      static_assert(kThreads % 32 == 0, "whole warps");
+      uint32_t loc[kPer], tot = 0;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) { loc[i] = part_sums[lane * kPer + i]; tot += loc[i]; }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      uint32_t run = incl - tot;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) { part_sums[lane * kPer + i] = run; run += loc[i]; }
+      if (lane == 31) sh.pre[B] = incl;
     }
     __syncthreads();
     uint32_t run = part_sums[tid];
@@ -675,6 +739,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.h * D;
     for (int e = tid; e < P.h * D; e += kThreads) ob[e] = __float2bfloat16_rn(0.f);
   }
+  if (P.pos != nullptr) append_uncovered_rows<D>(P, kThreads);
 
   const unsigned long long W = static_cast<unsigned long long>(P.g) * sh.pre[B];
   const unsigned long long x0 = W * blockIdx.x / P.num_ctas;
@@ -691,35 +756,59 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   if (warp >= NW) {
     // ================================ producer ================================================
-    if (warp != NW || lane != 0) return;
-    prefetch_tensor_map(&tm_k);
-    prefetch_tensor_map(&tm_v);
+    // Lane 0 issues the bulk copies; the whole warp runs only to write the fused append's rows.
+    if (warp != NW) return;
+    const bool fused = P.pos != nullptr;
+    if (!fused && lane != 0) return;
+    if (lane == 0) {
+      prefetch_tensor_map(&tm_k);
+      prefetch_tensor_map(&tm_v);
+    }
     const uint64_t policy = l2_policy_evict_first();
     TileCursor cur;
     cur.start(x0, sh.pre, B, P.g);
     int issued = 0;
+    int row_bi = -1, row_p = -1;  // the append row of sequence row_bi (-1: none to write)
     for (int k = 0; k < ntiles; ++k) {
       const int st = k % kStages;
       const uint32_t par = ((k / kStages) & 1) ^ 1;
-      if (!mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort)) {
-        if (!*sh.abort) give_up(sh);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
+      if (fused) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) {
+        if (lane == 0 && !*sh.abort) give_up(sh);
         break;
       }
-      mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
-      const int z = cur.bi * P.g + cur.j;
-      const int y = cur.tile * kTileKeys;
-      uint8_t* kdst = sh.stages + st * kStageBytes;
-      uint8_t* vdst = kdst + kKvBytes;
+      if (fused) {
+        if (cur.bi != row_bi) {
+          row_bi = cur.bi;
+          const int p = __ldg(P.pos + cur.bi);
+          row_p = (p >= 0 && p < P.n_max) ? p : -1;
+        }
+        if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
+          write_new_row<D>(P, cur.bi * P.g + cur.j, row_p, lane);
+          fence_proxy_async_global();  // each writer orders its store before the async proxy...
+          __syncwarp();                // ...and lane 0 issues the copy after every writer
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
+        const int z = cur.bi * P.g + cur.j;
+        const int y = cur.tile * kTileKeys;
+        uint8_t* kdst = sh.stages + st * kStageBytes;
+        uint8_t* vdst = kdst + kKvBytes;
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, &tm_k, &sh.full[st], half * 64, y,
-                    z, policy);
-        tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, &tm_v, &sh.full[st], half * 64, y,
-                    z, policy);
+        for (int half = 0; half < D / 64; ++half) {
+          tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, &tm_k, &sh.full[st], half * 64,
+                      y, z, policy);
+          tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, &tm_v, &sh.full[st], half * 64,
+                      y, z, policy);
+        }
       }
       ++issued;
       cur.advance(sh.pre, B, P.g);
     }
+    if (lane != 0) return;
     // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
     const volatile int never = 0;
     for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)

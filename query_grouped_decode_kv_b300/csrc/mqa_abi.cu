@@ -221,6 +221,9 @@ struct DecodePlan {
   const mqa_bf16 *q, *k_cache, *v_cache;
   const int32_t* seq_lens;
   mqa_bf16* out;
+  // fused append (mqa_decode_step only; null otherwise)
+  const mqa_bf16 *k_new = nullptr, *v_new = nullptr;
+  const int32_t* pos = nullptr;
   int b, h, g, d_h, n_max, G;
   float scale;
   bool tensor_cores;
@@ -315,6 +318,12 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.num_ctas = static_cast<int>(p.ctas);
   P.scale_log2 = p.scale * 1.4426950408889634f;
   P.timeout_ns = kWaitLimitNs;
+  P.pos = p.pos;
+  P.k_new = reinterpret_cast<const uint4*>(p.k_new);
+  P.v_new = reinterpret_cast<const uint4*>(p.v_new);
+  // the caches are written only at the rows the fused append targets
+  P.k_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.k_cache)) : nullptr;
+  P.v_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.v_cache)) : nullptr;
 
   const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.tensor_cores, p.G)
                                            : pick_kernel<64>(p.tensor_cores, p.G);
@@ -437,6 +446,31 @@ int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_b
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan))
     return st;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                    mqa_bf16* k_cache, mqa_bf16* v_cache, const int32_t* pos,
+                    const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
+                    int n_max, float scale, void* stream) {
+  if (!k_new || !v_new || !pos) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan))
+    return st;
+  plan.k_new = k_new;
+  plan.v_new = v_new;
+  plan.pos = pos;
   void* partials = nullptr;
   unsigned int* counters = nullptr;
   bool clear = false;

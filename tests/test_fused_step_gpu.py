@@ -1,0 +1,145 @@
+"""GPU parity of the fused decode step (mqa_decode_step: the append and the attention in one
+launch) against the fp64 oracle's append followed by its attention, on the same seeded inputs.
+
+The new rows are written by the CTA that loads the tile holding them, right before that tile's
+bulk copy, so the cases place the append row everywhere it can be: the last attended row (the
+normal decode step), a row inside the attended range, a row past the length but inside the last
+loaded tile, a row past every loaded tile, and an out-of-range row. CTA counts are forced so that
+the tile holding the row lands at the start, middle and end of CTA ranges.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from query_grouped_decode_kv_b300 import inputs
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mqa():
+    import query_grouped_decode_kv_b300 as m
+    m.debug_override(0, 0)
+    yield m
+    m.debug_override(0, 0)
+
+
+def fused_gpu_step(case, mqa, stream=None):
+    dev = torch.device("cuda")
+    q = case["q"].to(dev)
+    kn, vn = case["k_new"].to(dev), case["v_new"].to(dev)
+    k, v = case["k"].to(dev), case["v"].to(dev)
+    pos, lens = case["pos"].to(dev), case["lens"].to(dev)
+    out = mqa.decode_step(q, kn, vn, k, v, pos, lens, scale=case["scale"], stream=stream)
+    return k, v, out
+
+
+def oracle_step_any(case):
+    """The oracle's append then attention; tolerates an out-of-range pos (status 4)."""
+    kb, vb = P.bits(case["k"]).copy(), P.bits(case["v"]).copy()
+    st = oracle.kv_append(P.bits(case["k_new"]), P.bits(case["v_new"]), kb, vb,
+                          case["pos"].numpy())
+    out, ast = oracle.decode_attention(P.bits(case["q"]), kb, vb, case["lens"].numpy(),
+                                       case["scale"], return_status=True)
+    return kb, vb, out, st, ast
+
+
+SHAPES = [
+    # b, h, g, d_h, ctx_lo, ctx_hi
+    (1, 8, 1, 64, 128, 128),      # tiny MQA step, G = 8
+    (3, 8, 2, 64, 0, 300),        # G = 4, CUDA cores, lengths from 1
+    (2, 4, 4, 128, 60, 70),       # MHA around the tile edge
+    (2, 7, 1, 128, 1, 200),       # G = 7
+    (2, 16, 2, 128, 100, 700),    # G = 8, tensor cores
+    (2, 32, 1, 128, 1, 1000),     # G = 32
+    (4, 32, 8, 128, 0, 513),      # GQA 8B-class heads, short ragged contexts
+    (5, 2, 1, 64, 63, 65),        # G = 2, tile edges
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}h{}g{}d{}_{}-{}".format(*s))
+def test_fused_step_matches_oracle(mqa, shape):
+    case = P.make_case(*shape, seed_id=700 + SHAPES.index(shape))
+    k_ref, v_ref, out_ref = P.oracle_step(case)
+    k, v, out = fused_gpu_step(case, mqa)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    assert np.array_equal(P.bits(k), k_ref), "K append is not bit-exact"
+    assert np.array_equal(P.bits(v), v_ref), "V append is not bit-exact"
+    P.assert_close(out, out_ref, f"fused {shape}")
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
+@pytest.mark.parametrize("shape", [(2, 16, 2, 128, 0, 700), (3, 8, 4, 64, 100, 400)],
+                         ids=["mma", "cuda_cores"])
+def test_fused_step_any_cta_split(mqa, shape, ctas):
+    case = P.make_case(*shape, seed_id=720)
+    k_ref, v_ref, out_ref = P.oracle_step(case)
+    mqa.debug_override(ctas, 0)
+    try:
+        k, v, out = fused_gpu_step(case, mqa)
+        assert mqa.get_device_status() == 0
+    finally:
+        mqa.debug_override(0, 0)
+    assert np.array_equal(P.bits(k), k_ref) and np.array_equal(P.bits(v), v_ref)
+    P.assert_close(out, out_ref, f"fused {shape} ctas={ctas}")
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 5, 64])
+@pytest.mark.parametrize("path", [1, 2])
+def test_fused_step_append_row_anywhere(mqa, path, ctas):
+    # lengths 200, 300, 100, 70, 150, 129 with append rows: the last attended row; a row inside
+    # the attended range; past the length inside the last loaded tile; past every loaded tile;
+    # out of range (skipped, latched); and the first row of a tile
+    case = P.make_case(6, 8, 2, 128, 60, 300, seed_id=730)
+    n_max = case["w"].n_max
+    case["lens"] = torch.tensor([200, 300, 100, 70, 150, 129], dtype=torch.int32)
+    case["pos"] = torch.tensor([199, 37, 110, 250, n_max, 128], dtype=torch.int32)
+    # rows at or past each new length hold NaN (the append overwrites one of them or not)
+    case["k"], case["v"] = inputs.cache(case["w"], 0, "cpu", tail="nan", lengths=case["lens"])
+    k_ref, v_ref, out_ref, st, ast = oracle_step_any(case)
+    assert st == oracle.ERR_BOUNDS and ast == oracle.OK
+    mqa.debug_override(ctas, path)
+    try:
+        k, v, out = fused_gpu_step(case, mqa)
+        assert mqa.get_device_status() == 4     # the out-of-range pos
+    finally:
+        mqa.debug_override(0, 0)
+    assert np.array_equal(P.bits(k), k_ref), "K rows differ from the oracle's append"
+    assert np.array_equal(P.bits(v), v_ref), "V rows differ from the oracle's append"
+    P.assert_close(out, out_ref, f"append rows anywhere, path {path}, ctas {ctas}")
+
+
+def test_fused_step_appends_even_when_the_length_is_invalid(mqa):
+    case = P.make_case(4, 8, 2, 64, 10, 300, seed_id=740)
+    lens = case["lens"].clone()
+    lens[1] = 0
+    lens[2] = case["w"].n_max + 1
+    case["lens"] = lens
+    k_ref, v_ref, out_ref, st, ast = oracle_step_any(case)
+    assert st == oracle.OK
+    k, v, out = fused_gpu_step(case, mqa)
+    assert mqa.get_device_status() == 4
+    assert np.array_equal(P.bits(k), k_ref) and np.array_equal(P.bits(v), v_ref)
+    ob = P.bits(out)
+    assert np.all(ob[1] == 0) and np.all(ob[2] == 0)
+    keep = [0, 3]
+    P.assert_close(out[keep], out_ref[keep], "valid sequences next to invalid ones")
+
+
+@pytest.mark.parametrize("shape", [(3, 32, 8, 128, 100, 2000), (2, 8, 8, 128, 100, 2000)],
+                         ids=["G4", "G1"])
+def test_fused_step_equals_append_then_attention_bit_for_bit(mqa, shape):
+    # the fused launch runs the same arithmetic as the two-launch path, so outputs match exactly
+    case = P.make_case(*shape, seed_id=750)
+    k1, v1, o1 = fused_gpu_step(case, mqa)
+    k2, v2, o2 = P.gpu_step(case, mqa)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))

@@ -73,7 +73,7 @@ def test_single_layer_workloads(mqa, name, sample):
 def test_80_layer_step_sampled(mqa):
     """The full 80-layer GQA step (about 86 GB of cache), run as the benchmark runs it; the oracle
     checks three layers on two sequences each."""
-    from query_grouped_decode_kv_b300.decode_step import LayerState, StepInputs, decode_step
+    from query_grouped_decode_kv_b300.layers import LayerState, StepInputs, decode_layers
     w = inputs.WORKLOADS["gqa_70b_80l"]
     dev = torch.device("cuda")
     pos, lens = inputs.positions_and_lengths(w)
@@ -87,7 +87,7 @@ def test_80_layer_step_sampled(mqa):
         layers.append(LayerState(k, v))
         xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
         outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
-    decode_step(layers, xs, pos.to(dev), lens.to(dev), outs, w.scale)
+    decode_layers(layers, xs, pos.to(dev), lens.to(dev), outs, w.scale)
     torch.cuda.synchronize()
     assert mqa.get_device_status() == 0
     for li, (kh, vh) in check_layers.items():
