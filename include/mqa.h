@@ -196,14 +196,28 @@ MQA_API const char* mqa_status_string(int status);
  */
 MQA_API int mqa_get_device_status(void* stream, int* status_out);
 
+/*
+ * Diagnostics for MQA_ERR_TIMEOUT: synchronise the current device, then read and clear where the
+ * first in-kernel wait that ran out of time gave up. site_out[0] is the wait (0 = none since the
+ * last read; 1 producer waiting for a free stage, 2 consumers waiting for a stage's copy, 3 the
+ * consumer-wide barrier, 4 the tcgen05 issuer waiting for Q, 5 ... for a stage's copy, 6 ... for P,
+ * 7 the softmax warps waiting for S, 8 ... for O before a rescale, 9 ... for a stage's copy,
+ * 10 ... for the last O of a segment, 11 the issuer draining its MMAs, 12 the issuer waiting for
+ * the softmax warps at exit, 13 the issuer waiting for the P V product that last read an S buffer); site_out[1] the tile index within the CTA's range, site_out[2] the
+ * CTA, site_out[3] the thread. Returns MQA_OK, MQA_ERR_INVALID_ARG (NULL) or MQA_ERR_CUDA.
+ */
+MQA_API int mqa_debug_timeout_site(int* site_out);
+
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 MQA_API uint64_t mqa_kernel_launch_count(void);
 
 /*
  * Testing hook: force the number of CTAs that split the attention work (0 = automatic choice)
- * and the inner-product path (0 = automatic: tensor cores when h/g >= 8, CUDA cores otherwise;
- * 1 = CUDA cores; 2 = tensor cores). Process-wide; returns MQA_ERR_INVALID_ARG for a negative
- * CTA count or an unknown path. Results must not depend on either setting beyond rounding.
+ * and the inner-product path: 0 = automatic (CUDA cores when h/g < 8, mma.sync tensor cores
+ * otherwise); 1 = CUDA cores (h/g <= 7 only); 2 = mma.sync tensor cores; 3 = tcgen05 tensor cores
+ * with tensor-memory accumulators. Process-wide; returns
+ * MQA_ERR_INVALID_ARG for a negative CTA count or an unknown path. Results must not depend on
+ * either setting beyond rounding.
  */
 MQA_API int mqa_debug_override(int num_ctas, int path);
 

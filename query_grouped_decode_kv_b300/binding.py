@@ -38,6 +38,8 @@ _lib.mqa_get_device_status.restype = _i32
 _lib.mqa_get_device_status.argtypes = [_vp, ctypes.POINTER(_i32)]
 _lib.mqa_kernel_launch_count.restype = ctypes.c_uint64
 _lib.mqa_kernel_launch_count.argtypes = []
+_lib.mqa_debug_timeout_site.restype = _i32
+_lib.mqa_debug_timeout_site.argtypes = [ctypes.POINTER(_i32)]
 _lib.mqa_debug_override.restype = _i32
 _lib.mqa_debug_override.argtypes = [_i32, _i32]
 
@@ -71,6 +73,16 @@ def debug_override(num_ctas: int = 0, path: int = 0) -> None:
     st = _lib.mqa_debug_override(int(num_ctas), int(path))
     if st:
         raise MqaError(st, "mqa_debug_override")
+
+
+def debug_timeout_site() -> tuple[int, int, int, int]:
+    """(site, tile, block, thread) of the first in-kernel wait that timed out since the last
+    call; site 0 means none. Synchronises the current device."""
+    out = (_i32 * 4)()
+    st = _lib.mqa_debug_timeout_site(out)
+    if st:
+        raise MqaError(st, "mqa_debug_timeout_site")
+    return tuple(int(x) for x in out)
 
 
 def _stream_handle(stream) -> int:

@@ -216,7 +216,10 @@ __device__ __forceinline__ bool consumer_sync(const SharedLayout& sh, uint32_t& 
   return ok;
 }
 
-__device__ __forceinline__ void give_up(const SharedLayout& sh) {
+// A wait of this thread ran out of time at `site` (tile k of the CTA's range): record where,
+// latch MQA_ERR_TIMEOUT and tell the CTA's other warps to stop.
+__device__ __forceinline__ void give_up(const SharedLayout& sh, int site, int k) {
+  record_timeout_site(site, k);
   latch_status(kStatusTimeout);
   *sh.abort = 1;
 }
@@ -355,6 +358,164 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
   }
   // the scratch is written again by the next segment's combine
   return consumer_sync(sh, cphase, P.timeout_ns);
+}
+
+// ---------------------------------------------------------------------------------------------
+// After this CTA stored its partial state of segment (bi, j) (and fenced it, and the consumer
+// threads synchronised): count the arrival, and if this CTA is the last of the segment's pieces,
+// merge them into the output and reset the counter. Run by the 32 * NW consumer threads; returns
+// false if a barrier timed out.
+// ---------------------------------------------------------------------------------------------
+template <int D, int NW, int CR>
+__device__ __forceinline__ bool finish_split_segment(const DecodeParams& P, const SharedLayout& sh,
+                                                     uint32_t& cphase, int bi, int j, int nt,
+                                                     unsigned long long W) {
+  const int seg = bi * P.g + j;
+  const unsigned long long s0 =
+      static_cast<unsigned long long>(P.g) * sh.pre[bi] + static_cast<unsigned long long>(j) * nt;
+  const SegmentPieces pc(s0, s0 + nt - 1, W, P.num_ctas);
+  if (threadIdx.x == 0) {
+    // The partial rows were stored by many threads, ordered before this point by their fences and
+    // the consumer barrier (CTA scope). The counter is the only thing other CTAs observe, so this
+    // thread's fence before the increment is what releases those rows at device scope, and its
+    // fence after it acquires the other pieces' rows before this CTA may merge them.
+    __threadfence();
+    const unsigned int before = atomicAdd(P.seg_arrivals + seg, 1u);
+    __threadfence();
+    *sh.merge = (before + 1u == pc.count()) ? 1 : 0;
+  }
+  if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
+  if (*sh.merge) {
+    __threadfence();
+    if (!merge_split_segment<D, NW, CR>(P, sh, cphase, bi, j, seg, pc)) return false;
+    if (threadIdx.x == 0) P.seg_arrivals[seg] = 0u;  // ready for the next call
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Prologue shared by the kernels: the tiles of every sequence and their exclusive prefix, which
+// every CTA computes for itself into sh.pre[0 .. b] (so W = g * pre[b]). Ends with a CTA-wide
+// barrier, which also publishes barrier initialisation done before the call.
+// ---------------------------------------------------------------------------------------------
+template <int kThreads>
+__device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, const SharedLayout& sh,
+                                                  uint32_t* part_sums) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = P.b;
+  const int chunk = (B + kThreads - 1) / kThreads;
+  const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
+  uint32_t s = 0;
+  for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+  part_sums[tid] = s;
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the kThreads chunk sums: each lane takes kPer consecutive ones, the lanes'
+    // totals are scanned with shuffles
+    constexpr int kPer = kThreads / 32;
+    static_assert(kThreads % 32 == 0, "whole warps");
+    uint32_t loc[kPer], tot = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) { loc[i] = part_sums[lane * kPer + i]; tot += loc[i]; }
+    uint32_t incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    uint32_t run = incl - tot;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) { part_sums[lane * kPer + i] = run; run += loc[i]; }
+    if (lane == 31) sh.pre[B] = incl;
+  }
+  __syncthreads();
+  uint32_t run = part_sums[tid];
+  for (int i = lo; i < hi; ++i) {
+    sh.pre[i] = run;
+    run += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+  }
+  __syncthreads();
+}
+
+// Sequences whose length is out of range get a zero output and latch MQA_ERR_DEVICE_BOUNDS.
+template <int D>
+__device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, int nthreads) {
+  for (int bi = blockIdx.x; bi < P.b; bi += P.num_ctas) {
+    const int L = __ldg(P.seq_lens + bi);
+    if (L >= 1 && L <= P.n_max) continue;
+    if (threadIdx.x == 0) latch_status(kStatusDeviceBounds);
+    __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.h * D;
+    for (int e = threadIdx.x; e < P.h * D; e += nthreads) ob[e] = __float2bfloat16_rn(0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Producer warp: stream the CTA's tiles [x0, x0 + ntiles) into the stage ring with bulk tensor
+// copies (lane 0), after writing the fused append's new row into the cache when the tile holds it
+// (whole warp, one 16-byte chunk per lane). Stage st is refilled once its `empty` barrier has
+// completed the phase of its previous use.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                              const DecodeParams& P, const SharedLayout& sh,
+                                              unsigned long long x0, int ntiles, int lane) {
+  constexpr uint32_t kStageBytes = stage_bytes(D);
+  constexpr uint32_t kKvBytes = kStageBytes / 2;
+  const bool fused = P.pos != nullptr;
+  if (!fused && lane != 0) return;
+  if (lane == 0) {
+    prefetch_tensor_map(tm_k);
+    prefetch_tensor_map(tm_v);
+  }
+  const uint64_t policy = l2_policy_evict_first();
+  TileCursor cur;
+  cur.start(x0, sh.pre, P.b, P.g);
+  int issued = 0;
+  int row_bi = -1, row_p = -1;  // the append row of sequence row_bi (-1: none to write)
+  for (int k = 0; k < ntiles; ++k) {
+    const int st = k % kStages;
+    const uint32_t par = ((k / kStages) & 1) ^ 1;
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
+    if (fused) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (lane == 0 && !*sh.abort) give_up(sh, kSiteProducerEmpty, k);
+      break;
+    }
+    if (fused) {
+      if (cur.bi != row_bi) {
+        row_bi = cur.bi;
+        const int p = __ldg(P.pos + cur.bi);
+        row_p = (p >= 0 && p < P.n_max) ? p : -1;
+      }
+      if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
+        write_new_row<D>(P, cur.bi * P.g + cur.j, row_p, lane);
+        fence_proxy_async_global();  // each writer orders its store before the async proxy...
+        __syncwarp();                // ...and lane 0 issues the copy after every writer
+      }
+    }
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
+      const int z = cur.bi * P.g + cur.j;
+      const int y = cur.tile * kTileKeys;
+      uint8_t* kdst = sh.stages + st * kStageBytes;
+      uint8_t* vdst = kdst + kKvBytes;
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, tm_k, &sh.full[st], half * 64, y,
+                    z, policy);
+        tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, tm_v, &sh.full[st], half * 64, y,
+                    z, policy);
+      }
+    }
+    ++issued;
+    cur.advance(sh.pre, P.b, P.g);
+  }
+  if (lane != 0) return;
+  // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
+  const volatile int never = 0;
+  for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
+    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.timeout_ns, &never);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -684,61 +845,21 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   const int warp = tid >> 5, lane = tid & 31;
   const int B = P.b;
 
-  // ---- tiles per sequence and their exclusive prefix (every CTA computes the same) ----------
+  // ---- barriers, then the tiles of every sequence and their prefix ---------------------------
   __shared__ uint32_t part_sums[kThreads];
-  {
-    const int chunk = (B + kThreads - 1) / kThreads;
-    const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
-    uint32_t s = 0;
-    for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
-    part_sums[tid] = s;
-    if (tid == 0) {
-      *sh.abort = 0;
-      *sh.merge = 0;
-      for (int st = 0; st < kStages; ++st) {
-        mbar_init(&sh.full[st], 1);
-        mbar_init(&sh.empty[st], NW);
-      }
-      mbar_init(sh.cbar, NW * 32);
-      fence_barrier_init();
+  if (tid == 0) {
+    *sh.abort = 0;
+    *sh.merge = 0;
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&sh.full[st], 1);
+      mbar_init(&sh.empty[st], NW);
     }
-    __syncthreads();
-    if (warp == 0) {
-      // exclusive scan of the kThreads chunk sums: each lane takes kPer consecutive ones, the
-      // lanes' totals are scanned with shuffles
-      constexpr int kPer = kThreads / 32;
-      static_assert(kThreads % 32 == 0, "whole warps");
-      uint32_t loc[kPer], tot = 0;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) { loc[i] = part_sums[lane * kPer + i]; tot += loc[i]; }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      uint32_t run = incl - tot;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) { part_sums[lane * kPer + i] = run; run += loc[i]; }
-      if (lane == 31) sh.pre[B] = incl;
-    }
-    __syncthreads();
-    uint32_t run = part_sums[tid];
-    for (int i = lo; i < hi; ++i) {
-      sh.pre[i] = run;
-      run += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
-    }
-    __syncthreads();
+    mbar_init(sh.cbar, NW * 32);
+    fence_barrier_init();
   }
+  build_tile_prefix<kThreads>(P, sh, part_sums);
 
-  // ---- sequences with an out-of-range length: zero output, latch the error ------------------
-  for (int bi = blockIdx.x; bi < B; bi += P.num_ctas) {
-    const int L = __ldg(P.seq_lens + bi);
-    if (L >= 1 && L <= P.n_max) continue;
-    if (tid == 0) latch_status(kStatusDeviceBounds);
-    __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.h * D;
-    for (int e = tid; e < P.h * D; e += kThreads) ob[e] = __float2bfloat16_rn(0.f);
-  }
+  zero_invalid_sequences<D>(P, kThreads);
   if (P.pos != nullptr) append_uncovered_rows<D>(P, kThreads);
 
   const unsigned long long W = static_cast<unsigned long long>(P.g) * sh.pre[B];
@@ -756,63 +877,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   if (warp >= NW) {
     // ================================ producer ================================================
-    // Lane 0 issues the bulk copies; the whole warp runs only to write the fused append's rows.
-    if (warp != NW) return;
-    const bool fused = P.pos != nullptr;
-    if (!fused && lane != 0) return;
-    if (lane == 0) {
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
-    }
-    const uint64_t policy = l2_policy_evict_first();
-    TileCursor cur;
-    cur.start(x0, sh.pre, B, P.g);
-    int issued = 0;
-    int row_bi = -1, row_p = -1;  // the append row of sequence row_bi (-1: none to write)
-    for (int k = 0; k < ntiles; ++k) {
-      const int st = k % kStages;
-      const uint32_t par = ((k / kStages) & 1) ^ 1;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
-      if (fused) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) {
-        if (lane == 0 && !*sh.abort) give_up(sh);
-        break;
-      }
-      if (fused) {
-        if (cur.bi != row_bi) {
-          row_bi = cur.bi;
-          const int p = __ldg(P.pos + cur.bi);
-          row_p = (p >= 0 && p < P.n_max) ? p : -1;
-        }
-        if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
-          write_new_row<D>(P, cur.bi * P.g + cur.j, row_p, lane);
-          fence_proxy_async_global();  // each writer orders its store before the async proxy...
-          __syncwarp();                // ...and lane 0 issues the copy after every writer
-        }
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
-        const int z = cur.bi * P.g + cur.j;
-        const int y = cur.tile * kTileKeys;
-        uint8_t* kdst = sh.stages + st * kStageBytes;
-        uint8_t* vdst = kdst + kKvBytes;
-#pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, &tm_k, &sh.full[st], half * 64,
-                      y, z, policy);
-          tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, &tm_v, &sh.full[st], half * 64,
-                      y, z, policy);
-        }
-      }
-      ++issued;
-      cur.advance(sh.pre, B, P.g);
-    }
-    if (lane != 0) return;
-    // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
-    const volatile int never = 0;
-    for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-      mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.timeout_ns, &never);
+    if (warp == NW) produce_tiles<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
     return;
   }
 
@@ -829,7 +894,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
     if (!mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
-      if (!*sh.abort) give_up(sh);
+      if (!*sh.abort) give_up(sh, kSiteConsumerFull, k);
       return;
     }
     if (k == 0 || cur.tile == 0) {
@@ -874,28 +939,20 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       const bool complete = began_at_zero && seg_end;
       const int seg = cur.bi * P.g + cur.j;
       cons.publish(sh, warp, lane);
-      if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
-      combine_and_store<D, NW, CR>(P, sh, cur.bi, cur.j, complete, static_cast<int>(blockIdx.x) + seg,
-                               typename Consumer::Rows{});
+      if (!consumer_sync(sh, cphase, P.timeout_ns)) {
+        if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
+        return;
+      }
+      combine_and_store<D, NW, CR>(P, sh, cur.bi, cur.j, complete,
+                                   static_cast<int>(blockIdx.x) + seg, typename Consumer::Rows{});
       if (!complete) __threadfence();  // this CTA's partial is visible before it is counted
-      if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
-      if (!complete) {
-        const unsigned long long s0 = static_cast<unsigned long long>(P.g) * sh.pre[cur.bi] +
-                                      static_cast<unsigned long long>(cur.j) * cur.nt;
-        const SegmentPieces pc(s0, s0 + cur.nt - 1, W, P.num_ctas);
-        if (tid == 0) {
-          const unsigned int before = atomicAdd(P.seg_arrivals + seg, 1u);
-          *sh.merge = (before + 1u == pc.count()) ? 1 : 0;
-        }
-        if (!consumer_sync(sh, cphase, P.timeout_ns)) { if (!*sh.abort) give_up(sh); return; }
-        if (*sh.merge) {
-          __threadfence();
-          if (!merge_split_segment<D, NW, CR>(P, sh, cphase, cur.bi, cur.j, seg, pc)) {
-            if (!*sh.abort) give_up(sh);
-            return;
-          }
-          if (tid == 0) P.seg_arrivals[seg] = 0u;  // ready for the next call
-        }
+      if (!consumer_sync(sh, cphase, P.timeout_ns)) {
+        if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
+        return;
+      }
+      if (!complete && !finish_split_segment<D, NW, CR>(P, sh, cphase, cur.bi, cur.j, cur.nt, W)) {
+        if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
+        return;
       }
     }
     cur.advance(sh.pre, B, P.g);

@@ -12,6 +12,7 @@
 
 #include "../../include/mqa.h"
 #include "decode_attention.cuh"
+#include "decode_attention_tc.cuh"
 #include "kv_append.cuh"
 #include "status.cuh"
 
@@ -148,38 +149,63 @@ int device_info(int dev, DeviceInfo* info) {
 // ------------------------------------------------------------------------------------------------
 using AttnKernel = void (*)(const CUtensorMap, const CUtensorMap, const DecodeParams);
 
-// A kernel instance with the launch facts the host needs: consumer warps and combine rows.
+// The inner-product paths (mqa_debug_override's `path`): CUDA cores, mma.sync tensor cores, and
+// tcgen05 tensor cores with tensor-memory accumulators.
+enum Path { kPathAuto = 0, kPathCudaCores = 1, kPathMmaSync = 2, kPathTcgen05 = 3 };
+
+// Automatic choice. G < 8 (MHA-like grouping) has too few heads per K/V row for a contraction and
+// runs on CUDA cores. From G = 8 the heads of a group form a real matrix product and run on the
+// tensor cores; mma.sync is the automatic choice there, because the tcgen05 kernel (128-row MMA
+// tiles, accumulators in tensor memory) is not yet faster on any measured shape: its per-tile
+// hand-offs between the issuing thread and the softmax warps serialise the pipeline.
+Path auto_path(int G) { return G < 8 ? kPathCudaCores : kPathMmaSync; }
+
+// A kernel instance with the launch facts the host needs.
 struct AttnKernelChoice {
   AttnKernel fn = nullptr;
-  int nw = 0, cr = 0;
+  int threads = 0;
+  size_t smem = 0;
+  bool wide = false;  // eight consumer warps with a setmaxnreg split: check the register count
 };
 
 template <class Consumer, int D, bool TC, int WM>
-AttnKernelChoice choice() {
-  return {mqa::decode_attention_kernel<D, Consumer, TC, WM>, Consumer::kWarps, Consumer::kCombRows};
+AttnKernelChoice choice(int b) {
+  AttnKernelChoice c;
+  c.fn = mqa::decode_attention_kernel<D, Consumer, TC, WM>;
+  c.threads = mqa::threads_of(Consumer::kWarps);
+  c.smem = mqa::smem_bytes(D, Consumer::kWarps, Consumer::kCombRows, b);
+  c.wide = Consumer::kWarps == 8;
+  return c;
 }
 
 // Eight consumer warps (two per SM sub-partition) hide the latency of the per-tile dependency
 // chains of the CUDA-core path, where one warp per sub-partition leaves most issue slots idle. The
-// tensor-core path keeps four: its cost per tile is the mma.sync throughput itself, which a
-// second warp per sub-partition does not raise.
+// mma.sync path keeps four: its cost per tile is the mma.sync throughput itself, which a second
+// warp per sub-partition does not raise.
 template <int D>
-AttnKernelChoice pick_kernel(bool tensor_cores, int G) {
+AttnKernelChoice pick_kernel(Path path, int G, int b) {
   using mqa::CcConsumer;
   using mqa::MmaConsumer;
-  if (tensor_cores) {
-    if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, true, 1>();
-    if (G <= 32) return choice<MmaConsumer<D, 2, 4>, D, true, 2>();
-    return choice<MmaConsumer<D, 4, 4>, D, true, 4>();
+  if (path == kPathTcgen05) {
+    AttnKernelChoice c;
+    c.fn = mqa::decode_attention_tc_kernel<D>;
+    c.threads = mqa::kTcThreads;
+    c.smem = mqa::tc_smem_bytes(D, b);
+    return c;
+  }
+  if (path == kPathMmaSync) {
+    if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, true, 1>(b);
+    if (G <= 32) return choice<MmaConsumer<D, 2, 4>, D, true, 2>(b);
+    return choice<MmaConsumer<D, 4, 4>, D, true, 4>(b);
   }
   switch (G) {
-    case 1: return choice<CcConsumer<D, 1, 8>, D, false, 1>();
-    case 2: return choice<CcConsumer<D, 2, 8>, D, false, 1>();
-    case 3: return choice<CcConsumer<D, 3, 8>, D, false, 1>();
-    case 4: return choice<CcConsumer<D, 4, 8>, D, false, 1>();
-    case 5: return choice<CcConsumer<D, 5, 8>, D, false, 1>();
-    case 6: return choice<CcConsumer<D, 6, 8>, D, false, 1>();
-    case 7: return choice<CcConsumer<D, 7, 8>, D, false, 1>();
+    case 1: return choice<CcConsumer<D, 1, 8>, D, false, 1>(b);
+    case 2: return choice<CcConsumer<D, 2, 8>, D, false, 1>(b);
+    case 3: return choice<CcConsumer<D, 3, 8>, D, false, 1>(b);
+    case 4: return choice<CcConsumer<D, 4, 8>, D, false, 1>(b);
+    case 5: return choice<CcConsumer<D, 5, 8>, D, false, 1>(b);
+    case 6: return choice<CcConsumer<D, 6, 8>, D, false, 1>(b);
+    case 7: return choice<CcConsumer<D, 7, 8>, D, false, 1>(b);
     default: return {};
   }
 }
@@ -196,7 +222,7 @@ int prepare_kernel(int dev, const AttnKernelChoice& kc, size_t bytes) {
   const void* fn = reinterpret_cast<const void*>(kc.fn);
   auto it = g_smem_set.find({dev, fn});
   if (it == g_smem_set.end()) {
-    if (kc.nw == 8) {
+    if (kc.wide) {
       cudaFuncAttributes attr{};
       if (cudaFuncGetAttributes(&attr, fn) != cudaSuccess) return MQA_ERR_CUDA;
       if (attr.numRegs != mqa::kLaunchRegsWide) return MQA_ERR_UNSUPPORTED;
@@ -226,7 +252,7 @@ struct DecodePlan {
   const int32_t* pos = nullptr;
   int b, h, g, d_h, n_max, G;
   float scale;
-  bool tensor_cores;
+  Path path;
   cudaStream_t stream;
   int dev;
   long long bg, ctas;
@@ -256,8 +282,8 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
       static_cast<double>(bg) * n_max * d_h > 9.0e18)
     return MQA_ERR_UNSUPPORTED;
   const int force_path = g_force_path.load();
-  const bool tensor_cores = force_path == 0 ? (G >= 8) : (force_path == 2);
-  if (!tensor_cores && G > 7) return MQA_ERR_UNSUPPORTED;
+  const Path path = force_path == kPathAuto ? auto_path(G) : static_cast<Path>(force_path);
+  if (path == kPathCudaCores && G > 7) return MQA_ERR_UNSUPPORTED;
 
   // ---- device facts ----
   int dev = 0;
@@ -278,7 +304,7 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   p.q = q; p.k_cache = k_cache; p.v_cache = v_cache; p.seq_lens = seq_lens; p.out = out;
   p.b = b; p.h = h; p.g = g; p.d_h = d_h; p.n_max = n_max; p.G = G;
   p.scale = scale;
-  p.tensor_cores = tensor_cores;
+  p.path = path;
   p.stream = static_cast<cudaStream_t>(stream);
   p.dev = dev;
   p.bg = bg;
@@ -325,12 +351,11 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.k_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.k_cache)) : nullptr;
   P.v_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.v_cache)) : nullptr;
 
-  const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.tensor_cores, p.G)
-                                           : pick_kernel<64>(p.tensor_cores, p.G);
+  const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b)
+                                           : pick_kernel<64>(p.path, p.G, p.b);
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;
-  const size_t smem = mqa::smem_bytes(p.d_h, kc.nw, kc.cr, p.b);
-  if (int st = prepare_kernel(p.dev, kc, smem)) return st;
-  kc.fn<<<static_cast<unsigned>(p.ctas), mqa::threads_of(kc.nw), smem, p.stream>>>(tmk, tmv, P);
+  if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
+  kc.fn<<<static_cast<unsigned>(p.ctas), kc.threads, kc.smem, p.stream>>>(tmk, tmv, P);
   g_launches.fetch_add(1);
   return launch_error();
 }
@@ -388,7 +413,7 @@ const char* mqa_status_string(int status) {
 uint64_t mqa_kernel_launch_count(void) { return g_launches.load(); }
 
 int mqa_debug_override(int num_ctas, int path) {
-  if (num_ctas < 0 || path < 0 || path > 2) return MQA_ERR_INVALID_ARG;
+  if (num_ctas < 0 || path < 0 || path > 3) return MQA_ERR_INVALID_ARG;
   g_force_ctas.store(num_ctas);
   g_force_path.store(path);
   return MQA_OK;
@@ -409,6 +434,18 @@ int mqa_get_device_status(void* stream, int* status_out) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return MQA_ERR_CUDA;
   if (v == MQA_ERR_TIMEOUT) g_timeout_epoch.fetch_add(1);
   *status_out = v;
+  return MQA_OK;
+}
+
+int mqa_debug_timeout_site(int* site_out) {
+  if (!site_out) return MQA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MQA_ERR_CUDA;
+  int v[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(v, mqa::g_timeout_site, sizeof(v)) != cudaSuccess) return MQA_ERR_CUDA;
+  const int zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(mqa::g_timeout_site, zero, sizeof(zero)) != cudaSuccess)
+    return MQA_ERR_CUDA;
+  for (int i = 0; i < 4; ++i) site_out[i] = v[i];
   return MQA_OK;
 }
 

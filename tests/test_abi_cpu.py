@@ -33,6 +33,11 @@ def lib():
     L.mqa_debug_override.restype = i32
     L.mqa_debug_override.argtypes = [i32, i32]
     L.mqa_kernel_launch_count.restype = ctypes.c_uint64
+    L.mqa_decode_step.restype = i32
+    L.mqa_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                  ctypes.c_float, vp]
+    L.mqa_debug_timeout_site.restype = i32
+    L.mqa_debug_timeout_site.argtypes = [vp]
     return L
 
 
@@ -44,8 +49,8 @@ def declared_functions() -> list[str]:
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("mqa_kv_append", "mqa_decode_attention", "mqa_status_string",
-                     "mqa_get_device_status"):
+    for required in ("mqa_kv_append", "mqa_decode_attention", "mqa_decode_step",
+                     "mqa_status_string", "mqa_get_device_status"):
         assert required in names
 
 
@@ -112,8 +117,9 @@ def test_append_host_checks(lib, kw, code):
 
 def test_debug_override_validation(lib):
     assert lib.mqa_debug_override(-1, 0) == INVALID
-    assert lib.mqa_debug_override(0, 3) == INVALID
-    assert lib.mqa_debug_override(0, 0) == OK
+    assert lib.mqa_debug_override(0, 4) == INVALID     # paths are 0 (auto) .. 3 (tcgen05)
+    for path in (3, 2, 1, 0):
+        assert lib.mqa_debug_override(0, path) == OK
 
 
 def test_forced_cuda_core_path_rejects_large_groups(lib):
@@ -126,3 +132,26 @@ def test_forced_cuda_core_path_rejects_large_groups(lib):
 
 def test_device_status_needs_an_output(lib):
     assert lib.mqa_get_device_status(None, None) == INVALID
+
+
+def _step(lib, q=A, kn=A + 0x1000, vn=A + 0x2000, k=A + 0x3000, v=A + 0x4000, pos=A + 0x5000,
+          lens=A + 0x6000, out=A + 0x7000, b=2, h=8, g=2, d_h=128, n_max=100, scale=0.088):
+    return lib.mqa_decode_step(q, kn, vn, k, v, pos, lens, out, b, h, g, d_h, n_max, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    # the append's arguments ...
+    (dict(kn=0), INVALID), (dict(vn=0), INVALID), (dict(pos=0), INVALID),
+    (dict(kn=A + 8), INVALID), (dict(vn=A + 2), INVALID), (dict(pos=A + 0x5002), INVALID),
+    # ... and the attention's, checked the same way as mqa_decode_attention
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(lens=0), INVALID), (dict(out=0), INVALID),
+    (dict(b=0), INVALID), (dict(h=8, g=3), INVALID), (dict(scale=math.nan), INVALID),
+    (dict(k=A + 4), INVALID),
+    (dict(d_h=96), UNSUPPORTED), (dict(h=128, g=1), UNSUPPORTED), (dict(b=8193), UNSUPPORTED),
+])
+def test_fused_step_host_checks(lib, kw, code):
+    assert _step(lib, **kw) == code
+
+
+def test_timeout_site_rejects_null(lib):
+    assert lib.mqa_debug_timeout_site(None) == INVALID

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
 
 Small cases span several 64-row tiles with ragged tails, both head dimensions, every kernel
-family (CUDA-core G = 1..7, tensor-core G = 8..64) and rows past each sequence's length poisoned
-with NaN. Append is compared bit for bit over the whole cache.
+family (CUDA cores G = 1..7, mma.sync G = 8..64, tcgen05 G = 1..64 when forced) and rows past each sequence's length poisoned with NaN. Append is compared
+bit for bit over the whole cache.
 """
 from __future__ import annotations
 
@@ -53,12 +53,13 @@ def test_append_and_attention_match_oracle(mqa, shape):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
-@pytest.mark.parametrize("shape", [(2, 16, 2, 128, 0, 700), (3, 8, 4, 64, 100, 400)],
-                         ids=["mma", "cuda_cores"])
-def test_any_cta_split_gives_the_same_result(mqa, shape, ctas):
+@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 0),
+                                        ((2, 64, 2, 128, 0, 700), 3), ((2, 16, 2, 128, 0, 700), 3)],
+                         ids=["mma_sync", "cuda_cores", "tcgen05", "tcgen05_G8"])
+def test_any_cta_split_gives_the_same_result(mqa, shape, path, ctas):
     case = P.make_case(*shape, seed_id=200)
     _, _, out_ref = P.oracle_step(case)
-    mqa.debug_override(ctas, 0)
+    mqa.debug_override(ctas, path)
     try:
         _, _, out = P.gpu_step(case, mqa)
         assert mqa.get_device_status() == 0
@@ -67,21 +68,48 @@ def test_any_cta_split_gives_the_same_result(mqa, shape, ctas):
     P.assert_close(out, out_ref, f"{shape} ctas={ctas}")
 
 
+@pytest.mark.parametrize("path", [2, 3], ids=["mma_sync", "tcgen05"])
 @pytest.mark.parametrize("shape", [(2, 4, 1, 128, 10, 300), (3, 2, 2, 64, 0, 200),
                                    (2, 7, 1, 64, 60, 140)])
-def test_tensor_core_path_also_serves_small_groups(mqa, shape):
+def test_tensor_core_paths_also_serve_small_groups(mqa, shape, path):
     case = P.make_case(*shape, seed_id=300)
     _, _, out_ref = P.oracle_step(case)
-    mqa.debug_override(0, 2)
+    mqa.debug_override(0, path)
     try:
         _, _, out = P.gpu_step(case, mqa)
         assert mqa.get_device_status() == 0
     finally:
         mqa.debug_override(0, 0)
-    P.assert_close(out, out_ref, f"{shape} forced tensor cores")
+    P.assert_close(out, out_ref, f"{shape} forced path {path}")
 
 
-@pytest.mark.parametrize("path", [1, 2])
+TC_SHAPES = [
+    # b, h, g, d_h, ctx_lo, ctx_hi: G = 8 .. 64 on both tensor-core paths
+    (2, 16, 2, 128, 1, 900),     # G = 8
+    (2, 24, 2, 64, 100, 700),    # G = 12
+    (2, 32, 2, 128, 50, 1000),   # G = 16
+    (3, 24, 1, 128, 1, 400),     # G = 24
+    (2, 32, 1, 64, 500, 1300),   # G = 32, d_h = 64
+    (2, 96, 2, 128, 60, 300),    # G = 48
+    (2, 64, 1, 128, 0, 2100),    # G = 64
+]
+
+
+@pytest.mark.parametrize("path", [2, 3], ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "b{}h{}g{}d{}_{}-{}".format(*s))
+def test_both_tensor_core_paths_at_every_group_size(mqa, shape, path):
+    case = P.make_case(*shape, seed_id=310 + TC_SHAPES.index(shape))
+    _, _, out_ref = P.oracle_step(case)
+    mqa.debug_override(0, path)
+    try:
+        _, _, out = P.gpu_step(case, mqa)
+        assert mqa.get_device_status() == 0
+    finally:
+        mqa.debug_override(0, 0)
+    P.assert_close(out, out_ref, f"{shape} path {path}")
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_unit_values_give_exactly_one(mqa, path):
     b, h, g, d_h = 2, 8, 2, 128
     case = P.make_case(b, h, g, d_h, 50, 600, seed_id=400)
@@ -95,7 +123,7 @@ def test_unit_values_give_exactly_one(mqa, path):
     assert np.all(P.bits(out) == 0x3F80)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_length_one_returns_the_appended_value(mqa, path):
     case = P.make_case(3, 8, 2, 64, 0, 0, seed_id=401)
     mqa.debug_override(0, path)
@@ -108,7 +136,7 @@ def test_length_one_returns_the_appended_value(mqa, path):
     assert np.array_equal(P.bits(out), expect)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_identical_queries_in_a_group_give_identical_outputs(mqa, path):
     case = P.make_case(2, 8, 2, 128, 100, 900, seed_id=402)
     q = case["q"].clone()
@@ -124,13 +152,34 @@ def test_identical_queries_in_a_group_give_identical_outputs(mqa, path):
     assert np.array_equal(ob[:, 1], ob[:, 0]) and np.array_equal(ob[:, 7], ob[:, 5])
 
 
-def test_peaked_attention_large_scale(mqa):
-    # scale 1.0 instead of 1/sqrt(d_h): logits spread over about +-40, softmax nearly one-hot
-    case = P.make_case(2, 16, 2, 128, 200, 900, seed_id=403)
+@pytest.mark.parametrize("shape", [(2, 16, 2, 128, 200, 900), (2, 64, 2, 128, 200, 900)],
+                         ids=["G8", "G32"])
+def test_peaked_attention_large_scale(mqa, shape):
+    # scale 1.0 instead of 1/sqrt(d_h): logits spread over about +-40, softmax nearly one-hot; on
+    # the tcgen05 path the running reference is raised (and O rescaled) many times
+    case = P.make_case(*shape, seed_id=403)
     case["scale"] = 1.0
     _, _, out_ref = P.oracle_step(case)
     _, _, out = P.gpu_step(case, mqa)
     P.assert_close(out, out_ref, "scale 1.0")
+
+
+def test_growing_logits_force_rescales(mqa):
+    # keys scaled up along the sequence, so the row maximum keeps rising tile after tile
+    case = P.make_case(2, 32, 1, 128, 600, 1500, seed_id=404, tail="nan")
+    k = case["k"].float()
+    ramp = torch.linspace(0.2, 3.0, k.shape[2]).view(1, 1, -1, 1)
+    case["k"] = (k * ramp).to(torch.bfloat16)
+    case["scale"] = 0.25
+    _, _, out_ref = P.oracle_step(case)
+    for path in (2, 3):
+        mqa.debug_override(0, path)
+        try:
+            _, _, out = P.gpu_step(case, mqa)
+            assert mqa.get_device_status() == 0
+        finally:
+            mqa.debug_override(0, 0)
+        P.assert_close(out, out_ref, f"growing logits, path {path}")
 
 
 def test_out_of_range_lengths_latch_an_error_and_write_zeros(mqa):
