@@ -80,14 +80,14 @@ struct DecodeParams {
 __host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
 __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 
-// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort][prefix(b+1)].
+// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags].
 // CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
 __host__ __device__ constexpr int smem_fixed_bytes(int D, int NW, int CR) {
   return kStages * stage_bytes(D) + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * kStages + 1) * 8 + 16;  // + abort, merge flag
 }
-__host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR, int b) {
-  return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR)) + static_cast<size_t>(b + 1) * 4;
+__host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR) {
+  return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR));
 }
 
 __device__ __forceinline__ int tiles_of_length(int L, int n_max) {
@@ -147,29 +147,62 @@ __device__ __forceinline__ void write_new_row(const DecodeParams& P, int seg, in
   else if (lane < 2 * CH) P.v_rows[dst + lane - CH] = __ldg(P.v_new + src + lane - CH);
 }
 
+// The tile count of every sequence as the CTAs see it: the exclusive prefix `cs` of the tile sums
+// of nchunks chunks of `chunk` consecutive sequences (computed by each CTA in shared memory), and
+// the lengths themselves for the tiles of one sequence.
+struct TileIndex {
+  const uint32_t* cs;   // [nchunks + 1]; cs[nchunks] = tiles of all sequences (per KV head)
+  int chunk, nchunks;
+  const int32_t* seq_lens;
+  int B, g, n_max;
+  __device__ __forceinline__ int tiles(int bi) const {
+    return tiles_of_length(__ldg(seq_lens + bi), n_max);
+  }
+  // W: tiles of all segments
+  __device__ __forceinline__ unsigned long long total() const {
+    return static_cast<unsigned long long>(g) * cs[nchunks];
+  }
+};
+
 // Walks the tiles of one CTA's range in segment order.
 struct TileCursor {
   int bi, j, tile, nt;
-  __device__ __forceinline__ void start(unsigned long long x, const uint32_t* pre, int B, int g) {
-    // largest bi with g * pre[bi] <= x (that sequence then has at least one tile)
-    int lo = 0, hi = B - 1;
+  uint32_t pre;  // tiles of the sequences before bi (per KV head): segment (bi, j) starts at
+                 // global tile g * pre + j * nt
+  __device__ __forceinline__ void start(unsigned long long x, const TileIndex& ix) {
+    const unsigned long long g = static_cast<unsigned long long>(ix.g);
+    // the chunk holding tile x: the largest c with g * cs[c] <= x (it has tiles past x)
+    int lo = 0, hi = ix.nchunks - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (static_cast<unsigned long long>(g) * pre[mid] <= x) lo = mid; else hi = mid - 1;
+      if (g * ix.cs[mid] <= x) lo = mid; else hi = mid - 1;
     }
-    bi = lo;
-    nt = static_cast<int>(pre[bi + 1] - pre[bi]);
-    const unsigned long long rem = x - static_cast<unsigned long long>(g) * pre[bi];
+    uint32_t run = ix.cs[lo];
+    int i = lo * ix.chunk;
+    const int end = min(i + ix.chunk, ix.B);
+    int t = 0;
+    for (; i < end; ++i) {
+      t = ix.tiles(i);
+      if (g * (run + t) > x) break;
+      run += t;
+    }
+    bi = min(i, ix.B - 1);
+    pre = run;
+    nt = max(ix.tiles(bi), 1);
+    const unsigned long long rem = x - g * run;
     j = static_cast<int>(rem / nt);
     tile = static_cast<int>(rem % nt);
   }
-  __device__ __forceinline__ void advance(const uint32_t* pre, int B, int g) {
+  __device__ __forceinline__ void advance(const TileIndex& ix) {
     if (++tile < nt) return;
     tile = 0;
-    if (++j < g) return;
+    if (++j < ix.g) return;
     j = 0;
-    do { ++bi; } while (bi < B && pre[bi + 1] == pre[bi]);
-    nt = bi < B ? static_cast<int>(pre[bi + 1] - pre[bi]) : 0;
+    pre += nt;
+    do {
+      ++bi;
+      nt = bi < ix.B ? ix.tiles(bi) : 0;
+    } while (bi < ix.B && nt == 0);
   }
 };
 
@@ -182,7 +215,7 @@ struct SharedLayout {
   uint64_t* cbar;       // consumer-wide barrier
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
-  uint32_t* pre;        // [b + 1] tiles before each sequence
+  TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
 template <int D, int NW, int CR>
@@ -203,7 +236,6 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.abort = reinterpret_cast<volatile int*>(p);
   s.merge = s.abort + 1;
   p += 16;
-  s.pre = reinterpret_cast<uint32_t*>(p);
   return s;
 }
 
@@ -368,11 +400,12 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
 // ---------------------------------------------------------------------------------------------
 template <int D, int NW, int CR>
 __device__ __forceinline__ bool finish_split_segment(const DecodeParams& P, const SharedLayout& sh,
-                                                     uint32_t& cphase, int bi, int j, int nt,
+                                                     uint32_t& cphase, const TileCursor& cur,
                                                      unsigned long long W) {
+  const int bi = cur.bi, j = cur.j, nt = cur.nt;
   const int seg = bi * P.g + j;
-  const unsigned long long s0 =
-      static_cast<unsigned long long>(P.g) * sh.pre[bi] + static_cast<unsigned long long>(j) * nt;
+  const unsigned long long s0 = static_cast<unsigned long long>(P.g) * cur.pre +
+                                static_cast<unsigned long long>(j) * nt;
   const SegmentPieces pc(s0, s0 + nt - 1, W, P.num_ctas);
   if (threadIdx.x == 0) {
     // The partial rows were stored by many threads, ordered before this point by their fences and
@@ -394,20 +427,21 @@ __device__ __forceinline__ bool finish_split_segment(const DecodeParams& P, cons
 }
 
 // ---------------------------------------------------------------------------------------------
-// Prologue shared by the kernels: the tiles of every sequence and their exclusive prefix, which
-// every CTA computes for itself into sh.pre[0 .. b] (so W = g * pre[b]). Ends with a CTA-wide
-// barrier, which also publishes barrier initialisation done before the call.
+// Prologue shared by the kernels: thread t sums the tiles of sequences [t * chunk, (t+1) * chunk)
+// and the sums are scanned into sh.tix.cs[0 .. kThreads] (shared memory the caller provides), so
+// that every CTA knows W and can find its tiles. Ends with a CTA-wide barrier, which also
+// publishes barrier initialisation done before the call.
 // ---------------------------------------------------------------------------------------------
 template <int kThreads>
-__device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, const SharedLayout& sh,
-                                                  uint32_t* part_sums) {
+__device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, SharedLayout& sh,
+                                                  uint32_t* cs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = P.b;
   const int chunk = (B + kThreads - 1) / kThreads;
   const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
   uint32_t s = 0;
   for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
-  part_sums[tid] = s;
+  cs[tid] = s;
   __syncthreads();
   if (warp == 0) {
     // exclusive scan of the kThreads chunk sums: each lane takes kPer consecutive ones, the lanes'
@@ -416,7 +450,7 @@ __device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, const S
     static_assert(kThreads % 32 == 0, "whole warps");
     uint32_t loc[kPer], tot = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) { loc[i] = part_sums[lane * kPer + i]; tot += loc[i]; }
+    for (int i = 0; i < kPer; ++i) { loc[i] = cs[lane * kPer + i]; tot += loc[i]; }
     uint32_t incl = tot;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -425,16 +459,17 @@ __device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, const S
     }
     uint32_t run = incl - tot;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) { part_sums[lane * kPer + i] = run; run += loc[i]; }
-    if (lane == 31) sh.pre[B] = incl;
+    for (int i = 0; i < kPer; ++i) { cs[lane * kPer + i] = run; run += loc[i]; }
+    if (lane == 31) cs[kThreads] = incl;
   }
   __syncthreads();
-  uint32_t run = part_sums[tid];
-  for (int i = lo; i < hi; ++i) {
-    sh.pre[i] = run;
-    run += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
-  }
-  __syncthreads();
+  sh.tix.cs = cs;
+  sh.tix.chunk = max(chunk, 1);
+  sh.tix.nchunks = kThreads;
+  sh.tix.seq_lens = P.seq_lens;
+  sh.tix.B = B;
+  sh.tix.g = P.g;
+  sh.tix.n_max = P.n_max;
 }
 
 // Sequences whose length is out of range get a zero output and latch MQA_ERR_DEVICE_BOUNDS.
@@ -469,7 +504,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   }
   const uint64_t policy = l2_policy_evict_first();
   TileCursor cur;
-  cur.start(x0, sh.pre, P.b, P.g);
+  cur.start(x0, sh.tix);
   int issued = 0;
   int row_bi = -1, row_p = -1;  // the append row of sequence row_bi (-1: none to write)
   for (int k = 0; k < ntiles; ++k) {
@@ -509,7 +544,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
       }
     }
     ++issued;
-    cur.advance(sh.pre, P.b, P.g);
+    cur.advance(sh.tix);
   }
   if (lane != 0) return;
   // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
@@ -840,13 +875,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   constexpr int CR = Consumer::kCombRows;
   constexpr int kThreads = threads_of(NW);
   extern __shared__ uint8_t smem_raw[];
-  const SharedLayout sh = carve_shared<D, NW, CR>(smem_raw);
+  SharedLayout sh = carve_shared<D, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int B = P.b;
 
   // ---- barriers, then the tiles of every sequence and their prefix ---------------------------
-  __shared__ uint32_t part_sums[kThreads];
+  __shared__ uint32_t chunk_tiles[kThreads + 1];
   if (tid == 0) {
     *sh.abort = 0;
     *sh.merge = 0;
@@ -857,12 +891,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     mbar_init(sh.cbar, NW * 32);
     fence_barrier_init();
   }
-  build_tile_prefix<kThreads>(P, sh, part_sums);
+  build_tile_prefix<kThreads>(P, sh, chunk_tiles);
 
   zero_invalid_sequences<D>(P, kThreads);
   if (P.pos != nullptr) append_uncovered_rows<D>(P, kThreads);
 
-  const unsigned long long W = static_cast<unsigned long long>(P.g) * sh.pre[B];
+  const unsigned long long W = sh.tix.total();
   const unsigned long long x0 = W * blockIdx.x / P.num_ctas;
   const unsigned long long x1 = W * (blockIdx.x + 1) / P.num_ctas;
   if (x0 >= x1) return;
@@ -888,7 +922,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / NW : kTileKeys / NW;
   uint32_t cphase = 0;
   TileCursor cur;
-  cur.start(x0, sh.pre, B, P.g);
+  cur.start(x0, sh.tix);
   int L = 0;
   bool began_at_zero = false;
   for (int k = 0; k < ntiles; ++k) {
@@ -950,12 +984,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
         return;
       }
-      if (!complete && !finish_split_segment<D, NW, CR>(P, sh, cphase, cur.bi, cur.j, cur.nt, W)) {
+      if (!complete && !finish_split_segment<D, NW, CR>(P, sh, cphase, cur, W)) {
         if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
         return;
       }
     }
-    cur.advance(sh.pre, B, P.g);
+    cur.advance(sh.tix);
   }
 }
 

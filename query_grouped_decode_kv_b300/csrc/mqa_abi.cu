@@ -173,7 +173,7 @@ AttnKernelChoice choice(int b) {
   AttnKernelChoice c;
   c.fn = mqa::decode_attention_kernel<D, Consumer, TC, WM>;
   c.threads = mqa::threads_of(Consumer::kWarps);
-  c.smem = mqa::smem_bytes(D, Consumer::kWarps, Consumer::kCombRows, b);
+  c.smem = mqa::smem_bytes(D, Consumer::kWarps, Consumer::kCombRows);
   c.wide = Consumer::kWarps == 8;
   return c;
 }
@@ -187,10 +187,13 @@ AttnKernelChoice pick_kernel(Path path, int G, int b) {
   using mqa::CcConsumer;
   using mqa::MmaConsumer;
   if (path == kPathTcgen05) {
+    // the group's heads padded to 16, 32 or 64 rows of the 128-row MMA tile
     AttnKernelChoice c;
-    c.fn = mqa::decode_attention_tc_kernel<D>;
+    c.fn = G <= 16 ? mqa::decode_attention_tc_kernel<D, 16>
+                   : (G <= 32 ? mqa::decode_attention_tc_kernel<D, 32>
+                              : mqa::decode_attention_tc_kernel<D, 64>);
     c.threads = mqa::kTcThreads;
-    c.smem = mqa::tc_smem_bytes(D, b);
+    c.smem = mqa::tc_smem_bytes(D);
     return c;
   }
   if (path == kPathMmaSync) {
