@@ -48,8 +48,12 @@ METRIC = "decode-attention µs/step and KV-cache GB/s as % of B300 HBM peak"
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6400.0
 KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
+                  "query_grouped_decode_kv_b300/csrc/decode_attention_tc.cuh",
+                  "query_grouped_decode_kv_b300/csrc/kv_append.cuh",
                   "query_grouped_decode_kv_b300/csrc/ptx.cuh",
-                  "query_grouped_decode_kv_b300/csrc/mqa_abi.cu"]
+                  "query_grouped_decode_kv_b300/csrc/status.cuh",
+                  "query_grouped_decode_kv_b300/csrc/mqa_abi.cu",
+                  "include/mqa.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
 
 
