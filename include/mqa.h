@@ -203,10 +203,27 @@ MQA_API int mqa_get_device_status(void* stream, int* status_out);
  * consumer-wide barrier, 4 the tcgen05 issuer waiting for Q, 5 ... for a stage's copy, 6 ... for P,
  * 7 the softmax warps waiting for S, 8 ... for O before a rescale, 9 ... for a stage's copy,
  * 10 ... for the last O of a segment, 11 the issuer draining its MMAs, 12 the issuer waiting for
- * the softmax warps at exit, 13 the issuer waiting for the P V product that last read an S buffer); site_out[1] the tile index within the CTA's range, site_out[2] the
+ * the softmax warps at exit, 13 the issuer waiting for the P V product that last read an S buffer,
+ * 14 the testing stall of mqa_debug_stall); site_out[1] the tile index within the CTA's range, site_out[2] the
  * CTA, site_out[3] the thread. Returns MQA_OK, MQA_ERR_INVALID_ARG (NULL) or MQA_ERR_CUDA.
  */
 MQA_API int mqa_debug_timeout_site(int* site_out);
+
+/*
+ * Testing hooks for failure detection (process-wide).
+ *
+ * mqa_debug_set_wait_limit_ns: the limit, in nanoseconds, after which an in-kernel wait gives up
+ * and the launch reports MQA_ERR_TIMEOUT (0 restores the default of one second). The waits for a
+ * CTA's own copies and MMAs still in flight when it stops keep the one-second limit, so a launch
+ * that gave up leaves nothing running. Returns MQA_OK.
+ *
+ * mqa_debug_stall: with on = 1, the consumer warps of every following attention launch first wait
+ * on a barrier that nothing completes, so that wait runs out after the wait limit and the launch
+ * reports MQA_ERR_TIMEOUT at site 14 (a flag nothing sets; no fault and no hang). on = 0 turns it
+ * off. Returns MQA_OK, or MQA_ERR_INVALID_ARG for another value.
+ */
+MQA_API int mqa_debug_set_wait_limit_ns(uint64_t ns);
+MQA_API int mqa_debug_stall(int on);
 
 /* Number of kernels this library has launched in this process (all devices, all streams). */
 MQA_API uint64_t mqa_kernel_launch_count(void);

@@ -9,7 +9,7 @@ from __future__ import annotations
 
 _BINDING_NAMES = {
     "kv_append", "decode_attention", "decode_step", "get_device_status", "status_string", "MqaError",
-    "library_path", "kernel_launch_count", "debug_override", "debug_timeout_site", "raw",
+    "library_path", "kernel_launch_count", "debug_override", "debug_timeout_site", "debug_set_wait_limit_ns", "debug_stall", "raw",
 }
 
 

@@ -40,6 +40,10 @@ _lib.mqa_kernel_launch_count.restype = ctypes.c_uint64
 _lib.mqa_kernel_launch_count.argtypes = []
 _lib.mqa_debug_timeout_site.restype = _i32
 _lib.mqa_debug_timeout_site.argtypes = [ctypes.POINTER(_i32)]
+_lib.mqa_debug_stall.restype = _i32
+_lib.mqa_debug_stall.argtypes = [_i32]
+_lib.mqa_debug_set_wait_limit_ns.restype = _i32
+_lib.mqa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
 _lib.mqa_debug_override.restype = _i32
 _lib.mqa_debug_override.argtypes = [_i32, _i32]
 
@@ -83,6 +87,21 @@ def debug_timeout_site() -> tuple[int, int, int, int]:
     if st:
         raise MqaError(st, "mqa_debug_timeout_site")
     return tuple(int(x) for x in out)
+
+
+def debug_set_wait_limit_ns(ns: int = 0) -> None:
+    """Testing hook: in-kernel wait limit in nanoseconds (0 = the default of one second)."""
+    st = _lib.mqa_debug_set_wait_limit_ns(int(ns))
+    if st:
+        raise MqaError(st, "mqa_debug_set_wait_limit_ns")
+
+
+def debug_stall(on: bool) -> None:
+    """Testing hook: make the consumer warps of following launches wait on a barrier nothing
+    completes, so each launch times out after the wait limit."""
+    st = _lib.mqa_debug_stall(1 if on else 0)
+    if st:
+        raise MqaError(st, "mqa_debug_stall")
 
 
 def _stream_handle(stream) -> int:

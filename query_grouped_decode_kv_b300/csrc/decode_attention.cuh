@@ -67,7 +67,9 @@ struct DecodeParams {
   int b, h, g, G, n_max;
   int num_ctas;               // P
   float scale_log2;           // scale * log2(e)
-  unsigned long long timeout_ns;
+  unsigned long long timeout_ns;  // limit of every in-kernel wait
+  unsigned long long drain_ns;    // limit of the waits for a CTA's own work in flight at exit
+  int debug_stall;                // testing: consumers first wait on a barrier nothing completes
   // Fused append (mqa_decode_step): this step's K/V rows, written at row pos[bi] of the caches
   // before any tile holding that row is loaded. All null when the call only attends.
   const int32_t* pos;         // [b]
@@ -84,7 +86,7 @@ __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 // CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
 __host__ __device__ constexpr int smem_fixed_bytes(int D, int NW, int CR) {
   return kStages * stage_bytes(D) + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
-         (2 * kStages + 1) * 8 + 16;  // + abort, merge flag
+         (2 * kStages + 2) * 8 + 16;  // full, empty, cbar, stall; abort, merge flags
 }
 __host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR) {
   return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR));
@@ -213,6 +215,7 @@ struct SharedLayout {
   uint64_t* full;       // [kStages]
   uint64_t* empty;      // [kStages]
   uint64_t* cbar;       // consumer-wide barrier
+  uint64_t* stall;      // testing: a barrier nothing completes (DecodeParams::debug_stall)
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
@@ -232,7 +235,8 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.full = reinterpret_cast<uint64_t*>(p);
   s.empty = s.full + kStages;
   s.cbar = s.empty + kStages;
-  p += (2 * kStages + 1) * 8;
+  s.stall = s.cbar + 1;
+  p += (2 * kStages + 2) * 8;
   s.abort = reinterpret_cast<volatile int*>(p);
   s.merge = s.abort + 1;
   p += 16;
@@ -550,7 +554,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
   const volatile int never = 0;
   for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.timeout_ns, &never);
+    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -889,6 +893,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       mbar_init(&sh.empty[st], NW);
     }
     mbar_init(sh.cbar, NW * 32);
+    mbar_init(sh.stall, 1);
     fence_barrier_init();
   }
   build_tile_prefix<kThreads>(P, sh, chunk_tiles);
@@ -925,6 +930,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   cur.start(x0, sh.tix);
   int L = 0;
   bool began_at_zero = false;
+  if (P.debug_stall && !mbar_wait_bounded(sh.stall, 0, P.timeout_ns, sh.abort)) {
+    if (!*sh.abort) give_up(sh, kSiteStall, 0);
+    return;
+  }
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
     if (!mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {

@@ -67,7 +67,7 @@ static_assert(tc_k_stages(128) >= kTcBufs && tc_k_stages(64) >= kTcBufs,
 
 __host__ __device__ constexpr int tc_q_bytes(int D) { return kTcRows * D * 2; }
 __host__ __device__ constexpr int tc_barrier_count(int D) {
-  return 2 * tc_k_stages(D) + 2 * tc_v_stages(D) + 1 + 3 * kTcBufs + 4;
+  return 2 * tc_k_stages(D) + 2 * tc_v_stages(D) + 1 + 3 * kTcBufs + 5;
 }
 // shared scratch: the epilogue's [128][kTcStageStride] staging, or merge_split_segment's
 // 4 x kTcMergeRows rows of comb_row_floats(D)
@@ -130,6 +130,7 @@ __device__ __forceinline__ TcShared carve_tc_shared(uint8_t* raw) {
   t.q_full = t.pv_done + kTcBufs;
   t.tmem_done = t.q_full + 1;
   t.drain = t.tmem_done + 1;
+  t.base.stall = t.drain + 1;
   p += tc_barrier_count(D) * 8;
   t.base.abort = reinterpret_cast<volatile int*>(p);
   t.base.merge = t.base.abort + 1;
@@ -306,6 +307,11 @@ __device__ __forceinline__ bool tc_softmax_loop(const DecodeParams& P, const TcS
   float m_ref = -INFINITY, l = 0.f;
   int L = 0;
   bool began_at_zero = false;
+  if (P.debug_stall) {
+    const bool ok = mbar_wait_bounded(b.stall, 0, P.timeout_ns, b.abort);
+    if (!ok && !*b.abort) give_up(b, kSiteStall, 0);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+  }
   for (int k = 0; k < ntiles; ++k) {
     const bool first = (k == 0 || cur.tile == 0);
     if (first) {
@@ -581,9 +587,9 @@ __device__ __forceinline__ void tc_produce_tiles(const CUtensorMap* tm_k, const 
   // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
   const volatile int never = 0;
   for (int i = kk > NK ? kk - NK : 0; i < kk; ++i)
-    mbar_wait_bounded(&b.full[i % NK], (i / NK) & 1, P.timeout_ns, &never);
+    mbar_wait_bounded(&b.full[i % NK], (i / NK) & 1, P.drain_ns, &never);
   for (int i = kv > NV ? kv - NV : 0; i < kv; ++i)
-    mbar_wait_bounded(&sh.v_full[i % NV], (i / NV) & 1, P.timeout_ns, &never);
+    mbar_wait_bounded(&sh.v_full[i % NV], (i / NV) & 1, P.drain_ns, &never);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -625,6 +631,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(sh.q_full, 128);
     mbar_init(sh.tmem_done, 128);
     mbar_init(sh.drain, 1);
+    mbar_init(b.stall, 1);
     fence_barrier_init();
   }
   // rows of heads G .. GP-1 of every copy stay zero for the whole launch; the CTA-wide barrier
@@ -665,8 +672,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_issue_loop<D>(P, sh, tmem, x0, ntiles);
       // every MMA issued has finished, and the softmax warps are done, before the columns go
       umma_commit(sh.drain);
-      if (!mbar_wait_bounded(sh.drain, 0, P.timeout_ns, &never)) give_up(b, kSiteDrain, ntiles);
-      if (!mbar_wait_bounded(sh.tmem_done, 0, 3 * P.timeout_ns, &never))
+      if (!mbar_wait_bounded(sh.drain, 0, P.drain_ns, &never)) give_up(b, kSiteDrain, ntiles);
+      if (!mbar_wait_bounded(sh.tmem_done, 0, P.drain_ns + 2 * P.timeout_ns, &never))
         give_up(b, kSiteTmemDone, ntiles);
     }
     __syncwarp();

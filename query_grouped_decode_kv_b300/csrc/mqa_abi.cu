@@ -28,6 +28,10 @@ std::atomic<int> g_force_ctas{0};
 std::atomic<int> g_force_path{0};
 
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+// The in-kernel wait limit in force (testing hook: mqa_debug_set_wait_limit_ns); the waits for a
+// CTA's own copies and MMAs in flight at exit always keep kWaitLimitNs.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<int> g_debug_stall{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -346,7 +350,9 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.n_max = p.n_max;
   P.num_ctas = static_cast<int>(p.ctas);
   P.scale_log2 = p.scale * 1.4426950408889634f;
-  P.timeout_ns = kWaitLimitNs;
+  P.timeout_ns = g_wait_limit_ns.load();
+  P.drain_ns = kWaitLimitNs;
+  P.debug_stall = g_debug_stall.load();
   P.pos = p.pos;
   P.k_new = reinterpret_cast<const uint4*>(p.k_new);
   P.v_new = reinterpret_cast<const uint4*>(p.v_new);
@@ -437,6 +443,17 @@ int mqa_get_device_status(void* stream, int* status_out) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return MQA_ERR_CUDA;
   if (v == MQA_ERR_TIMEOUT) g_timeout_epoch.fetch_add(1);
   *status_out = v;
+  return MQA_OK;
+}
+
+int mqa_debug_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kWaitLimitNs : ns);
+  return MQA_OK;
+}
+
+int mqa_debug_stall(int on) {
+  if (on != 0 && on != 1) return MQA_ERR_INVALID_ARG;
+  g_debug_stall.store(on);
   return MQA_OK;
 }
 

@@ -30,6 +30,7 @@ enum TimeoutSite : int {
   kSiteDrain = 11,          // tcgen05 issuer at exit: its MMAs
   kSiteTmemDone = 12,       // tcgen05 issuer at exit: the softmax warps
   kSiteMmaPv = 13,          // tcgen05 issuer: O += P V of the tile whose S buffer it reuses
+  kSiteStall = 14,          // consumers: the testing stall (a barrier nothing completes)
 };
 __device__ int g_timeout_site[4] = {0, 0, 0, 0};
 
