@@ -55,6 +55,7 @@ static_assert(2 * 32 * kConsumerRegs + 32 * kProducerRegs <= 16384,
               "two consumer warps and one producer warp share a sub-partition's registers");
 constexpr int kMaxBatch = 8192;
 constexpr int kMaxGroup = 64;       // largest G = h / g served
+constexpr float kLazyLog2 = 8.f;    // softmax reference slack (log2 units), see MmaConsumer::tile
 constexpr int kSwizzleRowBytes = 128;
 
 struct DecodeParams {
@@ -636,12 +637,15 @@ struct MmaConsumer {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-    const float ref0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float ref1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float al0 = fast_exp2(m[0] - ref0), al1 = fast_exp2(m[1] - ref1);
-    m[0] = mn0;
-    m[1] = mn1;
+    // lazy reference: a row's reference m is raised (and its O and l rescaled) only when the
+    // tile's maximum exceeds it by more than kLazyLog2, so most tiles leave O untouched and the
+    // weights stay below 2^kLazyLog2. A row with no valid key yet keeps m = -inf.
+    const bool up0 = mx0 > m[0] + kLazyLog2, up1 = mx1 > m[1] + kLazyLog2;
+    float al0 = 1.f, al1 = 1.f;
+    if (up0) { al0 = fast_exp2(m[0] - mx0); m[0] = mx0; }  // 0 when m was -inf
+    if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
+    const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
+    const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
     // weights, rounded to bf16 once: the same rounded values feed P V and the running sum, so
     // the normalised weights still add up to one
     float ps0 = 0.f, ps1 = 0.f;
@@ -656,10 +660,12 @@ struct MmaConsumer {
     }
     l[0] = l[0] * al0 + ps0;
     l[1] = l[1] * al1 + ps1;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
 #pragma unroll
-    for (int n = 0; n < NT_O; ++n) {
-      o[n][0] *= al0; o[n][1] *= al0;
-      o[n][2] *= al1; o[n][3] *= al1;
+      for (int n = 0; n < NT_O; ++n) {
+        o[n][0] *= al0; o[n][1] *= al0;
+        o[n][2] *= al1; o[n][3] *= al1;
+      }
     }
     // O += P V  (the packing below is exact: the weights are already bf16 values)
 #pragma unroll

@@ -36,7 +36,7 @@
 // Online softmax with a lazy reference: a row's probabilities are exp2(s - m_ref), where m_ref is
 // the row's maximum when its segment started or when it was last raised; it is raised, and the
 // row of O and the running sum rescaled, only when a new maximum exceeds m_ref by more than
-// kRescaleLog2. (Merges take any reference.)
+// kLazyLog2. (Merges take any reference.)
 //
 // Every wait is bounded in time; on expiry the kernel records the wait, latches MQA_ERR_TIMEOUT,
 // and warp 5 waits (bounded) for its MMAs and for the softmax warps before it frees the tensor
@@ -57,7 +57,6 @@ constexpr int kTcOCol = kTcPCol + kTcBufs * kTileKeys / 2;  // O: d_h columns
 constexpr int kTcStageCols = 16;      // columns of O staged per round of the epilogue merge
 constexpr int kTcStageStride = kTcStageCols + 1;  // floats per staged row (padded)
 constexpr int kTcMergeRows = 4;       // merge scratch rows per warp (merge_split_segment)
-constexpr float kRescaleLog2 = 8.f;
 __host__ __device__ constexpr int tc_tile_bytes(int D) { return kTileKeys * D * 2; }  // K or V
 __host__ __device__ constexpr int tc_k_stages(int D) { return D == 128 ? 5 : 8; }
 __host__ __device__ constexpr int tc_v_stages(int D) { return D == 128 ? 6 : 8; }
@@ -348,7 +347,7 @@ __device__ __forceinline__ bool tc_softmax_loop(const DecodeParams& P, const TcS
     bool raise = false;
     if (first) {
       m_ref = mx;                     // -inf when this copy has no valid key in the tile
-    } else if (mx > m_ref + kRescaleLog2) {
+    } else if (mx > m_ref + kLazyLog2) {
       raise = true;
       alpha = fast_exp2(m_ref - mx);  // 0 when m_ref is -inf
       m_ref = mx;

@@ -183,9 +183,9 @@ AttnKernelChoice choice(int b) {
 }
 
 // Eight consumer warps (two per SM sub-partition) hide the latency of the per-tile dependency
-// chains of the CUDA-core path, where one warp per sub-partition leaves most issue slots idle. The
-// mma.sync path keeps four: its cost per tile is the mma.sync throughput itself, which a second
-// warp per sub-partition does not raise.
+// chains where one warp per sub-partition leaves most issue slots idle: the CUDA-core path, and
+// mma.sync above 16 heads, where each warp's MMA chains and softmax would otherwise serialise.
+// Up to 16 heads mma.sync keeps four warps (16 keys per warp is its smallest P V k-step).
 template <int D>
 AttnKernelChoice pick_kernel(Path path, int G, int b) {
   using mqa::CcConsumer;
@@ -202,8 +202,8 @@ AttnKernelChoice pick_kernel(Path path, int G, int b) {
   }
   if (path == kPathMmaSync) {
     if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, true, 1>(b);
-    if (G <= 32) return choice<MmaConsumer<D, 2, 4>, D, true, 2>(b);
-    return choice<MmaConsumer<D, 4, 4>, D, true, 4>(b);
+    if (G <= 32) return choice<MmaConsumer<D, 2, 8>, D, true, 2>(b);
+    return choice<MmaConsumer<D, 4, 8>, D, true, 4>(b);
   }
   switch (G) {
     case 1: return choice<CcConsumer<D, 1, 8>, D, false, 1>(b);
