@@ -13,8 +13,10 @@ with inputs resident in HBM (lower is better), from CUDA-graph replays of the wh
 layer's append and attention): K replays back to back between two events, or, for workloads small
 enough to sit in L2, one graph per step that flushes L2 (a 252 MB write) and then times the step
 between its own event nodes. ``e2e`` is the same step driven eagerly through the public Python
-API from pinned host buffers, with the host->device copy of the step's inputs (q, k_new, v_new of
-every layer) and the device->host read of its outputs inside the timed region. ``roofline``
+API from pinned host buffers (``layers.HostStepPipeline``, recorded once as a CUDA graph and
+replayed per step), with the host->device copy of the step's inputs (q, k_new, v_new of every
+layer) and the device->host read of its outputs inside the timed region of every step,
+overlapped with the kernels in runs of eight layers. ``roofline``
 reports the decode kernel's HBM throughput on algorithmic bytes (K/V rows read, q read, out
 written, new rows read and written) against the measured copy bandwidth; its launch durations
 come from a second timed pass of K steps whose graphs carry CUDA event nodes around every launch.
@@ -261,7 +263,8 @@ def workload_config(w):
 # ------------------------------------------------------------------------------------------------
 def run_ours(args, world, rank, local):
     import query_grouped_decode_kv_b300 as mqa
-    from query_grouped_decode_kv_b300.layers import LayerState, StepInputs, decode_layers
+    from query_grouped_decode_kv_b300.layers import (HostStepBuffers, HostStepPipeline,
+                                                     LayerState, StepInputs, decode_layers)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -366,35 +369,34 @@ def run_ours(args, world, rank, local):
     attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
     attn_avg_s = sum(attn_ms) / len(attn_ms) / 1000.0
 
-    # ---- end to end through host buffers ----
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    hq = [pin(x.q) for x in xs]
-    hk = [pin(x.k_new) for x in xs]
-    hv = [pin(x.v_new) for x in xs]
-    ho = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv)
-    d2h = sum(t.numel() * t.element_size() for t in ho)
+    # ---- end to end through host buffers: every step copies its inputs in from pinned host
+    # memory and its outputs out, overlapped with the kernels (layers.HostStepPipeline) ----
+    buf = HostStepBuffers.allocate(w.layers, w.b, w.h, w.g, w.d_h, dev)
+    for li, x in enumerate(xs):
+        buf.q_host[li].copy_(x.q.cpu())
+        buf.kn_host[li].copy_(x.k_new.cpu())
+        buf.vn_host[li].copy_(x.v_new.cpu())
+    pipeline = HostStepPipeline(layers, buf)
+    h2d, d2h = buf.h2d_bytes, buf.d2h_bytes
 
-    def e2e_step(pair=None):
-        # eager, through the public API: copy in, append + attention per layer, copy out; an L2
-        # flush (small workloads only) runs before the step's start event
+    def e2e_step(step_graph_e2e, pair=None):
+        # an L2 flush (small workloads only) runs before the step's start event
         if flush is not None:
             flush.fill_(1)
         if pair is not None:
             pair[0].record(stream)
-        for li in range(w.layers):
-            xs[li].q.copy_(hq[li], non_blocking=True)
-            xs[li].k_new.copy_(hk[li], non_blocking=True)
-            xs[li].v_new.copy_(hv[li], non_blocking=True)
-        decode_layers(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream)
-        for li in range(w.layers):
-            ho[li].copy_(outs[li], non_blocking=True)
+        step_graph_e2e.replay()
         if pair is not None:
             pair[1].record(stream)
 
+    # the step through the public API once eagerly (it sizes the workspace), then as one graph
+    with torch.cuda.stream(stream):
+        pipeline.run(pos_d, lens_d, w.scale, stream)
+    torch.cuda.synchronize()
+    e2e_graph = pipeline.capture(pos_d, lens_d, w.scale, stream)
     with torch.cuda.stream(stream):
         for _ in range(2):
-            e2e_step()
+            e2e_step(e2e_graph)
     torch.cuda.synchronize()
     e2e_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
@@ -402,9 +404,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for pair in e2e_events:
-            e2e_step(pair)
+            e2e_step(e2e_graph, pair)
     torch.cuda.synchronize()
     barrier()
+    assert mqa.get_device_status() == 0, "device status latched an error in the e2e region"
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_events)
 
     # ---- max over ranks ----

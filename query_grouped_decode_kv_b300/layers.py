@@ -46,3 +46,107 @@ def decode_layers(layers: list[LayerState], step_in: list[StepInputs], pos: torc
                                      stream=stream)
         if attn_events is not None:
             attn_events[li][1].record(stream)
+
+
+@dataclasses.dataclass
+class HostStepBuffers:
+    """A whole step's per-layer inputs and outputs, packed layer-major so that a run of layers is
+    one contiguous block: pinned host copies and their device mirrors."""
+    q_host: torch.Tensor      # [layers, b, h, d_h] bf16, pinned
+    kn_host: torch.Tensor     # [layers, b, g, d_h]
+    vn_host: torch.Tensor
+    out_host: torch.Tensor    # [layers, b, h, d_h]
+    q_dev: torch.Tensor
+    kn_dev: torch.Tensor
+    vn_dev: torch.Tensor
+    out_dev: torch.Tensor
+
+    @classmethod
+    def allocate(cls, layers: int, b: int, h: int, g: int, d_h: int, device) -> "HostStepBuffers":
+        def host(*shape):
+            return torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+
+        def dev(*shape):
+            return torch.empty(shape, dtype=torch.bfloat16, device=device)
+        return cls(host(layers, b, h, d_h), host(layers, b, g, d_h), host(layers, b, g, d_h),
+                   host(layers, b, h, d_h), dev(layers, b, h, d_h), dev(layers, b, g, d_h),
+                   dev(layers, b, g, d_h), dev(layers, b, h, d_h))
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.q_host, self.kn_host, self.vn_host))
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.out_host.numel() * self.out_host.element_size()
+
+
+class HostStepPipeline:
+    """Drives whole decode steps from pinned host inputs to pinned host outputs with the transfers
+    overlapped with the kernels: the inputs of each run of `chunk` layers are copied in on one
+    stream, that run's fused launches wait only for them, and its outputs are copied out on
+    another stream while the next run computes. A step of one run stays on the caller's stream.
+    Streams and events are created once, so a step costs only the enqueues."""
+
+    def __init__(self, layers: list[LayerState], buf: HostStepBuffers, chunk: int = 8):
+        self.layers, self.buf = layers, buf
+        n = len(layers)
+        self.runs = [(c0, min(n, c0 + chunk)) for c0 in range(0, n, chunk)]
+        if len(self.runs) > 1:
+            dev = buf.q_dev.device
+            self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+            self.start = torch.cuda.Event()
+            self.back = torch.cuda.Event()
+            self.ready = [torch.cuda.Event() for _ in self.runs]
+            self.done = [torch.cuda.Event() for _ in self.runs]
+
+    def _copy_in(self, c0: int, c1: int) -> None:
+        b = self.buf
+        b.q_dev[c0:c1].copy_(b.q_host[c0:c1], non_blocking=True)
+        b.kn_dev[c0:c1].copy_(b.kn_host[c0:c1], non_blocking=True)
+        b.vn_dev[c0:c1].copy_(b.vn_host[c0:c1], non_blocking=True)
+
+    def _compute(self, c0: int, c1: int, pos, seq_lens, scale: float, stream) -> None:
+        b = self.buf
+        for li in range(c0, c1):
+            lay = self.layers[li]
+            binding.decode_step(b.q_dev[li], b.kn_dev[li], b.vn_dev[li], lay.k_cache, lay.v_cache,
+                                pos, seq_lens, out=b.out_dev[li], scale=scale, stream=stream)
+
+    def run(self, pos: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+            stream: torch.cuda.Stream) -> None:
+        """Enqueue one step after the work already on `stream`; `stream` waits for the last copy
+        out before anything issued after this call."""
+        b = self.buf
+        if len(self.runs) == 1:
+            c0, c1 = self.runs[0]
+            with torch.cuda.stream(stream):
+                self._copy_in(c0, c1)
+                self._compute(c0, c1, pos, seq_lens, scale, stream)
+                b.out_host[c0:c1].copy_(b.out_dev[c0:c1], non_blocking=True)
+            return
+        self.start.record(stream)
+        self.h2d.wait_event(self.start)
+        with torch.cuda.stream(self.h2d):
+            for (c0, c1), ev in zip(self.runs, self.ready):
+                self._copy_in(c0, c1)
+                ev.record(self.h2d)
+        for (c0, c1), ready, done in zip(self.runs, self.ready, self.done):
+            stream.wait_event(ready)
+            self._compute(c0, c1, pos, seq_lens, scale, stream)
+            done.record(stream)
+            self.d2h.wait_event(done)
+            with torch.cuda.stream(self.d2h):
+                b.out_host[c0:c1].copy_(b.out_dev[c0:c1], non_blocking=True)
+        self.back.record(self.d2h)
+        stream.wait_event(self.back)
+
+    def capture(self, pos: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                stream: torch.cuda.Stream) -> torch.cuda.CUDAGraph:
+        """Record one step (copies in, launches, copies out) as a CUDA graph on `stream`; each
+        replay performs the whole step again, transfers included, for one host-side launch. The
+        library's workspace for this stream must already be large enough (run one step first)."""
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self.run(pos, seq_lens, scale, stream)
+        return graph

@@ -98,3 +98,57 @@ def test_80_layer_step_sampled(mqa):
         assert np.array_equal(P.bits(layers[li].v_cache[sample]), vh)
         ref = oracle.decode_attention(P.bits(x.q[sample]), kh, vh, lens[sample].numpy(), w.scale)
         print("layer", li, P.assert_close(outs[li][sample], ref, f"layer {li}"))
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+@pytest.mark.parametrize("chunk", [3, 8], ids=["runs_of_3", "one_run"])
+def test_host_driven_step_matches_the_device_step(mqa, chunk, graph):
+    """layers.HostStepPipeline (inputs copied in and outputs out, overlapped in runs of layers)
+    gives, bit for bit, the outputs and caches of the device-resident multi-layer step."""
+    from query_grouped_decode_kv_b300.layers import (HostStepBuffers, HostStepPipeline,
+                                                     LayerState, StepInputs, decode_layers)
+    w = inputs.custom("host_step", 3, 16, 2, 128, 100, 900)
+    n_layers = 7
+    dev = torch.device("cuda")
+    pos, lens = inputs.positions_and_lengths(w)
+    pos_d, lens_d = pos.to(dev), lens.to(dev)
+    xs, lay_a, lay_b = [], [], []
+    for li in range(n_layers):
+        lw = inputs.custom("host_step", 3, 16, 2, 128, 100, 900, wid=900 + li)
+        k, v = inputs.cache(lw, 0, dev, tail="nan", lengths=pos)
+        lay_a.append(LayerState(k.clone(), v.clone()))
+        lay_b.append(LayerState(k, v))
+        xs.append(StepInputs(*inputs.step_inputs(lw, 0, dev)))
+    outs = [torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev) for _ in range(n_layers)]
+    decode_layers(lay_a, xs, pos_d, lens_d, outs, w.scale)
+    buf = HostStepBuffers.allocate(n_layers, w.b, w.h, w.g, w.d_h, dev)
+    for li, x in enumerate(xs):
+        buf.q_host[li].copy_(x.q.cpu())
+        buf.kn_host[li].copy_(x.k_new.cpu())
+        buf.vn_host[li].copy_(x.v_new.cpu())
+    pipe = HostStepPipeline(lay_b, buf, chunk=chunk)
+    if graph:
+        # record the step on a side stream (the workspace of that stream is sized first by a run
+        # on caches that are then discarded), replay it once on the real caches' copies
+        side = torch.cuda.Stream()
+        keep = [(l.k_cache.clone(), l.v_cache.clone()) for l in lay_b]
+        with torch.cuda.stream(side):
+            pipe.run(pos_d, lens_d, w.scale, side)
+        side.synchronize()
+        for l, (k0, v0) in zip(lay_b, keep):
+            l.k_cache.copy_(k0)
+            l.v_cache.copy_(v0)
+        buf.out_host.zero_()
+        torch.cuda.synchronize()
+        g = pipe.capture(pos_d, lens_d, w.scale, side)
+        with torch.cuda.stream(side):
+            g.replay()
+        side.synchronize()
+    else:
+        pipe.run(pos_d, lens_d, w.scale, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    for li in range(n_layers):
+        assert torch.equal(buf.out_host[li].view(torch.int16), outs[li].cpu().view(torch.int16))
+        assert torch.equal(lay_b[li].k_cache.view(torch.int16), lay_a[li].k_cache.view(torch.int16))
+        assert torch.equal(lay_b[li].v_cache.view(torch.int16), lay_a[li].v_cache.view(torch.int16))
