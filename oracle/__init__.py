@@ -17,6 +17,10 @@ What each function computes, and the passage it follows:
   log-sum-exp combination (not on the pages; the identity that makes splitting a sequence exact).
 * :func:`bf16_to_f64` / :func:`f64_to_bf16` -- bfloat16 conversions from the bit layout
   (round to nearest, ties to even).
+* :func:`gather_pages` / :func:`kv_append_paged` -- the paged cache: a pool of fixed-size pages
+  found through a per-sequence page table (nanhubrain.csdn.net MQA article §3.3 on vLLM's
+  16-token blocks; ybb.press page §十 item 12); attention over it is attention over the gathered
+  rows.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms, the pages' printed
 numbers, invariants and library routines.
@@ -56,6 +60,10 @@ def _configure(lib):
                                                  i32, i32, vp, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, vp, i32, i32, vp]
+    lib.oracle_gather_pages.restype = i32
+    lib.oracle_gather_pages.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.oracle_kv_append_paged.restype = i32
+    lib.oracle_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -192,3 +200,37 @@ def lse_merge(m, l, o) -> np.ndarray:
     if st == ERR_INVALID_ARG:
         raise ValueError("bad merge arguments")
     return out
+
+
+def gather_pages(pool, table, page_size: int):
+    """Contiguous cache [b, g, max_pages * page_size, d_h] (uint16) from a page pool
+    [num_pages, g, page_size, d_h] and a page table [b, max_pages] (int32). Rows of pages whose
+    index is out of range come back zero and the status is 4. Returns (cache, status)."""
+    lib = _load()
+    pl = _c(pool, np.uint16)
+    tb = _c(table, np.int32)
+    num_pages, g, ps, d_h = pl.shape
+    if ps != page_size:
+        raise ValueError("page size mismatch")
+    b, max_pages = tb.shape
+    out = np.empty((b, g, max_pages * page_size, d_h), dtype=np.uint16)
+    st = int(lib.oracle_gather_pages(_ptr(pl), _ptr(tb), b, g, d_h, page_size, max_pages,
+                                     num_pages, _ptr(out)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return out, st
+
+
+def kv_append_paged(k_new, v_new, k_pool, v_pool, pos, table) -> int:
+    """Append through the page table, in place (pools: C-contiguous uint16 numpy arrays)."""
+    lib = _load()
+    for c in (k_pool, v_pool):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint16 and c.flags.c_contiguous):
+            raise TypeError("pools must be C-contiguous uint16 numpy arrays (updated in place)")
+    num_pages, g, page_size, d_h = k_pool.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    p = _c(pos, np.int32)
+    tb = _c(table, np.int32)
+    b, max_pages = tb.shape
+    return int(lib.oracle_kv_append_paged(_ptr(kn), _ptr(vn), _ptr(k_pool), _ptr(v_pool), _ptr(p),
+                                          _ptr(tb), b, g, d_h, page_size, max_pages, num_pages))

@@ -19,6 +19,8 @@
  *            new K/V row onto the cache along the sequence axis, then takes logits of every
  *            query head against the (shared) keys.
  *   [MQA-ENC] "多查詢注意力" (compassingai.com), section "KV Cache 結構與視訊記憶體佔用對比".
+ *   [MQA-CSDN] §3.3 and [GQA-MQA] §十 item 12: serving stacks (vLLM PagedAttention) keep the
+ *            cache in fixed blocks of 16 tokens found through a per-sequence block table.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   - attention covers rows 0 .. L_b-1 of sequence b, where L_b (seq_lens[b]) already counts the
@@ -126,6 +128,61 @@ int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_c
       size_t dst = (((size_t)bi * g + j) * (size_t)n_max + (size_t)p) * (size_t)d_h;
       memcpy(k_cache + dst, k_new + src, (size_t)d_h * sizeof(uint16_t));
       memcpy(v_cache + dst, v_new + src, (size_t)d_h * sizeof(uint16_t));
+    }
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Paged cache ([MQA-CSDN] §3.3; [GQA-MQA] §十 item 12). Reading: a pool of pages               */
+/* [num_pages][g][page_size][d_h], and for sequence b a table of max_pages page indices; the    */
+/* sequence's row t of KV head j is row t % page_size of KV head j in page                      */
+/* table[b][t / page_size]. Attention over a paged cache is attention over the rows this map   */
+/* gives, so the oracle gathers them into the contiguous layout and attends there.              */
+/* ------------------------------------------------------------------------------------------ */
+int oracle_gather_pages(const uint16_t* pool, const int32_t* table, int b, int g, int d_h,
+                        int page_size, int max_pages, int num_pages, uint16_t* cache) {
+  if (!pool || !table || !cache) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+    return ORACLE_ERR_INVALID_ARG;
+  const int n_max = max_pages * page_size;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi)
+    for (int j = 0; j < g; ++j)
+      for (int t = 0; t < n_max; ++t) {
+        uint16_t* dst = cache + (((size_t)bi * g + j) * (size_t)n_max + (size_t)t) * (size_t)d_h;
+        const int page = table[(size_t)bi * max_pages + t / page_size];
+        if (page < 0 || page >= num_pages) {
+          status = ORACLE_ERR_BOUNDS;
+          memset(dst, 0, (size_t)d_h * sizeof(uint16_t));
+          continue;
+        }
+        const uint16_t* src = pool + (((size_t)page * g + j) * (size_t)page_size +
+                                      (size_t)(t % page_size)) * (size_t)d_h;
+        memcpy(dst, src, (size_t)d_h * sizeof(uint16_t));
+      }
+  return status;
+}
+
+/* The append through the table: row pos[b] of sequence b's KV head j <- k_new[b][j] (and V). */
+int oracle_kv_append_paged(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pool,
+                           uint16_t* v_pool, const int32_t* pos, const int32_t* table, int b,
+                           int g, int d_h, int page_size, int max_pages, int num_pages) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !pos || !table) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+    return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    const int p = pos[bi];
+    if (p < 0 || p >= max_pages * page_size) { status = ORACLE_ERR_BOUNDS; continue; }
+    const int page = table[(size_t)bi * max_pages + p / page_size];
+    if (page < 0 || page >= num_pages) { status = ORACLE_ERR_BOUNDS; continue; }
+    for (int j = 0; j < g; ++j) {
+      size_t src = ((size_t)bi * g + j) * (size_t)d_h;
+      size_t dst = (((size_t)page * g + j) * (size_t)page_size + (size_t)(p % page_size)) *
+                   (size_t)d_h;
+      memcpy(k_pool + dst, k_new + src, (size_t)d_h * sizeof(uint16_t));
+      memcpy(v_pool + dst, v_new + src, (size_t)d_h * sizeof(uint16_t));
     }
   }
   return status;

@@ -31,6 +31,12 @@ MUTANTS = [
      "(size_t)n_max + (size_t)(p > 0 ? p - 1 : p)) * (size_t)d_h;"),
     ("bf16_subnormal_exponent", "mag = ldexp((double)frac, -133);", "mag = ldexp((double)frac, -134);"),
     ("bf16_round_half_up", "(rem == 0.5 && fmod(r, 2.0) != 0.0)", "(rem == 0.5)"),
+    ("paged_gather_wrong_page", "table[(size_t)bi * max_pages + t / page_size];",
+     "table[(size_t)bi * max_pages + (t / page_size + 1) % max_pages];"),
+    ("paged_gather_wrong_row", "(size_t)(t % page_size)) * (size_t)d_h;",
+     "(size_t)((t + 1) % page_size)) * (size_t)d_h;"),
+    ("paged_append_wrong_row", "(size_t)(p % page_size)) *",
+     "(size_t)((p + 1) % page_size)) *"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
@@ -50,6 +56,8 @@ def _run_pins() -> int:
             calls = [dict(ratio=r) for r in golden["ratios"]]
         elif set(params) == {"h", "g", "d_h"}:
             calls = [dict(h=8, g=2, d_h=64), dict(h=6, g=3, d_h=64)]
+        elif set(params) == {"page_size"}:
+            calls = [dict(page_size=p) for p in (1, 4, 16)]
         else:
             calls = [{}]
         for kw in calls:

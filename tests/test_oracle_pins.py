@@ -399,3 +399,106 @@ def test_single_partial_normalises_and_empty_partials_carry_no_weight():
     two = oracle.lse_merge(np.concatenate([m[0], me[0]]), np.concatenate([l[0], le[0]]),
                            np.concatenate([o[0], oe[0]]))
     assert np.array_equal(one, two)
+
+
+# ------------------------------------------------------------------------------------------------
+# Paged cache (nanhubrain.csdn.net MQA article §3.3, vLLM's 16-token blocks; ybb.press §十 item 12)
+# ------------------------------------------------------------------------------------------------
+def _paged_layout(b=2, g=2, max_pages=5, page_size=4, d_h=8, spare=3, seed=7):
+    """A contiguous cache C [b, g, max_pages * page_size, d_h] and the same rows cut into pages
+    by numpy reshapes alone, scattered over a pool with spare pages by a random permutation."""
+    rng = np.random.default_rng(seed)
+    n = max_pages * page_size
+    C = rng.integers(0, 1 << 16, size=(b, g, n, d_h), dtype=np.uint16)
+    blocks = C.reshape(b, g, max_pages, page_size, d_h).transpose(0, 2, 1, 3, 4)
+    blocks = blocks.reshape(b * max_pages, g, page_size, d_h)
+    num_pages = b * max_pages + spare
+    slot = rng.permutation(num_pages)[:b * max_pages]
+    pool = rng.integers(0, 1 << 16, size=(num_pages, g, page_size, d_h), dtype=np.uint16)
+    pool[slot] = blocks
+    table = slot.reshape(b, max_pages).astype(np.int32)
+    return C, pool, table
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_paged_gather_undoes_an_independent_paging(page_size):
+    C, pool, table = _paged_layout(page_size=page_size)
+    got, st = oracle.gather_pages(pool, table, page_size)
+    assert st == oracle.OK
+    assert np.array_equal(got, C)
+
+
+def test_paged_gather_reports_a_page_index_out_of_range():
+    C, pool, table = _paged_layout()
+    table = table.copy()
+    table[1, 2] = pool.shape[0]          # one past the pool
+    got, st = oracle.gather_pages(pool, table, 4)
+    assert st == oracle.ERR_BOUNDS
+    assert np.all(got[1, :, 8:12] == 0)  # the rows of that page
+    assert np.array_equal(got[0], C[0]) and np.array_equal(got[1, :, :8], C[1, :, :8])
+
+
+def test_paged_append_matches_the_contiguous_append():
+    C, kpool, table = _paged_layout(seed=8)
+    _, vpool, _ = _paged_layout(seed=8)
+    rng = np.random.default_rng(9)
+    kn = rng.integers(0, 1 << 16, size=(2, 2, 8), dtype=np.uint16)
+    vn = rng.integers(0, 1 << 16, size=(2, 2, 8), dtype=np.uint16)
+    pos = np.array([13, 6], dtype=np.int32)
+    kc, _ = oracle.gather_pages(kpool, table, 4)
+    vc, _ = oracle.gather_pages(vpool, table, 4)
+    assert oracle.kv_append(kn, vn, kc, vc, pos) == oracle.OK
+    kp, vp = kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged(kn, vn, kp, vp, pos, table) == oracle.OK
+    assert np.array_equal(oracle.gather_pages(kp, table, 4)[0], kc)
+    assert np.array_equal(oracle.gather_pages(vp, table, 4)[0], vc)
+    # pages no sequence maps stay as they were
+    unused = sorted(set(range(kpool.shape[0])) - set(table.ravel().tolist()))
+    assert np.array_equal(kp[unused], kpool[unused])
+
+
+def test_paged_append_rejects_a_bad_position_or_page_without_writing():
+    _, kpool, table = _paged_layout(seed=10)
+    vpool = kpool.copy()
+    kn = np.ones((2, 2, 8), dtype=np.uint16)
+    t2 = table.copy()
+    t2[0, 3] = -1
+    for pos, tb in ((np.array([20, 0], dtype=np.int32), table),    # past max_pages * page_size
+                    (np.array([13, -1], dtype=np.int32), table),   # negative
+                    (np.array([13, 99], dtype=np.int32), t2)):     # page index -1, then bad pos
+        kp, vp = kpool.copy(), vpool.copy()
+        st = oracle.kv_append_paged(kn, kn, kp, vp, pos, tb)
+        assert st == oracle.ERR_BOUNDS
+    kp, vp = kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged(kn, kn, kp, vp, np.array([13, 20], dtype=np.int32),
+                                  t2) == oracle.ERR_BOUNDS
+    assert np.array_equal(kp, kpool) and np.array_equal(vp, vpool)
+
+
+def test_paged_attention_brute_force_through_the_table():
+    """Attention computed with pure-Python loops that fetch every row through the page table
+    equals the oracle's attention over the gathered cache."""
+    b, h, g, d_h, ps, mp = 2, 4, 2, 8, 4, 4
+    rng = np.random.default_rng(11)
+    num_pages = b * mp + 2
+    kpool = oracle.f64_to_bf16(rng.standard_normal((num_pages, g, ps, d_h)))
+    vpool = oracle.f64_to_bf16(rng.standard_normal((num_pages, g, ps, d_h)))
+    q = oracle.f64_to_bf16(rng.standard_normal((b, h, d_h)))
+    table = rng.permutation(num_pages)[:b * mp].reshape(b, mp).astype(np.int32)
+    lens = np.array([13, 6], dtype=np.int32)
+    scale = 0.37
+    kc, _ = oracle.gather_pages(kpool, table, ps)
+    vc, _ = oracle.gather_pages(vpool, table, ps)
+    got = oracle.decode_attention(q, kc, vc, lens, scale)
+    qf, kf, vf = oracle.bf16_to_f64(q), oracle.bf16_to_f64(kpool), oracle.bf16_to_f64(vpool)
+    for bi in range(b):
+        for i in range(h):
+            j = i // (h // g)
+            rows = [(int(table[bi, t // ps]), t % ps) for t in range(int(lens[bi]))]
+            s = [scale * sum(qf[bi, i, d] * kf[p, j, r, d] for d in range(d_h)) for p, r in rows]
+            m = max(s)
+            w = [math.exp(x - m) for x in s]
+            tot = sum(w)
+            for d in range(d_h):
+                ref = sum(wt * vf[p, j, r, d] for wt, (p, r) in zip(w, rows)) / tot
+                assert abs(got[bi, i, d] - ref) <= 1e-12 * max(1.0, abs(ref))
