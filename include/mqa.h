@@ -150,6 +150,54 @@ MQA_API int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_
                             int n_max, float scale, void* stream);
 
 /*
+ * Paged caches: mqa_kv_append_paged, mqa_decode_attention_paged, mqa_decode_step_paged.
+ *
+ * The same three operations over a cache kept in fixed-size pages found through a per-sequence
+ * page table, the layout serving stacks use for ragged batches: the nanhubrain.csdn.net MQA
+ * article §3.3 describes vLLM's PagedAttention cutting the cache into pages of 16 tokens by
+ * default, and "GQA与MQA深度实战" (ybb.press) §十 item 12 pairs ragged per-request lengths with
+ * such paging. The pages fix no layout; this library's reading:
+ *
+ *   k_pool, v_pool   device, [num_pages][g][page_size][d_h] bf16, 16-byte aligned: page p holds
+ *                    page_size consecutive rows of every KV head
+ *   page_table       device, [b][max_pages] int32: row t of sequence bi (every KV head j) is row
+ *                    t % page_size of page page_table[bi][t / page_size], i.e.
+ *                    K[bi][j][t] = k_pool[page_table[bi][t / page_size]][j][t % page_size]
+ *   page_size        8, 16 or 32, or a multiple of 64 (else MQA_ERR_UNSUPPORTED)
+ *   max_pages        entries per table row; a sequence addresses n_max = max_pages * page_size
+ *                    rows (max_pages * page_size <= 2^31 - 1)
+ *   num_pages        pages in each pool (num_pages * g < 2^31 - 1)
+ *
+ * Each call computes exactly what its contiguous counterpart computes on the cache the table
+ * describes (the rows above, gathered into [b][g][n_max][d_h]); the tests compare the two through
+ * the oracle's gather. Only the table entries of pages a call touches are read: those holding
+ * rows t < seq_lens[bi] (attention) and row pos[bi] (append), so entries past a sequence's last
+ * page may hold anything (-1 for "no page", say). A touched entry outside [0, num_pages) latches
+ * MQA_ERR_DEVICE_BOUNDS; its rows read as zeros in attention and its append is skipped. Pages
+ * may be shared between sequences (a common prefix) and read by all of them, but a page that a
+ * call appends to must not be read by another sequence in the same call, and two sequences must
+ * not append to the same row: the order of those accesses is not defined. Only the mma.sync and
+ * CUDA-core paths read paged caches: with mqa_debug_override forcing path 3 (tcgen05) the paged
+ * attention and step calls return MQA_ERR_UNSUPPORTED. Everything else -- argument meaning,
+ * ownership, ordering, the workspace, the status word -- is as for the contiguous calls.
+ */
+MQA_API int mqa_kv_append_paged(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_pool,
+                                mqa_bf16* v_pool, const int32_t* pos, const int32_t* page_table,
+                                int b, int g, int d_h, int page_size, int max_pages,
+                                int num_pages, void* stream);
+MQA_API int mqa_decode_attention_paged(const mqa_bf16* q, const mqa_bf16* k_pool,
+                                       const mqa_bf16* v_pool, const int32_t* page_table,
+                                       const int32_t* seq_lens, mqa_bf16* out, int b, int h,
+                                       int g, int d_h, int page_size, int max_pages,
+                                       int num_pages, float scale, void* stream);
+MQA_API int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new,
+                                  const mqa_bf16* v_new, mqa_bf16* k_pool, mqa_bf16* v_pool,
+                                  const int32_t* pos, const int32_t* page_table,
+                                  const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g,
+                                  int d_h, int page_size, int max_pages, int num_pages,
+                                  float scale, void* stream);
+
+/*
  * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
  * memory. The source pages have no counterpart to this call; it exists for users of the library.
  *

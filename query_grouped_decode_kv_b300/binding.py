@@ -32,6 +32,15 @@ _lib.mqa_decode_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
 _lib.mqa_decode_step.restype = _i32
 _lib.mqa_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                  _i32, _f32, _vp]
+_lib.mqa_kv_append_paged.restype = _i32
+_lib.mqa_kv_append_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                     _i32, _vp]
+_lib.mqa_decode_attention_paged.restype = _i32
+_lib.mqa_decode_attention_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                            _i32, _i32, _i32, _f32, _vp]
+_lib.mqa_decode_step_paged.restype = _i32
+_lib.mqa_decode_step_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                       _i32, _i32, _i32, _i32, _i32, _f32, _vp]
 _lib.mqa_status_string.restype = ctypes.c_char_p
 _lib.mqa_status_string.argtypes = [_i32]
 _lib.mqa_get_device_status.restype = _i32
@@ -207,4 +216,101 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cac
                               float(scale), _vp(_stream_handle(stream)))
     if st:
         raise MqaError(st, "mqa_decode_step")
+    return out
+
+
+def _pool_shape(k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor, b: int,
+                what: str) -> tuple[int, int, int, int, int]:
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(page_table, "page_table", torch.int32, 2)
+    num_pages, g, page_size, d_h = k_pool.shape
+    if v_pool.shape != k_pool.shape or page_table.shape[0] != b:
+        raise ValueError(f"{what}: inconsistent shapes")
+    return num_pages, g, page_size, d_h, page_table.shape[1]
+
+
+def kv_append_paged(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor,
+                    v_pool: torch.Tensor, pos: torch.Tensor, page_table: torch.Tensor,
+                    stream=None) -> None:
+    """:func:`kv_append` into paged caches: pools ``[num_pages, g, page_size, d_h]`` and a page
+    table ``[b, max_pages]``; row ``pos[b]`` lives in page ``page_table[b, pos[b] // page_size]``."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(pos, "pos", torch.int32, 1)
+    b = pos.shape[0]
+    num_pages, g, page_size, d_h, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                          "kv_append_paged")
+    if k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h):
+        raise ValueError("kv_append_paged: inconsistent shapes")
+    st = _lib.mqa_kv_append_paged(k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                                  v_pool.data_ptr(), pos.data_ptr(), page_table.data_ptr(), b, g,
+                                  d_h, page_size, max_pages, num_pages,
+                                  _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append_paged")
+
+
+def decode_attention_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, seq_lens: torch.Tensor,
+                           out: torch.Tensor | None = None, scale: float | None = None,
+                           stream=None) -> torch.Tensor:
+    """:func:`decode_attention` over paged caches (see :func:`kv_append_paged` for the layout)."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                         "decode_attention_paged")
+    if dk != d_h or seq_lens.shape != (b,):
+        raise ValueError("decode_attention_paged: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_attention_paged: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention_paged(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                         page_table.data_ptr(), seq_lens.data_ptr(),
+                                         out.data_ptr(), b, h, g, d_h, page_size, max_pages,
+                                         num_pages, float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention_paged")
+    return out
+
+
+def decode_step_paged(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_pool: torch.Tensor, v_pool: torch.Tensor, pos: torch.Tensor,
+                      page_table: torch.Tensor, seq_lens: torch.Tensor,
+                      out: torch.Tensor | None = None, scale: float | None = None,
+                      stream=None) -> torch.Tensor:
+    """:func:`decode_step` over paged caches: one launch that appends through the page table and
+    attends over the first ``seq_lens[b]`` rows the table maps."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                         "decode_step_paged")
+    if dk != d_h or seq_lens.shape != (b,) or pos.shape != (b,) or k_new.shape != (b, g, d_h) \
+            or v_new.shape != (b, g, d_h):
+        raise ValueError("decode_step_paged: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_step_paged: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step_paged(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                    k_pool.data_ptr(), v_pool.data_ptr(), pos.data_ptr(),
+                                    page_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), b,
+                                    h, g, d_h, page_size, max_pages, num_pages, float(scale),
+                                    _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step_paged")
     return out

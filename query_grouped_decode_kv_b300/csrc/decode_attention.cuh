@@ -78,6 +78,11 @@ struct DecodeParams {
   const uint4* v_new;
   uint4* k_rows;              // the caches as 16-byte chunks, [b][g][n_max][D/8]
   uint4* v_rows;
+  // Paged caches (all null / zero for contiguous ones): the caches are pools of pages
+  // [num_pages][g][page_size][D], and row t of sequence bi lives in page
+  // page_table[bi][t / page_size] at row t % page_size; n_max = max_pages * page_size.
+  const int32_t* page_table;  // [b][max_pages]
+  int page_size, max_pages, num_pages;
 };
 
 __host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
@@ -118,6 +123,17 @@ __device__ __forceinline__ bool row_is_loaded(int p, int L, int n_max) {
   return static_cast<long long>(p) < static_cast<long long>(tiles_of_length(L, n_max)) * kTileKeys;
 }
 
+// First 16-byte chunk of cache row p of segment (bi, j) in the caches seen as chunks, or -1 when
+// the page holding the row is out of range (paged caches; the row is then not written).
+__device__ __forceinline__ long long row_chunk(const DecodeParams& P, int bi, int j, int p,
+                                               int CH) {
+  if (P.page_table == nullptr)
+    return ((static_cast<long long>(bi) * P.g + j) * P.n_max + p) * CH;
+  const int page = __ldg(P.page_table + static_cast<size_t>(bi) * P.max_pages + p / P.page_size);
+  if (page < 0 || page >= P.num_pages) return -1;
+  return ((static_cast<long long>(page) * P.g + j) * P.page_size + p % P.page_size) * CH;
+}
+
 template <int D>
 __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int nthreads) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
@@ -134,18 +150,28 @@ __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int
       continue;
     }
     if (row_is_loaded(p, __ldg(P.seq_lens + bi), P.n_max)) continue;
-    const long long dst = (row * P.n_max + p) * CH + c;
-    P.k_rows[dst] = __ldg(P.k_new + idx);
-    P.v_rows[dst] = __ldg(P.v_new + idx);
+    const long long dst = row_chunk(P, bi, static_cast<int>(row - static_cast<long long>(bi) * P.g),
+                                    p, CH);
+    if (dst < 0) {
+      if (c == 0) latch_status(kStatusDeviceBounds);
+      continue;
+    }
+    P.k_rows[dst + c] = __ldg(P.k_new + idx);
+    P.v_rows[dst + c] = __ldg(P.v_new + idx);
   }
 }
 
-// One warp writes the K and V row of segment `seg` at cache row `p` (lane = 16-byte chunk).
+// One warp writes the K and V row of segment (bi, j) at cache row `p` (lane = 16-byte chunk).
 template <int D>
-__device__ __forceinline__ void write_new_row(const DecodeParams& P, int seg, int p, int lane) {
+__device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int j, int p,
+                                              int lane) {
   constexpr int CH = D / 8;
-  const long long src = static_cast<long long>(seg) * CH;
-  const long long dst = (static_cast<long long>(seg) * P.n_max + p) * CH;
+  const long long src = (static_cast<long long>(bi) * P.g + j) * CH;
+  const long long dst = row_chunk(P, bi, j, p, CH);
+  if (dst < 0) {
+    if (lane == 0) latch_status(kStatusDeviceBounds);
+    return;
+  }
   if (lane < CH) P.k_rows[dst + lane] = __ldg(P.k_new + src + lane);
   else if (lane < 2 * CH) P.v_rows[dst + lane - CH] = __ldg(P.v_new + src + lane - CH);
 }
@@ -529,7 +555,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
         row_p = (p >= 0 && p < P.n_max) ? p : -1;
       }
       if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
-        write_new_row<D>(P, cur.bi * P.g + cur.j, row_p, lane);
+        write_new_row<D>(P, cur.bi, cur.j, row_p, lane);
         fence_proxy_async_global();  // each writer orders its store before the async proxy...
         __syncwarp();                // ...and lane 0 issues the copy after every writer
       }
@@ -553,6 +579,101 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   }
   if (lane != 0) return;
   // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
+  const volatile int never = 0;
+  for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
+    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Producer warp over paged caches. The tensor maps view each pool as (D, page_size,
+// num_pages * g) with boxes of R = min(page_size, kTileKeys) rows, so a tile's rows
+// [y, y + kTileKeys) arrive as kTileKeys / R boxes: box i holds rows y + i R .. y + (i+1) R - 1,
+// found at row (y + i R) % page_size of page page_table[bi][(y + i R) / page_size]. Every box
+// lands at a multiple of R * 128 bytes (>= 1 KB) inside the stage, so the 128-byte swizzle comes
+// out exactly as one box of the whole tile would give it. Boxes wholly at or past the length
+// are not loaded (those stage rows are never used). A page index out of range latches
+// MQA_ERR_DEVICE_BOUNDS and its box is read at a coordinate past the pool, which the copy
+// fills with zeros, so the sequence attends over zero rows there.
+// Lanes look up one box each (at most kTileKeys / 8 boxes) before the stage is free; lane 0
+// issues the copies.
+// ---------------------------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
+                                                    const CUtensorMap* tm_v,
+                                                    const DecodeParams& P, const SharedLayout& sh,
+                                                    unsigned long long x0, int ntiles, int lane) {
+  constexpr uint32_t kStageBytes = stage_bytes(D);
+  constexpr uint32_t kKvBytes = kStageBytes / 2;
+  const bool fused = P.pos != nullptr;
+  const int R = min(P.page_size, kTileKeys);
+  const int z_past_pool = P.num_pages * P.g;
+  if (lane == 0) {
+    prefetch_tensor_map(tm_k);
+    prefetch_tensor_map(tm_v);
+  }
+  const uint64_t policy = l2_policy_evict_first();
+  TileCursor cur;
+  cur.start(x0, sh.tix);
+  int issued = 0;
+  int seq = -1, L = 0, row_p = -1;  // the sequence of the last tile, its length and append row
+  for (int k = 0; k < ntiles; ++k) {
+    if (cur.bi != seq) {
+      seq = cur.bi;
+      L = __ldg(P.seq_lens + seq);
+      if (fused) {
+        const int p = __ldg(P.pos + seq);
+        row_p = (p >= 0 && p < P.n_max) ? p : -1;
+      }
+    }
+    const int y = cur.tile * kTileKeys;
+    const int nbox = (min(L - y, kTileKeys) + R - 1) / R;  // L > y for every tile
+    int z = 0, yr = 0;
+    if (lane < nbox) {
+      const int r = y + lane * R;
+      const int page = __ldg(P.page_table + static_cast<size_t>(seq) * P.max_pages +
+                             r / P.page_size);
+      const bool bad = page < 0 || page >= P.num_pages;
+      if (bad) latch_status(kStatusDeviceBounds);
+      z = bad ? z_past_pool : page * P.g + cur.j;
+      yr = r % P.page_size;
+    }
+    const int st = k % kStages;
+    const uint32_t par = ((k / kStages) & 1) ^ 1;
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (lane == 0 && !*sh.abort) give_up(sh, kSiteProducerEmpty, k);
+      break;
+    }
+    if (fused && row_p >= 0 && row_p / kTileKeys == cur.tile) {
+      write_new_row<D>(P, cur.bi, cur.j, row_p, lane);
+      fence_proxy_async_global();
+      __syncwarp();
+    }
+    if (lane == 0)
+      mbar_arrive_expect_tx(&sh.full[st],
+                            static_cast<uint32_t>(nbox * R) * kSwizzleRowBytes * (D / 64) * 2);
+    uint8_t* kdst = sh.stages + st * kStageBytes;
+    uint8_t* vdst = kdst + kKvBytes;
+    for (int i = 0; i < nbox; ++i) {
+      const int zi = __shfl_sync(0xffffffffu, z, i);
+      const int yi = __shfl_sync(0xffffffffu, yr, i);
+      if (lane == 0) {
+        const int off = i * R * kSwizzleRowBytes;
+#pragma unroll
+        for (int half = 0; half < D / 64; ++half) {
+          tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes + off, tm_k, &sh.full[st],
+                      half * 64, yi, zi, policy);
+          tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes + off, tm_v, &sh.full[st],
+                      half * 64, yi, zi, policy);
+        }
+      }
+    }
+    ++issued;
+    cur.advance(sh.tix);
+  }
+  if (lane != 0) return;
   const volatile int never = 0;
   for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
     mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
@@ -922,7 +1043,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   if (warp >= NW) {
     // ================================ producer ================================================
-    if (warp == NW) produce_tiles<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+    if (warp == NW) {
+      if (P.page_table != nullptr) produce_tiles_paged<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+      else produce_tiles<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+    }
     return;
   }
 

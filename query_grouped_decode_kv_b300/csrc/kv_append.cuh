@@ -37,4 +37,42 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
   }
 }
 
+// The same append into paged caches: pools [num_pages][g][page_size][chunks] of 16-byte chunks,
+// row p of sequence bi living at row p % page_size of page page_table[bi][p / page_size]
+// (the nanhubrain.csdn.net MQA article §3.3: vLLM keeps the cache in fixed pages, 16 tokens each
+// by default; "GQA与MQA深度实战" (ybb.press) §十 item 12 pairs ragged batches with such paging).
+// A position outside [0, max_pages * page_size) or a page index outside [0, num_pages) skips that
+// sequence and latches MQA_ERR_DEVICE_BOUNDS.
+__global__ void __launch_bounds__(256) kv_append_paged_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_pool,
+    uint4* __restrict__ v_pool, const int32_t* __restrict__ pos,
+    const int32_t* __restrict__ page_table, int b, int g, int chunks_per_row, int page_size,
+    int max_pages, int num_pages) {
+  const long long total = static_cast<long long>(b) * g * chunks_per_row;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long n_max = static_cast<long long>(max_pages) * page_size;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long row = idx / chunks_per_row;  // = bi * g + j
+    const int c = static_cast<int>(idx - row * chunks_per_row);
+    const int bi = static_cast<int>(row / g);
+    const int j = static_cast<int>(row - static_cast<long long>(bi) * g);
+    const int p = __ldg(pos + bi);
+    const bool first = c == 0 && j == 0;
+    if (p < 0 || p >= n_max) {
+      if (first) latch_status(kStatusDeviceBounds);
+      continue;
+    }
+    const int page = __ldg(page_table + static_cast<size_t>(bi) * max_pages + p / page_size);
+    if (page < 0 || page >= num_pages) {
+      if (first) latch_status(kStatusDeviceBounds);
+      continue;
+    }
+    const long long dst =
+        ((static_cast<long long>(page) * g + j) * page_size + p % page_size) * chunks_per_row + c;
+    k_pool[dst] = __ldg(k_new + idx);
+    v_pool[dst] = __ldg(v_new + idx);
+  }
+}
+
 }  // namespace mqa

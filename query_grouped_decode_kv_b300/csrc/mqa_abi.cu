@@ -72,6 +72,50 @@ bool make_cache_map(CUtensorMap* map, const void* base, int bg, int n_max, int d
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A page pool [num_pages][g][page_size][d_h] bf16 seen as (d_h, page_size, num_pages * g); box =
+// 64 columns x min(page_size, kTileKeys) rows, 128-byte swizzle. Coordinates past the pool read
+// as zeros.
+bool make_pool_map(CUtensorMap* map, const void* base, long long pages_g, int page_size,
+                   int d_h) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_h), static_cast<cuuint64_t>(page_size),
+                              static_cast<cuuint64_t>(pages_g)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * 2,
+                                 static_cast<cuuint64_t>(page_size) * d_h * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page_size < mqa::kTileKeys
+                                                             ? page_size : mqa::kTileKeys), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Paged caches: the page table and the pool's geometry (all zero for contiguous caches).
+struct PagedCache {
+  const int32_t* table = nullptr;
+  int page_size = 0, max_pages = 0, num_pages = 0;
+};
+
+// Host checks shared by the paged entry points. Page sizes: 8, 16 or 32 rows (a tile of 64 rows
+// spans several pages, one bulk copy each; a box of 8 or more rows keeps every copy on a 1 KB
+// boundary of the stage, where the 128-byte swizzle repeats), or a multiple of 64 (every tile
+// lies inside one page). Sets *n_max to the rows a sequence can address.
+int check_paged(const PagedCache& pg, int g, int d_h, int* n_max) {
+  if (!pg.table || (reinterpret_cast<uintptr_t>(pg.table) & 3u)) return MQA_ERR_INVALID_ARG;
+  if (pg.page_size <= 0 || pg.max_pages <= 0 || pg.num_pages <= 0) return MQA_ERR_INVALID_ARG;
+  if (!(pg.page_size == 8 || pg.page_size == 16 || pg.page_size == 32 ||
+        pg.page_size % mqa::kTileKeys == 0))
+    return MQA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(pg.max_pages) * pg.page_size;
+  if (rows > 0x7fffffffll) return MQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(pg.num_pages) * g > 0x7fffffffll - 1) return MQA_ERR_UNSUPPORTED;
+  if (static_cast<double>(pg.num_pages) * g * pg.page_size * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+  *n_max = static_cast<int>(rows);
+  return MQA_OK;
+}
+
 // ------------------------------------------------------------------------------------------------
 // Workspace, one per (device, stream), growing on demand. Two separate buffers: the split partial
 // states (written before they are read in every call), and one arrival counter per segment. The
@@ -257,6 +301,7 @@ struct DecodePlan {
   // fused append (mqa_decode_step only; null otherwise)
   const mqa_bf16 *k_new = nullptr, *v_new = nullptr;
   const int32_t* pos = nullptr;
+  PagedCache paged;  // table null: contiguous caches
   int b, h, g, d_h, n_max, G;
   float scale;
   Path path;
@@ -328,9 +373,15 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
 int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
                   bool clear_counters) {
   CUtensorMap tmk, tmv;
-  if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h) ||
-      !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h))
+  if (p.paged.table) {
+    const long long pages_g = static_cast<long long>(p.paged.num_pages) * p.g;
+    if (!make_pool_map(&tmk, p.k_cache, pages_g, p.paged.page_size, p.d_h) ||
+        !make_pool_map(&tmv, p.v_cache, pages_g, p.paged.page_size, p.d_h))
+      return MQA_ERR_CUDA;
+  } else if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h) ||
+             !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h)) {
     return MQA_ERR_CUDA;
+  }
 
   DecodeParams P;
   P.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
@@ -359,10 +410,15 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   // the caches are written only at the rows the fused append targets
   P.k_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.k_cache)) : nullptr;
   P.v_rows = p.pos ? reinterpret_cast<uint4*>(const_cast<mqa_bf16*>(p.v_cache)) : nullptr;
+  P.page_table = p.paged.table;
+  P.page_size = p.paged.page_size;
+  P.max_pages = p.paged.max_pages;
+  P.num_pages = p.paged.num_pages;
 
   const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b)
                                            : pick_kernel<64>(p.path, p.G, p.b);
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;
+  if (p.paged.table && p.path == kPathTcgen05) return MQA_ERR_UNSUPPORTED;
   if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
   kc.fn<<<static_cast<unsigned>(p.ctas), kc.threads, kc.smem, p.stream>>>(tmk, tmv, P);
   g_launches.fetch_add(1);
@@ -525,6 +581,102 @@ int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan))
     return st;
+  plan.k_new = k_new;
+  plan.v_new = v_new;
+  plan.pos = pos;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_kv_append_paged(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_pool,
+                        mqa_bf16* v_pool, const int32_t* pos, const int32_t* page_table, int b,
+                        int g, int d_h, int page_size, int max_pages, int num_pages,
+                        void* stream) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!k_new || !v_new || !k_pool || !v_pool || !pos) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  PagedCache pg;
+  pg.table = page_table;
+  pg.page_size = page_size;
+  pg.max_pages = max_pages;
+  pg.num_pages = num_pages;
+  int n_max = 0;
+  if (int st = check_paged(pg, g, d_h, &n_max)) return st;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(b) * g;
+  if (rows > (1ll << 31)) return MQA_ERR_UNSUPPORTED;
+
+  const int chunks = d_h / 8;
+  const long long total = rows * chunks;
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  mqa::kv_append_paged_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool), pos, page_table, b, g,
+      chunks, page_size, max_pages, num_pages);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+int mqa_decode_attention_paged(const mqa_bf16* q, const mqa_bf16* k_pool, const mqa_bf16* v_pool,
+                               const int32_t* page_table, const int32_t* seq_lens, mqa_bf16* out,
+                               int b, int h, int g, int d_h, int page_size, int max_pages,
+                               int num_pages, float scale, void* stream) {
+  if (g <= 0) return MQA_ERR_INVALID_ARG;
+  PagedCache pg;
+  pg.table = page_table;
+  pg.page_size = page_size;
+  pg.max_pages = max_pages;
+  pg.num_pages = num_pages;
+  int n_max = 0;
+  if (int st = check_paged(pg, g, d_h, &n_max)) return st;
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_pool, v_pool, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan))
+    return st;
+  plan.paged = pg;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                          mqa_bf16* k_pool, mqa_bf16* v_pool, const int32_t* pos,
+                          const int32_t* page_table, const int32_t* seq_lens, mqa_bf16* out,
+                          int b, int h, int g, int d_h, int page_size, int max_pages,
+                          int num_pages, float scale, void* stream) {
+  if (!k_new || !v_new || !pos || g <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  PagedCache pg;
+  pg.table = page_table;
+  pg.page_size = page_size;
+  pg.max_pages = max_pages;
+  pg.num_pages = num_pages;
+  int n_max = 0;
+  if (int st = check_paged(pg, g, d_h, &n_max)) return st;
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_pool, v_pool, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan))
+    return st;
+  plan.paged = pg;
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;

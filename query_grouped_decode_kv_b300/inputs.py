@@ -138,3 +138,38 @@ def custom(name: str, b: int, h: int, g: int, d_h: int, ctx_lo: int, ctx_hi: int
     """A workload of arbitrary shape (used for small parity cases)."""
     return Workload(name, wid, b=b, h=h, g=g, d_h=d_h, ctx_lo=ctx_lo, ctx_hi=ctx_hi,
                     kv_std=kv_std)
+
+
+def page_pool(k: torch.Tensor, v: torch.Tensor, rows: torch.Tensor, page_size: int, seed: int,
+              spare_pages: int = 0, max_pages: int | None = None, fill: str = "nan"):
+    """Lay contiguous caches [b, g, n_max, d_h] out as page pools and a page table.
+
+    Sequence bi gets ceil(rows[bi] / page_size) pages, drawn without replacement from a seeded
+    shuffle of all pages (``spare_pages`` more are left unused); its table row lists them in
+    order and holds -1 past them (``max_pages`` entries, by default enough for n_max rows).
+    Returns (k_pool, v_pool, table): pools [num_pages, g, page_size, d_h] on the caches' device,
+    table [b, max_pages] int32 on the CPU. Pool rows no sequence maps (spare pages, and rows of a
+    last page past n_max) hold ``fill``: NaN or zero.
+    """
+    b, g, n_max, d_h = k.shape
+    need = [(int(r) + page_size - 1) // page_size for r in rows]
+    if max_pages is None:
+        max_pages = (n_max + page_size - 1) // page_size
+    if max(need) > max_pages:
+        raise ValueError("a sequence needs more pages than its table row holds")
+    num_pages = sum(need) + spare_pages
+    order = torch.randperm(num_pages, generator=_gen("cpu", seed)).to(torch.int32)
+    table = torch.full((b, max_pages), -1, dtype=torch.int32)
+    value = 0.0 if fill == "zero" else float("nan")
+    k_pool = torch.full((num_pages, g, page_size, d_h), value, dtype=k.dtype, device=k.device)
+    v_pool = torch.full_like(k_pool, value)
+    used = 0
+    for bi in range(b):
+        for p in range(need[bi]):
+            page = int(order[used])
+            used += 1
+            table[bi, p] = page
+            r0, r1 = p * page_size, min((p + 1) * page_size, n_max)
+            k_pool[page, :, : r1 - r0] = k[bi, :, r0:r1]
+            v_pool[page, :, : r1 - r0] = v[bi, :, r0:r1]
+    return k_pool, v_pool, table

@@ -38,6 +38,12 @@ def lib():
                                   ctypes.c_float, vp]
     L.mqa_debug_timeout_site.restype = i32
     L.mqa_debug_timeout_site.argtypes = [vp]
+    L.mqa_kv_append_paged.restype = i32
+    L.mqa_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 6 + [vp]
+    L.mqa_decode_attention_paged.restype = i32
+    L.mqa_decode_attention_paged.argtypes = [vp] * 6 + [i32] * 7 + [ctypes.c_float, vp]
+    L.mqa_decode_step_paged.restype = i32
+    L.mqa_decode_step_paged.argtypes = [vp] * 9 + [i32] * 7 + [ctypes.c_float, vp]
     return L
 
 
@@ -155,3 +161,60 @@ def test_fused_step_host_checks(lib, kw, code):
 
 def test_timeout_site_rejects_null(lib):
     assert lib.mqa_debug_timeout_site(None) == INVALID
+
+
+# ---- paged caches: the page table and the pool geometry are checked on the host too ----------
+PAGED_GEOMETRY_CASES = [
+    (dict(table=0), INVALID), (dict(table=A + 0x8002), INVALID),
+    (dict(page_size=0), INVALID), (dict(max_pages=0), INVALID), (dict(num_pages=-1), INVALID),
+    (dict(page_size=24), UNSUPPORTED), (dict(page_size=48), UNSUPPORTED),
+    (dict(page_size=4), UNSUPPORTED),
+    (dict(page_size=64, max_pages=1 << 26), UNSUPPORTED),   # 2^32 addressable rows
+    (dict(num_pages=1 << 30), UNSUPPORTED),                 # num_pages * g past int32
+    (dict(d_h=96), UNSUPPORTED), (dict(b=0), INVALID), (dict(g=0), INVALID),
+]
+
+
+def _attn_paged(lib, q=A, k=A + 0x1000, v=A + 0x2000, table=A + 0x8000, lens=A + 0x3000,
+                out=A + 0x4000, b=2, h=8, g=2, d_h=128, page_size=16, max_pages=8, num_pages=20,
+                scale=0.088):
+    return lib.mqa_decode_attention_paged(q, k, v, table, lens, out, b, h, g, d_h, page_size,
+                                          max_pages, num_pages, scale, None)
+
+
+def _step_paged(lib, q=A, kn=A + 0x1000, vn=A + 0x2000, k=A + 0x3000, v=A + 0x4000,
+                pos=A + 0x5000, table=A + 0x8000, lens=A + 0x6000, out=A + 0x7000, b=2, h=8, g=2,
+                d_h=128, page_size=16, max_pages=8, num_pages=20, scale=0.088):
+    return lib.mqa_decode_step_paged(q, kn, vn, k, v, pos, table, lens, out, b, h, g, d_h,
+                                     page_size, max_pages, num_pages, scale, None)
+
+
+def _append_paged(lib, kn=A, vn=A + 0x1000, kc=A + 0x2000, vc=A + 0x3000, pos=A + 0x4000,
+                  table=A + 0x8000, b=2, g=2, d_h=128, page_size=16, max_pages=8, num_pages=20):
+    return lib.mqa_kv_append_paged(kn, vn, kc, vc, pos, table, b, g, d_h, page_size, max_pages,
+                                   num_pages, None)
+
+
+@pytest.mark.parametrize("kw,code", PAGED_GEOMETRY_CASES + [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(lens=0), INVALID), (dict(out=A + 4), INVALID),
+    (dict(h=8, g=3), INVALID), (dict(scale=math.inf), INVALID), (dict(h=128, g=1), UNSUPPORTED),
+])
+def test_paged_attention_host_checks(lib, kw, code):
+    assert _attn_paged(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", PAGED_GEOMETRY_CASES + [
+    (dict(kn=0), INVALID), (dict(vn=A + 0x2002), INVALID), (dict(pos=0), INVALID),
+    (dict(pos=A + 0x5001), INVALID), (dict(q=0), INVALID), (dict(k=A + 0x3008), INVALID),
+    (dict(h=8, g=3), INVALID),
+])
+def test_paged_step_host_checks(lib, kw, code):
+    assert _step_paged(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", PAGED_GEOMETRY_CASES + [
+    (dict(kn=0), INVALID), (dict(vc=0), INVALID), (dict(pos=0), INVALID),
+    (dict(kc=A + 0x2008), INVALID), (dict(pos=A + 0x4001), INVALID),
+])
+def test_paged_append_host_checks(lib, kw, code):
+    assert _append_paged(lib, **kw) == code
