@@ -6,7 +6,7 @@ step appends one token's K/V and runs attention in all 80 layers back to back, o
 (mqa_decode_step) per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--paged PAGE_SIZE]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
 with inputs resident in HBM (lower is better), from CUDA-graph replays of the whole step (every
@@ -22,6 +22,10 @@ written, new rows read and written) against the measured copy bandwidth; its lau
 come from a second timed pass of K steps whose graphs carry CUDA event nodes around every launch.
 ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same workload. The reference
 arm (``--impl reference``) times that oracle as the reference.
+
+``--paged PAGE_SIZE`` runs the same workload with every layer's cache held in page pools (the rows
+each sequence attends, laid out in pages of PAGE_SIZE rows in a seeded random order, one page table
+shared by all layers) through the paged calls (``mqa_decode_step_paged``).
 
 Every layer of the default workload reads about 0.7 GB of cache (above the 126 MB L2) and a step
 reads about 57 GB, so no L2 flush is needed between its timed steps.
@@ -229,7 +233,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config(w, args.paged),
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": detail},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -251,11 +255,20 @@ def needs_l2_flush(w) -> bool:
     return step_kv_bytes(w) < 2 * L2_BYTES
 
 
-def workload_config(w):
+def workload_config(w, paged: int = 0):
     return {"workload": w.name, "b": w.b, "h": w.h, "g": w.g, "d_h": w.d_h, "layers": w.layers,
             "context": [w.ctx_lo, w.ctx_hi], "n_max": w.n_max, "kv_dtype": "bf16",
+            "kv_layout": (f"paged, {paged}-row pages in a seeded random order" if paged
+                          else "contiguous [b, g, n_max, d_h]"),
             "l2": ("L2 flushed between steps (256 MB write)" if needs_l2_flush(w)
                    else "inputs larger than L2 (no flush)")}
+
+
+PAGE_TABLE_SEED = 4242
+
+
+def traffic_key(w, paged: int = 0) -> str:
+    return w.name + (f"_paged{paged}" if paged else "")
 
 
 # ------------------------------------------------------------------------------------------------
@@ -276,9 +289,16 @@ def run_ours(args, world, rank, local):
     pos, lens = inputs.positions_and_lengths(w)
     pos_d, lens_d = pos.to(dev), lens.to(dev)
     layers, xs, outs = [], [], []
+    table_d = None
     for li in range(w.layers):
         k, v = inputs.cache(w, li, dev, tail="random")
-        layers.append(LayerState(k, v))
+        if args.paged:
+            # the same rows in page pools; one page table (a seeded shuffle of the pages that the
+            # attended rows need) shared by every layer
+            k, v, table = inputs.page_pool(k, v, lens, args.paged, seed=PAGE_TABLE_SEED)
+            if table_d is None:
+                table_d = table.to(dev)
+        layers.append(LayerState(k, v, table_d))
         xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
         outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
     # small workloads fit in L2: flush it between steps by writing a buffer twice its size
@@ -423,7 +443,7 @@ def run_ours(args, world, rank, local):
         peak, peak_kind = measured_peak_hbm()
         nbytes = kv_bytes(w, lens)
         achieved = nbytes / attn_avg_s / 1e9
-        traffic = recorded_traffic(w.name)
+        traffic = recorded_traffic(traffic_key(w, args.paged))
         # weak scaling: every rank runs its own full step; N steps finish in ms_per_step
         value_us = ms_per_step * 1000.0 / world
         cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w)
@@ -431,7 +451,7 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(w),
+            "data": "synthetic", "config": workload_config(w, args.paged),
             "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
             "attention_us_per_layer": attn_avg_s * 1e6,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -461,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa_70b_80l", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
+                    help="keep the caches in page pools of this many rows (0: contiguous)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

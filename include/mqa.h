@@ -163,16 +163,17 @@ MQA_API int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_
  *   page_table       device, [b][max_pages] int32: row t of sequence bi (every KV head j) is row
  *                    t % page_size of page page_table[bi][t / page_size], i.e.
  *                    K[bi][j][t] = k_pool[page_table[bi][t / page_size]][j][t % page_size]
- *   page_size        8, 16 or 32, or a multiple of 64 (else MQA_ERR_UNSUPPORTED)
+ *   page_size        a power of two, at least 8 (else MQA_ERR_UNSUPPORTED)
  *   max_pages        entries per table row; a sequence addresses n_max = max_pages * page_size
  *                    rows (max_pages * page_size <= 2^31 - 1)
  *   num_pages        pages in each pool (num_pages * g < 2^31 - 1)
  *
  * Each call computes exactly what its contiguous counterpart computes on the cache the table
  * describes (the rows above, gathered into [b][g][n_max][d_h]); the tests compare the two through
- * the oracle's gather. Only the table entries of pages a call touches are read: those holding
+ * the oracle's gather. Only the table entries of pages a call touches are used: those holding
  * rows t < seq_lens[bi] (attention) and row pos[bi] (append), so entries past a sequence's last
- * page may hold anything (-1 for "no page", say). A touched entry outside [0, num_pages) latches
+ * page may hold anything (-1 for "no page", say; the table is read a batch of tiles ahead, so such
+ * entries may be loaded, but their values never matter). A used entry outside [0, num_pages) latches
  * MQA_ERR_DEVICE_BOUNDS; its rows read as zeros in attention and its append is skipped. Pages
  * may be shared between sequences (a common prefix) and read by all of them, but a page that a
  * call appends to must not be read by another sequence in the same call, and two sequences must

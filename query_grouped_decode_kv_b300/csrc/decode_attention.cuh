@@ -88,11 +88,12 @@ struct DecodeParams {
 __host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
 __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 
-// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags].
-// CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
+// Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags]
+// [page slots]. CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
 __host__ __device__ constexpr int smem_fixed_bytes(int D, int NW, int CR) {
   return kStages * stage_bytes(D) + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
-         (2 * kStages + 2) * 8 + 16;  // full, empty, cbar, stall; abort, merge flags
+         (2 * kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
+         32 * 4;                       // the paged producer's looked-up pages
 }
 __host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR) {
   return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR));
@@ -245,11 +246,15 @@ struct SharedLayout {
   uint64_t* stall;      // testing: a barrier nothing completes (DecodeParams::debug_stall)
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
+  int* pages;           // [32] paged caches: the pages of the tiles being issued (producer warp)
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
 template <int D, int NW, int CR>
 __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
+  static_assert((NW * CR * comb_row_floats(D) * 4) % 16 == 0 && (NW * CR * 8) % 16 == 0 &&
+                    ((2 * kStages + 2) * 8) % 16 == 0,
+                "regions keep 16-byte alignment (the page slots are read as int4)");
   SharedLayout s;
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
@@ -267,6 +272,8 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.abort = reinterpret_cast<volatile int*>(p);
   s.merge = s.abort + 1;
   p += 16;
+  s.pages = reinterpret_cast<int*>(p);  // 16-byte aligned: every region before it is a multiple
+  p += 32 * 4;                           // of 16 bytes
   return s;
 }
 
@@ -587,36 +594,111 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
 // ---------------------------------------------------------------------------------------------
 // Producer warp over paged caches. The tensor maps view each pool as (D, page_size,
 // num_pages * g) with boxes of R = min(page_size, kTileKeys) rows, so a tile's rows
-// [y, y + kTileKeys) arrive as kTileKeys / R boxes: box i holds rows y + i R .. y + (i+1) R - 1,
-// found at row (y + i R) % page_size of page page_table[bi][(y + i R) / page_size]. Every box
-// lands at a multiple of R * 128 bytes (>= 1 KB) inside the stage, so the 128-byte swizzle comes
-// out exactly as one box of the whole tile would give it. Boxes wholly at or past the length
-// are not loaded (those stage rows are never used). A page index out of range latches
-// MQA_ERR_DEVICE_BOUNDS and its box is read at a coordinate past the pool, which the copy
-// fills with zeros, so the sequence attends over zero rows there.
-// Lanes look up one box each (at most kTileKeys / 8 boxes) before the stage is free; lane 0
-// issues the copies.
+// [y, y + kTileKeys) arrive as up to NB = kTileKeys / R boxes: box i holds rows
+// y + i R .. y + (i+1) R - 1, found at row (y + i R) % page_size of page
+// page_table[bi][(y + i R) / page_size]. Every box lands at a multiple of R * 128 bytes (>= 1 KB)
+// inside the stage, so the 128-byte swizzle comes out exactly as one box of the whole tile would
+// give it. Boxes wholly at or past the length are not loaded (those stage rows are never used). A
+// page index out of range latches MQA_ERR_DEVICE_BOUNDS and its box is read at a coordinate past
+// the pool, which the copy fills with zeros, so the sequence attends over zero rows there.
+//
+// The producer is a single warp whose issue rate bounds the whole CTA once a tile takes several
+// copies, so its per-tile path is kept short: page sizes are powers of two (shifts and masks, no
+// division), NB is a compile-time constant, and the page-table reads are taken off the path. The
+// warp looks up the pages of T = 32 / NB tiles at once (lane l: box l % NB of tile l / NB of the
+// batch), one batch ahead of the tiles being issued, so each lookup's latency overlaps the batch
+// before it; at a batch's start the lanes leave its pages in 32 shared-memory slots, from which
+// one elected lane reads each tile's pages while it issues the tile's copies in one pass. A lookup reads only table entries below max_pages,
+// possibly some past the sequence's length, whose values are never used.
 // ---------------------------------------------------------------------------------------------
-template <int D>
+// Cursor of tile `base position + delta` of the CTA's range (global tile index x): the same
+// segment as `base` when it still has that many tiles, else a fresh search.
+__device__ __forceinline__ TileCursor cursor_ahead(const TileCursor& base, int delta,
+                                                   unsigned long long x, const TileIndex& ix) {
+  TileCursor c = base;
+  if (base.tile + delta < base.nt) c.tile = base.tile + delta;
+  else c.start(x, ix);
+  return c;
+}
+
+// The page holding box `lane % NB` of the tile at `c` (0 where that box starts past n_max).
+template <int NB>
+__device__ __forceinline__ int lookup_page(const DecodeParams& P, const TileCursor& c, int lane,
+                                           int page_shift) {
+  constexpr int R = kTileKeys / NB;
+  const int r = c.tile * kTileKeys + (lane % NB) * R;
+  if (r >= P.n_max) return 0;
+  return __ldg(P.page_table + static_cast<size_t>(c.bi) * P.max_pages + (r >> page_shift));
+}
+
+// The NB pages of tile kt of the current batch from the shared slots (16-byte aligned), with
+// vector loads.
+template <int NB>
+__device__ __forceinline__ void load_tile_pages(const int* slots, int kt, int (&pg)[NB]) {
+  if constexpr (NB == 8) {
+    const int4 a = reinterpret_cast<const int4*>(slots)[2 * kt];
+    const int4 b = reinterpret_cast<const int4*>(slots)[2 * kt + 1];
+    pg[0] = a.x; pg[1] = a.y; pg[2] = a.z; pg[3] = a.w;
+    pg[4] = b.x; pg[5] = b.y; pg[6] = b.z; pg[7] = b.w;
+  } else if constexpr (NB == 4) {
+    const int4 a = reinterpret_cast<const int4*>(slots)[kt];
+    pg[0] = a.x; pg[1] = a.y; pg[2] = a.z; pg[3] = a.w;
+  } else if constexpr (NB == 2) {
+    const int2 a = reinterpret_cast<const int2*>(slots)[kt];
+    pg[0] = a.x; pg[1] = a.y;
+  } else {
+    pg[0] = slots[kt];
+  }
+}
+
+template <int D, int NB>
 __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
                                                     const CUtensorMap* tm_v,
                                                     const DecodeParams& P, const SharedLayout& sh,
                                                     unsigned long long x0, int ntiles, int lane) {
   constexpr uint32_t kStageBytes = stage_bytes(D);
   constexpr uint32_t kKvBytes = kStageBytes / 2;
+  constexpr int R = kTileKeys / NB;  // rows per box
+  constexpr int T = 32 / NB;         // tiles per lookup batch
+  constexpr uint32_t kBoxBytes = R * kSwizzleRowBytes;
   const bool fused = P.pos != nullptr;
-  const int R = min(P.page_size, kTileKeys);
+  const int page_shift = __ffs(P.page_size) - 1;
+  const int page_mask = P.page_size - 1;
   const int z_past_pool = P.num_pages * P.g;
   if (lane == 0) {
     prefetch_tensor_map(tm_k);
     prefetch_tensor_map(tm_v);
   }
   const uint64_t policy = l2_policy_evict_first();
+  const int my_tile = lane / NB;  // this lane's tile within a lookup batch
   TileCursor cur;
   cur.start(x0, sh.tix);
+  // `pages_next`: this lane's page of the next batch; `ahead`: the cursor of that batch's first tile
+  TileCursor ahead = cur;
+  int pages_next = 0;
+  if (my_tile < ntiles)
+    pages_next = lookup_page<NB>(P, cursor_ahead(cur, my_tile, x0 + my_tile, sh.tix), lane,
+                                 page_shift);
   int issued = 0;
   int seq = -1, L = 0, row_p = -1;  // the sequence of the last tile, its length and append row
   for (int k = 0; k < ntiles; ++k) {
+    const int kt = k % T;
+    if (kt == 0) {
+      // batch k / T starts: publish its pages (looked up a batch ago) to lane 0 and look up the
+      // next batch
+      __syncwarp();
+      sh.pages[lane] = pages_next;
+      __syncwarp();
+      const int k1 = k + T;
+      if (k1 < ntiles) {
+        ahead = cursor_ahead(ahead, T, x0 + static_cast<unsigned long long>(k1), sh.tix);
+        if (k1 + my_tile < ntiles)
+          pages_next = lookup_page<NB>(P, cursor_ahead(ahead, my_tile,
+                                                       x0 + static_cast<unsigned long long>(
+                                                                k1 + my_tile), sh.tix),
+                                       lane, page_shift);
+      }
+    }
     if (cur.bi != seq) {
       seq = cur.bi;
       L = __ldg(P.seq_lens + seq);
@@ -626,22 +708,11 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       }
     }
     const int y = cur.tile * kTileKeys;
-    const int nbox = (min(L - y, kTileKeys) + R - 1) / R;  // L > y for every tile
-    int z = 0, yr = 0;
-    if (lane < nbox) {
-      const int r = y + lane * R;
-      const int page = __ldg(P.page_table + static_cast<size_t>(seq) * P.max_pages +
-                             r / P.page_size);
-      const bool bad = page < 0 || page >= P.num_pages;
-      if (bad) latch_status(kStatusDeviceBounds);
-      z = bad ? z_past_pool : page * P.g + cur.j;
-      yr = r % P.page_size;
-    }
     const int st = k % kStages;
     const uint32_t par = ((k / kStages) & 1) ^ 1;
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // the whole warp waits (no branch on the lane); a vote keeps the outcome warp-uniform
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort));
     if (!ok) {
       if (lane == 0 && !*sh.abort) give_up(sh, kSiteProducerEmpty, k);
       break;
@@ -651,25 +722,34 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       fence_proxy_async_global();
       __syncwarp();
     }
-    if (lane == 0)
-      mbar_arrive_expect_tx(&sh.full[st],
-                            static_cast<uint32_t>(nbox * R) * kSwizzleRowBytes * (D / 64) * 2);
-    uint8_t* kdst = sh.stages + st * kStageBytes;
-    uint8_t* vdst = kdst + kKvBytes;
-    for (int i = 0; i < nbox; ++i) {
-      const int zi = __shfl_sync(0xffffffffu, z, i);
-      const int yi = __shfl_sync(0xffffffffu, yr, i);
-      if (lane == 0) {
-        const int off = i * R * kSwizzleRowBytes;
+    // every lane holds the same values here; one elected lane issues the tile's copies
+    if (elect_one()) {
+      const int nbox = (min(L - y, kTileKeys) + R - 1) / R;  // L > y for every tile
+      mbar_arrive_expect_tx(&sh.full[st], static_cast<uint32_t>(nbox) * kBoxBytes * (D / 64) * 2);
+      uint8_t* kdst = sh.stages + st * kStageBytes;
+      uint8_t* vdst = kdst + kKvBytes;
+      int pg[NB];
+      load_tile_pages<NB>(sh.pages, kt, pg);
+      bool any_bad = false;
 #pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes + off, tm_k, &sh.full[st],
-                      half * 64, yi, zi, policy);
-          tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes + off, tm_v, &sh.full[st],
-                      half * 64, yi, zi, policy);
+      for (int i = 0; i < NB; ++i) {
+        if (i < nbox) {
+          const bool bad = static_cast<unsigned>(pg[i]) >= static_cast<unsigned>(P.num_pages);
+          any_bad |= bad;
+          const int z = bad ? z_past_pool : pg[i] * P.g + cur.j;
+          const int yr = (y + i * R) & page_mask;
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half) {
+            tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes + i * kBoxBytes, tm_k,
+                        &sh.full[st], half * 64, yr, z, policy);
+            tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes + i * kBoxBytes, tm_v,
+                        &sh.full[st], half * 64, yr, z, policy);
+          }
         }
       }
+      if (any_bad) latch_status(kStatusDeviceBounds);
     }
+    __syncwarp();
     ++issued;
     cur.advance(sh.tix);
   }
@@ -677,6 +757,22 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
   const volatile int never = 0;
   for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
     mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+}
+
+// Boxes per tile from the page size (8, 16, 32 rows; 64 or more: one box).
+template <int D>
+__device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
+                                                        const CUtensorMap* tm_v,
+                                                        const DecodeParams& P,
+                                                        const SharedLayout& sh,
+                                                        unsigned long long x0, int ntiles,
+                                                        int lane) {
+  switch (P.page_size) {
+    case 8: produce_tiles_paged<D, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 16: produce_tiles_paged<D, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 32: produce_tiles_paged<D, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    default: produce_tiles_paged<D, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1044,7 +1140,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   if (warp >= NW) {
     // ================================ producer ================================================
     if (warp == NW) {
-      if (P.page_table != nullptr) produce_tiles_paged<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+      if (P.page_table != nullptr) produce_tiles_paged_any<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
       else produce_tiles<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
     }
     return;

@@ -97,16 +97,14 @@ struct PagedCache {
   int page_size = 0, max_pages = 0, num_pages = 0;
 };
 
-// Host checks shared by the paged entry points. Page sizes: 8, 16 or 32 rows (a tile of 64 rows
-// spans several pages, one bulk copy each; a box of 8 or more rows keeps every copy on a 1 KB
-// boundary of the stage, where the 128-byte swizzle repeats), or a multiple of 64 (every tile
-// lies inside one page). Sets *n_max to the rows a sequence can address.
+// Host checks shared by the paged entry points. Page sizes: powers of two from 8 rows. With 8, 16
+// or 32 rows a tile of 64 rows spans several pages, one bulk copy each (a box of 8 or more rows
+// keeps every copy on a 1 KB boundary of the stage, where the 128-byte swizzle repeats); from 64
+// rows every tile lies inside one page. Sets *n_max to the rows a sequence can address.
 int check_paged(const PagedCache& pg, int g, int d_h, int* n_max) {
   if (!pg.table || (reinterpret_cast<uintptr_t>(pg.table) & 3u)) return MQA_ERR_INVALID_ARG;
   if (pg.page_size <= 0 || pg.max_pages <= 0 || pg.num_pages <= 0) return MQA_ERR_INVALID_ARG;
-  if (!(pg.page_size == 8 || pg.page_size == 16 || pg.page_size == 32 ||
-        pg.page_size % mqa::kTileKeys == 0))
-    return MQA_ERR_UNSUPPORTED;
+  if (pg.page_size < 8 || (pg.page_size & (pg.page_size - 1)) != 0) return MQA_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(pg.max_pages) * pg.page_size;
   if (rows > 0x7fffffffll) return MQA_ERR_UNSUPPORTED;
   if (static_cast<long long>(pg.num_pages) * g > 0x7fffffffll - 1) return MQA_ERR_UNSUPPORTED;

@@ -96,6 +96,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // ---------------------------------------------------------------------------------------------
 // Warpgroup register reallocation (all 128 threads of a warpgroup execute the same one).
 // ---------------------------------------------------------------------------------------------
+// One thread of the (fully active) warp is elected, the lowest active lane. A bulk tensor copy
+// takes warp-uniform operands; issuing it under an elected thread lets the compiler use the
+// values as they are, where a branch on the lane index costs a sequence of extra instructions per
+// copy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
   static_assert(N % 8 == 0 && N >= 24 && N <= 256, "register count");

@@ -165,11 +165,16 @@ def page_pool(k: torch.Tensor, v: torch.Tensor, rows: torch.Tensor, page_size: i
     v_pool = torch.full_like(k_pool, value)
     used = 0
     for bi in range(b):
-        for p in range(need[bi]):
-            page = int(order[used])
-            used += 1
-            table[bi, p] = page
-            r0, r1 = p * page_size, min((p + 1) * page_size, n_max)
-            k_pool[page, :, : r1 - r0] = k[bi, :, r0:r1]
-            v_pool[page, :, : r1 - r0] = v[bi, :, r0:r1]
+        n = need[bi]
+        pages = order[used:used + n]
+        used += n
+        table[bi, :n] = pages
+        r = min(n * page_size, n_max)
+        for src, pool in ((k, k_pool), (v, v_pool)):
+            rows_b = src[bi, :, :r]
+            if r < n * page_size:   # the last page runs past n_max: keep the fill there
+                rows_b = torch.cat([rows_b, torch.full((g, n * page_size - r, d_h), value,
+                                                       dtype=src.dtype, device=src.device)], 1)
+            pool[pages.to(src.device, torch.long)] = rows_b.reshape(g, n, page_size,
+                                                                    d_h).transpose(0, 1)
     return k_pool, v_pool, table

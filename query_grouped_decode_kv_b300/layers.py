@@ -16,8 +16,37 @@ from . import binding
 
 @dataclasses.dataclass
 class LayerState:
-    k_cache: torch.Tensor   # [b, g, n_max, d_h] bf16
+    """One layer's caches: contiguous [b, g, n_max, d_h] bf16, or, with a page table, page pools
+    [num_pages, g, page_size, d_h] whose pages ``page_table`` [b, max_pages] int32 lists per
+    sequence (the layers of a model normally share one table)."""
+    k_cache: torch.Tensor
     v_cache: torch.Tensor
+    page_table: torch.Tensor | None = None
+
+    def step(self, q, k_new, v_new, pos, seq_lens, out, scale, stream) -> None:
+        """One fused append + attention launch on this layer."""
+        if self.page_table is None:
+            binding.decode_step(q, k_new, v_new, self.k_cache, self.v_cache, pos, seq_lens,
+                                out=out, scale=scale, stream=stream)
+        else:
+            binding.decode_step_paged(q, k_new, v_new, self.k_cache, self.v_cache, pos,
+                                      self.page_table, seq_lens, out=out, scale=scale,
+                                      stream=stream)
+
+    def append(self, k_new, v_new, pos, stream) -> None:
+        if self.page_table is None:
+            binding.kv_append(k_new, v_new, self.k_cache, self.v_cache, pos, stream=stream)
+        else:
+            binding.kv_append_paged(k_new, v_new, self.k_cache, self.v_cache, pos,
+                                    self.page_table, stream=stream)
+
+    def attend(self, q, seq_lens, out, scale, stream) -> None:
+        if self.page_table is None:
+            binding.decode_attention(q, self.k_cache, self.v_cache, seq_lens, out=out,
+                                     scale=scale, stream=stream)
+        else:
+            binding.decode_attention_paged(q, self.k_cache, self.v_cache, self.page_table,
+                                           seq_lens, out=out, scale=scale, stream=stream)
 
 
 @dataclasses.dataclass
@@ -35,15 +64,13 @@ def decode_layers(layers: list[LayerState], step_in: list[StepInputs], pos: torc
     (the fused launch when ``fused``)."""
     for li, (lay, x, o) in enumerate(zip(layers, step_in, outs)):
         if not fused:
-            binding.kv_append(x.k_new, x.v_new, lay.k_cache, lay.v_cache, pos, stream=stream)
+            lay.append(x.k_new, x.v_new, pos, stream)
         if attn_events is not None:
             attn_events[li][0].record(stream)
         if fused:
-            binding.decode_step(x.q, x.k_new, x.v_new, lay.k_cache, lay.v_cache, pos, seq_lens,
-                                out=o, scale=scale, stream=stream)
+            lay.step(x.q, x.k_new, x.v_new, pos, seq_lens, o, scale, stream)
         else:
-            binding.decode_attention(x.q, lay.k_cache, lay.v_cache, seq_lens, out=o, scale=scale,
-                                     stream=stream)
+            lay.attend(x.q, seq_lens, o, scale, stream)
         if attn_events is not None:
             attn_events[li][1].record(stream)
 
@@ -109,9 +136,8 @@ class HostStepPipeline:
     def _compute(self, c0: int, c1: int, pos, seq_lens, scale: float, stream) -> None:
         b = self.buf
         for li in range(c0, c1):
-            lay = self.layers[li]
-            binding.decode_step(b.q_dev[li], b.kn_dev[li], b.vn_dev[li], lay.k_cache, lay.v_cache,
-                                pos, seq_lens, out=b.out_dev[li], scale=scale, stream=stream)
+            self.layers[li].step(b.q_dev[li], b.kn_dev[li], b.vn_dev[li], pos, seq_lens,
+                                 b.out_dev[li], scale, stream)
 
     def run(self, pos: torch.Tensor, seq_lens: torch.Tensor, scale: float,
             stream: torch.cuda.Stream) -> None:

@@ -168,7 +168,7 @@ PAGED_GEOMETRY_CASES = [
     (dict(table=0), INVALID), (dict(table=A + 0x8002), INVALID),
     (dict(page_size=0), INVALID), (dict(max_pages=0), INVALID), (dict(num_pages=-1), INVALID),
     (dict(page_size=24), UNSUPPORTED), (dict(page_size=48), UNSUPPORTED),
-    (dict(page_size=4), UNSUPPORTED),
+    (dict(page_size=4), UNSUPPORTED), (dict(page_size=192), UNSUPPORTED),
     (dict(page_size=64, max_pages=1 << 26), UNSUPPORTED),   # 2^32 addressable rows
     (dict(num_pages=1 << 30), UNSUPPORTED),                 # num_pages * g past int32
     (dict(d_h=96), UNSUPPORTED), (dict(b=0), INVALID), (dict(g=0), INVALID),
