@@ -54,7 +54,7 @@ typedef enum mqa_status {
   MQA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, non-positive size, h % g != 0, ... */
   MQA_ERR_UNSUPPORTED = 2,    /* a valid request outside what the kernels implement */
   MQA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
-  MQA_ERR_DEVICE_BOUNDS = 4,  /* (latched) a pos or seq_lens entry was out of range */
+  MQA_ERR_DEVICE_BOUNDS = 4,  /* (latched) a pos, seq_lens or used page-table entry was out of range */
   MQA_ERR_TIMEOUT = 5         /* (latched) an in-kernel wait exceeded its time limit */
 } mqa_status;
 

@@ -524,9 +524,9 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
 
 // ---------------------------------------------------------------------------------------------
 // Producer warp: stream the CTA's tiles [x0, x0 + ntiles) into the stage ring with bulk tensor
-// copies (lane 0), after writing the fused append's new row into the cache when the tile holds it
-// (whole warp, one 16-byte chunk per lane). Stage st is refilled once its `empty` barrier has
-// completed the phase of its previous use.
+// copies (one elected lane), after writing the fused append's new row into the cache when the
+// tile holds it (whole warp, one 16-byte chunk per lane). Stage st is refilled once its `empty`
+// barrier has completed the phase of its previous use.
 // ---------------------------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
@@ -535,7 +535,6 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   constexpr uint32_t kStageBytes = stage_bytes(D);
   constexpr uint32_t kKvBytes = kStageBytes / 2;
   const bool fused = P.pos != nullptr;
-  if (!fused && lane != 0) return;
   if (lane == 0) {
     prefetch_tensor_map(tm_k);
     prefetch_tensor_map(tm_v);
@@ -548,9 +547,9 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
     const uint32_t par = ((k / kStages) & 1) ^ 1;
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort);
-    if (fused) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // the whole warp waits (no branch on the lane); a vote keeps the outcome warp-uniform
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait_bounded(&sh.empty[st], par, P.timeout_ns, sh.abort));
     if (!ok) {
       if (lane == 0 && !*sh.abort) give_up(sh, kSiteProducerEmpty, k);
       break;
@@ -564,10 +563,11 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
       if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
         write_new_row<D>(P, cur.bi, cur.j, row_p, lane);
         fence_proxy_async_global();  // each writer orders its store before the async proxy...
-        __syncwarp();                // ...and lane 0 issues the copy after every writer
+        __syncwarp();                // ...and the copy is issued after every writer
       }
     }
-    if (lane == 0) {
+    // every lane holds the same values here; one elected lane issues the tile's copies
+    if (elect_one()) {
       mbar_arrive_expect_tx(&sh.full[st], kStageBytes);
       const int z = cur.bi * P.g + cur.j;
       const int y = cur.tile * kTileKeys;
@@ -581,6 +581,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
                     z, policy);
       }
     }
+    __syncwarp();
     ++issued;
     cur.advance(sh.tix);
   }

@@ -467,7 +467,8 @@ const char* mqa_status_string(int status) {
     case MQA_ERR_INVALID_ARG: return "MQA_ERR_INVALID_ARG: invalid argument";
     case MQA_ERR_UNSUPPORTED: return "MQA_ERR_UNSUPPORTED: shape or setting not supported";
     case MQA_ERR_CUDA: return "MQA_ERR_CUDA: CUDA runtime error";
-    case MQA_ERR_DEVICE_BOUNDS: return "MQA_ERR_DEVICE_BOUNDS: pos or seq_lens out of range";
+    case MQA_ERR_DEVICE_BOUNDS:
+      return "MQA_ERR_DEVICE_BOUNDS: a pos, seq_lens or page-table entry out of range";
     case MQA_ERR_TIMEOUT: return "MQA_ERR_TIMEOUT: an in-kernel wait timed out";
     default: return "unknown mqa status";
   }

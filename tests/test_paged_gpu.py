@@ -242,3 +242,77 @@ def test_paged_rejects_the_tcgen05_path(mqa):
         assert e.value.status == 2
     finally:
         mqa.debug_override(0, 0)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_launches"])
+def test_paged_layers_share_one_table(mqa, fused):
+    # four layers, each with its own page pools, one page table shared by all of them, driven by
+    # layers.decode_layers; every layer against the oracle's paged append + gather + attention
+    from query_grouped_decode_kv_b300.layers import LayerState, StepInputs, decode_layers
+    ps, n_layers = 16, 4
+    dev = torch.device("cuda")
+    w = inputs.custom("paged_layers", 3, 16, 2, 128, 50, 600, wid=1100)
+    pos, lens = inputs.positions_and_lengths(w)
+    cases, layers, xs = [], [], []
+    table = None
+    for li in range(n_layers):
+        lw = inputs.custom("paged_layers", 3, 16, 2, 128, 50, 600, wid=1100 + li)
+        k, v = inputs.cache(lw, 0, "cpu", tail="nan", lengths=pos)
+        kp, vp, t = inputs.page_pool(k, v, lens, ps, seed=1199, spare_pages=2)
+        assert table is None or torch.equal(t, table)   # same seed and lengths: the same table
+        table = t
+        q, kn, vn = inputs.step_inputs(lw, 0, "cpu")
+        cases.append(dict(q=q, k_new=kn, v_new=vn, k_pool=kp, v_pool=vp, table=t, pos=pos,
+                          lens=lens, page_size=ps, scale=w.scale))
+        layers.append(LayerState(kp.to(dev), vp.to(dev), None))
+        xs.append(StepInputs(q.to(dev), kn.to(dev), vn.to(dev)))
+    table_d = table.to(dev)
+    for lay in layers:
+        lay.page_table = table_d
+    outs = [torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev)
+            for _ in range(n_layers)]
+    decode_layers(layers, xs, pos.to(dev), lens.to(dev), outs, w.scale, fused=fused)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    for li, (case, lay, o) in enumerate(zip(cases, layers, outs)):
+        kp_ref, vp_ref, out_ref, st, _ = oracle_paged_step(case)
+        assert st == oracle.OK
+        assert np.array_equal(P.bits(lay.k_cache), kp_ref), f"layer {li} K pool"
+        assert np.array_equal(P.bits(lay.v_cache), vp_ref), f"layer {li} V pool"
+        P.assert_close(o, out_ref, f"paged layer {li}")
+
+
+def test_paged_host_pipeline_matches_the_device_step(mqa):
+    # the host-buffer pipeline drives paged layers through the same fused calls
+    from query_grouped_decode_kv_b300.layers import (HostStepBuffers, HostStepPipeline,
+                                                     LayerState, StepInputs, decode_layers)
+    ps, n_layers = 32, 5
+    dev = torch.device("cuda")
+    w = inputs.custom("paged_host", 2, 32, 4, 128, 100, 700, wid=1200)
+    pos, lens = inputs.positions_and_lengths(w)
+    pos_d, lens_d = pos.to(dev), lens.to(dev)
+    lay_a, lay_b, xs = [], [], []
+    for li in range(n_layers):
+        lw = inputs.custom("paged_host", 2, 32, 4, 128, 100, 700, wid=1200 + li)
+        k, v = inputs.cache(lw, 0, dev, tail="nan", lengths=pos)
+        kp, vp, t = inputs.page_pool(k, v, lens, ps, seed=1299)
+        td = t.to(dev)
+        lay_a.append(LayerState(kp.clone(), vp.clone(), td))
+        lay_b.append(LayerState(kp, vp, td))
+        xs.append(StepInputs(*inputs.step_inputs(lw, 0, dev)))
+    outs = [torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev)
+            for _ in range(n_layers)]
+    decode_layers(lay_a, xs, pos_d, lens_d, outs, w.scale)
+    buf = HostStepBuffers.allocate(n_layers, w.b, w.h, w.g, w.d_h, dev)
+    for li, x in enumerate(xs):
+        buf.q_host[li].copy_(x.q.cpu())
+        buf.kn_host[li].copy_(x.k_new.cpu())
+        buf.vn_host[li].copy_(x.v_new.cpu())
+    HostStepPipeline(lay_b, buf, chunk=2).run(pos_d, lens_d, w.scale,
+                                              torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    for li in range(n_layers):
+        assert torch.equal(buf.out_host[li].view(torch.int16), outs[li].cpu().view(torch.int16))
+        assert torch.equal(lay_b[li].k_cache.view(torch.int16), lay_a[li].k_cache.view(torch.int16))
+        assert torch.equal(lay_b[li].v_cache.view(torch.int16), lay_a[li].v_cache.view(torch.int16))
