@@ -22,6 +22,12 @@ What each function computes, and the passage it follows:
   16-token blocks; ybb.press page §十 item 12); attention over it is attention over the gathered
   rows.
 
+* :func:`e4m3_to_f64` / :func:`f64_to_e4m3` -- the 8-bit float format E4M3 from its bit layout
+  (round to nearest, ties to even, saturating at +-448); :func:`kv_append_fp8` quantizes the new
+  rows into fp8 caches with one scale per tensor, :func:`dequantize_e4m3` undoes it, and
+  :func:`decode_attention_fp8` is attention over the dequantized caches (quantized K/V caches:
+  ybb.press page §十 item 7, nanhubrain.csdn.net MQA article §4.3).
+
 Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms, the pages' printed
 numbers, invariants and library routines.
 """
@@ -64,6 +70,15 @@ def _configure(lib):
     lib.oracle_gather_pages.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.oracle_kv_append_paged.restype = i32
     lib.oracle_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
+    lib.oracle_e4m3_to_double.restype = dbl
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_double_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_double_to_e4m3.argtypes = [dbl]
+    lib.oracle_kv_append_fp8.restype = i32
+    lib.oracle_kv_append_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                         ctypes.c_float]
+    lib.oracle_dequantize_e4m3.restype = i32
+    lib.oracle_dequantize_e4m3.argtypes = [vp, ctypes.c_size_t, dbl, vp]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -234,3 +249,58 @@ def kv_append_paged(k_new, v_new, k_pool, v_pool, pos, table) -> int:
     b, max_pages = tb.shape
     return int(lib.oracle_kv_append_paged(_ptr(kn), _ptr(vn), _ptr(k_pool), _ptr(v_pool), _ptr(p),
                                           _ptr(tb), b, g, d_h, page_size, max_pages, num_pages))
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """E4M3 codes (uint8) -> float64 values (NaN for the two NaN codes)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_e4m3_to_double(int(x)) for x in c.ravel()],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def f64_to_e4m3(x) -> np.ndarray:
+    """float64 -> E4M3 codes: nearest, ties to even, saturating at +-448."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    return np.array([lib.oracle_double_to_e4m3(float(v)) for v in a.ravel()],
+                    dtype=np.uint8).reshape(a.shape)
+
+
+def dequantize_e4m3(codes, scale: float) -> np.ndarray:
+    """codes * scale in float64 (any shape)."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    st = int(lib.oracle_dequantize_e4m3(_ptr(c), c.size, float(scale), _ptr(out)))
+    if st:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, pos, k_scale: float, v_scale: float) -> int:
+    """Quantize this step's rows (bf16 bit patterns) into fp8 caches, in place (caches:
+    C-contiguous uint8 numpy arrays [b, g, n_max, d_h])."""
+    lib = _load()
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint8 and c.flags.c_contiguous):
+            raise TypeError("caches must be C-contiguous uint8 numpy arrays (updated in place)")
+    b, g, n_max, d_h = k_cache.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    p = _c(pos, np.int32)
+    st = int(lib.oracle_kv_append_fp8(_ptr(kn), _ptr(vn), _ptr(k_cache), _ptr(v_cache), _ptr(p),
+                                      b, g, d_h, n_max, float(k_scale), float(v_scale)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return st
+
+
+def decode_attention_fp8(q, k_codes, v_codes, seq_lens, k_scale: float, v_scale: float,
+                         scale: float, threads: int = 0, return_status: bool = False):
+    """Attention over fp8 caches: the caches dequantized (codes * scale, exact in float64), then
+    :func:`decode_attention` on them with ``q`` (bf16 bit patterns) widened exactly."""
+    qf = bf16_to_f64(np.asarray(q, dtype=np.uint16))
+    kf = dequantize_e4m3(k_codes, k_scale)
+    vf = dequantize_e4m3(v_codes, v_scale)
+    return decode_attention(qf, kf, vf, seq_lens, scale, threads=threads,
+                            return_status=return_status)

@@ -112,6 +112,93 @@ uint16_t oracle_double_to_bf16(double x) {
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* fp8 E4M3 (the OCP 8-bit format with 4 exponent bits and no infinities) <-> double, written  */
+/* from its bit layout: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits. Exponent field */
+/* 15 with fraction 7 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448; exponent    */
+/* field 0 holds the subnormals frac/8 * 2^-6. Quantized caches ([GQA-MQA] §十 item 7 and      */
+/* [MQA-CSDN] §4.3 on quantizing K/V at low bit widths; the format and scaling are this        */
+/* build's reading, see the design notes).                                                    */
+/* ------------------------------------------------------------------------------------------ */
+double oracle_e4m3_to_double(uint8_t code) {
+  int sign = (code >> 7) & 1;
+  int expo = (code >> 3) & 0xF;
+  int frac = code & 0x7;
+  double mag;
+  if (expo == 0xF && frac == 0x7) {
+    mag = NAN;
+  } else if (expo == 0) {
+    mag = ldexp((double)frac, -9);                  /* frac/8 * 2^-6 */
+  } else {
+    mag = ldexp((double)(8 + frac), expo - 7 - 3);  /* (1 + frac/8) * 2^(expo - 7) */
+  }
+  return sign ? -mag : mag;
+}
+
+/* Round a double to the nearest E4M3 value, ties to even; magnitudes beyond 448 saturate to   */
+/* +-448 (the largest finite value), NaN gives 0x7F. Returns the code.                         */
+uint8_t oracle_double_to_e4m3(double x) {
+  if (isnan(x)) return 0x7F;
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);
+  int E = e2 - 1;                              /* a in [2^E, 2^(E+1)) */
+  int spacing_exp = (E < -6) ? -9 : (E - 3);   /* grid step: 2^-9 below 2^-6, else 2^(E-3) */
+  double units = ldexp(a, -spacing_exp);
+  double r = floor(units);
+  double rem = units - r;
+  if (rem > 0.5 || (rem == 0.5 && fmod(r, 2.0) == 1.0)) r += 1.0;   /* ties to the even code */
+  double v = ldexp(r, spacing_exp);
+  if (v == 0.0) return sign;
+  if (v < ldexp(1.0, -6)) return sign | (uint8_t)r;   /* subnormal: the code is the fraction */
+  int ev;
+  frexp(v, &ev);
+  int Ev = ev - 1;                             /* v in [2^Ev, 2^(Ev+1)), Ev in [-6, 8] */
+  uint8_t frac = (uint8_t)(ldexp(v, 3 - Ev) - 8.0);
+  return sign | (uint8_t)((Ev + 7) << 3) | frac;
+}
+
+/* Quantized append: row pos[b] of every KV head j receives the codes                          */
+/*     e4m3( float(k_new[b][j][d]) / k_scale )   (and v_new with v_scale),                     */
+/* the division done once in binary32 (IEEE, rounded to nearest), then rounded to E4M3 as      */
+/* above. A position outside [0, n_max) skips that sequence and reports ORACLE_ERR_BOUNDS.     */
+int oracle_kv_append_fp8(const uint16_t* k_new, const uint16_t* v_new, uint8_t* k_cache,
+                         uint8_t* v_cache, const int32_t* pos, int b, int g, int d_h, int n_max,
+                         float k_scale, float v_scale) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return ORACLE_ERR_INVALID_ARG;
+  if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale))
+    return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    const int p = pos[bi];
+    if (p < 0 || p >= n_max) { status = ORACLE_ERR_BOUNDS; continue; }
+    for (int j = 0; j < g; ++j) {
+      const size_t src = ((size_t)bi * g + j) * (size_t)d_h;
+      const size_t row = ((size_t)bi * g + j) * (size_t)n_max + (size_t)p;
+      const size_t dst = row * (size_t)d_h;
+      for (int d = 0; d < d_h; ++d) {
+        volatile float kq = (float)oracle_bf16_to_double(k_new[src + d]) / k_scale;
+        volatile float vq = (float)oracle_bf16_to_double(v_new[src + d]) / v_scale;
+        k_cache[dst + d] = oracle_double_to_e4m3((double)kq);
+        v_cache[dst + d] = oracle_double_to_e4m3((double)vq);
+      }
+    }
+  }
+  return status;
+}
+
+/* Dequantize: out[i] = e4m3(codes[i]) * scale, in double (exact: a 4-bit significand times a  */
+/* binary32 scale).                                                                            */
+int oracle_dequantize_e4m3(const uint8_t* codes, size_t n, double scale, double* out) {
+  if (!codes || !out) return ORACLE_ERR_INVALID_ARG;
+  for (size_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_double(codes[i]) * scale;
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* KV append: [GQA-MQA] §八 (cache_k[:, start:start+T] = k with T = 1);                      */
 /* [MQA-CSDN] §2.2 (concat along the sequence axis). Bit copy of one row per (b, KV head).    */
 /* ------------------------------------------------------------------------------------------ */

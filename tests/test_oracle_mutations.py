@@ -37,6 +37,16 @@ MUTANTS = [
      "(size_t)((t + 1) % page_size)) * (size_t)d_h;"),
     ("paged_append_wrong_row", "(size_t)(p % page_size)) *",
      "(size_t)((p + 1) % page_size)) *"),
+    ("e4m3_exponent_bias", "mag = ldexp((double)(8 + frac), expo - 7 - 3);",
+     "mag = ldexp((double)(8 + frac), expo - 6 - 3);"),
+    ("e4m3_ties_away_from_zero", "(rem == 0.5 && fmod(r, 2.0) == 1.0)", "(rem == 0.5)"),
+    ("e4m3_subnormal_step", "int spacing_exp = (E < -6) ? -9 : (E - 3);",
+     "int spacing_exp = (E < -7) ? -10 : (E - 3);"),
+    ("e4m3_overflow_to_nan", "if (a >= 448.0) return sign | 0x7E;",
+     "if (a >= 448.0) return sign | 0x7F;"),
+    ("fp8_append_wrong_row", "(size_t)n_max + (size_t)p;\n", "(size_t)n_max + (size_t)(p ^ 1);\n"),
+    ("fp8_append_without_scale", "(float)oracle_bf16_to_double(k_new[src + d]) / k_scale;",
+     "(float)oracle_bf16_to_double(k_new[src + d]);"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

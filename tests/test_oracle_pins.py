@@ -502,3 +502,146 @@ def test_paged_attention_brute_force_through_the_table():
             for d in range(d_h):
                 ref = sum(wt * vf[p, j, r, d] for wt, (p, r) in zip(w, rows)) / tot
                 assert abs(got[bi, i, d] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+# --------------------------------------------------------------------------------------------
+# fp8 E4M3 and the quantized cache
+# --------------------------------------------------------------------------------------------
+def _torch_e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.float().numpy().astype(np.float64)
+
+
+def test_e4m3_decode_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours, ref = oracle.e4m3_to_f64(codes), _torch_e4m3_decode(codes)
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    assert np.array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)])
+    # the format's landmarks: largest finite, smallest normal, smallest subnormal, one
+    assert ours[0x7E] == 448.0 and ours[0x08] == 2.0 ** -6 and ours[0x01] == 2.0 ** -9
+    assert ours[0x38] == 1.0 and ours[0xB8] == -1.0 and np.isnan(ours[0x7F])
+
+
+def test_e4m3_encode_matches_torch_on_every_bf16_value_in_range():
+    """Every finite bfloat16 value of magnitude <= 448 rounds to the code torch's
+    float8_e4m3fn conversion gives (nearest, ties to even)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = oracle.bf16_to_f64(bits)
+    keep = np.isfinite(x) & (np.abs(x) <= 448.0)
+    xs = x[keep]
+    ref = torch.from_numpy(xs.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(oracle.f64_to_e4m3(xs), ref.numpy())
+
+
+def test_e4m3_encode_is_the_nearest_code_ties_to_even():
+    """Brute force over the 127 non-negative finite codes, on random values and on every
+    midpoint between neighbouring codes."""
+    codes = np.arange(0x7F, dtype=np.uint8)
+    vals = oracle.e4m3_to_f64(codes)                      # increasing
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.uniform(0, 448, 500), np.exp(rng.uniform(-12, 6, 500)),
+                         (vals[:-1] + vals[1:]) / 2])
+    for x in xs:
+        d = np.abs(vals - x)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]
+        assert oracle.f64_to_e4m3(np.array([x]))[0] == want, x
+        assert oracle.f64_to_e4m3(np.array([-x]))[0] == (want | 0x80 if x > 0 else 0x80), x
+
+
+def test_e4m3_encode_saturates_beyond_the_largest_finite_value():
+    got = oracle.f64_to_e4m3(np.array([448.0, 448.5, 464.0, 1e4, np.inf, -1e4, -np.inf]))
+    assert list(got) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+
+
+def test_fp8_append_quantizes_with_the_scale_in_binary32():
+    """The codes written are e4m3(float32(x) / float32(scale)): closed forms, and the
+    round trip code * scale stays within half a step of x."""
+    b, g, n_max, d_h = 2, 2, 5, 8
+    rng = np.random.default_rng(5)
+    kn = oracle.f64_to_bf16(rng.standard_normal((b, g, d_h)) * 3.0)
+    vn = oracle.f64_to_bf16(rng.standard_normal((b, g, d_h)) * 0.01)
+    kc = np.zeros((b, g, n_max, d_h), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    pos = np.array([4, 0], dtype=np.int32)
+    ks, vs = 0.05, 1.0 / 4096
+    assert oracle.kv_append_fp8(kn, vn, kc, vc, pos, ks, vs) == oracle.OK
+    kx, vx = oracle.bf16_to_f64(kn), oracle.bf16_to_f64(vn)
+    for bi in range(b):
+        for j in range(g):
+            for d in range(d_h):
+                for x, cache, sc in ((kx, kc, ks), (vx, vc, vs)):
+                    y = np.float32(np.float32(x[bi, j, d]) / np.float32(sc))
+                    code = cache[bi, j, pos[bi], d]
+                    assert code == _torch_e4m3_to_code(float(y))
+                    back = oracle.e4m3_to_f64(np.array([code]))[0] * np.float32(sc)
+                    step = 2.0 ** (math.floor(math.log2(max(abs(y), 2.0 ** -6))) - 3) * sc
+                    assert abs(back - x[bi, j, d]) <= step / 2 + 1e-12
+    # every other byte is untouched
+    mask = np.ones_like(kc, dtype=bool)
+    for bi in range(b):
+        mask[bi, :, pos[bi]] = False
+    assert not kc[mask].any() and not vc[mask].any()
+    # closed forms: 1.0 / 0.5 = 2 -> 0x40; 1.0 / 3.0 rounds to 11/32 -> 0x2B
+    one = oracle.f64_to_bf16(np.ones((1, 1, 1)))
+    for sc, want in ((0.5, 0x40), (3.0, 0x2B), (1.0 / 1024, 0x7E)):
+        c1 = np.zeros((1, 1, 1, 1), dtype=np.uint8)
+        c2 = np.zeros_like(c1)
+        assert oracle.kv_append_fp8(one, one, c1, c2, np.array([0], np.int32), sc, sc) == 0
+        assert c1[0, 0, 0, 0] == want and c2[0, 0, 0, 0] == want
+
+
+def _torch_e4m3_to_code(y: float) -> int:
+    if abs(y) > 448.0:
+        return 0x7E | (0x80 if y < 0 else 0)
+    return int(torch.tensor([y], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8))
+
+
+def test_fp8_append_rejects_a_bad_position_without_writing():
+    kn = oracle.f64_to_bf16(np.ones((2, 1, 4)))
+    kc = np.zeros((2, 1, 3, 4), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    st = oracle.kv_append_fp8(kn, kn, kc, vc, np.array([3, -1], np.int32), 1.0, 1.0)
+    assert st == oracle.ERR_BOUNDS and not kc.any() and not vc.any()
+
+
+def test_fp8_attention_brute_force_on_decoded_codes():
+    """Attention over fp8 caches equals pure-Python attention over torch's decoding of the codes
+    times the scales."""
+    b, h, g, d_h, n_max = 2, 4, 2, 8, 6
+    rng = np.random.default_rng(17)
+    kc = rng.integers(0, 256, (b, g, n_max, d_h), dtype=np.uint8)
+    vc = rng.integers(0, 256, (b, g, n_max, d_h), dtype=np.uint8)
+    for c in (kc, vc):                                     # no NaN codes
+        c[(c & 0x7F) == 0x7F] = 0x3C
+    q = oracle.f64_to_bf16(rng.standard_normal((b, h, d_h)))
+    lens = np.array([6, 3], dtype=np.int32)
+    ks, vs, scale = 0.01, 0.25, 0.3
+    got = oracle.decode_attention_fp8(q, kc, vc, lens, ks, vs, scale)
+    kf, vf = _torch_e4m3_decode(kc) * ks, _torch_e4m3_decode(vc) * vs
+    qf = oracle.bf16_to_f64(q)
+    for bi in range(b):
+        for i in range(h):
+            j = i // (h // g)
+            s = [scale * sum(qf[bi, i, d] * kf[bi, j, t, d] for d in range(d_h))
+                 for t in range(int(lens[bi]))]
+            m = max(s)
+            w = [math.exp(x - m) for x in s]
+            for d in range(d_h):
+                ref = sum(w[t] * vf[bi, j, t, d] for t in range(len(w))) / sum(w)
+                assert abs(got[bi, i, d] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_fp8_scales_fold_into_the_logit_scale_and_the_output():
+    """k_scale multiplies every logit and v_scale every output: doubling k_scale equals doubling
+    the logit scale, and doubling v_scale doubles the output exactly."""
+    b, h, g, d_h, n_max = 1, 4, 1, 16, 9
+    rng = np.random.default_rng(23)
+    kc = oracle.f64_to_e4m3(rng.standard_normal((b, g, n_max, d_h)) * 30)
+    vc = oracle.f64_to_e4m3(rng.standard_normal((b, g, n_max, d_h)) * 30)
+    q = oracle.f64_to_bf16(rng.standard_normal((b, h, d_h)))
+    lens = np.array([9], dtype=np.int32)
+    a = oracle.decode_attention_fp8(q, kc, vc, lens, 0.02, 0.5, 0.25)
+    assert np.allclose(oracle.decode_attention_fp8(q, kc, vc, lens, 0.04, 0.5, 0.25),
+                       oracle.decode_attention_fp8(q, kc, vc, lens, 0.02, 0.5, 0.5), rtol=1e-13)
+    assert np.array_equal(oracle.decode_attention_fp8(q, kc, vc, lens, 0.02, 1.0, 0.25), 2 * a)
