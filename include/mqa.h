@@ -199,6 +199,43 @@ MQA_API int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new,
                                   float scale, void* stream);
 
 /*
+ * fp8 caches: mqa_kv_append_fp8, mqa_decode_attention_fp8, mqa_decode_step_fp8.
+ *
+ * The same three operations over caches that hold 8-bit floating-point codes (E4M3: 1 sign, 4
+ * exponent and 3 fraction bits, exponent bias 7, no infinities, largest finite value 448) with
+ * one scale per tensor: an element's value is code * k_scale (K) or code * v_scale (V). This
+ * halves the bytes the bandwidth-bound path reads. The pages discuss quantizing the K/V cache
+ * ("GQA与MQA深度实战" (ybb.press) §十 item 7; the nanhubrain.csdn.net MQA article §4.3 warns that
+ * K/V shared by many query heads makes quantization error count more) but fix no format; this
+ * library's reading is E4M3 with per-tensor scales, the scales chosen by the caller.
+ *
+ *   k_cache, v_cache device, [b][g][n_max][d_h] uint8 E4M3 codes, 16-byte aligned
+ *   k_scale, v_scale finite and > 0 (else MQA_ERR_INVALID_ARG)
+ *   d_h              128 (else MQA_ERR_UNSUPPORTED)
+ *   everything else  as for the bf16 calls
+ *
+ * Append: for every element x of k_new[bi][j] (bf16), the code written is
+ * E4M3(fp32(x) / k_scale), the division rounded once in fp32 and the result rounded to the nearest
+ * E4M3 value, ties to even, magnitudes beyond 448 saturating to +-448 (V likewise with v_scale).
+ * Attention: as mqa_decode_attention over the values code * scale. q stays bf16 (rounded to fp16
+ * for the tensor-core products), the codes are widened exactly, products and sums are fp32, and
+ * the result matches the fp64 attention over the dequantized caches within the tolerances the
+ * tests state. The tcgen05 path does not read fp8 caches (path 3 returns MQA_ERR_UNSUPPORTED).
+ */
+MQA_API int mqa_kv_append_fp8(const mqa_bf16* k_new, const mqa_bf16* v_new, uint8_t* k_cache,
+                              uint8_t* v_cache, const int32_t* pos, int b, int g, int d_h,
+                              int n_max, float k_scale, float v_scale, void* stream);
+MQA_API int mqa_decode_attention_fp8(const mqa_bf16* q, const uint8_t* k_cache,
+                                     const uint8_t* v_cache, const int32_t* seq_lens,
+                                     mqa_bf16* out, int b, int h, int g, int d_h, int n_max,
+                                     float scale, float k_scale, float v_scale, void* stream);
+MQA_API int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                                uint8_t* k_cache, uint8_t* v_cache, const int32_t* pos,
+                                const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g,
+                                int d_h, int n_max, float scale, float k_scale, float v_scale,
+                                void* stream);
+
+/*
  * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
  * memory. The source pages have no counterpart to this call; it exists for users of the library.
  *

@@ -41,6 +41,15 @@ _lib.mqa_decode_attention_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, 
 _lib.mqa_decode_step_paged.restype = _i32
 _lib.mqa_decode_step_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
                                        _i32, _i32, _i32, _i32, _i32, _f32, _vp]
+_lib.mqa_kv_append_fp8.restype = _i32
+_lib.mqa_kv_append_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _f32, _f32,
+                                   _vp]
+_lib.mqa_decode_attention_fp8.restype = _i32
+_lib.mqa_decode_attention_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                          _f32, _f32, _f32, _vp]
+_lib.mqa_decode_step_fp8.restype = _i32
+_lib.mqa_decode_step_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                     _i32, _i32, _f32, _f32, _f32, _vp]
 _lib.mqa_status_string.restype = ctypes.c_char_p
 _lib.mqa_status_string.argtypes = [_i32]
 _lib.mqa_get_device_status.restype = _i32
@@ -313,4 +322,104 @@ def decode_step_paged(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                     _vp(_stream_handle(stream)))
     if st:
         raise MqaError(st, "mqa_decode_step_paged")
+    return out
+
+
+_FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _check_fp8_cache(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda or t.dtype not in _FP8_DTYPES or t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 / float8_e4m3fn tensor with 4 "
+                         f"dims, got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def kv_append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, pos: torch.Tensor, k_scale: float, v_scale: float,
+                  stream=None) -> None:
+    """:func:`kv_append` into fp8 E4M3 caches ``[b, g, n_max, d_h]`` (uint8 codes): row
+    ``pos[b]`` receives ``e4m3(k_new / k_scale)`` (and V with ``v_scale``)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_fp8_cache(t, n)
+    _check(pos, "pos", torch.int32, 1)
+    b, g, n_max, d_h = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h) \
+            or pos.shape != (b,):
+        raise ValueError("kv_append_fp8: inconsistent shapes")
+    st = _lib.mqa_kv_append_fp8(k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                                v_cache.data_ptr(), pos.data_ptr(), b, g, d_h, n_max,
+                                float(k_scale), float(v_scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append_fp8")
+
+
+def decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         seq_lens: torch.Tensor, k_scale: float, v_scale: float,
+                         out: torch.Tensor | None = None, scale: float | None = None,
+                         stream=None) -> torch.Tensor:
+    """:func:`decode_attention` over fp8 E4M3 caches whose values are ``code * k_scale`` and
+    ``code * v_scale``."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_fp8_cache(t, n)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,):
+        raise ValueError("decode_attention_fp8: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_attention_fp8: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention_fp8(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                       seq_lens.data_ptr(), out.data_ptr(), b, h, g, d_h, n_max,
+                                       float(scale), float(k_scale), float(v_scale),
+                                       _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention_fp8")
+    return out
+
+
+def decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    k_cache: torch.Tensor, v_cache: torch.Tensor, pos: torch.Tensor,
+                    seq_lens: torch.Tensor, k_scale: float, v_scale: float,
+                    out: torch.Tensor | None = None, scale: float | None = None,
+                    stream=None) -> torch.Tensor:
+    """:func:`decode_step` over fp8 E4M3 caches: one launch that quantizes and appends the new
+    rows and attends over the first ``seq_lens[b]`` rows."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_fp8_cache(t, n)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,) \
+            or pos.shape != (b,) or k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h):
+        raise ValueError("decode_step_fp8: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("decode_step_fp8: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step_fp8(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                  k_cache.data_ptr(), v_cache.data_ptr(), pos.data_ptr(),
+                                  seq_lens.data_ptr(), out.data_ptr(), b, h, g, d_h, n_max,
+                                  float(scale), float(k_scale), float(v_scale),
+                                  _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step_fp8")
     return out

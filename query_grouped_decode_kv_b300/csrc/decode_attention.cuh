@@ -38,7 +38,8 @@
 namespace mqa {
 
 constexpr int kTileKeys = 64;       // cache rows per pipeline stage
-constexpr int kStages = 4;          // stages in the shared-memory ring
+constexpr int kRingBytes = 128 * 1024;  // the shared-memory ring of K/V stages
+constexpr int kSwizzleRowBytes = 128;
 // NW (a template parameter below) is the number of consumer warps: 4 or 8.
 //  - NW = 4: one producer warp comes on top (160 threads, one warp per SM sub-partition each).
 //  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
@@ -56,7 +57,6 @@ static_assert(2 * 32 * kConsumerRegs + 32 * kProducerRegs <= 16384,
 constexpr int kMaxBatch = 8192;
 constexpr int kMaxGroup = 64;       // largest G = h / g served
 constexpr float kLazyLog2 = 8.f;    // softmax reference slack (log2 units), see MmaConsumer::tile
-constexpr int kSwizzleRowBytes = 128;
 
 struct DecodeParams {
   const __nv_bfloat16* q;     // [b][h][D]
@@ -83,34 +83,58 @@ struct DecodeParams {
   // page_table[bi][t / page_size] at row t % page_size; n_max = max_pages * page_size.
   const int32_t* page_table;  // [b][max_pages]
   int page_size, max_pages, num_pages;
+  // fp8 caches: the fused append stores e4m3(x / kq_scale) (and V with vq_scale); every final
+  // output is multiplied by out_scale (the V scale; 1 for bf16 caches, where it changes nothing)
+  float kq_scale, vq_scale, out_scale;
 };
 
-__host__ __device__ constexpr int stage_bytes(int D) { return 2 * kTileKeys * D * 2; }
+// Stage geometry for head dimension D stored with EB bytes per element (2: bf16; 1: fp8 E4M3
+// codes). A cache row is D * EB bytes, split into 128-byte swizzle rows ("halves"), one TMA box
+// column range each; a stage holds one tile's K rows then its V rows; the ring holds kRingBytes,
+// so the narrower rows get twice the stages (and twice the tiles in flight).
+template <int D, int EB>
+struct Geometry {
+  static constexpr int kRowBytes = D * EB;
+  static constexpr int kHalves = kRowBytes / kSwizzleRowBytes;
+  static constexpr int kBoxCols = kSwizzleRowBytes / EB;   // elements per 128-byte box row
+  static constexpr int kKvBytes = kTileKeys * kRowBytes;   // one tile of K (or of V)
+  static constexpr int kStageBytes = 2 * kKvBytes;
+  static constexpr int kStages = kRingBytes / kStageBytes;  // 4 (32 KB stages) or 8 (16 KB)
+  static_assert(kRowBytes % kSwizzleRowBytes == 0 && kStages >= 2 && kStages <= 8, "geometry");
+};
+
 __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 
 // Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags]
 // [page slots]. CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
-__host__ __device__ constexpr int smem_fixed_bytes(int D, int NW, int CR) {
-  return kStages * stage_bytes(D) + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
-         (2 * kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
-         32 * 4;                       // the paged producer's looked-up pages
+template <int D, int EB>
+__host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
+  using Geo = Geometry<D, EB>;
+  return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
+         (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
+         32 * 4;                            // the paged producer's looked-up pages
 }
-__host__ __device__ constexpr size_t smem_bytes(int D, int NW, int CR) {
-  return 1024 + static_cast<size_t>(smem_fixed_bytes(D, NW, CR));
+template <int D, int EB>
+__host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
+  return 1024 + static_cast<size_t>(smem_fixed_bytes<D, EB>(NW, CR));
 }
 
 __device__ __forceinline__ int tiles_of_length(int L, int n_max) {
   return (L >= 1 && L <= n_max) ? (L + kTileKeys - 1) / kTileKeys : 0;
 }
 
-// Byte offset of (key row, column d) inside one K or V stage: the row is split into 64-column
-// halves of 128 bytes (one TMA box each); inside a half the 16-byte chunk index is XORed with
-// (row % 8), the 128-byte swizzle the TMA applies. `d` must be a multiple of 8 here.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int key, int d) {
-  const int half = d >> 6;
-  const int chunk = (d >> 3) & 7;
+// Byte offset of (key row, byte column c) inside one K or V stage: the row is split into halves
+// of 128 bytes (one TMA box each); inside a half the 16-byte chunk index is XORed with (row % 8),
+// the 128-byte swizzle the TMA applies. `c` must be a multiple of 16 here.
+__device__ __forceinline__ uint32_t swz_bytes(uint32_t base, int key, int c) {
+  const int half = c >> 7;
+  const int chunk = (c >> 4) & 7;
   return base + static_cast<uint32_t>(half * (kTileKeys * kSwizzleRowBytes) +
                                       key * kSwizzleRowBytes + ((chunk ^ (key & 7)) << 4));
+}
+// The same for a bf16 stage and element column d (a multiple of 8).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int key, int d) {
+  return swz_bytes(base, key, d * 2);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -135,9 +159,36 @@ __device__ __forceinline__ long long row_chunk(const DecodeParams& P, int bi, in
   return ((static_cast<long long>(page) * P.g + j) * P.page_size + p % P.page_size) * CH;
 }
 
-template <int D>
+// 16-byte chunk c of the cache row written for source row `src` (D bf16 values as 16-byte
+// chunks): a copy for bf16 caches; for fp8 caches the codes e4m3(x / scale) of the 16 values
+// x = src[16c .. 16c + 15], the division rounded once in fp32 (IEEE).
+template <int EB>
+__device__ __forceinline__ uint4 new_row_chunk(const uint4* src, int c, float scale) {
+  if constexpr (EB == 2) {
+    return __ldg(src + c);
+  } else {
+    const uint4 a = __ldg(src + 2 * c), b = __ldg(src + 2 * c + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t q[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[2 * i + k]);
+        q[k] = f32x2_to_e4m3x2(__fdiv_rn(__low2float(x), scale),
+                               __fdiv_rn(__high2float(x), scale));
+      }
+      out[i] = q[0] | (q[1] << 16);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+template <int D, int EB>
 __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int nthreads) {
-  constexpr int CH = D / 8;  // 16-byte chunks per row
+  constexpr int CH = D * EB / 16;  // 16-byte chunks per cache row
+  constexpr int CS = D / 8;        // 16-byte chunks per source row (bf16)
   const long long total = static_cast<long long>(P.b) * P.g * CH;
   const long long stride = static_cast<long long>(P.num_ctas) * nthreads;
   for (long long idx = static_cast<long long>(blockIdx.x) * nthreads + threadIdx.x; idx < total;
@@ -157,24 +208,27 @@ __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int
       if (c == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
-    P.k_rows[dst + c] = __ldg(P.k_new + idx);
-    P.v_rows[dst + c] = __ldg(P.v_new + idx);
+    P.k_rows[dst + c] = new_row_chunk<EB>(P.k_new + row * CS, c, P.kq_scale);
+    P.v_rows[dst + c] = new_row_chunk<EB>(P.v_new + row * CS, c, P.vq_scale);
   }
 }
 
-// One warp writes the K and V row of segment (bi, j) at cache row `p` (lane = 16-byte chunk).
-template <int D>
+// One warp writes the K and V row of segment (bi, j) at cache row `p` (lane = 16-byte chunk of
+// the cache row).
+template <int D, int EB>
 __device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int j, int p,
                                               int lane) {
-  constexpr int CH = D / 8;
-  const long long src = (static_cast<long long>(bi) * P.g + j) * CH;
+  constexpr int CH = D * EB / 16;
+  constexpr int CS = D / 8;
+  const long long src = (static_cast<long long>(bi) * P.g + j) * CS;
   const long long dst = row_chunk(P, bi, j, p, CH);
   if (dst < 0) {
     if (lane == 0) latch_status(kStatusDeviceBounds);
     return;
   }
-  if (lane < CH) P.k_rows[dst + lane] = __ldg(P.k_new + src + lane);
-  else if (lane < 2 * CH) P.v_rows[dst + lane - CH] = __ldg(P.v_new + src + lane - CH);
+  if (lane < CH) P.k_rows[dst + lane] = new_row_chunk<EB>(P.k_new + src, lane, P.kq_scale);
+  else if (lane < 2 * CH)
+    P.v_rows[dst + lane - CH] = new_row_chunk<EB>(P.v_new + src, lane - CH, P.vq_scale);
 }
 
 // The tile count of every sequence as the CTAs see it: the exclusive prefix `cs` of the tile sums
@@ -237,11 +291,11 @@ struct TileCursor {
 };
 
 struct SharedLayout {
-  uint8_t* stages;      // kStages x stage_bytes(D), 1024-aligned
+  uint8_t* stages;      // Geometry::kStages x kStageBytes, 1024-aligned
   float* comb_o;        // [NW][CR][comb_row_floats(D)]
   float2* comb_ml;      // [NW][CR]
-  uint64_t* full;       // [kStages]
-  uint64_t* empty;      // [kStages]
+  uint64_t* full;       // [stages]
+  uint64_t* empty;      // [stages]
   uint64_t* cbar;       // consumer-wide barrier
   uint64_t* stall;      // testing: a barrier nothing completes (DecodeParams::debug_stall)
   volatile int* abort;  // set when any warp gives up
@@ -250,8 +304,10 @@ struct SharedLayout {
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
-template <int D, int NW, int CR>
+template <int D, int EB, int NW, int CR>
 __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
+  using Geo = Geometry<D, EB>;
+  constexpr int kStages = Geo::kStages;
   static_assert((NW * CR * comb_row_floats(D) * 4) % 16 == 0 && (NW * CR * 8) % 16 == 0 &&
                     ((2 * kStages + 2) * 8) % 16 == 0,
                 "regions keep 16-byte alignment (the page slots are read as int4)");
@@ -259,7 +315,7 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   s.stages = p;
-  p += kStages * stage_bytes(D);
+  p += kStages * Geo::kStageBytes;
   s.comb_o = reinterpret_cast<float*>(p);
   p += NW * CR * comb_row_floats(D) * 4;
   s.comb_ml = reinterpret_cast<float2*>(p);
@@ -321,7 +377,7 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& P, const S
     }
     if (complete) {
       const size_t o = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d;
-      P.out[o] = __float2bfloat16_rn(acc / den);
+      P.out[o] = __float2bfloat16_rn(acc / den * P.out_scale);
     } else {
       const size_t r = static_cast<size_t>(slot) * G + hr;
       P.part_o[r * D + d] = acc;
@@ -392,7 +448,7 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
         den += w * ml.y;
         acc += w * __ldcg(P.part_o + r * D + d);
       }
-      P.out[out0 + idx] = __float2bfloat16_rn(acc / den);
+      P.out[out0 + idx] = __float2bfloat16_rn(acc / den * P.out_scale);
     }
     return true;
   }
@@ -423,8 +479,9 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
       acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
     }
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(P.out + out0) + 2 * idx;
-    dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
-    dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+    const float os = P.out_scale;
+    dst[0] = __floats2bfloat162_rn(acc.x * os, acc.y * os);
+    dst[1] = __floats2bfloat162_rn(acc.z * os, acc.w * os);
   }
   // the scratch is written again by the next segment's combine
   return consumer_sync(sh, cphase, P.timeout_ns);
@@ -528,12 +585,14 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
 // tile holds it (whole warp, one 16-byte chunk per lane). Stage st is refilled once its `empty`
 // barrier has completed the phase of its previous use.
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, int EB>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                               const DecodeParams& P, const SharedLayout& sh,
                                               unsigned long long x0, int ntiles, int lane) {
-  constexpr uint32_t kStageBytes = stage_bytes(D);
-  constexpr uint32_t kKvBytes = kStageBytes / 2;
+  using Geo = Geometry<D, EB>;
+  constexpr int kStages = Geo::kStages;
+  constexpr uint32_t kStageBytes = Geo::kStageBytes;
+  constexpr uint32_t kKvBytes = Geo::kKvBytes;
   const bool fused = P.pos != nullptr;
   if (lane == 0) {
     prefetch_tensor_map(tm_k);
@@ -561,7 +620,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
         row_p = (p >= 0 && p < P.n_max) ? p : -1;
       }
       if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
-        write_new_row<D>(P, cur.bi, cur.j, row_p, lane);
+        write_new_row<D, EB>(P, cur.bi, cur.j, row_p, lane);
         fence_proxy_async_global();  // each writer orders its store before the async proxy...
         __syncwarp();                // ...and the copy is issued after every writer
       }
@@ -574,11 +633,11 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
       uint8_t* kdst = sh.stages + st * kStageBytes;
       uint8_t* vdst = kdst + kKvBytes;
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, tm_k, &sh.full[st], half * 64, y,
-                    z, policy);
-        tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, tm_v, &sh.full[st], half * 64, y,
-                    z, policy);
+      for (int half = 0; half < Geo::kHalves; ++half) {
+        tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes, tm_k, &sh.full[st],
+                    half * Geo::kBoxCols, y, z, policy);
+        tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes, tm_v, &sh.full[st],
+                    half * Geo::kBoxCols, y, z, policy);
       }
     }
     __syncwarp();
@@ -652,13 +711,15 @@ __device__ __forceinline__ void load_tile_pages(const int* slots, int kt, int (&
   }
 }
 
-template <int D, int NB>
+template <int D, int EB, int NB>
 __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
                                                     const CUtensorMap* tm_v,
                                                     const DecodeParams& P, const SharedLayout& sh,
                                                     unsigned long long x0, int ntiles, int lane) {
-  constexpr uint32_t kStageBytes = stage_bytes(D);
-  constexpr uint32_t kKvBytes = kStageBytes / 2;
+  using Geo = Geometry<D, EB>;
+  constexpr int kStages = Geo::kStages;
+  constexpr uint32_t kStageBytes = Geo::kStageBytes;
+  constexpr uint32_t kKvBytes = Geo::kKvBytes;
   constexpr int R = kTileKeys / NB;  // rows per box
   constexpr int T = 32 / NB;         // tiles per lookup batch
   constexpr uint32_t kBoxBytes = R * kSwizzleRowBytes;
@@ -719,14 +780,15 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       break;
     }
     if (fused && row_p >= 0 && row_p / kTileKeys == cur.tile) {
-      write_new_row<D>(P, cur.bi, cur.j, row_p, lane);
+      write_new_row<D, EB>(P, cur.bi, cur.j, row_p, lane);
       fence_proxy_async_global();
       __syncwarp();
     }
     // every lane holds the same values here; one elected lane issues the tile's copies
     if (elect_one()) {
       const int nbox = (min(L - y, kTileKeys) + R - 1) / R;  // L > y for every tile
-      mbar_arrive_expect_tx(&sh.full[st], static_cast<uint32_t>(nbox) * kBoxBytes * (D / 64) * 2);
+      mbar_arrive_expect_tx(&sh.full[st],
+                            static_cast<uint32_t>(nbox) * kBoxBytes * Geo::kHalves * 2);
       uint8_t* kdst = sh.stages + st * kStageBytes;
       uint8_t* vdst = kdst + kKvBytes;
       int pg[NB];
@@ -740,11 +802,11 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
           const int z = bad ? z_past_pool : pg[i] * P.g + cur.j;
           const int yr = (y + i * R) & page_mask;
 #pragma unroll
-          for (int half = 0; half < D / 64; ++half) {
+          for (int half = 0; half < Geo::kHalves; ++half) {
             tma_load_3d(kdst + half * kTileKeys * kSwizzleRowBytes + i * kBoxBytes, tm_k,
-                        &sh.full[st], half * 64, yr, z, policy);
+                        &sh.full[st], half * Geo::kBoxCols, yr, z, policy);
             tma_load_3d(vdst + half * kTileKeys * kSwizzleRowBytes + i * kBoxBytes, tm_v,
-                        &sh.full[st], half * 64, yr, z, policy);
+                        &sh.full[st], half * Geo::kBoxCols, yr, z, policy);
           }
         }
       }
@@ -761,7 +823,7 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
 }
 
 // Boxes per tile from the page size (8, 16, 32 rows; 64 or more: one box).
-template <int D>
+template <int D, int EB>
 __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
                                                         const CUtensorMap* tm_v,
                                                         const DecodeParams& P,
@@ -769,10 +831,10 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
                                                         unsigned long long x0, int ntiles,
                                                         int lane) {
   switch (P.page_size) {
-    case 8: produce_tiles_paged<D, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    case 16: produce_tiles_paged<D, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    case 32: produce_tiles_paged<D, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    default: produce_tiles_paged<D, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 8: produce_tiles_paged<D, EB, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 16: produce_tiles_paged<D, EB, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 32: produce_tiles_paged<D, EB, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    default: produce_tiles_paged<D, EB, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
   }
 }
 
@@ -939,10 +1001,198 @@ struct MmaConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer (G < 8). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
-// 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output.
+// Tensor-core consumer for fp8 E4M3 caches (G >= 8): the same tile split, softmax and combine as
+// MmaConsumer, with fp16 MMAs (m16n8k16, fp32 accumulate). The codes are widened exactly to fp16
+// in registers (two codes per instruction); q is rounded to fp16 once per segment; the weights P
+// are rounded to fp16 once, and the running sum takes the same rounded values. The per-tensor
+// scales never enter here: k_scale is part of scale_log2 and v_scale multiplies the final output.
+//
+// S = Q K^T: ldmatrix reads the K stage as 16-bit units, so a lane receives four consecutive
+// codes of one key (columns 4c .. 4c+3 of a 16-column block, c = lane % 4); widened, they are one
+// whole B fragment of a k16 step whose k order is the permutation 2c, 2c+1 -> 4c, 4c+1 and
+// 2c+8, 2c+9 -> 4c+2, 4c+3 of the block's columns. The A fragments of q use the same order, and
+// a dot product does not depend on the order of its terms.
+// O += P V: ldmatrix.trans on the V stage gives a lane two keys (rows 2c, 2c+1 of an 8-key block)
+// times two adjacent columns (2r, 2r+1, r = lane / 4) of a 16-column block; one byte permute and
+// two widenings give the B fragments of two n8 tiles, the block's even columns and its odd
+// columns. Output tile 2b + e (block b, e = 0 even, 1 odd) thus holds columns 16b + 2n + e, and
+// a lane's accumulators cover columns 16b + 4c + {0, 1, 2, 3}, which publish() writes back in
+// order.
 // ---------------------------------------------------------------------------------------------
-template <int D, int G, int NW>
+template <int D, int WM, int NW>
+struct MmaConsumerF8 {
+  static constexpr int kWarps = NW;
+  static constexpr int kCombRows = 16;  // head rows per warp
+  static constexpr int NGRP = NW / WM;
+  static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
+  static constexpr int NT_S = KPW / 8;          // score tiles (n = 8 keys)
+  static constexpr int KS_QK = D / 16;          // k-steps over the head dimension
+  static constexpr int NT_O = D / 8;            // output tiles (n = 8 columns)
+  static constexpr int KS_PV = KPW / 16;        // k-steps over keys
+  static_assert(D == 128 && NT_S % 2 == 0 && KS_PV >= 1 && KS_QK % 2 == 0, "tile split");
+
+  uint32_t qa[KS_QK][4];
+  float o[NT_O][4];
+  float m[2], l[2];
+
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
+                                                int lane) {
+    const int r0 = mi * 16 + (lane >> 2), r1 = r0 + 8;
+    const __nv_bfloat16* qb = P.q + (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * P.G) * D;
+    const bool v0 = r0 < P.G, v1 = r1 < P.G;
+    const uint2* q0 = reinterpret_cast<const uint2*>(qb + static_cast<size_t>(r0) * D);
+    const uint2* q1 = reinterpret_cast<const uint2*>(qb + static_cast<size_t>(r1) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ++ks) {
+      // columns 16 ks + 4c .. + 3 of rows r0 and r1 (one 8-byte load each)
+      const int c4 = ks * 4 + (lane & 3);
+      const uint2 x0 = v0 ? __ldg(q0 + c4) : make_uint2(0u, 0u);
+      const uint2 x1 = v1 ? __ldg(q1 + c4) : make_uint2(0u, 0u);
+      const __nv_bfloat162 a0 = *reinterpret_cast<const __nv_bfloat162*>(&x0.x);
+      const __nv_bfloat162 a1 = *reinterpret_cast<const __nv_bfloat162*>(&x0.y);
+      const __nv_bfloat162 b0 = *reinterpret_cast<const __nv_bfloat162*>(&x1.x);
+      const __nv_bfloat162 b1 = *reinterpret_cast<const __nv_bfloat162*>(&x1.y);
+      qa[ks][0] = pack_f16x2(__low2float(a0), __high2float(a0));
+      qa[ks][1] = pack_f16x2(__low2float(b0), __high2float(b0));
+      qa[ks][2] = pack_f16x2(__low2float(a1), __high2float(a1));
+      qa[ks][3] = pack_f16x2(__low2float(b1), __high2float(b1));
+    }
+#pragma unroll
+    for (int n = 0; n < NT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // One tile. `valid` = number of the tile's rows that lie below the sequence length.
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
+                                       int valid, float scale_log2) {
+    float s[NT_S][4];
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    const int mat = lane >> 3, rr = lane & 7;
+    // S = Q K^T: one ldmatrix.x4 = keys (8 or 8 + 8) x column blocks (ks, ks + 1)
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ks += 2) {
+#pragma unroll
+      for (int np = 0; np < NT_S / 2; ++np) {
+        const int key = grp * KPW + np * 16 + rr + ((mat & 2) ? 8 : 0);
+        uint32_t w0, w1, w2, w3;
+        ldsm_x4(swz_bytes(kbase, key, (ks + (mat & 1)) * 16), w0, w1, w2, w3);
+        uint32_t b[4][2];
+        e4m3x4_to_f16x2x2(w0, b[0][0], b[0][1]);  // keys 0-7,  block ks
+        e4m3x4_to_f16x2x2(w1, b[1][0], b[1][1]);  // keys 0-7,  block ks + 1
+        e4m3x4_to_f16x2x2(w2, b[2][0], b[2][1]);  // keys 8-15, block ks
+        e4m3x4_to_f16x2x2(w3, b[3][0], b[3][1]);  // keys 8-15, block ks + 1
+        mma_16816_f16(s[2 * np], qa[ks], b[0][0], b[0][1]);
+        mma_16816_f16(s[2 * np], qa[ks + 1], b[1][0], b[1][1]);
+        mma_16816_f16(s[2 * np + 1], qa[ks], b[2][0], b[2][1]);
+        mma_16816_f16(s[2 * np + 1], qa[ks + 1], b[3][0], b[3][1]);
+      }
+    }
+    // scale (log2 domain), mask rows at or beyond the length, running max per head row
+    const int c2 = (lane & 3) * 2;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      const int key = grp * KPW + n * 8 + c2;
+      const bool ok0 = key < valid, ok1 = key + 1 < valid;
+      s[n][0] = ok0 ? s[n][0] * scale_log2 : -INFINITY;
+      s[n][1] = ok1 ? s[n][1] * scale_log2 : -INFINITY;
+      s[n][2] = ok0 ? s[n][2] * scale_log2 : -INFINITY;
+      s[n][3] = ok1 ? s[n][3] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    // lazy reference, as in MmaConsumer::tile (weights stay below 2^kLazyLog2, well inside fp16)
+    const bool up0 = mx0 > m[0] + kLazyLog2, up1 = mx1 > m[1] + kLazyLog2;
+    float al0 = 1.f, al1 = 1.f;
+    if (up0) { al0 = fast_exp2(m[0] - mx0); m[0] = mx0; }
+    if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
+    const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
+    const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] = round_f16(fast_exp2(s[n][0] - ref0));
+      s[n][1] = round_f16(fast_exp2(s[n][1] - ref0));
+      s[n][2] = round_f16(fast_exp2(s[n][2] - ref1));
+      s[n][3] = round_f16(fast_exp2(s[n][3] - ref1));
+      ps0 += s[n][0] + s[n][1];
+      ps1 += s[n][2] + s[n][3];
+    }
+    l[0] = l[0] * al0 + ps0;
+    l[1] = l[1] * al1 + ps1;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+#pragma unroll
+      for (int n = 0; n < NT_O; ++n) {
+        o[n][0] *= al0; o[n][1] *= al0;
+        o[n][2] *= al1; o[n][3] *= al1;
+      }
+    }
+    // O += P V (the packing is exact: the weights are already fp16 values)
+#pragma unroll
+    for (int kk = 0; kk < KS_PV; ++kk) {
+      uint32_t a[4];
+      a[0] = pack_f16x2(s[2 * kk][0], s[2 * kk][1]);
+      a[1] = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
+      a[2] = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      a[3] = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int cb = 0; cb < D / 16; cb += 2) {
+        // matrices: keys 0-7 / 8-15 of this k-step x column blocks cb / cb + 1
+        const int key = grp * KPW + kk * 16 + rr + ((mat & 1) ? 8 : 0);
+        uint32_t w0, w1, w2, w3;
+        ldsm_x4_trans(swz_bytes(vbase, key, (cb + (mat >> 1)) * 16), w0, w1, w2, w3);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          // keys 0-7 and 8-15 of block cb + h: bytes (0, 2) are the even column, (1, 3) the odd
+          uint32_t e0, o0, e1, o1;
+          e4m3x4_to_f16x2x2(__byte_perm(h ? w2 : w0, 0u, 0x3120), e0, o0);
+          e4m3x4_to_f16x2x2(__byte_perm(h ? w3 : w1, 0u, 0x3120), e1, o1);
+          mma_16816_f16(o[2 * (cb + h)], a, e0, e1);
+          mma_16816_f16(o[2 * (cb + h) + 1], a, o0, o1);
+        }
+      }
+    }
+  }
+
+  // Publish this warp's state (rows mi*16 .. mi*16+15 of the group) to the combine scratch.
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+    float l0 = l[0], l1 = l[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int r = lane >> 2, c4 = (lane & 3) * 4;
+    float* row0 = sh.comb_o + (warp * kCombRows + r) * comb_row_floats(D);
+    float* row1 = sh.comb_o + (warp * kCombRows + r + 8) * comb_row_floats(D);
+#pragma unroll
+    for (int b = 0; b < D / 16; ++b) {
+      // tiles 2b (even columns) and 2b + 1 (odd): columns 16b + 4c + {0, 2} and {1, 3}
+      *reinterpret_cast<float4*>(row0 + b * 16 + c4) =
+          make_float4(o[2 * b][0], o[2 * b + 1][0], o[2 * b][1], o[2 * b + 1][1]);
+      *reinterpret_cast<float4*>(row1 + b * 16 + c4) =
+          make_float4(o[2 * b][2], o[2 * b + 1][2], o[2 * b][3], o[2 * b + 1][3]);
+    }
+    if ((lane & 3) == 0) {
+      sh.comb_ml[warp * kCombRows + r] = make_float2(m[0], l0);
+      sh.comb_ml[warp * kCombRows + r + 8] = make_float2(m[1], l1);
+    }
+  }
+
+  using Rows = typename MmaConsumer<D, WM, NW>::Rows;
+};
+
+// ---------------------------------------------------------------------------------------------
+// CUDA-core consumer (G < 8). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
+// 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output. EB: the cache's
+// bytes per element (fp8 codes are widened exactly on load).
+// ---------------------------------------------------------------------------------------------
+template <int D, int G, int NW, int EB = 2>
 struct CcConsumer {
   static constexpr int kWarps = NW;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
@@ -972,9 +1222,17 @@ struct CcConsumer {
   }
 
   __device__ __forceinline__ void load_row(uint32_t base, int key, int lane, float (&f)[DPL]) const {
-    const int d0 = lane * DPL;
-    const uint32_t addr = swz(base, key, d0 & ~7) + (d0 & 7) * 2;
-    if constexpr (DPL == 4) {
+    const int c = lane * DPL * EB;  // byte column
+    const uint32_t addr = swz_bytes(base, key, c & ~15) + (c & 15);
+    if constexpr (EB == 1) {
+      static_assert(DPL == 4, "fp8 rows of 128 columns: four codes per lane");
+      uint32_t x, lo, hi;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+      e4m3x4_to_f16x2x2(x, lo, hi);
+      const float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else if constexpr (DPL == 4) {
       uint32_t x, y;
       asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
       const __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);
@@ -1093,17 +1351,20 @@ struct CcConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// The kernel. `Consumer` is MmaConsumer<D, WM, NW> or CcConsumer<D, G, NW>.
+// The kernel. `Consumer` is MmaConsumer<D, WM, NW>, MmaConsumerF8<D, WM, NW> or
+// CcConsumer<D, G, NW, EB>; EB is the cache's bytes per element (2: bf16, 1: fp8 E4M3 codes).
 // ---------------------------------------------------------------------------------------------
-template <int D, class Consumer, bool kTensorCores, int WM>
+template <int D, int EB, class Consumer, bool kTensorCores, int WM>
 __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
+  using Geo = Geometry<D, EB>;
+  constexpr int kStages = Geo::kStages;
   constexpr int NW = Consumer::kWarps;
   constexpr int CR = Consumer::kCombRows;
   constexpr int kThreads = threads_of(NW);
   extern __shared__ uint8_t smem_raw[];
-  SharedLayout sh = carve_shared<D, NW, CR>(smem_raw);
+  SharedLayout sh = carve_shared<D, EB, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -1123,7 +1384,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   build_tile_prefix<kThreads>(P, sh, chunk_tiles);
 
   zero_invalid_sequences<D>(P, kThreads);
-  if (P.pos != nullptr) append_uncovered_rows<D>(P, kThreads);
+  if (P.pos != nullptr) append_uncovered_rows<D, EB>(P, kThreads);
 
   const unsigned long long W = sh.tix.total();
   const unsigned long long x0 = W * blockIdx.x / P.num_ctas;
@@ -1131,8 +1392,8 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   if (x0 >= x1) return;
   const int ntiles = static_cast<int>(x1 - x0);
   const uint32_t stages_base = smem_addr(sh.stages);
-  constexpr uint32_t kStageBytes = stage_bytes(D);
-  constexpr uint32_t kKvBytes = kStageBytes / 2;
+  constexpr uint32_t kStageBytes = Geo::kStageBytes;
+  constexpr uint32_t kKvBytes = Geo::kKvBytes;
 
   if constexpr (NW == 8) {
     if (warp >= NW) setmaxnreg_dec<kProducerRegs>();
@@ -1141,8 +1402,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   if (warp >= NW) {
     // ================================ producer ================================================
     if (warp == NW) {
-      if (P.page_table != nullptr) produce_tiles_paged_any<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
-      else produce_tiles<D>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+      if (P.page_table != nullptr)
+        produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+      else
+        produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
     }
     return;
   }
@@ -1185,7 +1448,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         uint8_t* vst = sh.stages + st * kStageBytes + kKvBytes;
         const int first = max(valid, g0);
         const int rows = g0 + kGroupKeys - first;
-        const int chunks_per_row = D * 2 / 16;
+        constexpr int chunks_per_row = Geo::kRowBytes / 16;
         for (int c = lane; c < rows * chunks_per_row; c += 32) {
           const int key = first + c / chunks_per_row;
           const int ch = c % chunks_per_row;

@@ -537,7 +537,7 @@ __device__ __forceinline__ void tc_produce_tiles(const CUtensorMap* tm_k, const 
           row_p = (p >= 0 && p < P.n_max) ? p : -1;
         }
         if (row_p >= 0 && row_p / kTileKeys == ck.tile) {
-          write_new_row<D>(P, ck.bi, ck.j, row_p, lane);
+          write_new_row<D, 2>(P, ck.bi, ck.j, row_p, lane);
           fence_proxy_async_global();  // each writer orders its stores before the async proxy...
           __syncwarp();                // ...and lane 0 copies the tile after every writer
         }
@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *sh.tmem_base;
 
   zero_invalid_sequences<D>(P, kTcThreads);
-  if (P.pos != nullptr) append_uncovered_rows<D>(P, kTcThreads);
+  if (P.pos != nullptr) append_uncovered_rows<D, 2>(P, kTcThreads);
 
   const unsigned long long W = b.tix.total();
   const unsigned long long x0 = W * blockIdx.x / P.num_ctas;

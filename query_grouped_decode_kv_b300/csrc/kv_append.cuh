@@ -7,6 +7,7 @@
 
 #include <stdint.h>
 
+#include "decode_attention.cuh"
 #include "status.cuh"
 
 namespace mqa {
@@ -72,6 +73,34 @@ __global__ void __launch_bounds__(256) kv_append_paged_kernel(
         ((static_cast<long long>(page) * g + j) * page_size + p % page_size) * chunks_per_row + c;
     k_pool[dst] = __ldg(k_new + idx);
     v_pool[dst] = __ldg(v_new + idx);
+  }
+}
+
+// The append into fp8 E4M3 caches [b][g][n_max][D] (one byte per element): one thread writes one
+// 16-byte chunk of codes, e4m3(x / scale) for 16 consecutive bf16 values x of the new row (the
+// division rounded once in fp32, nearest-even rounding to E4M3 saturating at +-448). Positions
+// out of range skip the sequence and latch MQA_ERR_DEVICE_BOUNDS.
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(
+    const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, uint4* __restrict__ k_cache,
+    uint4* __restrict__ v_cache, const int32_t* __restrict__ pos, int b, int g, int d_h,
+    int n_max, float k_scale, float v_scale) {
+  const int ch = d_h / 16;   // output chunks per row
+  const int cs = d_h / 8;    // source chunks per row
+  const long long total = static_cast<long long>(b) * g * ch;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long row = idx / ch;  // = bi * g + j
+    const int c = static_cast<int>(idx - row * ch);
+    const int bi = static_cast<int>(row / g);
+    const int p = __ldg(pos + bi);
+    if (p < 0 || p >= n_max) {
+      if (c == 0 && row == static_cast<long long>(bi) * g) latch_status(kStatusDeviceBounds);
+      continue;
+    }
+    const long long dst = (row * n_max + p) * ch + c;
+    k_cache[dst] = new_row_chunk<1>(k_new + row * cs, c, k_scale);
+    v_cache[dst] = new_row_chunk<1>(v_new + row * cs, c, v_scale);
   }
 }
 

@@ -56,39 +56,44 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Cache [b][g][n_max][d_h] bf16 seen as a 3-D tensor (d_h, n_max, b*g); box = 64 columns x
-// kTileKeys rows, 128-byte swizzle. Rows past n_max read as zeros.
-bool make_cache_map(CUtensorMap* map, const void* base, int bg, int n_max, int d_h) {
+// Cache [b][g][n_max][d_h] seen as a 3-D tensor (d_h, n_max, b*g) of bf16 (eb = 2) or of
+// one-byte fp8 codes (eb = 1); box = 128 bytes of columns x kTileKeys rows, 128-byte swizzle.
+// Rows past n_max read as zeros.
+bool make_cache_map(CUtensorMap* map, const void* base, int bg, int n_max, int d_h, int eb) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_h), static_cast<cuuint64_t>(n_max),
                               static_cast<cuuint64_t>(bg)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * 2,
-                                 static_cast<cuuint64_t>(n_max) * d_h * 2};
-  const cuuint32_t box[3] = {64, mqa::kTileKeys, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * eb,
+                                 static_cast<cuuint64_t>(n_max) * d_h * eb};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(mqa::kSwizzleRowBytes / eb), mqa::kTileKeys,
+                             1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // A page pool [num_pages][g][page_size][d_h] bf16 seen as (d_h, page_size, num_pages * g); box =
 // 64 columns x min(page_size, kTileKeys) rows, 128-byte swizzle. Coordinates past the pool read
 // as zeros.
 bool make_pool_map(CUtensorMap* map, const void* base, long long pages_g, int page_size,
-                   int d_h) {
+                   int d_h, int eb) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d_h), static_cast<cuuint64_t>(page_size),
                               static_cast<cuuint64_t>(pages_g)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * 2,
-                                 static_cast<cuuint64_t>(page_size) * d_h * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page_size < mqa::kTileKeys
-                                                             ? page_size : mqa::kTileKeys), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d_h) * eb,
+                                 static_cast<cuuint64_t>(page_size) * d_h * eb};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(mqa::kSwizzleRowBytes / eb),
+                             static_cast<cuuint32_t>(page_size < mqa::kTileKeys
+                                                         ? page_size : mqa::kTileKeys), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Paged caches: the page table and the pool's geometry (all zero for contiguous caches).
@@ -214,12 +219,12 @@ struct AttnKernelChoice {
   bool wide = false;  // eight consumer warps with a setmaxnreg split: check the register count
 };
 
-template <class Consumer, int D, bool TC, int WM>
+template <class Consumer, int D, int EB, bool TC, int WM>
 AttnKernelChoice choice(int b) {
   AttnKernelChoice c;
-  c.fn = mqa::decode_attention_kernel<D, Consumer, TC, WM>;
+  c.fn = mqa::decode_attention_kernel<D, EB, Consumer, TC, WM>;
   c.threads = mqa::threads_of(Consumer::kWarps);
-  c.smem = mqa::smem_bytes(D, Consumer::kWarps, Consumer::kCombRows);
+  c.smem = mqa::smem_bytes<D, EB>(Consumer::kWarps, Consumer::kCombRows);
   c.wide = Consumer::kWarps == 8;
   return c;
 }
@@ -243,18 +248,42 @@ AttnKernelChoice pick_kernel(Path path, int G, int b) {
     return c;
   }
   if (path == kPathMmaSync) {
-    if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, true, 1>(b);
-    if (G <= 32) return choice<MmaConsumer<D, 2, 8>, D, true, 2>(b);
-    return choice<MmaConsumer<D, 4, 8>, D, true, 4>(b);
+    if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, 2, true, 1>(b);
+    if (G <= 32) return choice<MmaConsumer<D, 2, 8>, D, 2, true, 2>(b);
+    return choice<MmaConsumer<D, 4, 8>, D, 2, true, 4>(b);
   }
   switch (G) {
-    case 1: return choice<CcConsumer<D, 1, 8>, D, false, 1>(b);
-    case 2: return choice<CcConsumer<D, 2, 8>, D, false, 1>(b);
-    case 3: return choice<CcConsumer<D, 3, 8>, D, false, 1>(b);
-    case 4: return choice<CcConsumer<D, 4, 8>, D, false, 1>(b);
-    case 5: return choice<CcConsumer<D, 5, 8>, D, false, 1>(b);
-    case 6: return choice<CcConsumer<D, 6, 8>, D, false, 1>(b);
-    case 7: return choice<CcConsumer<D, 7, 8>, D, false, 1>(b);
+    case 1: return choice<CcConsumer<D, 1, 8>, D, 2, false, 1>(b);
+    case 2: return choice<CcConsumer<D, 2, 8>, D, 2, false, 1>(b);
+    case 3: return choice<CcConsumer<D, 3, 8>, D, 2, false, 1>(b);
+    case 4: return choice<CcConsumer<D, 4, 8>, D, 2, false, 1>(b);
+    case 5: return choice<CcConsumer<D, 5, 8>, D, 2, false, 1>(b);
+    case 6: return choice<CcConsumer<D, 6, 8>, D, 2, false, 1>(b);
+    case 7: return choice<CcConsumer<D, 7, 8>, D, 2, false, 1>(b);
+    default: return {};
+  }
+}
+
+// fp8 E4M3 caches (d_h = 128): the same paths with fp16 tensor-core MMAs or CUDA cores over the
+// widened codes. The tcgen05 kernel does not read fp8 caches.
+AttnKernelChoice pick_kernel_fp8(Path path, int G, int b) {
+  using mqa::CcConsumer;
+  using mqa::MmaConsumerF8;
+  constexpr int D = 128;
+  if (path == kPathTcgen05) return {};
+  if (path == kPathMmaSync) {
+    if (G <= 16) return choice<MmaConsumerF8<D, 1, 4>, D, 1, true, 1>(b);
+    if (G <= 32) return choice<MmaConsumerF8<D, 2, 8>, D, 1, true, 2>(b);
+    return choice<MmaConsumerF8<D, 4, 8>, D, 1, true, 4>(b);
+  }
+  switch (G) {
+    case 1: return choice<CcConsumer<D, 1, 8, 1>, D, 1, false, 1>(b);
+    case 2: return choice<CcConsumer<D, 2, 8, 1>, D, 1, false, 1>(b);
+    case 3: return choice<CcConsumer<D, 3, 8, 1>, D, 1, false, 1>(b);
+    case 4: return choice<CcConsumer<D, 4, 8, 1>, D, 1, false, 1>(b);
+    case 5: return choice<CcConsumer<D, 5, 8, 1>, D, 1, false, 1>(b);
+    case 6: return choice<CcConsumer<D, 6, 8, 1>, D, 1, false, 1>(b);
+    case 7: return choice<CcConsumer<D, 7, 8, 1>, D, 1, false, 1>(b);
     default: return {};
   }
 }
@@ -300,6 +329,8 @@ struct DecodePlan {
   const mqa_bf16 *k_new = nullptr, *v_new = nullptr;
   const int32_t* pos = nullptr;
   PagedCache paged;  // table null: contiguous caches
+  int eb = 2;        // cache bytes per element: 2 bf16, 1 fp8 E4M3 codes
+  float k_scale = 1.f, v_scale = 1.f;  // fp8 caches: value = code * scale
   int b, h, g, d_h, n_max, G;
   float scale;
   Path path;
@@ -373,11 +404,11 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   CUtensorMap tmk, tmv;
   if (p.paged.table) {
     const long long pages_g = static_cast<long long>(p.paged.num_pages) * p.g;
-    if (!make_pool_map(&tmk, p.k_cache, pages_g, p.paged.page_size, p.d_h) ||
-        !make_pool_map(&tmv, p.v_cache, pages_g, p.paged.page_size, p.d_h))
+    if (!make_pool_map(&tmk, p.k_cache, pages_g, p.paged.page_size, p.d_h, p.eb) ||
+        !make_pool_map(&tmv, p.v_cache, pages_g, p.paged.page_size, p.d_h, p.eb))
       return MQA_ERR_CUDA;
-  } else if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h) ||
-             !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h)) {
+  } else if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h, p.eb) ||
+             !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h, p.eb)) {
     return MQA_ERR_CUDA;
   }
 
@@ -398,7 +429,11 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.G = p.G;
   P.n_max = p.n_max;
   P.num_ctas = static_cast<int>(p.ctas);
-  P.scale_log2 = p.scale * 1.4426950408889634f;
+  // fp8: the logits are scale * k_scale * (q . codes); the output is v_scale * (P codes) / l
+  P.scale_log2 = p.scale * (p.eb == 1 ? p.k_scale : 1.f) * 1.4426950408889634f;
+  P.kq_scale = p.k_scale;
+  P.vq_scale = p.v_scale;
+  P.out_scale = p.eb == 1 ? p.v_scale : 1.f;
   P.timeout_ns = g_wait_limit_ns.load();
   P.drain_ns = kWaitLimitNs;
   P.debug_stall = g_debug_stall.load();
@@ -413,8 +448,9 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.max_pages = p.paged.max_pages;
   P.num_pages = p.paged.num_pages;
 
-  const AttnKernelChoice kc = p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b)
-                                           : pick_kernel<64>(p.path, p.G, p.b);
+  const AttnKernelChoice kc = p.eb == 1       ? pick_kernel_fp8(p.path, p.G, p.b)
+                              : p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b)
+                                             : pick_kernel<64>(p.path, p.G, p.b);
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;
   if (p.paged.table && p.path == kPathTcgen05) return MQA_ERR_UNSUPPORTED;
   if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
@@ -676,6 +712,94 @@ int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf
                            &plan))
     return st;
   plan.paged = pg;
+  plan.k_new = k_new;
+  plan.v_new = v_new;
+  plan.pos = pos;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+// fp8 caches: the scales must be finite and positive; the kernels read d_h = 128 rows.
+static bool valid_fp8_scales(float k_scale, float v_scale) {
+  return std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f && v_scale > 0.f;
+}
+
+int mqa_kv_append_fp8(const mqa_bf16* k_new, const mqa_bf16* v_new, uint8_t* k_cache,
+                      uint8_t* v_cache, const int32_t* pos, int b, int g, int d_h, int n_max,
+                      float k_scale, float v_scale, void* stream) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (!valid_fp8_scales(k_scale, v_scale)) return MQA_ERR_INVALID_ARG;
+  if (d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(b) * g;
+  if (rows > (1ll << 31) || static_cast<double>(rows) * n_max * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+
+  const long long total = rows * (d_h / 16);
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  mqa::kv_append_fp8_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, g, d_h, n_max,
+      k_scale, v_scale);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+int mqa_decode_attention_fp8(const mqa_bf16* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                             const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g,
+                             int d_h, int n_max, float scale, float k_scale, float v_scale,
+                             void* stream) {
+  if (!valid_fp8_scales(k_scale, v_scale)) return MQA_ERR_INVALID_ARG;
+  if (d_h > 0 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  if (int st = plan_decode(q, reinterpret_cast<const mqa_bf16*>(k_cache),
+                           reinterpret_cast<const mqa_bf16*>(v_cache), seq_lens, out, b, h, g,
+                           d_h, n_max, scale, stream, &plan))
+    return st;
+  plan.eb = 1;
+  plan.k_scale = k_scale;
+  plan.v_scale = v_scale;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                        uint8_t* k_cache, uint8_t* v_cache, const int32_t* pos,
+                        const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h,
+                        int n_max, float scale, float k_scale, float v_scale, void* stream) {
+  if (!k_new || !v_new || !pos) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (!valid_fp8_scales(k_scale, v_scale)) return MQA_ERR_INVALID_ARG;
+  if (d_h > 0 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  DecodePlan plan;
+  if (int st = plan_decode(q, reinterpret_cast<const mqa_bf16*>(k_cache),
+                           reinterpret_cast<const mqa_bf16*>(v_cache), seq_lens, out, b, h, g,
+                           d_h, n_max, scale, stream, &plan))
+    return st;
+  plan.eb = 1;
+  plan.k_scale = k_scale;
+  plan.v_scale = v_scale;
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;

@@ -178,3 +178,18 @@ def page_pool(k: torch.Tensor, v: torch.Tensor, rows: torch.Tensor, page_size: i
             pool[pages.to(src.device, torch.long)] = rows_b.reshape(g, n, page_size,
                                                                     d_h).transpose(0, 1)
     return k_pool, v_pool, table
+
+
+def fp8_codes(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """E4M3 codes (uint8) of x / scale by torch's float8_e4m3fn conversion (a library routine;
+    magnitudes are clamped to 448 first, NaN stays NaN): synthetic contents for fp8 caches."""
+    y = (x.float() / scale).clamp(-448.0, 448.0)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def amax_scale(x: torch.Tensor) -> float:
+    """A per-tensor scale that maps the largest finite magnitude of x to 448."""
+    a = x.float()
+    a = a[torch.isfinite(a)].abs()
+    m = float(a.max()) if a.numel() else 1.0
+    return (m if m > 0 else 1.0) / 448.0

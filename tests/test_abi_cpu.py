@@ -42,6 +42,12 @@ def lib():
     L.mqa_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, vp] + [i32] * 6 + [vp]
     L.mqa_decode_attention_paged.restype = i32
     L.mqa_decode_attention_paged.argtypes = [vp] * 6 + [i32] * 7 + [ctypes.c_float, vp]
+    L.mqa_kv_append_fp8.restype = i32
+    L.mqa_kv_append_fp8.argtypes = [vp] * 5 + [i32] * 4 + [ctypes.c_float] * 2 + [vp]
+    L.mqa_decode_attention_fp8.restype = i32
+    L.mqa_decode_attention_fp8.argtypes = [vp] * 5 + [i32] * 5 + [ctypes.c_float] * 3 + [vp]
+    L.mqa_decode_step_fp8.restype = i32
+    L.mqa_decode_step_fp8.argtypes = [vp] * 8 + [i32] * 5 + [ctypes.c_float] * 3 + [vp]
     L.mqa_decode_step_paged.restype = i32
     L.mqa_decode_step_paged.argtypes = [vp] * 9 + [i32] * 7 + [ctypes.c_float, vp]
     return L
@@ -218,3 +224,54 @@ def test_paged_step_host_checks(lib, kw, code):
 ])
 def test_paged_append_host_checks(lib, kw, code):
     assert _append_paged(lib, **kw) == code
+
+
+# ---- fp8 caches: the scales and the head dimension are checked on the host too ---------------
+FP8_SCALE_CASES = [
+    (dict(ks=0.0), INVALID), (dict(vs=-1.0), INVALID), (dict(ks=math.inf), INVALID),
+    (dict(vs=math.nan), INVALID), (dict(d_h=64), UNSUPPORTED), (dict(d_h=256), UNSUPPORTED),
+]
+
+
+def _attn_fp8(lib, q=A, k=A + 0x1000, v=A + 0x2000, lens=A + 0x3000, out=A + 0x4000, b=2, h=8,
+              g=2, d_h=128, n_max=100, scale=0.088, ks=0.01, vs=0.02):
+    return lib.mqa_decode_attention_fp8(q, k, v, lens, out, b, h, g, d_h, n_max, scale, ks, vs,
+                                        None)
+
+
+def _step_fp8(lib, q=A, kn=A + 0x1000, vn=A + 0x2000, k=A + 0x3000, v=A + 0x4000, pos=A + 0x5000,
+              lens=A + 0x6000, out=A + 0x7000, b=2, h=8, g=2, d_h=128, n_max=100, scale=0.088,
+              ks=0.01, vs=0.02):
+    return lib.mqa_decode_step_fp8(q, kn, vn, k, v, pos, lens, out, b, h, g, d_h, n_max, scale,
+                                   ks, vs, None)
+
+
+def _append_fp8(lib, kn=A, vn=A + 0x1000, kc=A + 0x2000, vc=A + 0x3000, pos=A + 0x4000, b=2, g=2,
+                d_h=128, n_max=100, ks=0.01, vs=0.02):
+    return lib.mqa_kv_append_fp8(kn, vn, kc, vc, pos, b, g, d_h, n_max, ks, vs, None)
+
+
+@pytest.mark.parametrize("kw,code", FP8_SCALE_CASES + [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(lens=0), INVALID), (dict(out=A + 4), INVALID),
+    (dict(k=A + 0x1008), INVALID), (dict(b=0), INVALID), (dict(h=8, g=3), INVALID),
+    (dict(scale=math.nan), INVALID), (dict(h=128, g=1), UNSUPPORTED), (dict(b=8193), UNSUPPORTED),
+])
+def test_fp8_attention_host_checks(lib, kw, code):
+    assert _attn_fp8(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", FP8_SCALE_CASES + [
+    (dict(kn=0), INVALID), (dict(vn=A + 0x2002), INVALID), (dict(pos=0), INVALID),
+    (dict(pos=A + 0x5001), INVALID), (dict(q=0), INVALID), (dict(v=A + 0x4008), INVALID),
+    (dict(h=8, g=3), INVALID),
+])
+def test_fp8_step_host_checks(lib, kw, code):
+    assert _step_fp8(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", FP8_SCALE_CASES + [
+    (dict(kn=0), INVALID), (dict(vc=0), INVALID), (dict(pos=0), INVALID), (dict(b=0), INVALID),
+    (dict(n_max=0), INVALID), (dict(kc=A + 0x2008), INVALID), (dict(pos=A + 0x4001), INVALID),
+])
+def test_fp8_append_host_checks(lib, kw, code):
+    assert _append_fp8(lib, **kw) == code
