@@ -6,7 +6,7 @@ step appends one token's K/V and runs attention in all 80 layers back to back, o
 (mqa_decode_step) per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--paged PAGE_SIZE]
+                    [--workload NAME] [--paged PAGE_SIZE] [--kv bf16|fp8]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
 with inputs resident in HBM (lower is better), from CUDA-graph replays of the whole step (every
@@ -22,6 +22,10 @@ written, new rows read and written) against the measured copy bandwidth; its lau
 come from a second timed pass of K steps whose graphs carry CUDA event nodes around every launch.
 ``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same workload. The reference
 arm (``--impl reference``) times that oracle as the reference.
+
+``--kv fp8`` runs the same workload with every layer's caches held as fp8 E4M3 codes of the same
+draws, one scale per tensor (the largest magnitude maps to 448), through ``mqa_decode_step_fp8``;
+the algorithmic bytes count one byte per cached element.
 
 ``--paged PAGE_SIZE`` runs the same workload with every layer's cache held in page pools (the rows
 each sequence attends, laid out in pages of PAGE_SIZE rows in a seeded random order, one page table
@@ -167,13 +171,14 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
-def kv_bytes(w, lens) -> int:
+def kv_bytes(w, lens, eb: int = 2) -> int:
     """Algorithmic bytes of one fused decode-step launch (one layer): K and V rows read
-    (2 * g * L_b * d_h * 2 over the batch), q read and out written (b * h * d_h * 2 each), and the
-    append's new rows read and written (2 * b * g * d_h * 2 each)."""
+    (2 * g * L_b * d_h * eb over the batch; eb = 2 bf16, 1 fp8), q read and out written
+    (b * h * d_h * 2 each), and the append's new rows read (2 * b * g * d_h * 2, bf16) and
+    written (2 * b * g * d_h * eb)."""
     total_rows = int(lens.sum())
-    return (2 * w.g * total_rows * w.d_h * 2 + 2 * w.b * w.h * w.d_h * 2
-            + 2 * 2 * w.b * w.g * w.d_h * 2)
+    return (2 * w.g * total_rows * w.d_h * eb + 2 * w.b * w.h * w.d_h * 2
+            + 2 * w.b * w.g * w.d_h * 2 + 2 * w.b * w.g * w.d_h * eb)
 
 
 def attention_flops(w, lens) -> int:
@@ -233,7 +238,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, args.paged),
+        "data": "synthetic", "config": workload_config(w, args.paged, args.kv),
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": detail},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -245,30 +250,33 @@ def run_reference(args, world, rank):
 L2_BYTES = 126 * 1024 * 1024
 
 
-def step_kv_bytes(w) -> int:
+def step_kv_bytes(w, eb: int = 2) -> int:
     _, lens = inputs.positions_and_lengths(w)
-    return kv_bytes(w, lens) * w.layers
+    return kv_bytes(w, lens, eb) * w.layers
 
 
-def needs_l2_flush(w) -> bool:
+def needs_l2_flush(w, eb: int = 2) -> bool:
     """A step that reads less than twice the L2 could be served from it on the next step."""
-    return step_kv_bytes(w) < 2 * L2_BYTES
+    return step_kv_bytes(w, eb) < 2 * L2_BYTES
 
 
-def workload_config(w, paged: int = 0):
+def workload_config(w, paged: int = 0, kv: str = "bf16"):
+    eb = 1 if kv == "fp8" else 2
     return {"workload": w.name, "b": w.b, "h": w.h, "g": w.g, "d_h": w.d_h, "layers": w.layers,
-            "context": [w.ctx_lo, w.ctx_hi], "n_max": w.n_max, "kv_dtype": "bf16",
+            "context": [w.ctx_lo, w.ctx_hi], "n_max": w.n_max,
+            "kv_dtype": ("fp8 e4m3, one scale per tensor (largest magnitude -> 448)"
+                         if kv == "fp8" else "bf16"),
             "kv_layout": (f"paged, {paged}-row pages in a seeded random order" if paged
                           else "contiguous [b, g, n_max, d_h]"),
-            "l2": ("L2 flushed between steps (256 MB write)" if needs_l2_flush(w)
+            "l2": ("L2 flushed between steps (256 MB write)" if needs_l2_flush(w, eb)
                    else "inputs larger than L2 (no flush)")}
 
 
 PAGE_TABLE_SEED = 4242
 
 
-def traffic_key(w, paged: int = 0) -> str:
-    return w.name + (f"_paged{paged}" if paged else "")
+def traffic_key(w, paged: int = 0, kv: str = "bf16") -> str:
+    return w.name + (f"_paged{paged}" if paged else "") + ("_fp8" if kv == "fp8" else "")
 
 
 # ------------------------------------------------------------------------------------------------
@@ -292,6 +300,14 @@ def run_ours(args, world, rank, local):
     table_d = None
     for li in range(w.layers):
         k, v = inputs.cache(w, li, dev, tail="random")
+        if args.kv == "fp8":
+            # codes of the same draws, one scale per tensor (largest magnitude -> 448)
+            ks, vs = inputs.amax_scale(k), inputs.amax_scale(v)
+            k, v = inputs.fp8_codes(k, ks), inputs.fp8_codes(v, vs)
+            layers.append(LayerState(k, v, fp8_scales=(ks, vs)))
+            xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
+            outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
+            continue
         if args.paged:
             # the same rows in page pools; one page table (a seeded shuffle of the pages that the
             # attended rows need) shared by every layer
@@ -302,7 +318,8 @@ def run_ours(args, world, rank, local):
         xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
         outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
     # small workloads fit in L2: flush it between steps by writing a buffer twice its size
-    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if needs_l2_flush(w)
+    eb = 1 if args.kv == "fp8" else 2
+    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if needs_l2_flush(w, eb)
              else None)
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
@@ -441,17 +458,18 @@ def run_ours(args, world, rank, local):
 
     if rank == 0:
         peak, peak_kind = measured_peak_hbm()
-        nbytes = kv_bytes(w, lens)
+        nbytes = kv_bytes(w, lens, eb)
         achieved = nbytes / attn_avg_s / 1e9
-        traffic = recorded_traffic(traffic_key(w, args.paged))
+        traffic = recorded_traffic(traffic_key(w, args.paged, args.kv))
         # weak scaling: every rank runs its own full step; N steps finish in ms_per_step
         value_us = ms_per_step * 1000.0 / world
         cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w)
         line = {
             "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(w, args.paged),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16" if args.kv == "fp8" else "bf16",
+            "data": "synthetic", "config": workload_config(w, args.paged, args.kv),
             "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
             "attention_us_per_layer": attn_avg_s * 1e6,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -483,7 +501,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="gqa_70b_80l", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
                     help="keep the caches in page pools of this many rows (0: contiguous)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache element type: bf16, or fp8 E4M3 codes with per-tensor scales")
     args = ap.parse_args(argv)
+    if args.kv == "fp8" and args.paged:
+        ap.error("--kv fp8 runs on contiguous caches")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()

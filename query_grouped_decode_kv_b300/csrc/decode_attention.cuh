@@ -845,6 +845,7 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
 template <int D, int WM, int NW>
 struct MmaConsumer {
   static constexpr int kWarps = NW;
+  static constexpr int kTileGroups = 1;
   static constexpr int kCombRows = 16;  // head rows per warp
   static constexpr int NGRP = NW / WM;
   static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
@@ -1018,12 +1019,18 @@ struct MmaConsumer {
 // columns. Output tile 2b + e (block b, e = 0 even, 1 odd) thus holds columns 16b + 2n + e, and
 // a lane's accumulators cover columns 16b + 4c + {0, 1, 2, 3}, which publish() writes back in
 // order.
+// Tile groups (TG = 2): an fp8 tile carries half the bytes of a bf16 one, so its HBM time is half
+// while a warp's per-tile chain of dependent steps (ldmatrix, widening, MMAs, softmax, MMAs) is
+// not shorter. Eight warps then form two groups of four that take alternate tiles of the CTA's
+// range, each with its own softmax state, merged with the key groups at the segment's end; every
+// warp still does a whole tile's worth of work per tile it owns.
 // ---------------------------------------------------------------------------------------------
-template <int D, int WM, int NW>
+template <int D, int WM, int NW, int TG = 1>
 struct MmaConsumerF8 {
   static constexpr int kWarps = NW;
+  static constexpr int kTileGroups = TG;
   static constexpr int kCombRows = 16;  // head rows per warp
-  static constexpr int NGRP = NW / WM;
+  static constexpr int NGRP = NW / (WM * TG);  // key groups per tile group
   static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
   static constexpr int NT_S = KPW / 8;          // score tiles (n = 8 keys)
   static constexpr int KS_QK = D / 16;          // k-steps over the head dimension
@@ -1184,7 +1191,19 @@ struct MmaConsumerF8 {
     }
   }
 
-  using Rows = typename MmaConsumer<D, WM, NW>::Rows;
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int t = 0; t < TG; ++t) {
+#pragma unroll
+        for (int grp = 0; grp < NGRP; ++grp) {
+          ws[t * NGRP + grp] = t * (NW / TG) + grp * WM + (hr >> 4);
+          rs[t * NGRP + grp] = hr & 15;
+        }
+      }
+      return TG * NGRP;
+    }
+  };
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -1195,6 +1214,7 @@ struct MmaConsumerF8 {
 template <int D, int G, int NW, int EB = 2>
 struct CcConsumer {
   static constexpr int kWarps = NW;
+  static constexpr int kTileGroups = 1;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
   static constexpr int DPL = D / 32;
   static constexpr int KPW = kTileKeys / NW;
@@ -1375,7 +1395,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     *sh.merge = 0;
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&sh.full[st], 1);
-      mbar_init(&sh.empty[st], NW);
+      mbar_init(&sh.empty[st], NW / Consumer::kTileGroups);  // the warps of one tile group
     }
     mbar_init(sh.cbar, NW * 32);
     mbar_init(sh.stall, 1);
@@ -1412,9 +1432,15 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
 
   // ================================== consumers ================================================
   Consumer cons;
-  const int grp = kTensorCores ? warp / WM : warp;
-  const int mi = kTensorCores ? warp % WM : 0;
-  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / NW : kTileKeys / NW;
+  // tile groups: warp group tg owns the tiles k with k % TG == tg (TG = 1: every warp, every tile)
+  constexpr int TG = Consumer::kTileGroups;
+  constexpr int WPG = NW / TG;  // warps per tile group
+  static_assert(TG == 1 || kTensorCores, "tile groups are a tensor-core consumer option");
+  const int tg = warp / WPG;
+  const int gw = warp % WPG;
+  const int grp = kTensorCores ? gw / WM : warp;
+  const int mi = kTensorCores ? gw % WM : 0;
+  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / WPG : kTileKeys / NW;
   uint32_t cphase = 0;
   TileCursor cur;
   cur.start(x0, sh.tix);
@@ -1426,7 +1452,8 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
-    if (!mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
+    const bool mine = TG == 1 || k % TG == tg;
+    if (mine && !mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
       if (!*sh.abort) give_up(sh, kSiteConsumerFull, k);
       return;
     }
@@ -1440,7 +1467,9 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     const int valid = min(L - tile_start, kTileKeys);  // >= 1
     const uint32_t kbase = stages_base + st * kStageBytes;
     const uint32_t vbase = kbase + kKvBytes;
-    if constexpr (kTensorCores) {
+    if (!mine) {
+      // another tile group's tile: only the segment bookkeeping below
+    } else if constexpr (kTensorCores) {
       // V rows at or beyond the length may hold anything (NaN included) and 0 * NaN = NaN on
       // the tensor cores: zero this group's invalid V rows before P V reads them.
       const int g0 = grp * kGroupKeys;
@@ -1464,8 +1493,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       const int nvalid = max(0, min(valid - warp * kGroupKeys, kGroupKeys));
       cons.tile(kbase, vbase, warp, lane, nvalid, P.scale_log2);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[st]);
+    if (mine) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[st]);
+    }
 
     const bool seg_end = (cur.tile == cur.nt - 1);
     if (seg_end || k == ntiles - 1) {

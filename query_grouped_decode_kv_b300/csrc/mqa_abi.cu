@@ -272,7 +272,9 @@ AttnKernelChoice pick_kernel_fp8(Path path, int G, int b) {
   constexpr int D = 128;
   if (path == kPathTcgen05) return {};
   if (path == kPathMmaSync) {
-    if (G <= 16) return choice<MmaConsumerF8<D, 1, 4>, D, 1, true, 1>(b);
+    // up to 16 heads: two tile groups of four warps (an fp8 tile's HBM time is half a bf16
+    // tile's, so one group alone would wait on its own per-tile chain)
+    if (G <= 16) return choice<MmaConsumerF8<D, 1, 8, 2>, D, 1, true, 1>(b);
     if (G <= 32) return choice<MmaConsumerF8<D, 2, 8>, D, 1, true, 2>(b);
     return choice<MmaConsumerF8<D, 4, 8>, D, 1, true, 4>(b);
   }

@@ -18,14 +18,24 @@ from . import binding
 class LayerState:
     """One layer's caches: contiguous [b, g, n_max, d_h] bf16, or, with a page table, page pools
     [num_pages, g, page_size, d_h] whose pages ``page_table`` [b, max_pages] int32 lists per
-    sequence (the layers of a model normally share one table)."""
+    sequence (the layers of a model normally share one table). With ``fp8_scales`` = (k_scale,
+    v_scale) the contiguous caches hold fp8 E4M3 codes (uint8) of value code * scale."""
     k_cache: torch.Tensor
     v_cache: torch.Tensor
     page_table: torch.Tensor | None = None
+    fp8_scales: tuple[float, float] | None = None
+
+    def __post_init__(self):
+        if self.fp8_scales is not None and self.page_table is not None:
+            raise ValueError("fp8 caches are contiguous; paged caches are bf16")
 
     def step(self, q, k_new, v_new, pos, seq_lens, out, scale, stream) -> None:
         """One fused append + attention launch on this layer."""
-        if self.page_table is None:
+        if self.fp8_scales is not None:
+            ks, vs = self.fp8_scales
+            binding.decode_step_fp8(q, k_new, v_new, self.k_cache, self.v_cache, pos, seq_lens,
+                                    ks, vs, out=out, scale=scale, stream=stream)
+        elif self.page_table is None:
             binding.decode_step(q, k_new, v_new, self.k_cache, self.v_cache, pos, seq_lens,
                                 out=out, scale=scale, stream=stream)
         else:
@@ -34,14 +44,20 @@ class LayerState:
                                       stream=stream)
 
     def append(self, k_new, v_new, pos, stream) -> None:
-        if self.page_table is None:
+        if self.fp8_scales is not None:
+            binding.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, pos,
+                                  *self.fp8_scales, stream=stream)
+        elif self.page_table is None:
             binding.kv_append(k_new, v_new, self.k_cache, self.v_cache, pos, stream=stream)
         else:
             binding.kv_append_paged(k_new, v_new, self.k_cache, self.v_cache, pos,
                                     self.page_table, stream=stream)
 
     def attend(self, q, seq_lens, out, scale, stream) -> None:
-        if self.page_table is None:
+        if self.fp8_scales is not None:
+            binding.decode_attention_fp8(q, self.k_cache, self.v_cache, seq_lens,
+                                         *self.fp8_scales, out=out, scale=scale, stream=stream)
+        elif self.page_table is None:
             binding.decode_attention(q, self.k_cache, self.v_cache, seq_lens, out=out,
                                      scale=scale, stream=stream)
         else:

@@ -213,3 +213,27 @@ def test_fp8_invalid_length_writes_zeros(mqa):
     assert np.all(P.bits(out)[2] == 0)
     keep = [0, 1, 3]
     P.assert_close(out[keep], out_ref[keep], "valid sequences next to an invalid one")
+
+
+def test_fp8_layers_through_the_multi_layer_driver(mqa):
+    # three fp8 layers (each with its own scales) through layers.decode_layers, fused and not
+    from query_grouped_decode_kv_b300.layers import LayerState, StepInputs, decode_layers
+    dev = torch.device("cuda")
+    for fused in (True, False):
+        c0 = fp8_case((3, 32, 4, 128, 50, 600), 1400)
+        cases = [c0] + [fp8_case((3, 32, 4, 128, 50, 600), 1400 + li, lens=c0["lens"].tolist(),
+                                 pos=c0["pos"].tolist()) for li in (1, 2)]
+        lays = [LayerState(c["k8"].to(dev), c["v8"].to(dev), fp8_scales=(c["k_scale"], c["v_scale"]))
+                for c in cases]
+        xs = [StepInputs(c["q"].to(dev), c["k_new"].to(dev), c["v_new"].to(dev)) for c in cases]
+        outs = [torch.empty_like(x.q) for x in xs]
+        pos, lens = cases[0]["pos"].to(dev), cases[0]["lens"].to(dev)
+        assert all(torch.equal(c["lens"], cases[0]["lens"]) for c in cases)
+        decode_layers(lays, xs, pos, lens, outs, cases[0]["scale"], fused=fused)
+        torch.cuda.synchronize()
+        assert mqa.get_device_status() == 0
+        for c, lay, o in zip(cases, lays, outs):
+            k_ref, v_ref, out_ref, _, _ = oracle_fp8_step(c)
+            assert np.array_equal(lay.k_cache.cpu().numpy(), k_ref)
+            assert np.array_equal(lay.v_cache.cpu().numpy(), v_ref)
+            P.assert_close(o, out_ref, f"fp8 layers fused={fused}")
