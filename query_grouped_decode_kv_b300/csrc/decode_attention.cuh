@@ -40,6 +40,8 @@ namespace mqa {
 constexpr int kTileKeys = 64;       // cache rows per pipeline stage
 constexpr int kRingBytes = 128 * 1024;  // the shared-memory ring of K/V stages
 constexpr int kSwizzleRowBytes = 128;
+constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;  // two bf16 ones (the B fragment of P 1)
+constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 // NW (a template parameter below) is the number of consumer warps: 4 or 8.
 //  - NW = 4: one producer warp comes on top (160 threads, one warp per SM sub-partition each).
 //  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
@@ -857,7 +859,8 @@ struct MmaConsumer {
 
   uint32_t qa[KS_QK][4];
   float o[NT_O][4];
-  float m[2], l[2];
+  float ol[4];  // P 1: the running sums of the rounded weights, rescaled with O (all columns equal)
+  float m[2];
 
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
                                                 int lane) {
@@ -876,18 +879,21 @@ struct MmaConsumer {
     }
 #pragma unroll
     for (int n = 0; n < NT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    ol[0] = ol[1] = ol[2] = ol[3] = 0.f;
     m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
   }
 
   // One tile. `valid` = number of the tile's rows that lie below the sequence length.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
                                        int valid, float scale_log2) {
-    float s[NT_S][4];
+    // S = Q K^T, even and odd k-steps into separate accumulators (half the dependent chain)
+    float s[NT_S][4], s2[NT_S][4];
 #pragma unroll
-    for (int n = 0; n < NT_S; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.f;
+    }
     const int mat = lane >> 3, rr = lane & 7;
-    // S = Q K^T
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ++ks) {
 #pragma unroll
@@ -896,9 +902,15 @@ struct MmaConsumer {
         const int d = ks * 16 + ((mat & 1) ? 8 : 0);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(swz(kbase, key, d), b0, b1, b2, b3);
-        mma_16816(s[2 * np], qa[ks], b0, b1);
-        mma_16816(s[2 * np + 1], qa[ks], b2, b3);
+        float (&acc0)[4] = (ks & 1) ? s2[2 * np] : s[2 * np];
+        float (&acc1)[4] = (ks & 1) ? s2[2 * np + 1] : s[2 * np + 1];
+        mma_16816(acc0, qa[ks], b0, b1);
+        mma_16816(acc1, qa[ks], b2, b3);
       }
+    }
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] += s2[n][0]; s[n][1] += s2[n][1]; s[n][2] += s2[n][2]; s[n][3] += s2[n][3];
     }
     // scale (log2 domain), mask rows at or beyond the length, running max per head row
     const int c2 = (lane & 3) * 2;
@@ -927,28 +939,23 @@ struct MmaConsumer {
     if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
     const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
     const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
-    // weights, rounded to bf16 once: the same rounded values feed P V and the running sum, so
-    // the normalised weights still add up to one
-    float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
-      s[n][0] = round_bf16(fast_exp2(s[n][0] - ref0));
-      s[n][1] = round_bf16(fast_exp2(s[n][1] - ref0));
-      s[n][2] = round_bf16(fast_exp2(s[n][2] - ref1));
-      s[n][3] = round_bf16(fast_exp2(s[n][3] - ref1));
-      ps0 += s[n][0] + s[n][1];
-      ps1 += s[n][2] + s[n][3];
+      s[n][0] = fast_exp2(s[n][0] - ref0);
+      s[n][1] = fast_exp2(s[n][1] - ref0);
+      s[n][2] = fast_exp2(s[n][2] - ref1);
+      s[n][3] = fast_exp2(s[n][3] - ref1);
     }
-    l[0] = l[0] * al0 + ps0;
-    l[1] = l[1] * al1 + ps1;
     if (__any_sync(0xffffffffu, up0 || up1)) {
 #pragma unroll
       for (int n = 0; n < NT_O; ++n) {
         o[n][0] *= al0; o[n][1] *= al0;
         o[n][2] *= al1; o[n][3] *= al1;
       }
+      ol[0] *= al0; ol[1] *= al0; ol[2] *= al1; ol[3] *= al1;
     }
-    // O += P V  (the packing below is exact: the weights are already bf16 values)
+    // O += P V with the weights rounded to bf16 once; P 1 on the tensor cores sums exactly those
+    // rounded weights (fp32), so the normalised weights still add up to one
 #pragma unroll
     for (int kk = 0; kk < KS_PV; ++kk) {
       uint32_t a[4];
@@ -956,6 +963,7 @@ struct MmaConsumer {
       a[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
       a[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       a[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      mma_16816(ol, a, kOnesBf16x2, kOnesBf16x2);
 #pragma unroll
       for (int dp = 0; dp < NT_O / 2; ++dp) {
         const int key = grp * KPW + kk * 16 + rr + ((mat & 1) ? 8 : 0);
@@ -970,11 +978,7 @@ struct MmaConsumer {
 
   // Publish this warp's state (rows mi*16 .. mi*16+15 of the group) to the combine scratch.
   __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
-    float l0 = l[0], l1 = l[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float l0 = ol[0], l1 = ol[2];  // row sums over all of this warp's keys
     const int r = lane >> 2, c2 = (lane & 3) * 2;
     float* row0 = sh.comb_o + (warp * kCombRows + r) * comb_row_floats(D);
     float* row1 = sh.comb_o + (warp * kCombRows + r + 8) * comb_row_floats(D);
@@ -1040,7 +1044,8 @@ struct MmaConsumerF8 {
 
   uint32_t qa[KS_QK][4];
   float o[NT_O][4];
-  float m[2], l[2];
+  float ol[4];  // P 1: the running sums of the rounded weights, rescaled with O (all columns equal)
+  float m[2];
 
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
                                                 int lane) {
@@ -1066,18 +1071,22 @@ struct MmaConsumerF8 {
     }
 #pragma unroll
     for (int n = 0; n < NT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    ol[0] = ol[1] = ol[2] = ol[3] = 0.f;
     m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
   }
 
   // One tile. `valid` = number of the tile's rows that lie below the sequence length.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
                                        int valid, float scale_log2) {
-    float s[NT_S][4];
+    // S = Q K^T, block ks into s and block ks + 1 into s2 (half the dependent chain)
+    float s[NT_S][4], s2[NT_S][4];
 #pragma unroll
-    for (int n = 0; n < NT_S; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.f;
+    }
     const int mat = lane >> 3, rr = lane & 7;
-    // S = Q K^T: one ldmatrix.x4 = keys (8 or 8 + 8) x column blocks (ks, ks + 1)
+    // one ldmatrix.x4 = keys (8 or 8 + 8) x column blocks (ks, ks + 1)
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ks += 2) {
 #pragma unroll
@@ -1091,10 +1100,14 @@ struct MmaConsumerF8 {
         e4m3x4_to_f16x2x2(w2, b[2][0], b[2][1]);  // keys 8-15, block ks
         e4m3x4_to_f16x2x2(w3, b[3][0], b[3][1]);  // keys 8-15, block ks + 1
         mma_16816_f16(s[2 * np], qa[ks], b[0][0], b[0][1]);
-        mma_16816_f16(s[2 * np], qa[ks + 1], b[1][0], b[1][1]);
+        mma_16816_f16(s2[2 * np], qa[ks + 1], b[1][0], b[1][1]);
         mma_16816_f16(s[2 * np + 1], qa[ks], b[2][0], b[2][1]);
-        mma_16816_f16(s[2 * np + 1], qa[ks + 1], b[3][0], b[3][1]);
+        mma_16816_f16(s2[2 * np + 1], qa[ks + 1], b[3][0], b[3][1]);
       }
+    }
+#pragma unroll
+    for (int n = 0; n < NT_S; ++n) {
+      s[n][0] += s2[n][0]; s[n][1] += s2[n][1]; s[n][2] += s2[n][2]; s[n][3] += s2[n][3];
     }
     // scale (log2 domain), mask rows at or beyond the length, running max per head row
     const int c2 = (lane & 3) * 2;
@@ -1121,26 +1134,22 @@ struct MmaConsumerF8 {
     if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
     const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
     const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
-    float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
-      s[n][0] = round_f16(fast_exp2(s[n][0] - ref0));
-      s[n][1] = round_f16(fast_exp2(s[n][1] - ref0));
-      s[n][2] = round_f16(fast_exp2(s[n][2] - ref1));
-      s[n][3] = round_f16(fast_exp2(s[n][3] - ref1));
-      ps0 += s[n][0] + s[n][1];
-      ps1 += s[n][2] + s[n][3];
+      s[n][0] = fast_exp2(s[n][0] - ref0);
+      s[n][1] = fast_exp2(s[n][1] - ref0);
+      s[n][2] = fast_exp2(s[n][2] - ref1);
+      s[n][3] = fast_exp2(s[n][3] - ref1);
     }
-    l[0] = l[0] * al0 + ps0;
-    l[1] = l[1] * al1 + ps1;
     if (__any_sync(0xffffffffu, up0 || up1)) {
 #pragma unroll
       for (int n = 0; n < NT_O; ++n) {
         o[n][0] *= al0; o[n][1] *= al0;
         o[n][2] *= al1; o[n][3] *= al1;
       }
+      ol[0] *= al0; ol[1] *= al0; ol[2] *= al1; ol[3] *= al1;
     }
-    // O += P V (the packing is exact: the weights are already fp16 values)
+    // O += P V with the weights rounded to fp16 once; P 1 sums exactly those rounded weights
 #pragma unroll
     for (int kk = 0; kk < KS_PV; ++kk) {
       uint32_t a[4];
@@ -1148,6 +1157,7 @@ struct MmaConsumerF8 {
       a[1] = pack_f16x2(s[2 * kk][2], s[2 * kk][3]);
       a[2] = pack_f16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       a[3] = pack_f16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      mma_16816_f16(ol, a, kOnesF16x2, kOnesF16x2);
 #pragma unroll
       for (int cb = 0; cb < D / 16; cb += 2) {
         // matrices: keys 0-7 / 8-15 of this k-step x column blocks cb / cb + 1
@@ -1169,11 +1179,7 @@ struct MmaConsumerF8 {
 
   // Publish this warp's state (rows mi*16 .. mi*16+15 of the group) to the combine scratch.
   __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
-    float l0 = l[0], l1 = l[1];
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float l0 = ol[0], l1 = ol[2];  // row sums over all of this warp's keys
     const int r = lane >> 2, c4 = (lane & 3) * 4;
     float* row0 = sh.comb_o + (warp * kCombRows + r) * comb_row_floats(D);
     float* row1 = sh.comb_o + (warp * kCombRows + r + 8) * comb_row_floats(D);
