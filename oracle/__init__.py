@@ -28,6 +28,11 @@ What each function computes, and the passage it follows:
   :func:`decode_attention_fp8` is attention over the dequantized caches (quantized K/V caches:
   ybb.press page §十 item 7, nanhubrain.csdn.net MQA article §4.3).
 
+* :func:`kv_append_multi` / :func:`decode_attention_multi` -- T new tokens per sequence
+  (ybb.press page §八: ``forward(x, start)`` writes T rows and attends over ``start + T`` rows;
+  §十 item 10: the causal mask still applies per query position): token t attends the first
+  ``seq_lens[b] - T + 1 + t`` rows.
+
 Every function is pinned by ``tests/test_oracle_pins.py`` against closed forms, the pages' printed
 numbers, invariants and library routines.
 """
@@ -79,6 +84,11 @@ def _configure(lib):
                                          ctypes.c_float]
     lib.oracle_dequantize_e4m3.restype = i32
     lib.oracle_dequantize_e4m3.argtypes = [vp, ctypes.c_size_t, dbl, vp]
+    lib.oracle_kv_append_multi.restype = i32
+    lib.oracle_kv_append_multi.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_decode_attention_multi_bf16.restype = i32
+    lib.oracle_decode_attention_multi_bf16.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                       i32, i32, dbl, i32]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -304,3 +314,41 @@ def decode_attention_fp8(q, k_codes, v_codes, seq_lens, k_scale: float, v_scale:
     vf = dequantize_e4m3(v_codes, v_scale)
     return decode_attention(qf, kf, vf, seq_lens, scale, threads=threads,
                             return_status=return_status)
+
+
+def kv_append_multi(k_new, v_new, k_cache, v_cache, pos) -> int:
+    """Append T rows per sequence (``k_new`` [b, T, g, d_h]) at rows ``pos[b] .. pos[b]+T-1``,
+    in place (caches: C-contiguous uint16 numpy arrays)."""
+    lib = _load()
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint16 and c.flags.c_contiguous):
+            raise TypeError("caches must be C-contiguous uint16 numpy arrays (updated in place)")
+    b, g, n_max, d_h = k_cache.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    T = kn.shape[1]
+    p = _c(pos, np.int32)
+    st = int(lib.oracle_kv_append_multi(_ptr(kn), _ptr(vn), _ptr(k_cache), _ptr(v_cache), _ptr(p),
+                                        b, T, g, d_h, n_max))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return st
+
+
+def decode_attention_multi(q, k_cache, v_cache, seq_lens, scale: float, threads: int = 0,
+                           return_status: bool = False):
+    """Causal attention of T query tokens per sequence (``q`` [b, T, h, d_h], bf16 bit
+    patterns) over bf16 caches; token t sees the first ``seq_lens[b] - T + 1 + t`` rows.
+    Returns float64 [b, T, h, d_h]."""
+    lib = _load()
+    qq = _c(q, np.uint16)
+    kk, vv = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+    lens = _c(seq_lens, np.int32)
+    b, T, h, d_h = qq.shape
+    _, g, n_max, _ = kk.shape
+    out = np.empty((b, T, h, d_h), dtype=np.float64)
+    st = int(lib.oracle_decode_attention_multi_bf16(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(lens),
+                                                    _ptr(out), b, T, h, g, d_h, n_max,
+                                                    float(scale), int(threads)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return (out, st) if return_status else out

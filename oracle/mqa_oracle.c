@@ -385,6 +385,91 @@ int oracle_decode_attention_f64(const double* q, const double* k_cache, const do
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Several new tokens per sequence ([GQA-MQA] §八: forward(x, start) appends T rows at          */
+/* start .. start+T-1 and attends over the first start+T rows; §十 item 10: the causal mask     */
+/* still applies per query position when K/V are shared). Query token t of sequence b sits at  */
+/* row L_b - T + t, where L_b = seq_lens[b] counts all T new rows, and attends rows             */
+/* 0 .. L_b - T + t: the first L_b - T + 1 + t rows.                                           */
+/* q and out are [b][T][h][d_h]; k_new, v_new [b][T][g][d_h].                                  */
+/* ------------------------------------------------------------------------------------------ */
+int oracle_kv_append_multi(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_cache,
+                           uint16_t* v_cache, const int32_t* pos, int b, int T, int g, int d_h,
+                           int n_max) {
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || T <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    const int p0 = pos[bi];
+    if (p0 < 0 || (long long)p0 + T > n_max) { status = ORACLE_ERR_BOUNDS; continue; }
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < g; ++j) {
+        const size_t src = (((size_t)bi * T + t) * g + j) * (size_t)d_h;
+        const size_t row = ((size_t)bi * g + j) * (size_t)n_max + (size_t)(p0 + t);
+        memcpy(k_cache + row * (size_t)d_h, k_new + src, (size_t)d_h * sizeof(uint16_t));
+        memcpy(v_cache + row * (size_t)d_h, v_new + src, (size_t)d_h * sizeof(uint16_t));
+      }
+  }
+  return status;
+}
+
+int oracle_decode_attention_multi_bf16(const uint16_t* q, const uint16_t* k_cache,
+                                       const uint16_t* v_cache, const int32_t* seq_lens,
+                                       double* out, int b, int T, int h, int g, int d_h,
+                                       int n_max, double scale, int threads) {
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || T <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0 || h % g)
+    return ORACLE_ERR_INVALID_ARG;
+  int bad = 0;
+  for (int bi = 0; bi < b; ++bi)
+    if (seq_lens[bi] < T || seq_lens[bi] > n_max) bad = 1;
+#ifdef _OPENMP
+  if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel num_threads(threads)
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)n_max);
+    double* qf = (double*)malloc(sizeof(double) * (size_t)d_h);
+#ifdef _OPENMP
+#pragma omp for collapse(3) schedule(dynamic, 1)
+#endif
+    for (int bi = 0; bi < b; ++bi) {
+      for (int tq = 0; tq < T; ++tq) {
+        for (int i = 0; i < h; ++i) {
+          const size_t row_off = (((size_t)bi * T + tq) * h + i) * (size_t)d_h;
+          double* o = out + row_off;
+          for (int d = 0; d < d_h; ++d) o[d] = 0.0;
+          const int Lb = seq_lens[bi];
+          if (Lb < T || Lb > n_max) continue;
+          const int visible = Lb - T + 1 + tq;             /* causal: rows 0 .. Lb - T + tq */
+          const int j = i / (h / g);                       /* §五: j = i // (h/g) */
+          const size_t kv_off = ((size_t)bi * g + j) * (size_t)n_max * (size_t)d_h;
+          for (int d = 0; d < d_h; ++d) qf[d] = oracle_bf16_to_double(q[row_off + d]);
+          double m = -INFINITY;
+          for (int t = 0; t < visible; ++t) {
+            double s = 0.0;
+            for (int d = 0; d < d_h; ++d)
+              s += qf[d] * oracle_bf16_to_double(k_cache[kv_off + (size_t)t * d_h + d]);
+            scores[t] = scale * s;
+            if (scores[t] > m) m = scores[t];
+          }
+          double l = 0.0;
+          for (int t = 0; t < visible; ++t) {
+            const double w = exp(scores[t] - m);
+            l += w;
+            for (int d = 0; d < d_h; ++d)
+              o[d] += w * oracle_bf16_to_double(v_cache[kv_off + (size_t)t * d_h + d]);
+          }
+          for (int d = 0; d < d_h; ++d) o[d] /= l;
+        }
+      }
+    }
+    free(scores);
+    free(qf);
+  }
+  return bad ? ORACLE_ERR_BOUNDS : ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Split-sequence partials and their log-sum-exp merge. The pages do not describe splitting;  */
 /* this is the identity  softmax over a union of ranges = exp-weighted combination of the     */
 /* per-range softmax states, used to check that splitting a sequence changes nothing.         */

@@ -45,6 +45,14 @@ MUTANTS = [
     ("e4m3_overflow_to_nan", "if (a >= 448.0) return sign | 0x7E;",
      "if (a >= 448.0) return sign | 0x7F;"),
     ("fp8_append_wrong_row", "(size_t)n_max + (size_t)p;\n", "(size_t)n_max + (size_t)(p ^ 1);\n"),
+    ("multi_token_no_causal_offset", "const int visible = Lb - T + 1 + tq;",
+     "const int visible = Lb;"),
+    ("multi_token_causal_off_by_one", "const int visible = Lb - T + 1 + tq;",
+     "const int visible = Lb - T + tq;"),
+    ("multi_token_wrong_query_token", "const size_t row_off = (((size_t)bi * T + tq) * h + i)",
+     "const size_t row_off = (((size_t)bi * T + (T - 1 - tq)) * h + i)"),
+    ("multi_token_append_wrong_row", "(size_t)n_max + (size_t)(p0 + t);",
+     "(size_t)n_max + (size_t)(p0 + T - 1 - t);"),
     ("fp8_append_without_scale", "(float)oracle_bf16_to_double(k_new[src + d]) / k_scale;",
      "(float)oracle_bf16_to_double(k_new[src + d]);"),
 ]

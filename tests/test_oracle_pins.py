@@ -645,3 +645,82 @@ def test_fp8_scales_fold_into_the_logit_scale_and_the_output():
     assert np.allclose(oracle.decode_attention_fp8(q, kc, vc, lens, 0.04, 0.5, 0.25),
                        oracle.decode_attention_fp8(q, kc, vc, lens, 0.02, 0.5, 0.5), rtol=1e-13)
     assert np.array_equal(oracle.decode_attention_fp8(q, kc, vc, lens, 0.02, 1.0, 0.25), 2 * a)
+
+
+# --------------------------------------------------------------------------------------------
+# T new tokens per sequence, causal
+# --------------------------------------------------------------------------------------------
+def _multi_case(b, T, h, g, d_h, n_max, seed):
+    rng = np.random.default_rng(seed)
+    q = oracle.f64_to_bf16(rng.standard_normal((b, T, h, d_h)))
+    k = oracle.f64_to_bf16(rng.standard_normal((b, g, n_max, d_h)))
+    v = oracle.f64_to_bf16(rng.standard_normal((b, g, n_max, d_h)))
+    return q, k, v
+
+
+def test_multi_token_attention_with_one_token_is_decode_attention():
+    q, k, v = _multi_case(2, 1, 8, 2, 16, 40, seed=31)
+    lens = np.array([40, 17], dtype=np.int32)
+    got = oracle.decode_attention_multi(q, k, v, lens, 0.25)
+    assert np.array_equal(got[:, 0], oracle.decode_attention(q[:, 0], k, v, lens, 0.25))
+
+
+def test_multi_token_attention_token_t_is_a_decode_step_at_its_own_length():
+    """Token t of T sees exactly the rows a single-token step at length L - T + 1 + t sees."""
+    T = 5
+    q, k, v = _multi_case(3, T, 8, 4, 16, 50, seed=37)
+    lens = np.array([50, 5, 23], dtype=np.int32)
+    got = oracle.decode_attention_multi(q, k, v, lens, 0.3)
+    for t in range(T):
+        ref = oracle.decode_attention(np.ascontiguousarray(q[:, t]), k, v, lens - (T - 1 - t), 0.3)
+        assert np.array_equal(got[:, t], ref)
+
+
+def test_multi_token_attention_matches_the_pages_module_with_a_causal_mask():
+    """The ybb.press §八 module (repeat_interleave K/V to h heads, einsum scores / sqrt(d_h),
+    softmax, einsum with V) in float64 torch, with the causal mask of §十 item 10 added: query
+    token t at row start + t may not see rows after it."""
+    b, T, h, g, d_h, start = 1, 4, 8, 2, 16, 9
+    q, k, v = _multi_case(b, T, h, g, d_h, start + T, seed=41)
+    L = start + T
+    qf = torch.from_numpy(oracle.bf16_to_f64(q))                     # (B, T, h, d_h)
+    kc = torch.from_numpy(oracle.bf16_to_f64(k))[0, :, :L]           # (g, L, d_h)
+    vc = torch.from_numpy(oracle.bf16_to_f64(v))[0, :, :L]
+    krep = kc.repeat_interleave(h // g, dim=0)                       # (h, L, d_h)
+    vrep = vc.repeat_interleave(h // g, dim=0)
+    scores = torch.einsum("bthd,hld->bhtl", qf, krep) / (d_h ** 0.5)
+    rows = torch.arange(L).view(1, L)
+    causal = rows > (start + torch.arange(T)).view(T, 1)             # (T, L): future rows
+    scores = scores.masked_fill(causal.view(1, 1, T, L), float("-inf"))
+    attn = torch.softmax(scores, dim=-1)
+    ref = torch.einsum("bhtl,hld->bthd", attn, vrep).numpy()
+    got = oracle.decode_attention_multi(q, k, v, np.array([L], np.int32), 1 / math.sqrt(d_h))
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_multi_token_attention_rejects_lengths_shorter_than_the_tokens():
+    q, k, v = _multi_case(2, 3, 4, 1, 8, 10, seed=43)
+    out, st = oracle.decode_attention_multi(q, k, v, np.array([2, 10], np.int32), 0.5,
+                                            return_status=True)
+    assert st == oracle.ERR_BOUNDS and np.all(out[0] == 0) and np.all(np.isfinite(out[1]))
+
+
+def test_multi_token_append_is_t_single_appends():
+    b, T, g, d_h, n_max = 2, 3, 2, 8, 9
+    rng = np.random.default_rng(47)
+    kn = oracle.f64_to_bf16(rng.standard_normal((b, T, g, d_h)))
+    vn = oracle.f64_to_bf16(rng.standard_normal((b, T, g, d_h)))
+    k0 = oracle.f64_to_bf16(rng.standard_normal((b, g, n_max, d_h)))
+    v0 = oracle.f64_to_bf16(rng.standard_normal((b, g, n_max, d_h)))
+    pos = np.array([6, 0], dtype=np.int32)
+    k1, v1 = k0.copy(), v0.copy()
+    assert oracle.kv_append_multi(kn, vn, k1, v1, pos) == oracle.OK
+    k2, v2 = k0.copy(), v0.copy()
+    for t in range(T):
+        assert oracle.kv_append(np.ascontiguousarray(kn[:, t]), np.ascontiguousarray(vn[:, t]),
+                                k2, v2, pos + t) == oracle.OK
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    # rows past the cache: that sequence is skipped, nothing written
+    k3, v3 = k0.copy(), v0.copy()
+    assert oracle.kv_append_multi(kn, vn, k3, v3, np.array([7, 0], np.int32)) == oracle.ERR_BOUNDS
+    assert np.array_equal(k3[0], k0[0]) and np.array_equal(k3[1], k2[1])
