@@ -236,6 +236,43 @@ MQA_API int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const 
                                 void* stream);
 
 /*
+ * Several new tokens per sequence: mqa_kv_append_multi, mqa_decode_attention_multi,
+ * mqa_decode_step_multi.
+ *
+ * The decode step for T tokens at once (draft tokens of speculative decoding, or a chunk of a
+ * prompt): "GQA与MQA深度实战" (ybb.press) §八's module takes T new tokens, writes their K/V rows at
+ * start .. start + T - 1 and attends over the first start + T rows; its checklist §十 item 10 keeps
+ * the causal mask per query position when K/V are shared. Reading: token t (0-based) of sequence bi
+ * sits at row L - T + t, where L = seq_lens[bi] counts all T new rows, and attends the first
+ * L - T + 1 + t rows; T = 1 is mqa_decode_attention. Every K/V byte is read once for all T tokens.
+ *
+ *   q, out           device, [b][T][h][d_h] bf16 (token-major), 16-byte aligned
+ *   k_new, v_new     device, [b][T][g][d_h] bf16, 16-byte aligned
+ *   pos              device, [b] int32: token t is written at row pos[bi] + t;
+ *                    0 <= pos[bi] and pos[bi] + T <= n_max, else that sequence is not written
+ *   seq_lens         device, [b] int32, T <= seq_lens[bi] <= n_max (normally pos[bi] + T), else
+ *                    zeros for that sequence
+ *   T                tokens per sequence, >= 1, with T * (h / g) <= 64
+ *   everything else  as for mqa_kv_append / mqa_decode_attention / mqa_decode_step
+ *
+ * The attention runs on the mma.sync tensor-core path whatever the group size (a forced CUDA-core
+ * or tcgen05 path returns MQA_ERR_UNSUPPORTED when T > 1); both latched errors are
+ * MQA_ERR_DEVICE_BOUNDS. The workspace is that of mqa_decode_attention.
+ */
+MQA_API int mqa_kv_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
+                                mqa_bf16* v_cache, const int32_t* pos, int b, int T, int g,
+                                int d_h, int n_max, void* stream);
+MQA_API int mqa_decode_attention_multi(const mqa_bf16* q, const mqa_bf16* k_cache,
+                                       const mqa_bf16* v_cache, const int32_t* seq_lens,
+                                       mqa_bf16* out, int b, int T, int h, int g, int d_h,
+                                       int n_max, float scale, void* stream);
+MQA_API int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new,
+                                  const mqa_bf16* v_new, mqa_bf16* k_cache, mqa_bf16* v_cache,
+                                  const int32_t* pos, const int32_t* seq_lens, mqa_bf16* out,
+                                  int b, int T, int h, int g, int d_h, int n_max, float scale,
+                                  void* stream);
+
+/*
  * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
  * memory. The source pages have no counterpart to this call; it exists for users of the library.
  *

@@ -50,6 +50,14 @@ _lib.mqa_decode_attention_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _
 _lib.mqa_decode_step_fp8.restype = _i32
 _lib.mqa_decode_step_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                      _i32, _i32, _f32, _f32, _f32, _vp]
+_lib.mqa_kv_append_multi.restype = _i32
+_lib.mqa_kv_append_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp]
+_lib.mqa_decode_attention_multi.restype = _i32
+_lib.mqa_decode_attention_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                            _i32, _f32, _vp]
+_lib.mqa_decode_step_multi.restype = _i32
+_lib.mqa_decode_step_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                       _i32, _i32, _i32, _f32, _vp]
 _lib.mqa_status_string.restype = ctypes.c_char_p
 _lib.mqa_status_string.argtypes = [_i32]
 _lib.mqa_get_device_status.restype = _i32
@@ -422,4 +430,87 @@ def decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                   _vp(_stream_handle(stream)))
     if st:
         raise MqaError(st, "mqa_decode_step_fp8")
+    return out
+
+
+def kv_append_multi(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                    v_cache: torch.Tensor, pos: torch.Tensor, stream=None) -> None:
+    """Append T rows per sequence: ``k_new`` [b, T, g, d_h]; token t goes to row ``pos[b] + t``."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 4)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    b, g, n_max, d_h = k_cache.shape
+    T = k_new.shape[1]
+    if v_cache.shape != k_cache.shape or k_new.shape != (b, T, g, d_h) \
+            or v_new.shape != (b, T, g, d_h) or pos.shape != (b,):
+        raise ValueError("kv_append_multi: inconsistent shapes")
+    st = _lib.mqa_kv_append_multi(k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                                  v_cache.data_ptr(), pos.data_ptr(), b, T, g, d_h, n_max,
+                                  _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append_multi")
+
+
+def decode_attention_multi(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           seq_lens: torch.Tensor, out: torch.Tensor | None = None,
+                           scale: float | None = None, stream=None) -> torch.Tensor:
+    """Causal attention of T tokens per sequence: ``q`` [b, T, h, d_h]; token t attends the first
+    ``seq_lens[b] - T + 1 + t`` cache rows. Returns [b, T, h, d_h]."""
+    _check(q, "q", torch.bfloat16, 4)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, T, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,):
+        raise ValueError("decode_attention_multi: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 4)
+        if out.shape != q.shape:
+            raise ValueError("decode_attention_multi: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention_multi(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         seq_lens.data_ptr(), out.data_ptr(), b, T, h, g, d_h,
+                                         n_max, float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention_multi")
+    return out
+
+
+def decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, pos: torch.Tensor,
+                      seq_lens: torch.Tensor, out: torch.Tensor | None = None,
+                      scale: float | None = None, stream=None) -> torch.Tensor:
+    """One launch doing :func:`kv_append_multi` then :func:`decode_attention_multi`."""
+    _check(q, "q", torch.bfloat16, 4)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 4)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, T, h, d_h = q.shape
+    bk, g, n_max, dk = k_cache.shape
+    if bk != b or dk != d_h or v_cache.shape != k_cache.shape or seq_lens.shape != (b,) \
+            or pos.shape != (b,) or k_new.shape != (b, T, g, d_h) or v_new.shape != (b, T, g, d_h):
+        raise ValueError("decode_step_multi: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 4)
+        if out.shape != q.shape:
+            raise ValueError("decode_step_multi: out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step_multi(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                    k_cache.data_ptr(), v_cache.data_ptr(), pos.data_ptr(),
+                                    seq_lens.data_ptr(), out.data_ptr(), b, T, h, g, d_h, n_max,
+                                    float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step_multi")
     return out

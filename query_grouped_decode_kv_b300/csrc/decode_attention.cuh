@@ -50,7 +50,7 @@ constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 //    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Only one producer lane works.
 __host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 1); }
 constexpr int kLaunchRegsWide = 168;
-constexpr int kProducerRegs = 56;
+constexpr int kProducerRegs = 72;
 constexpr int kConsumerRegs = 216;
 static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= 384 * kLaunchRegsWide,
               "the register split must fit in what the launch allocated");
@@ -61,22 +61,26 @@ constexpr int kMaxGroup = 64;       // largest G = h / g served
 constexpr float kLazyLog2 = 8.f;    // softmax reference slack (log2 units), see MmaConsumer::tile
 
 struct DecodeParams {
-  const __nv_bfloat16* q;     // [b][h][D]
+  const __nv_bfloat16* q;     // [b][T][h][D]
   const int32_t* seq_lens;    // [b]
-  __nv_bfloat16* out;         // [b][h][D]
+  __nv_bfloat16* out;         // [b][T][h][D]
   float* part_o;              // [slots][G][D]   un-normalised partial outputs
   float2* part_ml;            // [slots][G]      (running max in log2 units, running sum)
   unsigned int* seg_arrivals; // [b*g] CTAs that have stored a partial; zero between calls
+  // A segment (sequence bi, KV head j) has G = T * Gh rows: the Gh query heads of the group for
+  // each of the T new tokens, row r = t * Gh + hh. Token t attends the first L - T + 1 + t rows of
+  // the cache (causal); with T = 1 a row is a head and every row attends all L rows.
   int b, h, g, G, n_max;
+  int T, Gh;
   int num_ctas;               // P
   float scale_log2;           // scale * log2(e)
   unsigned long long timeout_ns;  // limit of every in-kernel wait
   unsigned long long drain_ns;    // limit of the waits for a CTA's own work in flight at exit
   int debug_stall;                // testing: consumers first wait on a barrier nothing completes
-  // Fused append (mqa_decode_step): this step's K/V rows, written at row pos[bi] of the caches
-  // before any tile holding that row is loaded. All null when the call only attends.
+  // Fused append (mqa_decode_step): this step's K/V rows, token t written at row pos[bi] + t of
+  // the caches before any tile holding that row is loaded. All null when the call only attends.
   const int32_t* pos;         // [b]
-  const uint4* k_new;         // [b][g][D/8] 16-byte chunks
+  const uint4* k_new;         // [b][T][g][D/8] 16-byte chunks
   const uint4* v_new;
   uint4* k_rows;              // the caches as 16-byte chunks, [b][g][n_max][D/8]
   uint4* v_rows;
@@ -121,8 +125,22 @@ __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
   return 1024 + static_cast<size_t>(smem_fixed_bytes<D, EB>(NW, CR));
 }
 
-__device__ __forceinline__ int tiles_of_length(int L, int n_max) {
-  return (L >= 1 && L <= n_max) ? (L + kTileKeys - 1) / kTileKeys : 0;
+// Element offset of row r (= t * Gh + hh) of segment (bi, j) in q or out ([b][T][h][D]).
+__device__ __forceinline__ size_t row_offset(const DecodeParams& P, int bi, int j, int r, int D) {
+  const int t = r / P.Gh, hh = r - t * P.Gh;
+  return ((static_cast<size_t>(bi) * P.T + t) * P.h + static_cast<size_t>(j) * P.Gh + hh) * D;
+}
+
+// Rows of the cache that row r of a segment does not see, relative to the sequence's last
+// token: T - 1 - t (0 with one token); padding rows (r >= G) see nothing.
+__device__ __forceinline__ int row_lag(const DecodeParams& P, int r) {
+  return r < P.G ? P.T - 1 - r / P.Gh : 0x7FFF;  // 0x7FFF > any tile: every key masked
+}
+
+// Tiles of a sequence of length L (0 when L is out of range: below the T new tokens, or past
+// n_max).
+__device__ __forceinline__ int tiles_of_length(int L, int n_max, int T) {
+  return (L >= T && L >= 1 && L <= n_max) ? (L + kTileKeys - 1) / kTileKeys : 0;
 }
 
 // Byte offset of (key row, byte column c) inside one K or V stage: the row is split into halves
@@ -146,8 +164,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int key, int d) {
 // generic-to-async proxy fence), so attention sees the new row. Every other valid row is written
 // by append_uncovered_rows, spread over all CTAs; no tile of this launch reads it.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ bool row_is_loaded(int p, int L, int n_max) {
-  return static_cast<long long>(p) < static_cast<long long>(tiles_of_length(L, n_max)) * kTileKeys;
+__device__ __forceinline__ bool row_is_loaded(int p, int L, int n_max, int T) {
+  return static_cast<long long>(p) <
+         static_cast<long long>(tiles_of_length(L, n_max, T)) * kTileKeys;
 }
 
 // First 16-byte chunk of cache row p of segment (bi, j) in the caches seen as chunks, or -1 when
@@ -191,38 +210,42 @@ template <int D, int EB>
 __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int nthreads) {
   constexpr int CH = D * EB / 16;  // 16-byte chunks per cache row
   constexpr int CS = D / 8;        // 16-byte chunks per source row (bf16)
-  const long long total = static_cast<long long>(P.b) * P.g * CH;
+  const int T = P.T;
+  const long long total = static_cast<long long>(P.b) * T * P.g * CH;
   const long long stride = static_cast<long long>(P.num_ctas) * nthreads;
   for (long long idx = static_cast<long long>(blockIdx.x) * nthreads + threadIdx.x; idx < total;
        idx += stride) {
-    const long long row = idx / CH;  // = bi * g + j
-    const int c = static_cast<int>(idx - row * CH);
-    const int bi = static_cast<int>(row / P.g);
-    const int p = __ldg(P.pos + bi);
-    if (p < 0 || p >= P.n_max) {
-      if (c == 0 && row == static_cast<long long>(bi) * P.g) latch_status(kStatusDeviceBounds);
+    const long long src_row = idx / CH;  // = (bi * T + t) * g + j, the row of k_new / v_new
+    const int c = static_cast<int>(idx - src_row * CH);
+    const long long bt = src_row / P.g;
+    const int j = static_cast<int>(src_row - bt * P.g);
+    const int bi = static_cast<int>(bt / T);
+    const int t = static_cast<int>(bt - static_cast<long long>(bi) * T);
+    const int p0 = __ldg(P.pos + bi);
+    if (p0 < 0 || static_cast<long long>(p0) + T > P.n_max) {
+      if (c == 0 && t == 0 && j == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
-    if (row_is_loaded(p, __ldg(P.seq_lens + bi), P.n_max)) continue;
-    const long long dst = row_chunk(P, bi, static_cast<int>(row - static_cast<long long>(bi) * P.g),
-                                    p, CH);
+    const int p = p0 + t;
+    if (row_is_loaded(p, __ldg(P.seq_lens + bi), P.n_max, T)) continue;
+    const long long dst = row_chunk(P, bi, j, p, CH);
     if (dst < 0) {
       if (c == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
-    P.k_rows[dst + c] = new_row_chunk<EB>(P.k_new + row * CS, c, P.kq_scale);
-    P.v_rows[dst + c] = new_row_chunk<EB>(P.v_new + row * CS, c, P.vq_scale);
+    P.k_rows[dst + c] = new_row_chunk<EB>(P.k_new + src_row * CS, c, P.kq_scale);
+    P.v_rows[dst + c] = new_row_chunk<EB>(P.v_new + src_row * CS, c, P.vq_scale);
   }
 }
 
-// One warp writes the K and V row of segment (bi, j) at cache row `p` (lane = 16-byte chunk of
-// the cache row).
+// One warp writes the K and V row of token t of segment (bi, j) at cache row `p` (lane = 16-byte
+// chunk of the cache row).
 template <int D, int EB>
-__device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int j, int p,
+__device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int j, int t, int p,
                                               int lane) {
   constexpr int CH = D * EB / 16;
   constexpr int CS = D / 8;
-  const long long src = (static_cast<long long>(bi) * P.g + j) * CS;
+  const long long src = ((static_cast<long long>(bi) * P.T + t) * P.g + j) * CS;
   const long long dst = row_chunk(P, bi, j, p, CH);
   if (dst < 0) {
     if (lane == 0) latch_status(kStatusDeviceBounds);
@@ -233,6 +256,16 @@ __device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int
     P.v_rows[dst + lane - CH] = new_row_chunk<EB>(P.v_new + src, lane - CH, P.vq_scale);
 }
 
+// The new rows of segment (bi, j) that tile `tile` holds ([p0, p0 + T) meets the tile's rows),
+// written by the whole warp before the tile's copy; the caller fences and syncs the warp.
+template <int D, int EB>
+__device__ __forceinline__ bool write_tile_rows(const DecodeParams& P, int bi, int j, int tile,
+                                                int p0, int lane) {
+  const int lo = max(p0, tile * kTileKeys), hi = min(p0 + P.T, (tile + 1) * kTileKeys);
+  for (int p = lo; p < hi; ++p) write_new_row<D, EB>(P, bi, j, p - p0, p, lane);
+  return lo < hi;
+}
+
 // The tile count of every sequence as the CTAs see it: the exclusive prefix `cs` of the tile sums
 // of nchunks chunks of `chunk` consecutive sequences (computed by each CTA in shared memory), and
 // the lengths themselves for the tiles of one sequence.
@@ -240,9 +273,9 @@ struct TileIndex {
   const uint32_t* cs;   // [nchunks + 1]; cs[nchunks] = tiles of all sequences (per KV head)
   int chunk, nchunks;
   const int32_t* seq_lens;
-  int B, g, n_max;
+  int B, g, n_max, T;
   __device__ __forceinline__ int tiles(int bi) const {
-    return tiles_of_length(__ldg(seq_lens + bi), n_max);
+    return tiles_of_length(__ldg(seq_lens + bi), n_max, T);
   }
   // W: tiles of all segments
   __device__ __forceinline__ unsigned long long total() const {
@@ -373,12 +406,13 @@ __device__ __forceinline__ void combine_and_store(const DecodeParams& P, const S
     float acc = 0.f, den = 0.f;
     for (int c = 0; c < n; ++c) {
       const float2 ml = sh.comb_ml[ws[c] * CR + rs[c]];
-      const float wgt = fast_exp2(ml.x - M);
+      // a row that saw no key in this piece (an earlier token, T > 1) adds nothing
+      const float wgt = (M == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
       den += wgt * ml.y;
       acc += wgt * sh.comb_o[(ws[c] * CR + rs[c]) * comb_row_floats(D) + d];
     }
     if (complete) {
-      const size_t o = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G + hr) * D + d;
+      const size_t o = row_offset(P, bi, j, hr, D) + d;
       P.out[o] = __float2bfloat16_rn(acc / den * P.out_scale);
     } else {
       const size_t r = static_cast<size_t>(slot) * G + hr;
@@ -430,7 +464,6 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
                                                     const SegmentPieces& pc) {
   const int G = P.G;
   const int tid = threadIdx.x;
-  const size_t out0 = (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * G) * D;
   const int np = pc.c_last - pc.c_first + 1;
   constexpr int kScratchFloats = NW * CR * comb_row_floats(D);
   if (!pc.all_own || 3 * np * G > kScratchFloats) {
@@ -450,7 +483,7 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
         den += w * ml.y;
         acc += w * __ldcg(P.part_o + r * D + d);
       }
-      P.out[out0 + idx] = __float2bfloat16_rn(acc / den * P.out_scale);
+      P.out[row_offset(P, bi, j, hr, D) + d] = __float2bfloat16_rn(acc / den * P.out_scale);
     }
     return true;
   }
@@ -480,7 +513,8 @@ __device__ __forceinline__ bool merge_split_segment(const DecodeParams& P, const
       const float4 o = __ldcg(po + (slot0 + pi) * G * (D / 4) + idx);
       acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
     }
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(P.out + out0) + 2 * idx;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
+        P.out + row_offset(P, bi, j, hr, D) + (idx - hr * (D / 4)) * 4);
     const float os = P.out_scale;
     dst[0] = __floats2bfloat162_rn(acc.x * os, acc.y * os);
     dst[1] = __floats2bfloat162_rn(acc.z * os, acc.w * os);
@@ -537,7 +571,7 @@ __device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, SharedL
   const int chunk = (B + kThreads - 1) / kThreads;
   const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
   uint32_t s = 0;
-  for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max);
+  for (int i = lo; i < hi; ++i) s += tiles_of_length(__ldg(P.seq_lens + i), P.n_max, P.T);
   cs[tid] = s;
   __syncthreads();
   if (warp == 0) {
@@ -567,6 +601,7 @@ __device__ __forceinline__ void build_tile_prefix(const DecodeParams& P, SharedL
   sh.tix.B = B;
   sh.tix.g = P.g;
   sh.tix.n_max = P.n_max;
+  sh.tix.T = P.T;
 }
 
 // Sequences whose length is out of range get a zero output and latch MQA_ERR_DEVICE_BOUNDS.
@@ -574,10 +609,10 @@ template <int D>
 __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, int nthreads) {
   for (int bi = blockIdx.x; bi < P.b; bi += P.num_ctas) {
     const int L = __ldg(P.seq_lens + bi);
-    if (L >= 1 && L <= P.n_max) continue;
+    if (L >= P.T && L <= P.n_max) continue;
     if (threadIdx.x == 0) latch_status(kStatusDeviceBounds);
-    __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.h * D;
-    for (int e = threadIdx.x; e < P.h * D; e += nthreads) ob[e] = __float2bfloat16_rn(0.f);
+    __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.T * P.h * D;
+    for (int e = threadIdx.x; e < P.T * P.h * D; e += nthreads) ob[e] = __float2bfloat16_rn(0.f);
   }
 }
 
@@ -604,7 +639,7 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
   TileCursor cur;
   cur.start(x0, sh.tix);
   int issued = 0;
-  int row_bi = -1, row_p = -1;  // the append row of sequence row_bi (-1: none to write)
+  int row_bi = -1, row_p = -1;  // the first append row of sequence row_bi (-1: none to write)
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
     const uint32_t par = ((k / kStages) & 1) ^ 1;
@@ -619,10 +654,9 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
       if (cur.bi != row_bi) {
         row_bi = cur.bi;
         const int p = __ldg(P.pos + cur.bi);
-        row_p = (p >= 0 && p < P.n_max) ? p : -1;
+        row_p = (p >= 0 && static_cast<long long>(p) + P.T <= P.n_max) ? p : -1;
       }
-      if (row_p >= 0 && row_p / kTileKeys == cur.tile) {
-        write_new_row<D, EB>(P, cur.bi, cur.j, row_p, lane);
+      if (row_p >= 0 && write_tile_rows<D, EB>(P, cur.bi, cur.j, cur.tile, row_p, lane)) {
         fence_proxy_async_global();  // each writer orders its store before the async proxy...
         __syncwarp();                // ...and the copy is issued after every writer
       }
@@ -768,7 +802,7 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       L = __ldg(P.seq_lens + seq);
       if (fused) {
         const int p = __ldg(P.pos + seq);
-        row_p = (p >= 0 && p < P.n_max) ? p : -1;
+        row_p = (p >= 0 && static_cast<long long>(p) + P.T <= P.n_max) ? p : -1;
       }
     }
     const int y = cur.tile * kTileKeys;
@@ -781,8 +815,7 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       if (lane == 0 && !*sh.abort) give_up(sh, kSiteProducerEmpty, k);
       break;
     }
-    if (fused && row_p >= 0 && row_p / kTileKeys == cur.tile) {
-      write_new_row<D, EB>(P, cur.bi, cur.j, row_p, lane);
+    if (fused && row_p >= 0 && write_tile_rows<D, EB>(P, cur.bi, cur.j, cur.tile, row_p, lane)) {
       fence_proxy_async_global();
       __syncwarp();
     }
@@ -861,14 +894,16 @@ struct MmaConsumer {
   float o[NT_O][4];
   float ol[4];  // P 1: the running sums of the rounded weights, rescaled with O (all columns equal)
   float m[2];
+  int lags;  // keys of a tile that rows r0 (low 16 bits) and r1 (high) do not see, relative to
+             // the last token
 
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
                                                 int lane) {
     const int r0 = mi * 16 + (lane >> 2), r1 = r0 + 8;
-    const __nv_bfloat16* qb = P.q + (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * P.G) * D;
-    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + static_cast<size_t>(r0) * D);
-    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + static_cast<size_t>(r1) * D);
     const bool v0 = r0 < P.G, v1 = r1 < P.G;
+    const uint32_t* q0 = reinterpret_cast<const uint32_t*>(P.q + (v0 ? row_offset(P, bi, j, r0, D) : 0));
+    const uint32_t* q1 = reinterpret_cast<const uint32_t*>(P.q + (v1 ? row_offset(P, bi, j, r1, D) : 0));
+    lags = row_lag(P, r0) | (row_lag(P, r1) << 16);
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ++ks) {
       const int c = (ks * 16 + (lane & 3) * 2) >> 1;  // in bf16 pairs
@@ -883,10 +918,13 @@ struct MmaConsumer {
     m[0] = m[1] = -INFINITY;
   }
 
-  // One tile. `valid` = number of the tile's rows that lie below the sequence length.
+  // One tile. `valid` = rows of the sequence from this tile's first row on (at least 1; may
+  // exceed the tile): key k of the tile is below the length when k < valid.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
                                        int valid, float scale_log2) {
-    // S = Q K^T, even and odd k-steps into separate accumulators (half the dependent chain)
+    // S = Q K^T; with four warps (one per SM sub-partition) even and odd k-steps go into separate
+    // accumulators (half the dependent chain), with eight the registers matter more
+    constexpr bool kSplit = NW == 4;
     float s[NT_S][4], s2[NT_S][4];
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
@@ -902,8 +940,8 @@ struct MmaConsumer {
         const int d = ks * 16 + ((mat & 1) ? 8 : 0);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(swz(kbase, key, d), b0, b1, b2, b3);
-        float (&acc0)[4] = (ks & 1) ? s2[2 * np] : s[2 * np];
-        float (&acc1)[4] = (ks & 1) ? s2[2 * np + 1] : s[2 * np + 1];
+        float (&acc0)[4] = (kSplit && (ks & 1)) ? s2[2 * np] : s[2 * np];
+        float (&acc1)[4] = (kSplit && (ks & 1)) ? s2[2 * np + 1] : s[2 * np + 1];
         mma_16816(acc0, qa[ks], b0, b1);
         mma_16816(acc1, qa[ks], b2, b3);
       }
@@ -912,17 +950,18 @@ struct MmaConsumer {
     for (int n = 0; n < NT_S; ++n) {
       s[n][0] += s2[n][0]; s[n][1] += s2[n][1]; s[n][2] += s2[n][2]; s[n][3] += s2[n][3];
     }
-    // scale (log2 domain), mask rows at or beyond the length, running max per head row
+    // scale (log2 domain), mask keys a row does not see (at or past the length, or after the
+    // row's token), running max per head row
     const int c2 = (lane & 3) * 2;
+    const int va0 = valid - (lags & 0xFFFF), va1 = valid - (lags >> 16);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
       const int key = grp * KPW + n * 8 + c2;
-      const bool ok0 = key < valid, ok1 = key + 1 < valid;
-      s[n][0] = ok0 ? s[n][0] * scale_log2 : -INFINITY;
-      s[n][1] = ok1 ? s[n][1] * scale_log2 : -INFINITY;
-      s[n][2] = ok0 ? s[n][2] * scale_log2 : -INFINITY;
-      s[n][3] = ok1 ? s[n][3] * scale_log2 : -INFINITY;
+      s[n][0] = key < va0 ? s[n][0] * scale_log2 : -INFINITY;
+      s[n][1] = key + 1 < va0 ? s[n][1] * scale_log2 : -INFINITY;
+      s[n][2] = key < va1 ? s[n][2] * scale_log2 : -INFINITY;
+      s[n][3] = key + 1 < va1 ? s[n][3] * scale_log2 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
       mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
     }
@@ -1046,14 +1085,16 @@ struct MmaConsumerF8 {
   float o[NT_O][4];
   float ol[4];  // P 1: the running sums of the rounded weights, rescaled with O (all columns equal)
   float m[2];
+  int lags;  // keys of a tile that rows r0 (low 16 bits) and r1 (high) do not see, relative to
+             // the last token
 
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
                                                 int lane) {
     const int r0 = mi * 16 + (lane >> 2), r1 = r0 + 8;
-    const __nv_bfloat16* qb = P.q + (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * P.G) * D;
     const bool v0 = r0 < P.G, v1 = r1 < P.G;
-    const uint2* q0 = reinterpret_cast<const uint2*>(qb + static_cast<size_t>(r0) * D);
-    const uint2* q1 = reinterpret_cast<const uint2*>(qb + static_cast<size_t>(r1) * D);
+    const uint2* q0 = reinterpret_cast<const uint2*>(P.q + (v0 ? row_offset(P, bi, j, r0, D) : 0));
+    const uint2* q1 = reinterpret_cast<const uint2*>(P.q + (v1 ? row_offset(P, bi, j, r1, D) : 0));
+    lags = row_lag(P, r0) | (row_lag(P, r1) << 16);
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ++ks) {
       // columns 16 ks + 4c .. + 3 of rows r0 and r1 (one 8-byte load each)
@@ -1075,7 +1116,8 @@ struct MmaConsumerF8 {
     m[0] = m[1] = -INFINITY;
   }
 
-  // One tile. `valid` = number of the tile's rows that lie below the sequence length.
+  // One tile. `valid` = rows of the sequence from this tile's first row on (at least 1; may
+  // exceed the tile): key k of the tile is below the length when k < valid.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
                                        int valid, float scale_log2) {
     // S = Q K^T, block ks into s and block ks + 1 into s2 (half the dependent chain)
@@ -1111,15 +1153,15 @@ struct MmaConsumerF8 {
     }
     // scale (log2 domain), mask rows at or beyond the length, running max per head row
     const int c2 = (lane & 3) * 2;
+    const int va0 = valid - (lags & 0xFFFF), va1 = valid - (lags >> 16);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
       const int key = grp * KPW + n * 8 + c2;
-      const bool ok0 = key < valid, ok1 = key + 1 < valid;
-      s[n][0] = ok0 ? s[n][0] * scale_log2 : -INFINITY;
-      s[n][1] = ok1 ? s[n][1] * scale_log2 : -INFINITY;
-      s[n][2] = ok0 ? s[n][2] * scale_log2 : -INFINITY;
-      s[n][3] = ok1 ? s[n][3] * scale_log2 : -INFINITY;
+      s[n][0] = key < va0 ? s[n][0] * scale_log2 : -INFINITY;
+      s[n][1] = key + 1 < va0 ? s[n][1] * scale_log2 : -INFINITY;
+      s[n][2] = key < va1 ? s[n][2] * scale_log2 : -INFINITY;
+      s[n][3] = key + 1 < va1 ? s[n][3] * scale_log2 : -INFINITY;
       mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
       mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
     }
@@ -1494,7 +1536,9 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      cons.tile(kbase, vbase, grp, lane, valid, P.scale_log2);
+      // the consumer masks by the rows left from this tile's start (not capped at the tile), so
+      // that a row's causal lag applies at the sequence's end only
+      cons.tile(kbase, vbase, grp, lane, L - tile_start, P.scale_log2);
     } else {
       const int nvalid = max(0, min(valid - warp * kGroupKeys, kGroupKeys));
       cons.tile(kbase, vbase, warp, lane, nvalid, P.scale_log2);

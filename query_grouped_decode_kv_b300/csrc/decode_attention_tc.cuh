@@ -537,7 +537,7 @@ __device__ __forceinline__ void tc_produce_tiles(const CUtensorMap* tm_k, const 
           row_p = (p >= 0 && p < P.n_max) ? p : -1;
         }
         if (row_p >= 0 && row_p / kTileKeys == ck.tile) {
-          write_new_row<D, 2>(P, ck.bi, ck.j, row_p, lane);
+          write_new_row<D, 2>(P, ck.bi, ck.j, 0, row_p, lane);
           fence_proxy_async_global();  // each writer orders its stores before the async proxy...
           __syncwarp();                // ...and lane 0 copies the tile after every writer
         }

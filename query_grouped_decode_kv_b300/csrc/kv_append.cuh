@@ -12,27 +12,33 @@
 
 namespace mqa {
 
-// One thread moves one 16-byte chunk of one (sequence, KV head) row of K and the matching chunk
-// of V. Rows whose position is out of range are skipped and latch MQA_ERR_DEVICE_BOUNDS.
+// One thread moves one 16-byte chunk of one (sequence, token, KV head) row of K and the matching
+// chunk of V: token t of sequence bi goes to row pos[bi] + t. A sequence whose rows
+// pos .. pos + T - 1 are not all in range is skipped and latches MQA_ERR_DEVICE_BOUNDS.
 __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict__ k_new,
                                                         const uint4* __restrict__ v_new,
                                                         uint4* __restrict__ k_cache,
                                                         uint4* __restrict__ v_cache,
                                                         const int32_t* __restrict__ pos, int b,
-                                                        int g, int chunks_per_row, int n_max) {
-  const long long total = static_cast<long long>(b) * g * chunks_per_row;
+                                                        int T, int g, int chunks_per_row,
+                                                        int n_max) {
+  const long long total = static_cast<long long>(b) * T * g * chunks_per_row;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += stride) {
-    const long long row = idx / chunks_per_row;  // = bi * g + j
-    const int c = static_cast<int>(idx - row * chunks_per_row);
-    const int bi = static_cast<int>(row / g);
+    const long long src_row = idx / chunks_per_row;  // = (bi * T + t) * g + j
+    const int c = static_cast<int>(idx - src_row * chunks_per_row);
+    const long long bt = src_row / g;
+    const int j = static_cast<int>(src_row - bt * g);
+    const int bi = static_cast<int>(bt / T);
+    const int t = static_cast<int>(bt - static_cast<long long>(bi) * T);
     const int p = __ldg(pos + bi);
-    if (p < 0 || p >= n_max) {
-      if (c == 0 && row == static_cast<long long>(bi) * g) latch_status(kStatusDeviceBounds);
+    if (p < 0 || static_cast<long long>(p) + T > n_max) {
+      if (c == 0 && t == 0 && j == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
-    const long long dst = (row * n_max + p) * chunks_per_row + c;
+    const long long dst =
+        ((static_cast<long long>(bi) * g + j) * n_max + p + t) * chunks_per_row + c;
     k_cache[dst] = __ldg(k_new + idx);
     v_cache[dst] = __ldg(v_new + idx);
   }

@@ -332,6 +332,7 @@ struct DecodePlan {
   const int32_t* pos = nullptr;
   PagedCache paged;  // table null: contiguous caches
   int eb = 2;        // cache bytes per element: 2 bf16, 1 fp8 E4M3 codes
+  int T = 1, Gh = 0; // new tokens per sequence; query heads per KV head (G = T * Gh rows)
   float k_scale = 1.f, v_scale = 1.f;  // fp8 caches: value = code * scale
   int b, h, g, d_h, n_max, G;
   float scale;
@@ -346,7 +347,7 @@ struct DecodePlan {
 
 int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_cache,
                 const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g, int d_h, int n_max,
-                float scale, void* stream, DecodePlan* plan) {
+                float scale, void* stream, DecodePlan* plan, int T = 1) {
   // ---- host checks (no CUDA call before this block is done) ----
   if (!q || !k_cache || !v_cache || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
   if (b <= 0 || h <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
@@ -355,9 +356,13 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return MQA_ERR_INVALID_ARG;
+  if (T <= 0) return MQA_ERR_INVALID_ARG;
   if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
-  const int G = h / g;
-  if (G > mqa::kMaxGroup || b > mqa::kMaxBatch) return MQA_ERR_UNSUPPORTED;
+  const int Gh = h / g;
+  // rows of a segment: the group's heads for each of the T tokens
+  if (static_cast<long long>(T) * Gh > mqa::kMaxGroup || b > mqa::kMaxBatch)
+    return MQA_ERR_UNSUPPORTED;
+  const int G = T * Gh;
   const long long bg = static_cast<long long>(b) * g;
   const long long tiles_per_seg =
       (static_cast<long long>(n_max) + mqa::kTileKeys - 1) / mqa::kTileKeys;
@@ -365,8 +370,11 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
       static_cast<double>(bg) * n_max * d_h > 9.0e18)
     return MQA_ERR_UNSUPPORTED;
   const int force_path = g_force_path.load();
-  const Path path = force_path == kPathAuto ? auto_path(G) : static_cast<Path>(force_path);
+  // several tokens: only the mma.sync consumer masks rows by token
+  const Path path = force_path == kPathAuto ? (T > 1 ? kPathMmaSync : auto_path(G))
+                                            : static_cast<Path>(force_path);
   if (path == kPathCudaCores && G > 7) return MQA_ERR_UNSUPPORTED;
+  if (T > 1 && path != kPathMmaSync) return MQA_ERR_UNSUPPORTED;
 
   // ---- device facts ----
   int dev = 0;
@@ -386,6 +394,7 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   DecodePlan& p = *plan;
   p.q = q; p.k_cache = k_cache; p.v_cache = v_cache; p.seq_lens = seq_lens; p.out = out;
   p.b = b; p.h = h; p.g = g; p.d_h = d_h; p.n_max = n_max; p.G = G;
+  p.T = T; p.Gh = Gh;
   p.scale = scale;
   p.path = path;
   p.stream = static_cast<cudaStream_t>(stream);
@@ -429,6 +438,8 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.h = p.h;
   P.g = p.g;
   P.G = p.G;
+  P.T = p.T;
+  P.Gh = p.Gh;
   P.n_max = p.n_max;
   P.num_ctas = static_cast<int>(p.ctas);
   // fp8: the logits are scale * k_scale * (q . codes); the output is v_scale * (P codes) / l
@@ -583,7 +594,7 @@ int mqa_kv_append(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cach
   const int blocks = static_cast<int>(want < 65535 ? want : 65535);
   mqa::kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
       reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
-      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, g, chunks,
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, 1, g, chunks,
       n_max);
   g_launches.fetch_add(1);
   return launch_error();
@@ -802,6 +813,77 @@ int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16
   plan.eb = 1;
   plan.k_scale = k_scale;
   plan.v_scale = v_scale;
+  plan.k_new = k_new;
+  plan.v_new = v_new;
+  plan.pos = pos;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_kv_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
+                        mqa_bf16* v_cache, const int32_t* pos, int b, int T, int g, int d_h,
+                        int n_max, void* stream) {
+  // ---- host checks (no CUDA call before this block is done) ----
+  if (!k_new || !v_new || !k_cache || !v_cache || !pos) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || T <= 0 || g <= 0 || d_h <= 0 || n_max <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(b) * T * g;
+  if (rows > (1ll << 31) || static_cast<double>(b) * g * n_max * d_h > 9.0e18)
+    return MQA_ERR_UNSUPPORTED;
+
+  const int chunks = d_h / 8;
+  const long long total = rows * chunks;
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  mqa::kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, T, g, chunks,
+      n_max);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+int mqa_decode_attention_multi(const mqa_bf16* q, const mqa_bf16* k_cache,
+                               const mqa_bf16* v_cache, const int32_t* seq_lens, mqa_bf16* out,
+                               int b, int T, int h, int g, int d_h, int n_max, float scale,
+                               void* stream) {
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan, T))
+    return st;
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  bool clear = false;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
+                               &partials, &counters, &clear))
+      return st;
+  }
+  return launch_decode(plan, partials, counters, clear);
+}
+
+int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                          mqa_bf16* k_cache, mqa_bf16* v_cache, const int32_t* pos,
+                          const int32_t* seq_lens, mqa_bf16* out, int b, int T, int h, int g,
+                          int d_h, int n_max, float scale, void* stream) {
+  if (!k_new || !v_new || !pos) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
+                           &plan, T))
+    return st;
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;

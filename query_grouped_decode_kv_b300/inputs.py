@@ -193,3 +193,13 @@ def amax_scale(x: torch.Tensor) -> float:
     a = a[torch.isfinite(a)].abs()
     m = float(a.max()) if a.numel() else 1.0
     return (m if m > 0 else 1.0) / 448.0
+
+
+def multi_step_inputs(w: Workload, T: int, layer: int = 0, device="cpu"):
+    """q [b, T, h, d_h] and new K/V rows [b, T, g, d_h] for T new tokens per sequence (token-
+    major, like the single-token tensors with a token axis after the batch)."""
+    seed = seed_for(w, layer, _Q) * 131 + T
+    q = normal_bf16((w.b, T, w.h, w.d_h), w.qkv_std, seed, device)
+    k_new = normal_bf16((w.b, T, w.g, w.d_h), w.qkv_std, seed + 1, device)
+    v_new = normal_bf16((w.b, T, w.g, w.d_h), w.qkv_std, seed + 2, device)
+    return q, k_new, v_new

@@ -48,6 +48,12 @@ def lib():
     L.mqa_decode_attention_fp8.argtypes = [vp] * 5 + [i32] * 5 + [ctypes.c_float] * 3 + [vp]
     L.mqa_decode_step_fp8.restype = i32
     L.mqa_decode_step_fp8.argtypes = [vp] * 8 + [i32] * 5 + [ctypes.c_float] * 3 + [vp]
+    L.mqa_kv_append_multi.restype = i32
+    L.mqa_kv_append_multi.argtypes = [vp] * 5 + [i32] * 5 + [vp]
+    L.mqa_decode_attention_multi.restype = i32
+    L.mqa_decode_attention_multi.argtypes = [vp] * 5 + [i32] * 6 + [ctypes.c_float, vp]
+    L.mqa_decode_step_multi.restype = i32
+    L.mqa_decode_step_multi.argtypes = [vp] * 8 + [i32] * 6 + [ctypes.c_float, vp]
     L.mqa_decode_step_paged.restype = i32
     L.mqa_decode_step_paged.argtypes = [vp] * 9 + [i32] * 7 + [ctypes.c_float, vp]
     return L
@@ -275,3 +281,58 @@ def test_fp8_step_host_checks(lib, kw, code):
 ])
 def test_fp8_append_host_checks(lib, kw, code):
     assert _append_fp8(lib, **kw) == code
+
+
+# ---- several tokens per sequence ----------------------------------------------------------------
+def _attn_multi(lib, q=A, k=A + 0x1000, v=A + 0x2000, lens=A + 0x3000, out=A + 0x4000, b=2, T=4,
+                h=8, g=2, d_h=128, n_max=100, scale=0.088):
+    return lib.mqa_decode_attention_multi(q, k, v, lens, out, b, T, h, g, d_h, n_max, scale, None)
+
+
+def _step_multi(lib, q=A, kn=A + 0x1000, vn=A + 0x2000, k=A + 0x3000, v=A + 0x4000,
+                pos=A + 0x5000, lens=A + 0x6000, out=A + 0x7000, b=2, T=4, h=8, g=2, d_h=128,
+                n_max=100, scale=0.088):
+    return lib.mqa_decode_step_multi(q, kn, vn, k, v, pos, lens, out, b, T, h, g, d_h, n_max,
+                                     scale, None)
+
+
+def _append_multi(lib, kn=A, vn=A + 0x1000, kc=A + 0x2000, vc=A + 0x3000, pos=A + 0x4000, b=2,
+                  T=4, g=2, d_h=128, n_max=100):
+    return lib.mqa_kv_append_multi(kn, vn, kc, vc, pos, b, T, g, d_h, n_max, None)
+
+
+MULTI_CASES = [
+    (dict(T=0), INVALID), (dict(T=-3), INVALID), (dict(q=0), INVALID), (dict(out=A + 4), INVALID),
+    (dict(h=8, g=3), INVALID), (dict(d_h=96), UNSUPPORTED),
+    (dict(T=17, h=8, g=2), UNSUPPORTED),           # 17 tokens x 4 heads = 68 rows > 64
+    (dict(T=2, h=64, g=1), UNSUPPORTED),           # 2 x 64 rows
+]
+
+
+@pytest.mark.parametrize("kw,code", MULTI_CASES)
+def test_multi_attention_host_checks(lib, kw, code):
+    assert _attn_multi(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", MULTI_CASES + [
+    (dict(kn=0), INVALID), (dict(pos=A + 0x5001), INVALID), (dict(vn=A + 0x2008), INVALID),
+])
+def test_multi_step_host_checks(lib, kw, code):
+    assert _step_multi(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), INVALID), (dict(kn=0), INVALID), (dict(pos=0), INVALID), (dict(b=0), INVALID),
+    (dict(kc=A + 0x2008), INVALID), (dict(d_h=80), UNSUPPORTED),
+])
+def test_multi_append_host_checks(lib, kw, code):
+    assert _append_multi(lib, **kw) == code
+
+
+def test_multi_rejects_forced_paths_other_than_mma_sync(lib):
+    for path in (1, 3):
+        assert lib.mqa_debug_override(0, path) == OK
+        try:
+            assert _attn_multi(lib, h=4, g=4) == UNSUPPORTED
+        finally:
+            lib.mqa_debug_override(0, 0)
