@@ -126,7 +126,10 @@ __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
 }
 
 // Element offset of row r (= t * Gh + hh) of segment (bi, j) in q or out ([b][T][h][D]).
+// (One token: row r is head j * Gh + r, no division; the combine and merge loops call this per
+// element.)
 __device__ __forceinline__ size_t row_offset(const DecodeParams& P, int bi, int j, int r, int D) {
+  if (P.T == 1) return (static_cast<size_t>(bi) * P.h + static_cast<size_t>(j) * P.Gh + r) * D;
   const int t = r / P.Gh, hh = r - t * P.Gh;
   return ((static_cast<size_t>(bi) * P.T + t) * P.h + static_cast<size_t>(j) * P.Gh + hh) * D;
 }
@@ -134,7 +137,8 @@ __device__ __forceinline__ size_t row_offset(const DecodeParams& P, int bi, int 
 // Rows of the cache that row r of a segment does not see, relative to the sequence's last
 // token: T - 1 - t (0 with one token); padding rows (r >= G) see nothing.
 __device__ __forceinline__ int row_lag(const DecodeParams& P, int r) {
-  return r < P.G ? P.T - 1 - r / P.Gh : 0x7FFF;  // 0x7FFF > any tile: every key masked
+  if (r >= P.G) return 0x7FFF;  // more than any tile: every key masked
+  return P.T == 1 ? 0 : P.T - 1 - r / P.Gh;
 }
 
 // Tiles of a sequence of length L (0 when L is out of range: below the T new tokens, or past
@@ -875,9 +879,11 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
 
 // ---------------------------------------------------------------------------------------------
 // Tensor-core consumer (G >= 8). WM warps (one per 16 heads) form a group; NW / WM groups split
-// each tile's keys.
+// each tile's keys. kTokens: rows are (token, head) pairs of several new tokens, each masked by
+// its own causal limit (instances used only when T > 1, so the single-token kernels carry no
+// per-row state).
 // ---------------------------------------------------------------------------------------------
-template <int D, int WM, int NW>
+template <int D, int WM, int NW, bool kTokens = false>
 struct MmaConsumer {
   static constexpr int kWarps = NW;
   static constexpr int kTileGroups = 1;
@@ -903,7 +909,7 @@ struct MmaConsumer {
     const bool v0 = r0 < P.G, v1 = r1 < P.G;
     const uint32_t* q0 = reinterpret_cast<const uint32_t*>(P.q + (v0 ? row_offset(P, bi, j, r0, D) : 0));
     const uint32_t* q1 = reinterpret_cast<const uint32_t*>(P.q + (v1 ? row_offset(P, bi, j, r1, D) : 0));
-    lags = row_lag(P, r0) | (row_lag(P, r1) << 16);
+    if constexpr (kTokens) lags = row_lag(P, r0) | (row_lag(P, r1) << 16);
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ++ks) {
       const int c = (ks * 16 + (lane & 3) * 2) >> 1;  // in bf16 pairs
@@ -922,9 +928,8 @@ struct MmaConsumer {
   // exceed the tile): key k of the tile is below the length when k < valid.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
                                        int valid, float scale_log2) {
-    // S = Q K^T; with four warps (one per SM sub-partition) even and odd k-steps go into separate
-    // accumulators (half the dependent chain), with eight the registers matter more
-    constexpr bool kSplit = NW == 4;
+    // S = Q K^T, even and odd k-steps into separate accumulators (half the dependent chain)
+    constexpr bool kSplit = true;
     float s[NT_S][4], s2[NT_S][4];
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
@@ -953,7 +958,8 @@ struct MmaConsumer {
     // scale (log2 domain), mask keys a row does not see (at or past the length, or after the
     // row's token), running max per head row
     const int c2 = (lane & 3) * 2;
-    const int va0 = valid - (lags & 0xFFFF), va1 = valid - (lags >> 16);
+    const int va0 = kTokens ? valid - (lags & 0xFFFF) : valid;
+    const int va1 = kTokens ? valid - (lags >> 16) : valid;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {
@@ -1085,8 +1091,6 @@ struct MmaConsumerF8 {
   float o[NT_O][4];
   float ol[4];  // P 1: the running sums of the rounded weights, rescaled with O (all columns equal)
   float m[2];
-  int lags;  // keys of a tile that rows r0 (low 16 bits) and r1 (high) do not see, relative to
-             // the last token
 
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
                                                 int lane) {
@@ -1094,7 +1098,6 @@ struct MmaConsumerF8 {
     const bool v0 = r0 < P.G, v1 = r1 < P.G;
     const uint2* q0 = reinterpret_cast<const uint2*>(P.q + (v0 ? row_offset(P, bi, j, r0, D) : 0));
     const uint2* q1 = reinterpret_cast<const uint2*>(P.q + (v1 ? row_offset(P, bi, j, r1, D) : 0));
-    lags = row_lag(P, r0) | (row_lag(P, r1) << 16);
 #pragma unroll
     for (int ks = 0; ks < KS_QK; ++ks) {
       // columns 16 ks + 4c .. + 3 of rows r0 and r1 (one 8-byte load each)
@@ -1153,7 +1156,7 @@ struct MmaConsumerF8 {
     }
     // scale (log2 domain), mask rows at or beyond the length, running max per head row
     const int c2 = (lane & 3) * 2;
-    const int va0 = valid - (lags & 0xFFFF), va1 = valid - (lags >> 16);
+    const int va0 = valid, va1 = valid;  // one token: every row sees the same keys
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int n = 0; n < NT_S; ++n) {

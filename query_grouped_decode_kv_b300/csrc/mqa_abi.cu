@@ -234,7 +234,7 @@ AttnKernelChoice choice(int b) {
 // mma.sync above 16 heads, where each warp's MMA chains and softmax would otherwise serialise.
 // Up to 16 heads mma.sync keeps four warps (16 keys per warp is its smallest P V k-step).
 template <int D>
-AttnKernelChoice pick_kernel(Path path, int G, int b) {
+AttnKernelChoice pick_kernel(Path path, int G, int b, int T) {
   using mqa::CcConsumer;
   using mqa::MmaConsumer;
   if (path == kPathTcgen05) {
@@ -246,6 +246,12 @@ AttnKernelChoice pick_kernel(Path path, int G, int b) {
     c.threads = mqa::kTcThreads;
     c.smem = mqa::tc_smem_bytes(D);
     return c;
+  }
+  if (path == kPathMmaSync && T > 1) {
+    // rows = T x heads, each masked by its token's causal limit
+    if (G <= 16) return choice<MmaConsumer<D, 1, 4, true>, D, 2, true, 1>(b);
+    if (G <= 32) return choice<MmaConsumer<D, 2, 8, true>, D, 2, true, 2>(b);
+    return choice<MmaConsumer<D, 4, 8, true>, D, 2, true, 4>(b);
   }
   if (path == kPathMmaSync) {
     if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, 2, true, 1>(b);
@@ -462,8 +468,8 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.num_pages = p.paged.num_pages;
 
   const AttnKernelChoice kc = p.eb == 1       ? pick_kernel_fp8(p.path, p.G, p.b)
-                              : p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b)
-                                             : pick_kernel<64>(p.path, p.G, p.b);
+                              : p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b, p.T)
+                                             : pick_kernel<64>(p.path, p.G, p.b, p.T);
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;
   if (p.paged.table && p.path == kPathTcgen05) return MQA_ERR_UNSUPPORTED;
   if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
