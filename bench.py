@@ -6,7 +6,7 @@ step appends one token's K/V and runs attention in all 80 layers back to back, o
 (mqa_decode_step) per layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--paged PAGE_SIZE] [--kv bf16|fp8]
+                    [--workload NAME] [--paged PAGE_SIZE] [--kv bf16|fp8] [--tokens T]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
 with inputs resident in HBM (lower is better), from CUDA-graph replays of the whole step (every
@@ -26,6 +26,11 @@ arm (``--impl reference``) times that oracle as the reference.
 ``--kv fp8`` runs the same workload with every layer's caches held as fp8 E4M3 codes of the same
 draws, one scale per tensor (the largest magnitude maps to 448), through ``mqa_decode_step_fp8``;
 the algorithmic bytes count one byte per cached element.
+
+``--tokens T`` runs every step with T new tokens per sequence (causal; speculative decoding):
+each sequence appends T rows and attends with T query rows per head, through
+``mqa_decode_step_multi``; the caches get T - 1 more rows, and every K/V byte is still read once
+per step.
 
 ``--paged PAGE_SIZE`` runs the same workload with every layer's cache held in page pools (the rows
 each sequence attends, laid out in pages of PAGE_SIZE rows in a seeded random order, one page table
@@ -171,26 +176,29 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
-def kv_bytes(w, lens, eb: int = 2) -> int:
-    """Algorithmic bytes of one fused decode-step launch (one layer): K and V rows read
-    (2 * g * L_b * d_h * eb over the batch; eb = 2 bf16, 1 fp8), q read and out written
-    (b * h * d_h * 2 each), and the append's new rows read (2 * b * g * d_h * 2, bf16) and
-    written (2 * b * g * d_h * eb)."""
+def kv_bytes(w, lens, eb: int = 2, T: int = 1) -> int:
+    """Algorithmic bytes of one fused decode-step launch (one layer) with T new tokens per
+    sequence: K and V rows read once for all tokens (2 * g * L_b * d_h * eb over the batch; eb = 2
+    bf16, 1 fp8), q read and out written (b * T * h * d_h * 2 each), and the append's new rows
+    read (2 * b * T * g * d_h * 2, bf16) and written (2 * b * T * g * d_h * eb)."""
     total_rows = int(lens.sum())
-    return (2 * w.g * total_rows * w.d_h * eb + 2 * w.b * w.h * w.d_h * 2
-            + 2 * w.b * w.g * w.d_h * 2 + 2 * w.b * w.g * w.d_h * eb)
+    return (2 * w.g * total_rows * w.d_h * eb + 2 * w.b * T * w.h * w.d_h * 2
+            + 2 * w.b * T * w.g * w.d_h * 2 + 2 * w.b * T * w.g * w.d_h * eb)
 
 
-def attention_flops(w, lens) -> int:
-    return 4 * w.h * int(lens.sum()) * w.d_h
+def attention_flops(w, lens, T: int = 1) -> int:
+    """4 h d_h FLOPs per (query row, visible key): token t of T sees L - T + 1 + t rows."""
+    rows = sum(T * int(L) - T * (T - 1) // 2 for L in lens.tolist())
+    return 4 * w.h * rows * w.d_h
 
 
 # ------------------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (our arm's cpu_baseline and the reference arm)
 # ------------------------------------------------------------------------------------------------
-def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0):
-    """Time the fp64 oracle on whole sequences of this workload's shape (one layer), adding
-    sequences until about ``target_s`` seconds of CPU work; return (us_per_step, details)."""
+def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0, T: int = 1):
+    """Time the fp64 oracle on whole sequences of this workload's shape (one layer, T new tokens
+    per sequence), adding sequences until about ``target_s`` seconds of CPU work; return
+    (us_per_step, details)."""
     import numpy as np
 
     import oracle
@@ -203,14 +211,20 @@ def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0):
         L = int(lens[bi])
         sw = inputs.custom("oracle_sample", 1, w.h, w.g, w.d_h, L - 1, L - 1, kv_std=w.kv_std,
                            wid=500 + bi)
-        q, _, _ = inputs.step_inputs(sw, 0, "cpu")
+        if T > 1:
+            q, _, _ = inputs.multi_step_inputs(sw, T, 0, "cpu")
+        else:
+            q, _, _ = inputs.step_inputs(sw, 0, "cpu")
         k, v = inputs.cache(sw, 0, "cpu")
-        qb = q.view(torch.int16).numpy().view(np.uint16)
+        qb = q.contiguous().view(torch.int16).numpy().view(np.uint16)
         kb = k.view(torch.int16).numpy().view(np.uint16)
         vb = v.view(torch.int16).numpy().view(np.uint16)
         lb = np.array([L], dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.decode_attention(qb, kb, vb, lb, sw.scale, threads=threads)
+        if T > 1:
+            oracle.decode_attention_multi(qb, kb, vb, lb, sw.scale, threads=threads)
+        else:
+            oracle.decode_attention(qb, kb, vb, lb, sw.scale, threads=threads)
         spent += time.perf_counter() - t0
         rows_done += L
         seqs.append(L)
@@ -218,7 +232,8 @@ def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0):
             break
     total_rows = int(lens.sum()) * w.layers
     us_per_step = spent / rows_done * total_rows * 1e6
-    detail = (f"{len(seqs)} whole sequence(s) of one layer (lengths {seqs}, all {w.h} heads), "
+    detail = (f"{len(seqs)} whole sequence(s) of one layer (lengths {seqs}, all {w.h} heads"
+              + (f", {T} tokens" if T > 1 else "") + "), "
               f"{spent:.1f} s of oracle time, scaled by attended rows to {w.layers} layer(s) x "
               f"{w.b} sequences")
     return us_per_step, threads, detail, spent
@@ -275,8 +290,9 @@ def workload_config(w, paged: int = 0, kv: str = "bf16"):
 PAGE_TABLE_SEED = 4242
 
 
-def traffic_key(w, paged: int = 0, kv: str = "bf16") -> str:
-    return w.name + (f"_paged{paged}" if paged else "") + ("_fp8" if kv == "fp8" else "")
+def traffic_key(w, paged: int = 0, kv: str = "bf16", T: int = 1) -> str:
+    return (w.name + (f"_paged{paged}" if paged else "") + ("_fp8" if kv == "fp8" else "")
+            + (f"_T{T}" if T > 1 else ""))
 
 
 # ------------------------------------------------------------------------------------------------
@@ -290,11 +306,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = inputs.WORKLOADS[args.workload]
+    T = args.tokens
+    if T > 1:
+        import dataclasses
+        w = dataclasses.replace(w, extra_rows=T - 1)   # room for the T new rows
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
     pos, lens = inputs.positions_and_lengths(w)
+    lens = (pos + T).to(torch.int32)                    # all T new rows attended by the last
     pos_d, lens_d = pos.to(dev), lens.to(dev)
     layers, xs, outs = [], [], []
     table_d = None
@@ -315,6 +336,10 @@ def run_ours(args, world, rank, local):
             if table_d is None:
                 table_d = table.to(dev)
         layers.append(LayerState(k, v, table_d))
+        if T > 1:
+            xs.append(StepInputs(*inputs.multi_step_inputs(w, T, li, dev)))
+            outs.append(torch.empty(w.b, T, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
+            continue
         xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
         outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
     # small workloads fit in L2: flush it between steps by writing a buffer twice its size
@@ -408,7 +433,7 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end through host buffers: every step copies its inputs in from pinned host
     # memory and its outputs out, overlapped with the kernels (layers.HostStepPipeline) ----
-    buf = HostStepBuffers.allocate(w.layers, w.b, w.h, w.g, w.d_h, dev)
+    buf = HostStepBuffers.allocate(w.layers, w.b, w.h, w.g, w.d_h, dev, tokens=T)
     for li, x in enumerate(xs):
         buf.q_host[li].copy_(x.q.cpu())
         buf.kn_host[li].copy_(x.k_new.cpu())
@@ -458,18 +483,19 @@ def run_ours(args, world, rank, local):
 
     if rank == 0:
         peak, peak_kind = measured_peak_hbm()
-        nbytes = kv_bytes(w, lens, eb)
+        nbytes = kv_bytes(w, lens, eb, T)
         achieved = nbytes / attn_avg_s / 1e9
-        traffic = recorded_traffic(traffic_key(w, args.paged, args.kv))
+        traffic = recorded_traffic(traffic_key(w, args.paged, args.kv, T))
         # weak scaling: every rank runs its own full step; N steps finish in ms_per_step
         value_us = ms_per_step * 1000.0 / world
-        cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w)
+        cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w, T=T)
         line = {
             "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16" if args.kv == "fp8" else "bf16",
-            "data": "synthetic", "config": workload_config(w, args.paged, args.kv),
+            "data": "synthetic", "config": dict(workload_config(w, args.paged, args.kv),
+                                                tokens_per_step=T),
             "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
             "attention_us_per_layer": attn_avg_s * 1e6,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -477,7 +503,7 @@ def run_ours(args, world, rank, local):
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "kernel": "decode_attention_kernel (one fused append + attention launch per layer)",
                          "algorithmic_bytes_per_launch": nbytes,
-                         "flops_per_launch": attention_flops(w, lens)},
+                         "flops_per_launch": attention_flops(w, lens, T)},
             "e2e": {"value": e2e_per_step * 1000.0 / world, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches),
@@ -503,9 +529,13 @@ def main(argv=None):
                     help="keep the caches in page pools of this many rows (0: contiguous)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache element type: bf16, or fp8 E4M3 codes with per-tensor scales")
+    ap.add_argument("--tokens", type=int, default=1, metavar="T",
+                    help="new tokens per sequence per step (causal; T > 1: speculative decoding)")
     args = ap.parse_args(argv)
     if args.kv == "fp8" and args.paged:
         ap.error("--kv fp8 runs on contiguous caches")
+    if args.tokens < 1 or (args.tokens > 1 and (args.kv == "fp8" or args.paged)):
+        ap.error("--tokens T > 1 runs on contiguous bf16 caches")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()

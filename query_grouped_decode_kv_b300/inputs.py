@@ -38,6 +38,7 @@ class Workload:
     layers: int = 1
     kv_std: float = 1.0
     qkv_std: float = 1.0
+    extra_rows: int = 0  # cache rows past ctx_hi + 1 (room for several new tokens)
 
     @property
     def group_size(self) -> int:
@@ -45,8 +46,9 @@ class Workload:
 
     @property
     def n_max(self) -> int:
-        """Cache capacity in rows: the longest context plus the appended token."""
-        return self.ctx_hi + 1
+        """Cache capacity in rows: the longest context plus the appended token (and extra_rows
+        more)."""
+        return self.ctx_hi + 1 + self.extra_rows
 
     @property
     def scale(self) -> float:

@@ -30,8 +30,14 @@ class LayerState:
             raise ValueError("fp8 caches are contiguous; paged caches are bf16")
 
     def step(self, q, k_new, v_new, pos, seq_lens, out, scale, stream) -> None:
-        """One fused append + attention launch on this layer."""
-        if self.fp8_scales is not None:
+        """One fused append + attention launch on this layer (q of shape [b, T, h, d_h]: T new
+        tokens per sequence, causal)."""
+        if q.dim() == 4:
+            if self.fp8_scales is not None or self.page_table is not None:
+                raise ValueError("several tokens per step run on contiguous bf16 caches")
+            binding.decode_step_multi(q, k_new, v_new, self.k_cache, self.v_cache, pos,
+                                      seq_lens, out=out, scale=scale, stream=stream)
+        elif self.fp8_scales is not None:
             ks, vs = self.fp8_scales
             binding.decode_step_fp8(q, k_new, v_new, self.k_cache, self.v_cache, pos, seq_lens,
                                     ks, vs, out=out, scale=scale, stream=stream)
@@ -44,7 +50,9 @@ class LayerState:
                                       stream=stream)
 
     def append(self, k_new, v_new, pos, stream) -> None:
-        if self.fp8_scales is not None:
+        if k_new.dim() == 4:
+            binding.kv_append_multi(k_new, v_new, self.k_cache, self.v_cache, pos, stream=stream)
+        elif self.fp8_scales is not None:
             binding.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, pos,
                                   *self.fp8_scales, stream=stream)
         elif self.page_table is None:
@@ -54,7 +62,10 @@ class LayerState:
                                     self.page_table, stream=stream)
 
     def attend(self, q, seq_lens, out, scale, stream) -> None:
-        if self.fp8_scales is not None:
+        if q.dim() == 4:
+            binding.decode_attention_multi(q, self.k_cache, self.v_cache, seq_lens, out=out,
+                                           scale=scale, stream=stream)
+        elif self.fp8_scales is not None:
             binding.decode_attention_fp8(q, self.k_cache, self.v_cache, seq_lens,
                                          *self.fp8_scales, out=out, scale=scale, stream=stream)
         elif self.page_table is None:
@@ -105,15 +116,21 @@ class HostStepBuffers:
     out_dev: torch.Tensor
 
     @classmethod
-    def allocate(cls, layers: int, b: int, h: int, g: int, d_h: int, device) -> "HostStepBuffers":
+    def allocate(cls, layers: int, b: int, h: int, g: int, d_h: int, device,
+                 tokens: int = 1) -> "HostStepBuffers":
+        """Buffers for one new token per sequence ([layers, b, h, d_h] ...) or, with tokens = T
+        > 1, for T ([layers, b, T, h, d_h] ...)."""
+        t = () if tokens == 1 else (tokens,)
+
         def host(*shape):
             return torch.empty(shape, dtype=torch.bfloat16).pin_memory()
 
         def dev(*shape):
             return torch.empty(shape, dtype=torch.bfloat16, device=device)
-        return cls(host(layers, b, h, d_h), host(layers, b, g, d_h), host(layers, b, g, d_h),
-                   host(layers, b, h, d_h), dev(layers, b, h, d_h), dev(layers, b, g, d_h),
-                   dev(layers, b, g, d_h), dev(layers, b, h, d_h))
+        return cls(host(layers, b, *t, h, d_h), host(layers, b, *t, g, d_h),
+                   host(layers, b, *t, g, d_h), host(layers, b, *t, h, d_h),
+                   dev(layers, b, *t, h, d_h), dev(layers, b, *t, g, d_h),
+                   dev(layers, b, *t, g, d_h), dev(layers, b, *t, h, d_h))
 
     @property
     def h2d_bytes(self) -> int:
