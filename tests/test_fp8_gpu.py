@@ -74,8 +74,8 @@ def gpu_fp8(case, mqa, fused=True, stream=None):
 SHAPES = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 128, 128, 128),     # G = 8, mma.sync (four consumer warps)
-    (3, 8, 2, 128, 0, 300),       # G = 4, CUDA cores
-    (2, 7, 1, 128, 60, 200),      # G = 7, CUDA cores
+    (3, 8, 2, 128, 0, 300),       # G = 4
+    (2, 7, 1, 128, 60, 200),      # G = 7
     (2, 4, 4, 128, 60, 70),       # G = 1 (MHA) around the tile edge
     (2, 32, 2, 128, 100, 700),    # G = 16
     (2, 32, 1, 128, 1, 1000),     # G = 32, eight consumer warps
@@ -99,13 +99,13 @@ def test_fp8_step_matches_oracle(mqa, shape, fused):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
-@pytest.mark.parametrize("shape", [(2, 16, 2, 128, 0, 700), (3, 8, 4, 128, 100, 400),
-                                   (2, 64, 2, 128, 0, 700)],
-                         ids=["mma_sync", "cuda_cores", "mma_sync_G32"])
-def test_fp8_any_cta_split(mqa, shape, ctas):
+@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 128, 100, 400), 1),
+                                        ((3, 8, 4, 128, 100, 400), 0), ((2, 64, 2, 128, 0, 700), 0)],
+                         ids=["mma_sync", "cuda_cores", "mma_sync_G2", "mma_sync_G32"])
+def test_fp8_any_cta_split(mqa, shape, path, ctas):
     case = fp8_case(shape, seed_id=1320)
     k_ref, v_ref, out_ref, _, _ = oracle_fp8_step(case)
-    mqa.debug_override(ctas, 0)
+    mqa.debug_override(ctas, path)
     try:
         kc, vc, out = gpu_fp8(case, mqa)
         assert mqa.get_device_status() == 0

@@ -51,7 +51,7 @@ def oracle_step_any(case):
 SHAPES = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 64, 128, 128),      # tiny MQA step, G = 8
-    (3, 8, 2, 64, 0, 300),        # G = 4, CUDA cores, lengths from 1
+    (3, 8, 2, 64, 0, 300),        # G = 4, lengths from 1
     (2, 4, 4, 128, 60, 70),       # MHA around the tile edge
     (2, 7, 1, 128, 1, 200),       # G = 7
     (2, 16, 2, 128, 100, 700),    # G = 8, tensor cores
@@ -74,7 +74,7 @@ def test_fused_step_matches_oracle(mqa, shape):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
-@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 0),
+@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 1),
                                         ((2, 64, 2, 128, 0, 700), 3)],
                          ids=["mma_sync", "cuda_cores", "tcgen05"])
 def test_fused_step_any_cta_split(mqa, shape, path, ctas):

@@ -69,7 +69,7 @@ SHAPES = [
     (2, 2, 16, 2, 128, 100, 700),     # T=2, G=8: 16 rows
     (3, 4, 64, 8, 128, 0, 513),       # T=4, G=8 (the 70B-class grouping): 32 rows
     (2, 8, 64, 8, 128, 60, 300),      # T=8, G=8: 64 rows
-    (2, 3, 8, 2, 128, 1, 200),        # T=3, G=4: 12 rows (CUDA-core grouping, tensor cores here)
+    (2, 3, 8, 2, 128, 1, 200),        # T=3, G=4: 12 rows
     (2, 4, 4, 4, 128, 60, 70),        # T=4, MHA (G=1): 4 rows
     (2, 2, 32, 1, 128, 1, 1000),      # T=2, G=32: 64 rows
     (3, 5, 9, 3, 64, 10, 129),        # T=5, G=3, d_h=64: 15 rows

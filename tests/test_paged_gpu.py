@@ -79,11 +79,11 @@ def gpu_paged(case, mqa, fused=True, stream=None):
 SHAPES = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 64, 128, 128),      # tiny MQA step, G = 8 (mma.sync)
-    (3, 8, 2, 64, 0, 300),        # G = 4, CUDA cores, lengths from 1
+    (3, 8, 2, 64, 0, 300),        # G = 4, lengths from 1
     (2, 16, 2, 128, 100, 700),    # G = 8, mma.sync
     (2, 32, 1, 128, 1, 1000),     # G = 32, eight consumer warps
     (4, 32, 8, 128, 0, 513),      # GQA 8B-class heads, short ragged contexts
-    (2, 7, 1, 128, 60, 200),      # G = 7, CUDA cores
+    (2, 7, 1, 128, 60, 200),      # G = 7
 ]
 PAGE_SIZES = [8, 16, 32, 64, 128]
 
@@ -104,12 +104,12 @@ def test_paged_step_matches_oracle(mqa, shape, page_size, fused):
 
 
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
-@pytest.mark.parametrize("shape", [(2, 16, 2, 128, 0, 700), (3, 8, 4, 64, 100, 400)],
+@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 1)],
                          ids=["mma_sync", "cuda_cores"])
-def test_paged_step_any_cta_split(mqa, shape, ctas):
+def test_paged_step_any_cta_split(mqa, shape, path, ctas):
     case = paged_case(shape, 16, seed_id=920)
     kp_ref, vp_ref, out_ref, _, _ = oracle_paged_step(case)
-    mqa.debug_override(ctas, 0)
+    mqa.debug_override(ctas, path)
     try:
         kp, vp, out = gpu_paged(case, mqa)
         assert mqa.get_device_status() == 0

@@ -1,8 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
 
 Small cases span several 64-row tiles with ragged tails, both head dimensions, every kernel
-family (CUDA cores G = 1..7, mma.sync G = 8..64, tcgen05 G = 1..64 when forced) and rows past each sequence's length poisoned with NaN. Append is compared
-bit for bit over the whole cache.
+family (mma.sync G = 1..64, the automatic path; CUDA cores G = 1..7 and tcgen05 G = 1..64 when
+forced) and rows past each sequence's length poisoned with NaN. Append is compared bit for bit
+over the whole cache.
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ def mqa():
 SMALL = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 64, 128, 128),      # the tiny MQA step: G = 8, one partial tile
-    (3, 8, 2, 64, 0, 300),        # G = 4, CUDA cores, lengths from 1
+    (3, 8, 2, 64, 0, 300),        # G = 4, lengths from 1
     (2, 4, 4, 128, 60, 70),       # MHA (G = 1) around the 64-row tile edge
     (2, 7, 1, 128, 1, 200),       # G = 7
     (2, 6, 2, 64, 5, 130),        # G = 3
@@ -52,8 +53,23 @@ def test_append_and_attention_match_oracle(mqa, shape):
     P.assert_close(out, out_ref, str(shape))
 
 
+@pytest.mark.parametrize("shape", [s for s in SMALL if s[1] // s[2] < 8],
+                         ids=lambda s: "b{}h{}g{}d{}_{}-{}".format(*s))
+def test_cuda_core_path_matches_oracle(mqa, shape):
+    # the CUDA-core consumer (forced; the automatic choice is mma.sync for every group size)
+    case = P.make_case(*shape, seed_id=100 + SMALL.index(shape))
+    _, _, out_ref = P.oracle_step(case)
+    mqa.debug_override(0, 1)
+    try:
+        _, _, out = P.gpu_step(case, mqa)
+        assert mqa.get_device_status() == 0
+    finally:
+        mqa.debug_override(0, 0)
+    P.assert_close(out, out_ref, f"CUDA cores {shape}")
+
+
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 148, 1000])
-@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 0),
+@pytest.mark.parametrize("shape,path", [((2, 16, 2, 128, 0, 700), 0), ((3, 8, 4, 64, 100, 400), 1),
                                         ((2, 64, 2, 128, 0, 700), 3), ((2, 16, 2, 128, 0, 700), 3)],
                          ids=["mma_sync", "cuda_cores", "tcgen05", "tcgen05_G8"])
 def test_any_cta_split_gives_the_same_result(mqa, shape, path, ctas):

@@ -53,7 +53,7 @@ def test_noalloc_matches_the_allocating_entry_point_on_two_calls_in_a_row(api):
     B, lib = api
     dev = torch.device("cuda")
     # both shapes split their sequences across many CTAs, so the scratch array is used:
-    # G = 4 on CUDA cores with d_h = 128, then G = 16 on tensor cores with d_h = 64
+    # G = 4 with d_h = 128, then G = 16 with d_h = 64
     for b, h, g, d_h, lo, hi, seed in [(4, 32, 8, 128, 100, 3000, 600),
                                         (3, 16, 1, 64, 10, 900, 601)]:
         case = P.make_case(b, h, g, d_h, lo, hi, seed_id=seed)
