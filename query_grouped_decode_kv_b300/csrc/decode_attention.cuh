@@ -21,9 +21,9 @@
 // sum l in fp32, log2 domain) for its slice of the tile's keys; at a segment's end the warps'
 // states are combined through shared memory.
 //
-// Inner products: the grouped heads form a dense contraction on the tensor cores (bf16 mma.sync
-// m16n8k16, fp32 accumulate; S = Q K^T with the heads as M, then O += P V), padded to 16 rows
-// below 16 heads; an fp32 CUDA-core consumer (G < 8) is kept as an alternative.
+// Inner products: for G >= 8 the grouped heads form a real dense contraction and run on tensor
+// cores (bf16 mma.sync m16n8k16, fp32 accumulate; S = Q K^T with the heads as M, then O += P V).
+// For G < 8 (MHA-like grouping) CUDA cores do fp32 FMAs.
 //
 // Every wait is bounded in time: on expiry the kernel latches MQA_ERR_TIMEOUT and returns.
 #pragma once
@@ -1258,7 +1258,7 @@ struct MmaConsumerF8 {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer (G < 8; chosen only when forced). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
+// CUDA-core consumer (G < 8). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
 // 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output. EB: the cache's
 // bytes per element (fp8 codes are widened exactly on load).
 // ---------------------------------------------------------------------------------------------

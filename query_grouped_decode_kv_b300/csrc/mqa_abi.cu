@@ -204,16 +204,12 @@ using AttnKernel = void (*)(const CUtensorMap, const CUtensorMap, const DecodePa
 // tcgen05 tensor cores with tensor-memory accumulators.
 enum Path { kPathAuto = 0, kPathCudaCores = 1, kPathMmaSync = 2, kPathTcgen05 = 3 };
 
-// Automatic choice: mma.sync for every group size. Below 8 heads most rows of its 16-row MMA tile
-// are padding, but the launch is bound by HBM either way, and the tensor-core consumer's per-tile
-// chain is shorter than the CUDA-core consumer's (shuffle reductions, one FMA per element): on B300
-// the 8 x 32 x 8192 MHA step takes 160 us instead of 234, the G = 4 workload 29 us instead of 41.
-// The tcgen05 kernel (128-row MMA tiles, accumulators in tensor memory) is not yet faster on any
-// measured shape. The CUDA-core consumer stays available as path 1.
-Path auto_path(int G) {
-  (void)G;
-  return kPathMmaSync;
-}
+// Automatic choice. G < 8 (MHA-like grouping) has too few heads per K/V row for a real
+// contraction and runs on CUDA cores; from G = 8 the heads of a group form a dense matrix product
+// on the tensor cores (mma.sync: the tcgen05 kernel, 128-row MMA tiles with accumulators in
+// tensor memory, is not yet faster on any measured shape). Forcing mma.sync below 8 heads (path 2,
+// MMA rows mostly padding) is supported and tested.
+Path auto_path(int G) { return G < 8 ? kPathCudaCores : kPathMmaSync; }
 
 // A kernel instance with the launch facts the host needs.
 struct AttnKernelChoice {

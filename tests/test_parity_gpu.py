@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
 
 Small cases span several 64-row tiles with ragged tails, both head dimensions, every kernel
-family (mma.sync G = 1..64, the automatic path; CUDA cores G = 1..7 and tcgen05 G = 1..64 when
-forced) and rows past each sequence's length poisoned with NaN. Append is compared bit for bit
+family (CUDA cores G = 1..7 and mma.sync G = 8..64, the automatic paths; mma.sync G = 1..7 and
+tcgen05 G = 1..64 when forced) and rows past each sequence's length poisoned with NaN. Append is compared bit for bit
 over the whole cache.
 """
 from __future__ import annotations
@@ -56,7 +56,7 @@ def test_append_and_attention_match_oracle(mqa, shape):
 @pytest.mark.parametrize("shape", [s for s in SMALL if s[1] // s[2] < 8],
                          ids=lambda s: "b{}h{}g{}d{}_{}-{}".format(*s))
 def test_cuda_core_path_matches_oracle(mqa, shape):
-    # the CUDA-core consumer (forced; the automatic choice is mma.sync for every group size)
+    # the CUDA-core consumer, forced (it is also the automatic choice for these groups)
     case = P.make_case(*shape, seed_id=100 + SMALL.index(shape))
     _, _, out_ref = P.oracle_step(case)
     mqa.debug_override(0, 1)
