@@ -58,6 +58,7 @@ static_assert(2 * 32 * kConsumerRegs + 32 * kProducerRegs <= 16384,
               "two consumer warps and one producer warp share a sub-partition's registers");
 constexpr int kMaxBatch = 8192;
 constexpr int kMaxGroup = 64;       // largest G = h / g served
+constexpr int kMaxCcHeads = 7;      // the CUDA-core consumers serve G < 8
 constexpr float kLazyLog2 = 8.f;    // softmax reference slack (log2 units), see MmaConsumer::tile
 
 struct DecodeParams {
@@ -118,7 +119,8 @@ __host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
   using Geo = Geometry<D, EB>;
   return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
-         32 * 4;                            // the paged producer's looked-up pages
+         32 * 4 +                           // the paged producer's looked-up pages
+         kMaxCcHeads * D * 4;               // q of the segment in fp32 (CUDA-core consumer)
 }
 template <int D, int EB>
 __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
@@ -340,6 +342,7 @@ struct SharedLayout {
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
   int* pages;           // [32] paged caches: the pages of the tiles being issued (producer warp)
+  float* q_f32;         // [kMaxCcHeads][D] the segment's q in fp32 (CcConsumer2)
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
@@ -369,6 +372,8 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   p += 16;
   s.pages = reinterpret_cast<int*>(p);  // 16-byte aligned: every region before it is a multiple
   p += 32 * 4;                           // of 16 bytes
+  s.q_f32 = reinterpret_cast<float*>(p);
+  p += kMaxCcHeads * D * 4;
   return s;
 }
 
@@ -887,6 +892,7 @@ template <int D, int WM, int NW, bool kTokens = false>
 struct MmaConsumer {
   static constexpr int kWarps = NW;
   static constexpr int kTileGroups = 1;
+  static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 16;  // head rows per warp
   static constexpr int NGRP = NW / WM;
   static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
@@ -1078,6 +1084,7 @@ template <int D, int WM, int NW, int TG = 1>
 struct MmaConsumerF8 {
   static constexpr int kWarps = NW;
   static constexpr int kTileGroups = TG;
+  static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 16;  // head rows per warp
   static constexpr int NGRP = NW / (WM * TG);  // key groups per tile group
   static constexpr int KPW = kTileKeys / NGRP;  // keys per group per tile
@@ -1266,6 +1273,7 @@ template <int D, int G, int NW, int EB = 2>
 struct CcConsumer {
   static constexpr int kWarps = NW;
   static constexpr int kTileGroups = 1;
+  static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
   static constexpr int DPL = D / 32;
   static constexpr int KPW = kTileKeys / NW;
@@ -1422,6 +1430,141 @@ struct CcConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
+// CUDA-core consumer for G < 8, lanes owning keys (bf16 caches). In S = Q K^T each lane takes one
+// key of its warp's 32 and forms the whole dot product itself: the key's row from the stage
+// (16-byte loads), q from shared memory in fp32 (one copy per segment, every lane reading the same
+// address), so no shuffle reduction is needed per key. The softmax takes one warp-wide max per
+// head and tile; each lane keeps a partial sum over its own keys, reduced across the warp only
+// when the segment's state is published. In O += P V each lane owns D/32 output columns and takes
+// each key's weight from the key's lane by a shuffle. Eight warps form four tile groups of two,
+// each group taking every fourth tile of the CTA's range and each warp 32 of its 64 keys.
+// ---------------------------------------------------------------------------------------------
+template <int D, int G>
+struct CcConsumer2 {
+  static constexpr int kWarps = 8;
+  static constexpr int kTileGroups = 4;
+  static constexpr bool kSharedQ = true;
+  static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
+  static constexpr int DPL = D / 32;    // output columns per lane
+  static_assert(G <= kMaxCcHeads && (D == 64 || D == 128), "CUDA-core consumer shapes");
+
+  float o[G][DPL];
+  float m[G];   // running reference, the same in every lane
+  float l[G];   // this lane's share of the running sum (its own keys)
+  const float* qs;
+
+  // Stage q of segment (bi, j) in shared memory as fp32 (all consumer threads; the caller
+  // synchronises the consumer warps before the first tile).
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, const SharedLayout& sh,
+                                                int bi, int j, int lane) {
+    qs = sh.q_f32;
+    const __nv_bfloat16* qb = P.q + row_offset(P, bi, j, 0, D);  // the group's G heads, adjacent
+    for (int e = threadIdx.x; e < G * D; e += kWarps * 32) sh.q_f32[e] = __bfloat162float(qb[e]);
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[hh][e] = 0.f;
+      m[hh] = -INFINITY;
+      l[hh] = 0.f;
+    }
+  }
+
+  // bf16 pair -> two floats (exact)
+  __device__ __forceinline__ static float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+  __device__ __forceinline__ static float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+  // One tile: this warp's keys are gw * 32 .. gw * 32 + 31 of the tile; `nvalid` of them (warp-
+  // uniform, 0..32) lie below the sequence length.
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int gw, int lane,
+                                       int nvalid, float scale_log2) {
+    const int key = gw * 32 + lane;
+    float s[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) s[hh] = 0.f;
+    // a few 8-column chunks at a time: unrolled further, the q reads of all heads stay live
+#pragma unroll 2
+    for (int c = 0; c < D / 8; ++c) {
+      uint32_t w0, w1, w2, w3;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                   : "r"(swz(kbase, key, c * 8)));
+      const float kf[8] = {lo_f(w0), hi_f(w0), lo_f(w1), hi_f(w1),
+                           lo_f(w2), hi_f(w2), lo_f(w3), hi_f(w3)};
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * D + c * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * D + c * 8 + 4);
+        float acc = s[hh];
+        acc = fmaf(qa.x, kf[0], acc); acc = fmaf(qa.y, kf[1], acc);
+        acc = fmaf(qa.z, kf[2], acc); acc = fmaf(qa.w, kf[3], acc);
+        acc = fmaf(qb.x, kf[4], acc); acc = fmaf(qb.y, kf[5], acc);
+        acc = fmaf(qb.z, kf[6], acc); acc = fmaf(qb.w, kf[7], acc);
+        s[hh] = acc;
+      }
+    }
+    const bool mine_valid = lane < nvalid;
+    float p[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const float sc = mine_valid ? s[hh] * scale_log2 : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m[hh], mx);
+      const float ref = (mn == -INFINITY) ? 0.f : mn;
+      const float al = fast_exp2(m[hh] - ref);
+      m[hh] = mn;
+      p[hh] = fast_exp2(sc - ref);
+      l[hh] = l[hh] * al + p[hh];
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[hh][e] *= al;
+    }
+    // O += P V over the valid keys; key kk's weight sits in lane kk
+    const int d0 = lane * DPL;
+    for (int kk = 0; kk < nvalid; ++kk) {
+      const uint32_t addr = swz(vbase, gw * 32 + kk, d0 & ~7) + (d0 & 7) * 2;
+      float vf[DPL];
+      if constexpr (DPL == 4) {
+        uint32_t x, y;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
+        vf[0] = lo_f(x); vf[1] = hi_f(x); vf[2] = lo_f(y); vf[3] = hi_f(y);
+      } else {
+        uint32_t x;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+        vf[0] = lo_f(x); vf[1] = hi_f(x);
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float pk = __shfl_sync(0xffffffffu, p[hh], kk);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float lsum = l[hh];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      float* row = sh.comb_o + (warp * kCombRows + hh) * comb_row_floats(D);
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) row[lane * DPL + e] = o[hh][e];
+      if (lane == 0) sh.comb_ml[warp * kCombRows + hh] = make_float2(m[hh], lsum);
+    }
+  }
+
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) { ws[w] = w; rs[w] = hr; }
+      return kWarps;
+    }
+  };
+};
+
+// ---------------------------------------------------------------------------------------------
 // The kernel. `Consumer` is MmaConsumer<D, WM, NW>, MmaConsumerF8<D, WM, NW> or
 // CcConsumer<D, G, NW, EB>; EB is the cache's bytes per element (2: bf16, 1: fp8 E4M3 codes).
 // ---------------------------------------------------------------------------------------------
@@ -1486,12 +1629,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   // tile groups: warp group tg owns the tiles k with k % TG == tg (TG = 1: every warp, every tile)
   constexpr int TG = Consumer::kTileGroups;
   constexpr int WPG = NW / TG;  // warps per tile group
-  static_assert(TG == 1 || kTensorCores, "tile groups are a tensor-core consumer option");
+  static_assert(TG == 1 || kTensorCores || Consumer::kSharedQ, "tile groups of this consumer");
   const int tg = warp / WPG;
   const int gw = warp % WPG;
   const int grp = kTensorCores ? gw / WM : warp;
   const int mi = kTensorCores ? gw % WM : 0;
-  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / WPG : kTileKeys / NW;
+  constexpr int kGroupKeys = kTensorCores ? kTileKeys * WM / WPG : kTileKeys / WPG;
   uint32_t cphase = 0;
   TileCursor cur;
   cur.start(x0, sh.tix);
@@ -1511,8 +1654,19 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     if (k == 0 || cur.tile == 0) {
       L = __ldg(P.seq_lens + cur.bi);
       began_at_zero = (cur.tile == 0);
-      if constexpr (kTensorCores) cons.begin_segment(P, cur.bi, cur.j, mi, lane);
-      else cons.begin_segment(P, cur.bi, cur.j, lane);
+      if constexpr (kTensorCores) {
+        cons.begin_segment(P, cur.bi, cur.j, mi, lane);
+      } else if constexpr (Consumer::kSharedQ) {
+        // every consumer warp is at this segment start (the last segment's end synchronised
+        // them); q is staged in shared memory before any warp's first tile of the segment
+        cons.begin_segment(P, sh, cur.bi, cur.j, lane);
+        if (!consumer_sync(sh, cphase, P.timeout_ns)) {
+          if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
+          return;
+        }
+      } else {
+        cons.begin_segment(P, cur.bi, cur.j, lane);
+      }
     }
     const int tile_start = cur.tile * kTileKeys;
     const int valid = min(L - tile_start, kTileKeys);  // >= 1
@@ -1543,8 +1697,8 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       // that a row's causal lag applies at the sequence's end only
       cons.tile(kbase, vbase, grp, lane, L - tile_start, P.scale_log2);
     } else {
-      const int nvalid = max(0, min(valid - warp * kGroupKeys, kGroupKeys));
-      cons.tile(kbase, vbase, warp, lane, nvalid, P.scale_log2);
+      const int nvalid = max(0, min(valid - gw * kGroupKeys, kGroupKeys));
+      cons.tile(kbase, vbase, gw, lane, nvalid, P.scale_log2);
     }
     if (mine) {
       __syncwarp();

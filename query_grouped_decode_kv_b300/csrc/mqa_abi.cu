@@ -259,13 +259,13 @@ AttnKernelChoice pick_kernel(Path path, int G, int b, int T) {
     return choice<MmaConsumer<D, 4, 8>, D, 2, true, 4>(b);
   }
   switch (G) {
-    case 1: return choice<CcConsumer<D, 1, 8>, D, 2, false, 1>(b);
-    case 2: return choice<CcConsumer<D, 2, 8>, D, 2, false, 1>(b);
-    case 3: return choice<CcConsumer<D, 3, 8>, D, 2, false, 1>(b);
-    case 4: return choice<CcConsumer<D, 4, 8>, D, 2, false, 1>(b);
-    case 5: return choice<CcConsumer<D, 5, 8>, D, 2, false, 1>(b);
-    case 6: return choice<CcConsumer<D, 6, 8>, D, 2, false, 1>(b);
-    case 7: return choice<CcConsumer<D, 7, 8>, D, 2, false, 1>(b);
+    case 1: return choice<mqa::CcConsumer2<D, 1>, D, 2, false, 1>(b);
+    case 2: return choice<mqa::CcConsumer2<D, 2>, D, 2, false, 1>(b);
+    case 3: return choice<mqa::CcConsumer2<D, 3>, D, 2, false, 1>(b);
+    case 4: return choice<mqa::CcConsumer2<D, 4>, D, 2, false, 1>(b);
+    case 5: return choice<mqa::CcConsumer2<D, 5>, D, 2, false, 1>(b);
+    case 6: return choice<mqa::CcConsumer2<D, 6>, D, 2, false, 1>(b);
+    case 7: return choice<mqa::CcConsumer2<D, 7>, D, 2, false, 1>(b);
     default: return {};
   }
 }
