@@ -1519,26 +1519,35 @@ struct CcConsumer2 {
 #pragma unroll
       for (int e = 0; e < DPL; ++e) o[hh][e] *= al;
     }
-    // O += P V over the valid keys; key kk's weight sits in lane kk
+    // O += P V over the valid keys; key kk's weight sits in lane kk (a whole warp's keys valid:
+    // unrolled, so the row loads and shuffles of several keys are in flight together)
+    if (nvalid == 32) {
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) add_key(vbase, gw, lane, kk, p);
+    } else {
+      for (int kk = 0; kk < nvalid; ++kk) add_key(vbase, gw, lane, kk, p);
+    }
+  }
+
+  __device__ __forceinline__ void add_key(uint32_t vbase, int gw, int lane, int kk,
+                                          const float (&p)[G]) {
     const int d0 = lane * DPL;
-    for (int kk = 0; kk < nvalid; ++kk) {
-      const uint32_t addr = swz(vbase, gw * 32 + kk, d0 & ~7) + (d0 & 7) * 2;
-      float vf[DPL];
-      if constexpr (DPL == 4) {
-        uint32_t x, y;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
-        vf[0] = lo_f(x); vf[1] = hi_f(x); vf[2] = lo_f(y); vf[3] = hi_f(y);
-      } else {
-        uint32_t x;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
-        vf[0] = lo_f(x); vf[1] = hi_f(x);
-      }
+    const uint32_t addr = swz(vbase, gw * 32 + kk, d0 & ~7) + (d0 & 7) * 2;
+    float vf[DPL];
+    if constexpr (DPL == 4) {
+      uint32_t x, y;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
+      vf[0] = lo_f(x); vf[1] = hi_f(x); vf[2] = lo_f(y); vf[3] = hi_f(y);
+    } else {
+      uint32_t x;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+      vf[0] = lo_f(x); vf[1] = hi_f(x);
+    }
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float pk = __shfl_sync(0xffffffffu, p[hh], kk);
+    for (int hh = 0; hh < G; ++hh) {
+      const float pk = __shfl_sync(0xffffffffu, p[hh], kk);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
-      }
+      for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
     }
   }
 
