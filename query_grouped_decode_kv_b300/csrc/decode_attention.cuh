@@ -1451,13 +1451,14 @@ struct CcConsumer2 {
   float o[G][DPL];
   float m[G];   // running reference, the same in every lane
   float l[G];   // this lane's share of the running sum (its own keys)
-  const float* qs;
+  uint32_t qs;  // shared-window address of the staged q (explicit ld.shared: a generic pointer
+                // would make every q read wait like a global load)
 
   // Stage q of segment (bi, j) in shared memory as fp32 (all consumer threads; the caller
   // synchronises the consumer warps before the first tile).
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, const SharedLayout& sh,
                                                 int bi, int j, int lane) {
-    qs = sh.q_f32;
+    qs = smem_addr(sh.q_f32);
     const __nv_bfloat16* qb = P.q + row_offset(P, bi, j, 0, D);  // the group's G heads, adjacent
     for (int e = threadIdx.x; e < G * D; e += kWarps * 32) sh.q_f32[e] = __bfloat162float(qb[e]);
 #pragma unroll
@@ -1492,8 +1493,13 @@ struct CcConsumer2 {
                            lo_f(w2), hi_f(w2), lo_f(w3), hi_f(w3)};
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * D + c * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * D + c * 8 + 4);
+        float4 qa, qb;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(qa.x), "=f"(qa.y), "=f"(qa.z), "=f"(qa.w)
+                     : "r"(qs + (hh * D + c * 8) * 4));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(qb.x), "=f"(qb.y), "=f"(qb.z), "=f"(qb.w)
+                     : "r"(qs + (hh * D + c * 8 + 4) * 4));
         float acc = s[hh];
         acc = fmaf(qa.x, kf[0], acc); acc = fmaf(qa.y, kf[1], acc);
         acc = fmaf(qa.z, kf[2], acc); acc = fmaf(qa.w, kf[3], acc);
