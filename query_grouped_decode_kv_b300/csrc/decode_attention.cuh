@@ -112,6 +112,14 @@ struct Geometry {
 
 __host__ __device__ constexpr int comb_row_floats(int D) { return D + 8; }
 
+// q of a segment in fp32 for the CUDA-core consumer: head hh's columns at hh * (D + 8), the upper
+// half of them 4 floats further on, so that the two half-warps' same-address reads of the two
+// halves land in different banks.
+__host__ __device__ constexpr int cc_q_row_floats(int D) { return D + 8; }
+__host__ __device__ constexpr int cc_q_index(int D, int hh, int d) {
+  return hh * cc_q_row_floats(D) + d + (d >= D / 2 ? 4 : 0);
+}
+
 // Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags]
 // [page slots]. CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
 template <int D, int EB>
@@ -120,7 +128,7 @@ __host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
   return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
          32 * 4 +                           // the paged producer's looked-up pages
-         kMaxCcHeads * D * 4;               // q of the segment in fp32 (CUDA-core consumer)
+         kMaxCcHeads * cc_q_row_floats(D) * 4;  // q of the segment in fp32 (CUDA-core consumer)
 }
 template <int D, int EB>
 __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
@@ -342,7 +350,7 @@ struct SharedLayout {
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
   int* pages;           // [32] paged caches: the pages of the tiles being issued (producer warp)
-  float* q_f32;         // [kMaxCcHeads][D] the segment's q in fp32 (CcConsumer2)
+  float* q_f32;         // the segment's q in fp32 (CcConsumer2), laid out by cc_q_index
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
@@ -373,7 +381,7 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.pages = reinterpret_cast<int*>(p);  // 16-byte aligned: every region before it is a multiple
   p += 32 * 4;                           // of 16 bytes
   s.q_f32 = reinterpret_cast<float*>(p);
-  p += kMaxCcHeads * D * 4;
+  p += kMaxCcHeads * cc_q_row_floats(D) * 4;
   return s;
 }
 
@@ -1430,29 +1438,36 @@ struct CcConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer for G < 8, lanes owning keys (bf16 caches). In S = Q K^T each lane takes one
-// key of its warp's 32 and forms the whole dot product itself: the key's row from the stage
-// (16-byte loads), q from shared memory in fp32 (one copy per segment, every lane reading the same
-// address), so no shuffle reduction is needed per key. The softmax takes one warp-wide max per
-// head and tile; each lane keeps a partial sum over its own keys, reduced across the warp only
-// when the segment's state is published. In O += P V each lane owns D/32 output columns and takes
-// each key's weight from the key's lane by a shuffle. Eight warps form four tile groups of two,
-// each group taking every fourth tile of the CTA's range and each warp 32 of its 64 keys.
+// CUDA-core consumer for G < 8, lanes owning keys (bf16 caches). Eight warps form two tile groups
+// of four; a group takes every other tile of the CTA's range, so each group has two of the four
+// stages (one being computed, one loading), and each warp 16 of a tile's 64 keys.
+// In S = Q K^T each key belongs to two lanes, l and l + 16, which form the dot product over the
+// lower and the upper half of the columns (the key's row from the stage in 16-byte loads, q from
+// shared memory in fp32, every half-warp reading one address) and add the halves with one
+// shuffle. The softmax takes one max over the warp's keys per head and tile; each lane keeps a
+// partial sum over its key, reduced across the warp only when the segment's state is published.
+// In O += P V each lane owns D/32 output columns and takes each key's weight from the key's lane
+// by a shuffle. The products run as packed fp32 pairs (fma.rn.f32x2): in S the two lanes of a
+// pair sum the even and the odd columns, in P V the even and the odd keys; each pair is added up
+// once, at the end of the tile (S) or of the segment (O).
 // ---------------------------------------------------------------------------------------------
 template <int D, int G>
 struct CcConsumer2 {
   static constexpr int kWarps = 8;
-  static constexpr int kTileGroups = 4;
+  static constexpr int kTileGroups = 2;
   static constexpr bool kSharedQ = true;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
   static constexpr int DPL = D / 32;    // output columns per lane
+  static constexpr int kKeys = kTileKeys * kTileGroups / kWarps;  // keys per warp and tile
+  static constexpr int QH = D / 2;      // columns per half-warp in S
   static_assert(G <= kMaxCcHeads && (D == 64 || D == 128), "CUDA-core consumer shapes");
+  static_assert(kKeys == 16, "two lanes per key");
 
-  float o[G][DPL];
-  float m[G];   // running reference, the same in every lane
-  float l[G];   // this lane's share of the running sum (its own keys)
-  uint32_t qs;  // shared-window address of the staged q (explicit ld.shared: a generic pointer
-                // would make every q read wait like a global load)
+  uint64_t o2[G][DPL];  // O columns, as (even keys, odd keys) partial pairs
+  float m[G];           // running reference, the same in every lane
+  float l[G];           // this lane's share of the running sum (its key; lanes l, l + 16 agree)
+  uint32_t qs;          // shared-window address of the staged q (explicit ld.shared: a generic
+                        // pointer would make every q read wait like a global load)
 
   // Stage q of segment (bi, j) in shared memory as fp32 (all consumer threads; the caller
   // synchronises the consumer warps before the first tile).
@@ -1460,11 +1475,12 @@ struct CcConsumer2 {
                                                 int bi, int j, int lane) {
     qs = smem_addr(sh.q_f32);
     const __nv_bfloat16* qb = P.q + row_offset(P, bi, j, 0, D);  // the group's G heads, adjacent
-    for (int e = threadIdx.x; e < G * D; e += kWarps * 32) sh.q_f32[e] = __bfloat162float(qb[e]);
+    for (int e = threadIdx.x; e < G * D; e += kWarps * 32)
+      sh.q_f32[cc_q_index(D, e / D, e % D)] = __bfloat162float(qb[e]);
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[hh][e] = 0.f;
+      for (int e = 0; e < DPL; ++e) o2[hh][e] = 0ull;
       m[hh] = -INFINITY;
       l[hh] = 0.f;
     }
@@ -1474,98 +1490,109 @@ struct CcConsumer2 {
   __device__ __forceinline__ static float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
   __device__ __forceinline__ static float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-  // One tile: this warp's keys are gw * 32 .. gw * 32 + 31 of the tile; `nvalid` of them (warp-
-  // uniform, 0..32) lie below the sequence length.
+  // One tile: this warp's keys are gw * 16 .. gw * 16 + 15 of the tile; `nvalid` of them (warp-
+  // uniform, 0..16) lie below the sequence length.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int gw, int lane,
                                        int nvalid, float scale_log2) {
-    const int key = gw * 32 + lane;
-    float s[G];
+    const int kl = lane & 15, dh = lane >> 4;
+    const int key = gw * kKeys + kl;
+    const uint32_t qh = qs + cc_q_index(D, 0, dh * QH) * 4;
+    uint64_t acc[G];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) s[hh] = 0.f;
+    for (int hh = 0; hh < G; ++hh) acc[hh] = 0ull;
     // a few 8-column chunks at a time: unrolled further, the q reads of all heads stay live
 #pragma unroll 2
-    for (int c = 0; c < D / 8; ++c) {
+    for (int c = 0; c < QH / 8; ++c) {
       uint32_t w0, w1, w2, w3;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                   : "r"(swz(kbase, key, c * 8)));
-      const float kf[8] = {lo_f(w0), hi_f(w0), lo_f(w1), hi_f(w1),
-                           lo_f(w2), hi_f(w2), lo_f(w3), hi_f(w3)};
+                   : "r"(swz(kbase, key, dh * QH + c * 8)));
+      const uint64_t k01 = pack_f32x2(lo_f(w0), hi_f(w0)), k23 = pack_f32x2(lo_f(w1), hi_f(w1));
+      const uint64_t k45 = pack_f32x2(lo_f(w2), hi_f(w2)), k67 = pack_f32x2(lo_f(w3), hi_f(w3));
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float4 qa, qb;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(qa.x), "=f"(qa.y), "=f"(qa.z), "=f"(qa.w)
-                     : "r"(qs + (hh * D + c * 8) * 4));
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(qb.x), "=f"(qb.y), "=f"(qb.z), "=f"(qb.w)
-                     : "r"(qs + (hh * D + c * 8 + 4) * 4));
-        float acc = s[hh];
-        acc = fmaf(qa.x, kf[0], acc); acc = fmaf(qa.y, kf[1], acc);
-        acc = fmaf(qa.z, kf[2], acc); acc = fmaf(qa.w, kf[3], acc);
-        acc = fmaf(qb.x, kf[4], acc); acc = fmaf(qb.y, kf[5], acc);
-        acc = fmaf(qb.z, kf[6], acc); acc = fmaf(qb.w, kf[7], acc);
-        s[hh] = acc;
+        uint64_t q01, q23, q45, q67;
+        const uint32_t qa = qh + (hh * cc_q_row_floats(D) + c * 8) * 4;
+        asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(q01), "=l"(q23) : "r"(qa));
+        asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(q45), "=l"(q67) : "r"(qa + 16));
+        uint64_t a = acc[hh];
+        a = fma_f32x2(q01, k01, a);
+        a = fma_f32x2(q23, k23, a);
+        a = fma_f32x2(q45, k45, a);
+        a = fma_f32x2(q67, k67, a);
+        acc[hh] = a;
       }
     }
-    const bool mine_valid = lane < nvalid;
+    const bool mine_valid = kl < nvalid;
     float p[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      const float sc = mine_valid ? s[hh] * scale_log2 : -INFINITY;
+      float part = sum_f32x2(acc[hh]);
+      part += __shfl_xor_sync(0xffffffffu, part, 16);  // both halves of the columns
+      const float sc = mine_valid ? part * scale_log2 : -INFINITY;
       float mx = sc;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float mn = fmaxf(m[hh], mx);
       const float ref = (mn == -INFINITY) ? 0.f : mn;
       const float al = fast_exp2(m[hh] - ref);
       m[hh] = mn;
-      p[hh] = fast_exp2(sc - ref);
+      p[hh] = fast_exp2(sc - ref);  // 0 for keys at or beyond the length
       l[hh] = l[hh] * al + p[hh];
+      const uint64_t al2 = pack_f32x2(al, al);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[hh][e] *= al;
+      for (int e = 0; e < DPL; ++e) o2[hh][e] = mul_f32x2(o2[hh][e], al2);
     }
-    // O += P V over the valid keys; key kk's weight sits in lane kk (a whole warp's keys valid:
-    // unrolled, so the row loads and shuffles of several keys are in flight together)
-    if (nvalid == 32) {
-#pragma unroll 8
-      for (int kk = 0; kk < 32; ++kk) add_key(vbase, gw, lane, kk, p);
+    // O += P V over the valid keys, two keys at a time; key kk's weight sits in lane kk
+    if (nvalid == kKeys) {
+#pragma unroll
+      for (int kk = 0; kk < kKeys; kk += 2) add_key_pair(vbase, gw, lane, kk, true, p);
     } else {
-      for (int kk = 0; kk < nvalid; ++kk) add_key(vbase, gw, lane, kk, p);
+      for (int kk = 0; kk < nvalid; kk += 2) add_key_pair(vbase, gw, lane, kk, kk + 1 < nvalid, p);
     }
   }
 
-  __device__ __forceinline__ void add_key(uint32_t vbase, int gw, int lane, int kk,
-                                          const float (&p)[G]) {
+  // keys kk (valid) and kk + 1 (valid when `second`; a row at or beyond the length may hold
+  // anything, NaN included, so it is not read)
+  __device__ __forceinline__ void add_key_pair(uint32_t vbase, int gw, int lane, int kk,
+                                               bool second, const float (&p)[G]) {
     const int d0 = lane * DPL;
-    const uint32_t addr = swz(vbase, gw * 32 + kk, d0 & ~7) + (d0 & 7) * 2;
-    float vf[DPL];
+    const uint32_t a0 = swz(vbase, gw * kKeys + kk, d0 & ~7) + (d0 & 7) * 2;
+    const uint32_t a1 = swz(vbase, gw * kKeys + kk + 1, d0 & ~7) + (d0 & 7) * 2;
+    uint64_t v2[DPL];
     if constexpr (DPL == 4) {
-      uint32_t x, y;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
-      vf[0] = lo_f(x); vf[1] = hi_f(x); vf[2] = lo_f(y); vf[3] = hi_f(y);
+      uint32_t x0, y0, x1 = 0, y1 = 0;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(y0) : "r"(a0));
+      if (second) asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x1), "=r"(y1) : "r"(a1));
+      v2[0] = pack_f32x2(lo_f(x0), lo_f(x1));
+      v2[1] = pack_f32x2(hi_f(x0), hi_f(x1));
+      v2[2] = pack_f32x2(lo_f(y0), lo_f(y1));
+      v2[3] = pack_f32x2(hi_f(y0), hi_f(y1));
     } else {
-      uint32_t x;
-      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
-      vf[0] = lo_f(x); vf[1] = hi_f(x);
+      uint32_t x0, x1 = 0;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(a0));
+      if (second) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1) : "r"(a1));
+      v2[0] = pack_f32x2(lo_f(x0), lo_f(x1));
+      v2[1] = pack_f32x2(hi_f(x0), hi_f(x1));
     }
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      const float pk = __shfl_sync(0xffffffffu, p[hh], kk);
+      const uint64_t pp = pack_f32x2(__shfl_sync(0xffffffffu, p[hh], kk),
+                                     __shfl_sync(0xffffffffu, p[hh], kk + 1));
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[hh][e] = fmaf(pk, vf[e], o[hh][e]);
+      for (int e = 0; e < DPL; ++e) o2[hh][e] = fma_f32x2(pp, v2[e], o2[hh][e]);
     }
   }
 
   __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      float lsum = l[hh];
+      float lsum = l[hh];  // over the 16 keys (lanes l and l + 16 hold the same key's share)
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      for (int off = 8; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
       float* row = sh.comb_o + (warp * kCombRows + hh) * comb_row_floats(D);
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) row[lane * DPL + e] = o[hh][e];
+      for (int e = 0; e < DPL; ++e) row[lane * DPL + e] = sum_f32x2(o2[hh][e]);
       if (lane == 0) sh.comb_ml[warp * kCombRows + hh] = make_float2(m[hh], lsum);
     }
   }
