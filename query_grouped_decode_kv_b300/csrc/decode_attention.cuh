@@ -59,6 +59,7 @@ static_assert(2 * 32 * kConsumerRegs + 32 * kProducerRegs <= 16384,
 constexpr int kMaxBatch = 8192;
 constexpr int kMaxGroup = 64;       // largest G = h / g served
 constexpr int kMaxCcHeads = 7;      // the CUDA-core consumers serve G < 8
+constexpr int kCcWarpKeys = 16;     // keys per warp and tile in the CUDA-core consumer
 constexpr float kLazyLog2 = 8.f;    // softmax reference slack (log2 units), see MmaConsumer::tile
 
 struct DecodeParams {
@@ -128,7 +129,8 @@ __host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
   return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
          32 * 4 +                           // the paged producer's looked-up pages
-         kMaxCcHeads * cc_q_row_floats(D) * 4;  // q of the segment in fp32 (CUDA-core consumer)
+         kMaxCcHeads * cc_q_row_floats(D) * 4 +  // q of the segment in fp32 (CUDA-core consumer)
+         NW * kMaxCcHeads * kCcWarpKeys * 4;     // its key weights, per warp
 }
 template <int D, int EB>
 __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
@@ -351,6 +353,7 @@ struct SharedLayout {
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
   int* pages;           // [32] paged caches: the pages of the tiles being issued (producer warp)
   float* q_f32;         // the segment's q in fp32 (CcConsumer2), laid out by cc_q_index
+  float* p_cc;          // [NW][kMaxCcHeads][kCcWarpKeys] key weights of a tile (CcConsumer2)
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
@@ -382,6 +385,8 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   p += 32 * 4;                           // of 16 bytes
   s.q_f32 = reinterpret_cast<float*>(p);
   p += kMaxCcHeads * cc_q_row_floats(D) * 4;
+  s.p_cc = reinterpret_cast<float*>(p);
+  p += NW * kMaxCcHeads * kCcWarpKeys * 4;
   return s;
 }
 
@@ -1446,10 +1451,11 @@ struct CcConsumer {
 // shared memory in fp32, every half-warp reading one address) and add the halves with one
 // shuffle. The softmax takes one max over the warp's keys per head and tile; each lane keeps a
 // partial sum over its key, reduced across the warp only when the segment's state is published.
-// In O += P V each lane owns D/32 output columns and takes each key's weight from the key's lane
-// by a shuffle. The products run as packed fp32 pairs (fma.rn.f32x2): in S the two lanes of a
-// pair sum the even and the odd columns, in P V the even and the odd keys; each pair is added up
-// once, at the end of the tile (S) or of the segment (O).
+// In O += P V each lane owns D/32 output columns and takes the keys' weights from a per-warp row
+// in shared memory (written once per tile, read four keys at a time). The products run as packed
+// fp32 pairs (fma.rn.f32x2): in S the two lanes of a pair sum the even and the odd columns, in
+// P V the even and the odd keys; each pair is added up once, at the end of the tile (S) or of the
+// segment (O).
 // ---------------------------------------------------------------------------------------------
 template <int D, int G>
 struct CcConsumer2 {
@@ -1461,19 +1467,22 @@ struct CcConsumer2 {
   static constexpr int kKeys = kTileKeys * kTileGroups / kWarps;  // keys per warp and tile
   static constexpr int QH = D / 2;      // columns per half-warp in S
   static_assert(G <= kMaxCcHeads && (D == 64 || D == 128), "CUDA-core consumer shapes");
-  static_assert(kKeys == 16, "two lanes per key");
+  static_assert(kKeys == kCcWarpKeys, "two lanes per key");
+  static constexpr int kPvUnroll = G >= 6 ? 2 : 4;  // groups of four keys (more spills at G >= 6)
 
   uint64_t o2[G][DPL];  // O columns, as (even keys, odd keys) partial pairs
   float m[G];           // running reference, the same in every lane
   float l[G];           // this lane's share of the running sum (its key; lanes l, l + 16 agree)
   uint32_t qs;          // shared-window address of the staged q (explicit ld.shared: a generic
                         // pointer would make every q read wait like a global load)
+  uint32_t pw;          // shared-window address of this warp's key weights [G][kKeys]
 
   // Stage q of segment (bi, j) in shared memory as fp32 (all consumer threads; the caller
   // synchronises the consumer warps before the first tile).
   __device__ __forceinline__ void begin_segment(const DecodeParams& P, const SharedLayout& sh,
                                                 int bi, int j, int lane) {
     qs = smem_addr(sh.q_f32);
+    pw = smem_addr(sh.p_cc) + (threadIdx.x >> 5) * kMaxCcHeads * kKeys * 4;
     const __nv_bfloat16* qb = P.q + row_offset(P, bi, j, 0, D);  // the group's G heads, adjacent
     for (int e = threadIdx.x; e < G * D; e += kWarps * 32)
       sh.q_f32[cc_q_index(D, e / D, e % D)] = __bfloat162float(qb[e]);
@@ -1543,44 +1552,63 @@ struct CcConsumer2 {
 #pragma unroll
       for (int e = 0; e < DPL; ++e) o2[hh][e] = mul_f32x2(o2[hh][e], al2);
     }
-    // O += P V over the valid keys, two keys at a time; key kk's weight sits in lane kk
-    if (nvalid == kKeys) {
+    // the weights to this warp's rows (the previous tile's reads of them are done)
+    __syncwarp();
+    if (dh == 0) {
 #pragma unroll
-      for (int kk = 0; kk < kKeys; kk += 2) add_key_pair(vbase, gw, lane, kk, true, p);
+      for (int hh = 0; hh < G; ++hh)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(pw + (hh * kKeys + kl) * 4), "f"(p[hh])
+                     : "memory");
+    }
+    __syncwarp();
+    // O += P V over the valid keys, four at a time
+    if (nvalid == kKeys) {
+#pragma unroll(kPvUnroll)
+      for (int kq = 0; kq < kKeys; kq += 4) add_keys(vbase, gw, lane, kq, 4);
     } else {
-      for (int kk = 0; kk < nvalid; kk += 2) add_key_pair(vbase, gw, lane, kk, kk + 1 < nvalid, p);
+      for (int kq = 0; kq < nvalid; kq += 4) add_keys(vbase, gw, lane, kq, nvalid - kq);
     }
   }
 
-  // keys kk (valid) and kk + 1 (valid when `second`; a row at or beyond the length may hold
-  // anything, NaN included, so it is not read)
-  __device__ __forceinline__ void add_key_pair(uint32_t vbase, int gw, int lane, int kk,
-                                               bool second, const float (&p)[G]) {
+  // keys kq .. kq + 3 of the warp, the first `nv` (>= 1) of them valid; a row at or beyond the
+  // length may hold anything, NaN included, so it is not read (its weight is 0)
+  __device__ __forceinline__ void add_keys(uint32_t vbase, int gw, int lane, int kq, int nv) {
     const int d0 = lane * DPL;
-    const uint32_t a0 = swz(vbase, gw * kKeys + kk, d0 & ~7) + (d0 & 7) * 2;
-    const uint32_t a1 = swz(vbase, gw * kKeys + kk + 1, d0 & ~7) + (d0 & 7) * 2;
-    uint64_t v2[DPL];
+    uint32_t x[4], y[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      x[r] = 0u;
+      y[r] = 0u;
+      const uint32_t a = swz(vbase, gw * kKeys + kq + r, d0 & ~7) + (d0 & 7) * 2;
+      if (r < nv) {
+        if constexpr (DPL == 4)
+          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x[r]), "=r"(y[r]) : "r"(a));
+        else
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x[r]) : "r"(a));
+      }
+    }
+    uint64_t va[DPL], vb[DPL];  // column e of keys (kq, kq + 1) and (kq + 2, kq + 3)
+    va[0] = pack_f32x2(lo_f(x[0]), lo_f(x[1]));
+    va[1] = pack_f32x2(hi_f(x[0]), hi_f(x[1]));
+    vb[0] = pack_f32x2(lo_f(x[2]), lo_f(x[3]));
+    vb[1] = pack_f32x2(hi_f(x[2]), hi_f(x[3]));
     if constexpr (DPL == 4) {
-      uint32_t x0, y0, x1 = 0, y1 = 0;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x0), "=r"(y0) : "r"(a0));
-      if (second) asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x1), "=r"(y1) : "r"(a1));
-      v2[0] = pack_f32x2(lo_f(x0), lo_f(x1));
-      v2[1] = pack_f32x2(hi_f(x0), hi_f(x1));
-      v2[2] = pack_f32x2(lo_f(y0), lo_f(y1));
-      v2[3] = pack_f32x2(hi_f(y0), hi_f(y1));
-    } else {
-      uint32_t x0, x1 = 0;
-      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(a0));
-      if (second) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1) : "r"(a1));
-      v2[0] = pack_f32x2(lo_f(x0), lo_f(x1));
-      v2[1] = pack_f32x2(hi_f(x0), hi_f(x1));
+      va[2] = pack_f32x2(lo_f(y[0]), lo_f(y[1]));
+      va[3] = pack_f32x2(hi_f(y[0]), hi_f(y[1]));
+      vb[2] = pack_f32x2(lo_f(y[2]), lo_f(y[3]));
+      vb[3] = pack_f32x2(hi_f(y[2]), hi_f(y[3]));
     }
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      const uint64_t pp = pack_f32x2(__shfl_sync(0xffffffffu, p[hh], kk),
-                                     __shfl_sync(0xffffffffu, p[hh], kk + 1));
+      uint64_t p01, p23;
+      asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];"
+                   : "=l"(p01), "=l"(p23)
+                   : "r"(pw + (hh * kKeys + kq) * 4));
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o2[hh][e] = fma_f32x2(pp, v2[e], o2[hh][e]);
+      for (int e = 0; e < DPL; ++e) {
+        o2[hh][e] = fma_f32x2(p01, va[e], o2[hh][e]);
+        o2[hh][e] = fma_f32x2(p23, vb[e], o2[hh][e]);
+      }
     }
   }
 
