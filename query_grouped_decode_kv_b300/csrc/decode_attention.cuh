@@ -1635,8 +1635,8 @@ struct CcConsumer2 {
 };
 
 // ---------------------------------------------------------------------------------------------
-// The kernel. `Consumer` is MmaConsumer<D, WM, NW>, MmaConsumerF8<D, WM, NW> or
-// CcConsumer<D, G, NW, EB>; EB is the cache's bytes per element (2: bf16, 1: fp8 E4M3 codes).
+// The kernel. `Consumer` is MmaConsumer<D, WM, NW>, MmaConsumerF8<D, WM, NW>,
+// CcConsumer2<D, G> or CcConsumer<D, G, NW, EB>; EB: the cache's bytes per element (2 bf16, 1 fp8).
 // ---------------------------------------------------------------------------------------------
 template <int D, int EB, class Consumer, bool kTensorCores, int WM>
 __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)

@@ -235,7 +235,6 @@ AttnKernelChoice choice(int b) {
 // Up to 16 heads mma.sync keeps four warps (16 keys per warp is its smallest P V k-step).
 template <int D>
 AttnKernelChoice pick_kernel(Path path, int G, int b, int T) {
-  using mqa::CcConsumer;
   using mqa::MmaConsumer;
   if (path == kPathTcgen05) {
     // the group's heads padded to 16, 32 or 64 rows of the 128-row MMA tile
