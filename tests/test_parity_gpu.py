@@ -180,6 +180,31 @@ def test_peaked_attention_large_scale(mqa, shape):
     P.assert_close(out, out_ref, "scale 1.0")
 
 
+@pytest.mark.parametrize("d_h", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7])
+def test_cuda_core_path_at_every_group_size(mqa, G, d_h):
+    # every CUDA-core instance: lengths from 1 (a warp's 16 keys partly valid, odd counts, the
+    # last pair or quad of keys cut short) to several tiles, NaN past each length
+    case = P.make_case(3, 2 * G, 2, d_h, 1, 300, seed_id=700 + 10 * G + d_h // 64, tail="nan")
+    _, _, out_ref = P.oracle_step(case)
+    _, _, out = P.gpu_step(case, mqa)
+    assert mqa.get_device_status() == 0
+    P.assert_close(out, out_ref, f"CUDA cores G={G} d_h={d_h}")
+
+
+def test_growing_logits_force_rescales_on_cuda_cores(mqa):
+    # as below, on the CUDA-core consumer (G = 6): the running maximum rises tile after tile
+    case = P.make_case(2, 6, 1, 128, 600, 1500, seed_id=405, tail="nan")
+    k = case["k"].float()
+    ramp = torch.linspace(0.2, 3.0, k.shape[2]).view(1, 1, -1, 1)
+    case["k"] = (k * ramp).to(torch.bfloat16)
+    case["scale"] = 0.25
+    _, _, out_ref = P.oracle_step(case)
+    _, _, out = P.gpu_step(case, mqa)
+    assert mqa.get_device_status() == 0
+    P.assert_close(out, out_ref, "growing logits, CUDA cores")
+
+
 def test_growing_logits_force_rescales(mqa):
     # keys scaled up along the sequence, so the row maximum keeps rising tile after tile
     case = P.make_case(2, 32, 1, 128, 600, 1500, seed_id=404, tail="nan")
