@@ -1717,10 +1717,9 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   for (int k = 0; k < ntiles; ++k) {
     const int st = k % kStages;
     const bool mine = TG == 1 || k % TG == tg;
-    if (mine && !mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
-      if (!*sh.abort) give_up(sh, kSiteConsumerFull, k);
-      return;
-    }
+    // a segment's q and length are read before its first tile is waited for, so that their
+    // global-memory latency overlaps the tile's copy (every warp is past the previous segment's
+    // end: that end synchronised the consumer warps)
     if (k == 0 || cur.tile == 0) {
       L = __ldg(P.seq_lens + cur.bi);
       began_at_zero = (cur.tile == 0);
@@ -1737,6 +1736,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       } else {
         cons.begin_segment(P, cur.bi, cur.j, lane);
       }
+    }
+    if (mine && !mbar_wait_bounded(&sh.full[st], (k / kStages) & 1, P.timeout_ns, sh.abort)) {
+      if (!*sh.abort) give_up(sh, kSiteConsumerFull, k);
+      return;
     }
     const int tile_start = cur.tile * kTileKeys;
     const int valid = min(L - tile_start, kTileKeys);  // >= 1
