@@ -191,6 +191,17 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
+def step_shape(w, T: int = 1):
+    """The workload as a step with T new tokens per sequence runs it: room for the T new rows
+    in the cache, and the new rows' positions with the lengths attended (all T rows, by the
+    last token)."""
+    if T > 1:
+        import dataclasses
+        w = dataclasses.replace(w, extra_rows=T - 1)
+    pos, _ = inputs.positions_and_lengths(w)
+    return w, pos, (pos + T).to(torch.int32)
+
+
 def kv_bytes(w, lens, eb: int = 2, T: int = 1) -> int:
     """Algorithmic bytes of one fused decode-step launch (one layer) with T new tokens per
     sequence: K and V rows read once for all tokens (2 * g * L_b * d_h * eb over the batch; eb = 2
@@ -322,15 +333,11 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     w = inputs.WORKLOADS[args.workload]
     T = args.tokens
-    if T > 1:
-        import dataclasses
-        w = dataclasses.replace(w, extra_rows=T - 1)   # room for the T new rows
+    w, pos, lens = step_shape(w, T)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    pos, lens = inputs.positions_and_lengths(w)
-    lens = (pos + T).to(torch.int32)                    # all T new rows attended by the last
     pos_d, lens_d = pos.to(dev), lens.to(dev)
     layers, xs, outs = [], [], []
     table_d = None

@@ -1,0 +1,113 @@
+"""Host logic of bench.py on CPU.
+
+Covers the clock record, the stored DRAM traffic and its tie to the kernel sources, the variant
+keys, the L2-flush rule and the causal FLOP count. The benchmark's timing rules and its
+`roofline` object rest on these.
+"""
+from __future__ import annotations
+
+import json
+import re
+
+import pytest
+import torch
+
+import bench
+from query_grouped_decode_kv_b300 import inputs
+
+
+def _sampler_reading(tmp_path, lines):
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "clocks.csv")
+    (tmp_path / "clocks.csv").write_text("".join(ln + "\n" for ln in lines))
+    return s
+
+
+def test_clock_summary_takes_the_median_clock_and_the_active_reasons(tmp_path):
+    # nvidia-smi --format=csv,noheader,nounits rows, in the sampler's field order
+    rows = ["0, 2032, 2032, 600.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2032, 700.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+            "0, 2032, 2032, 650.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"]
+    got = _sampler_reading(tmp_path, rows).summary()
+    assert got["sm_mhz"] == 2032.0 and got["sm_max_mhz"] == 2032.0
+    assert got["reasons"] == ["sw_power_cap"]
+    assert got["samples"] == 3 and got["power_w_max"] == 700.0
+
+
+def test_clock_summary_reports_hardware_and_thermal_slowdowns(tmp_path):
+    rows = ["0, 1500, 2032, 900, 0x8, Active, Not Active, Active, Not Active",
+            "0, 1490, 2032, 910, 0x8, Not Active, Active, Not Active, Not Active"]
+    got = _sampler_reading(tmp_path, rows).summary()
+    assert got["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert got["sm_mhz"] == 1495.0
+
+
+def test_clock_summary_without_samples_says_unavailable(tmp_path):
+    got = _sampler_reading(tmp_path, []).summary()
+    assert got["reasons"] == ["unavailable"] and got["samples"] == 0 and got["sm_mhz"] is None
+
+
+def test_stored_traffic_is_used_only_on_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.json"
+    rec = {"source_hash": bench.kernel_source_hash(),
+           "per_workload": {"w": {"dram_bytes_per_launch": 123}}}
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("w") == 123
+    assert bench.recorded_traffic("another") is None
+    rec["source_hash"] = "0" * 16              # taken on other kernel sources
+    f.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("w") is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.json"))
+    assert bench.recorded_traffic("w") is None
+
+
+_KEY = re.compile(r"^(?P<wl>[a-z0-9_]+?)(?:_paged(?P<p>\d+))?(?P<f8>_fp8)?(?:_T(?P<T>\d+))?$")
+
+
+def test_committed_traffic_is_close_above_the_algorithmic_bytes():
+    # every stored capture must read at least the bytes the launch needs and not much more;
+    # a capture filed under the wrong variant or workload fails one side
+    with open(bench.TRAFFIC_FILE) as fh:
+        rec = json.load(fh)
+    assert rec["per_workload"], "no stored captures"
+    for key, entry in rec["per_workload"].items():
+        m = _KEY.match(key)
+        assert m and m.group("wl") in inputs.WORKLOADS, key
+        T = int(m.group("T") or 1)
+        w, _, lens = bench.step_shape(inputs.WORKLOADS[m.group("wl")], T)
+        algorithmic = bench.kv_bytes(w, lens, 1 if m.group("f8") else 2, T)
+        ratio = entry["dram_bytes_per_launch"] / algorithmic
+        assert 0.999 <= ratio <= 1.04, (key, ratio)
+
+
+def test_traffic_keys_name_the_variant():
+    w = inputs.WORKLOADS["gqa_70b_80l"]
+    assert bench.traffic_key(w) == "gqa_70b_80l"
+    assert bench.traffic_key(w, paged=16) == "gqa_70b_80l_paged16"
+    assert bench.traffic_key(w, paged=16, kv="fp8", T=4) == "gqa_70b_80l_paged16_fp8_T4"
+
+
+def test_l2_is_flushed_only_where_a_step_fits_twice_in_it():
+    assert bench.needs_l2_flush(inputs.WORKLOADS["gqa_8b"])
+    assert bench.needs_l2_flush(inputs.WORKLOADS["mqa_tiny"])
+    assert not bench.needs_l2_flush(inputs.WORKLOADS["gqa_70b_80l"])
+    assert not bench.needs_l2_flush(inputs.WORKLOADS["mha_ref"])
+
+
+@pytest.mark.parametrize("T", [1, 2, 4])
+def test_attention_flops_count_each_tokens_visible_keys(T):
+    w = inputs.WORKLOADS["mqa_long"]
+    lens = torch.tensor([5, 9, 64], dtype=torch.int32)
+    # token t of T (t = 0 oldest) sees the rows up to its own: L - (T - 1 - t) of them
+    brute = sum(4 * w.h * w.d_h * (int(L) - (T - 1 - t)) for L in lens for t in range(T))
+    assert bench.attention_flops(w, lens, T) == brute
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_step_shape_attends_every_new_row(T):
+    w0 = inputs.WORKLOADS["gqa_8b"]
+    w, pos, lens = bench.step_shape(w0, T)
+    assert w.n_max == w0.n_max + T - 1
+    assert torch.equal(lens, pos + T) and lens.dtype == torch.int32
+    assert int(lens.max()) <= w.n_max
