@@ -39,7 +39,6 @@ numbers, invariants and library routines.
 from __future__ import annotations
 
 import ctypes
-import os
 
 import numpy as np
 

@@ -4,7 +4,6 @@ oracle's C source (on the CPU), build it, and check that at least one pin reject
 from __future__ import annotations
 
 import os
-import shutil
 import subprocess
 
 import pytest

@@ -11,7 +11,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from tests import _parity as P
 
 pytestmark = pytest.mark.gpu
