@@ -1,49 +1,49 @@
 """Benchmark: the MQA/GQA decode step (KV append + grouped attention) on B300.
 
-Default workload: the 80-layer GQA decode step of a 70B-class model (b=8 sequences, h=64 query
-heads, g=8 KV heads, d_h=128, contexts uniform in [1024, 32768], about 86 GB of bf16 cache): one
-step appends one token's K/V and runs attention in all 80 layers back to back, one fused launch
-(mqa_decode_step) per layer.
-
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--paged PAGE_SIZE] [--kv bf16|fp8] [--tokens T]
 
-Prints one JSON line (rank 0). ``value`` is microseconds per decode step measured on the device
-with inputs resident in HBM (lower is better), from CUDA-graph replays of the whole step (every
-layer's append and attention): K replays back to back between two events, or, for workloads small
-enough to sit in L2, one graph per step that flushes L2 (a 252 MB write) and then times the step
-between its own event nodes. ``e2e`` is the same step driven eagerly through the public Python
-API from pinned host buffers (``layers.HostStepPipeline``, recorded once as a CUDA graph and
-replayed per step), with the host->device copy of the step's inputs (q, k_new, v_new of every
-layer) and the device->host read of its outputs inside the timed region of every step,
-overlapped with the kernels in runs of eight layers. ``roofline``
-reports the decode kernel's HBM throughput on algorithmic bytes (K/V rows read, q read, out
-written, new rows read and written) against the measured copy bandwidth; its launch durations
-come from a second timed pass of K steps whose graphs carry CUDA event nodes around every launch.
-``cpu_baseline`` times the fp64 CPU oracle on a bounded sample of the same workload. The reference
-arm (``--impl reference``) times that oracle as the reference.
+With no ``--workload`` the run measures all five decode workloads and prints one JSON line (rank
+0) whose headline is the 80-layer GQA step of a 70B-class model (b=8 sequences, h=64 query
+heads, g=8 KV heads, d_h=128, contexts uniform in [1024, 32768], about 86 GB of bf16 cache): one
+step appends one token's K/V and runs attention in all 80 layers back to back, one fused launch
+(``mqa_decode_step``) per layer. The four one-layer workloads (``mqa_tiny``, ``gqa_8b``,
+``mqa_long``, ``mha_ref``) are measured the same way and reported under ``configs``.
 
-``--kv fp8`` runs the same workload with every layer's caches held as fp8 E4M3 codes of the same
-draws, one scale per tensor (the largest magnitude maps to 448), through ``mqa_decode_step_fp8``;
-the algorithmic bytes count one byte per cached element.
+How a workload is timed (``value``, ``configs[*].us_per_step``): K steps are recorded as one CUDA
+graph through the public calls and replayed once between two events, after W eager warm-up
+steps; consecutive launches may overlap (``mqa_set_launch_overlap`` on the benchmark's stream:
+a launch's fill runs under the previous launch's drain). No step reads data that L2 could still
+hold from an earlier step: a multi-layer step reads every layer once (57 GB), and a one-layer
+workload rotates through as many distinct copies of its layer (other seeds, same shapes and
+lengths) as make four times the L2 between two reads of the same copy. The tiny workload cannot
+(one copy is 33 KB), so every one of its steps is preceded by an L2 flush (a 252 MB write) and
+bracketed by its own events, the flush untimed. ``us_per_launch`` is the step time divided by the
+launches in it, so launches x us_per_launch = us_per_step exactly; ``us_per_launch_isolated`` is
+one launch alone (L2 flushed before it, no overlap), the fixed cost included.
 
-``--tokens T`` runs every step with T new tokens per sequence (causal; speculative decoding):
-each sequence appends T rows and attends with T query rows per head, through
-``mqa_decode_step_multi``; the caches get T - 1 more rows, and every K/V byte is still read once
-per step.
+``roofline`` is the headline kernel's HBM throughput on algorithmic bytes (K/V rows read, q
+read, out written, new rows read and written) per launch divided by ``us_per_launch``, against the
+measured copy bandwidth. ``e2e`` is the same step driven eagerly through the C ABI every step
+(``layers.HostStepPipeline``: one ``mqa_decode_step`` call per layer from the host, no graph), with
+the host->device copy of the step's inputs (q, k_new, v_new of every layer, pos, seq_lens) from
+pinned memory and the device->host read of every layer's output inside the timed region of every
+step. ``cpu_baseline`` times the fp64 CPU oracle on one whole layer of the workload and scales by
+the layer count. The reference arm (``--impl reference``) times that oracle the same way, one
+whole layer per step.
 
-``--paged PAGE_SIZE`` runs the same workload with every layer's cache held in page pools (the rows
-each sequence attends, laid out in pages of PAGE_SIZE rows in a seeded random order, one page table
-shared by all layers) through the paged calls (``mqa_decode_step_paged``).
-
-Every layer of the default workload reads about 0.7 GB of cache (above the 126 MB L2) and a step
-reads about 57 GB, so no L2 flush is needed between its timed steps.
+``--kv fp8`` (caches as fp8 E4M3 codes of the same draws, one scale per tensor), ``--tokens T``
+(T new tokens per sequence, causal) and ``--paged PAGE_SIZE`` (caches in page pools, one seeded
+random page table shared by all layers) measure the named workload (default: the 80-layer step)
+in that variant alone.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -61,6 +61,8 @@ from query_grouped_decode_kv_b300 import inputs  # noqa: E402
 METRIC = "decode-attention µs/step and KV-cache GB/s as % of B300 HBM peak"
 UNIT = "us/step"
 FALLBACK_HBM_GBS = 6400.0
+HEADLINE = "gqa_70b_80l"
+ALL_WORKLOADS = ["mqa_tiny", "gqa_8b", "mqa_long", "mha_ref", "gqa_70b_80l"]
 KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
                   "query_grouped_decode_kv_b300/csrc/decode_attention_tc.cuh",
                   "query_grouped_decode_kv_b300/csrc/kv_append.cuh",
@@ -69,6 +71,10 @@ KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
                   "query_grouped_decode_kv_b300/csrc/mqa_abi.cu",
                   "include/mqa.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+L2_BYTES = 126 * 1024 * 1024
+ROTATION_L2_MULTIPLE = 4   # bytes read between two reads of the same copy, in L2 sizes
+MAX_COPIES = 8             # beyond this a workload is flushed instead of rotated
+PAGE_TABLE_SEED = 4242
 
 
 # ------------------------------------------------------------------------------------------------
@@ -195,7 +201,6 @@ def step_shape(w, T: int = 1):
     in the cache, and the new rows' positions with the lengths attended (all T rows, by the
     last token)."""
     if T > 1:
-        import dataclasses
         w = dataclasses.replace(w, extra_rows=T - 1)
     pos, _ = inputs.positions_and_lengths(w)
     return w, pos, (pos + T).to(torch.int32)
@@ -217,102 +222,41 @@ def attention_flops(w, lens, T: int = 1) -> int:
     return 4 * w.h * rows * w.d_h
 
 
-# ------------------------------------------------------------------------------------------------
-# the CPU oracle on a bounded sample (our arm's cpu_baseline and the reference arm)
-# ------------------------------------------------------------------------------------------------
-def oracle_sample_timing(w, target_s: float = 12.0, max_s: float = 40.0, T: int = 1):
-    """Time the fp64 oracle on whole sequences of this workload's shape (one layer, T new tokens
-    per sequence), adding sequences until about ``target_s`` seconds of CPU work; return
-    (us_per_step, details)."""
-    import numpy as np
-
-    import oracle
-    _, lens = inputs.positions_and_lengths(w)
-    threads = oracle.num_threads()
-    # sample sequences: one per length quantile, longest first, generated on the host
-    order = sorted(range(w.b), key=lambda i: -int(lens[i]))
-    spent, rows_done, seqs = 0.0, 0, []
-    for bi in order:
-        L = int(lens[bi])
-        sw = inputs.custom("oracle_sample", 1, w.h, w.g, w.d_h, L - 1, L - 1, kv_std=w.kv_std,
-                           wid=500 + bi)
-        if T > 1:
-            q, _, _ = inputs.multi_step_inputs(sw, T, 0, "cpu")
-        else:
-            q, _, _ = inputs.step_inputs(sw, 0, "cpu")
-        k, v = inputs.cache(sw, 0, "cpu")
-        qb = q.contiguous().view(torch.int16).numpy().view(np.uint16)
-        kb = k.view(torch.int16).numpy().view(np.uint16)
-        vb = v.view(torch.int16).numpy().view(np.uint16)
-        lb = np.array([L], dtype=np.int32)
-        t0 = time.perf_counter()
-        if T > 1:
-            oracle.decode_attention_multi(qb, kb, vb, lb, sw.scale, threads=threads)
-        else:
-            oracle.decode_attention(qb, kb, vb, lb, sw.scale, threads=threads)
-        spent += time.perf_counter() - t0
-        rows_done += L
-        seqs.append(L)
-        if spent >= target_s or spent >= max_s:
-            break
-    total_rows = int(lens.sum()) * w.layers
-    us_per_step = spent / rows_done * total_rows * 1e6
-    detail = (f"{len(seqs)} whole sequence(s) of one layer (lengths {seqs}, all {w.h} heads"
-              + (f", {T} tokens" if T > 1 else "") + "), "
-              f"{spent:.1f} s of oracle time, scaled by attended rows to {w.layers} layer(s) x "
-              f"{w.b} sequences")
-    return us_per_step, threads, detail, spent
-
-
-def run_reference(args, world, rank):
-    if rank != 0:
-        return 0
-    w = inputs.WORKLOADS[args.workload]
-    times = []
-    for it in range(args.warmup + args.steps):
-        us, threads, detail, _ = oracle_sample_timing(w, target_s=2.0, max_s=10.0)
-        if it >= args.warmup:
-            times.append(us)
-    us = statistics.median(times)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, args.paged, args.kv),
-        "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": detail},
-        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-    return 0
-
-
-L2_BYTES = 126 * 1024 * 1024
-
-
 def step_kv_bytes(w, eb: int = 2) -> int:
     _, lens = inputs.positions_and_lengths(w)
     return kv_bytes(w, lens, eb) * w.layers
 
 
+def copies_for(w, eb: int = 2) -> int:
+    """Distinct copies of a workload's layers that consecutive steps rotate through, so that
+    ROTATION_L2_MULTIPLE L2 sizes of other data are read between two reads of the same copy (a
+    multi-layer workload's own layers count as one copy each); 0 when that would take more than
+    MAX_COPIES (the workload is then flushed from L2 before every step instead)."""
+    n = math.ceil(ROTATION_L2_MULTIPLE * L2_BYTES / step_kv_bytes(w, eb))
+    n = max(n, 1)
+    return n if n <= MAX_COPIES else 0
+
+
 def needs_l2_flush(w, eb: int = 2) -> bool:
-    """A step that reads less than twice the L2 could be served from it on the next step."""
-    return step_kv_bytes(w, eb) < 2 * L2_BYTES
+    """Only a workload too small to rotate through distinct copies is flushed between steps."""
+    return copies_for(w, eb) == 0
 
 
-def workload_config(w, paged: int = 0, kv: str = "bf16"):
+def workload_config(w, paged: int = 0, kv: str = "bf16", T: int = 1):
     eb = 1 if kv == "fp8" else 2
+    n = copies_for(w, eb)
     return {"workload": w.name, "b": w.b, "h": w.h, "g": w.g, "d_h": w.d_h, "layers": w.layers,
             "context": [w.ctx_lo, w.ctx_hi], "n_max": w.n_max,
             "kv_dtype": ("fp8 e4m3, one scale per tensor (largest magnitude -> 448)"
                          if kv == "fp8" else "bf16"),
             "kv_layout": (f"paged, {paged}-row pages in a seeded random order" if paged
                           else "contiguous [b, g, n_max, d_h]"),
-            "l2": ("L2 flushed between steps (256 MB write)" if needs_l2_flush(w, eb)
-                   else "inputs larger than L2 (no flush)")}
-
-
-PAGE_TABLE_SEED = 4242
+            "l2": ("L2 flushed before every step (252 MB write, untimed)" if n == 0 else
+                   ("inputs larger than L2 (no flush; every layer read once per step)"
+                    if w.layers > 1 else
+                    f"inputs larger than L2: steps rotate through {n} copies of the layer "
+                    f"({n * step_kv_bytes(w, eb) / 2**20:.0f} MiB)")),
+            "tokens_per_step": T}
 
 
 def traffic_key(w, paged: int = 0, kv: str = "bf16", T: int = 1) -> str:
@@ -320,214 +264,340 @@ def traffic_key(w, paged: int = 0, kv: str = "bf16", T: int = 1) -> str:
             + (f"_T{T}" if T > 1 else ""))
 
 
+def path_name(w, kv: str = "bf16", T: int = 1) -> str:
+    """The inner-product path the library picks for this workload (its automatic rule)."""
+    G = w.h // w.g
+    if T > 1:
+        return f"mma.sync tensor cores, {T} tokens x {G} heads = {T * G} rows per KV head"
+    if G < 8:
+        return f"CUDA cores (fp32 FMA), G={G}" + (" over widened fp8 codes" if kv == "fp8" else "")
+    return f"mma.sync tensor cores, G={G}" + (" (fp16 over widened fp8 codes)" if kv == "fp8"
+                                              else " (bf16)")
+
+
+# ------------------------------------------------------------------------------------------------
+# the CPU oracle on whole layers (our arm's cpu_baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+class OracleLayer:
+    """Layer 0 of a workload on the host, ready for the fp64 oracle: q and the caches as bf16
+    bit patterns, with this step's rows appended."""
+
+    def __init__(self, w, T: int = 1):
+        import numpy as np
+
+        import oracle
+        self.w, self.T = w, T
+        w2, pos, lens = step_shape(w, T)
+        q, kn, vn = (inputs.multi_step_inputs(w2, T, 0, "cpu") if T > 1
+                     else inputs.step_inputs(w2, 0, "cpu"))
+        k, v = inputs.cache(w2, 0, "cpu")
+
+        def bits(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        self.q = bits(q)
+        self.k, self.v = bits(k), bits(v)
+        # the step's append, by the oracle itself (untimed)
+        if T > 1:
+            oracle.kv_append_multi(bits(kn), bits(vn), self.k, self.v, pos.numpy())
+        else:
+            oracle.kv_append(bits(kn), bits(vn), self.k, self.v, pos.numpy())
+        self.lens = lens.numpy().astype(np.int32)
+        self.scale = w2.scale
+        self.threads = oracle.num_threads()
+
+    def time_layer(self) -> float:
+        """Seconds of one whole-layer attention by the oracle (all sequences, all heads)."""
+        import oracle
+        t0 = time.perf_counter()
+        if self.T > 1:
+            oracle.decode_attention_multi(self.q, self.k, self.v, self.lens, self.scale,
+                                          threads=self.threads)
+        else:
+            oracle.decode_attention(self.q, self.k, self.v, self.lens, self.scale,
+                                    threads=self.threads)
+        return time.perf_counter() - t0
+
+    def describe(self, seconds: float) -> str:
+        w = self.w
+        return (f"one whole layer measured ({w.b} sequences, lengths {self.lens.tolist()}, all "
+                f"{w.h} heads" + (f", {self.T} tokens" if self.T > 1 else "")
+                + f"): {seconds:.2f} s of oracle time, x {w.layers} identical layer(s)")
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = inputs.WORKLOADS[args.workload or HEADLINE]
+    T = args.tokens
+    lay = OracleLayer(w, T)
+    times = []
+    for it in range(args.warmup + args.steps):
+        s = lay.time_layer()
+        if it >= args.warmup:
+            times.append(s)
+    us = statistics.median(times) * w.layers * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, args.paged, args.kv, T),
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": lay.threads, "kind": "oracle",
+                         "sample": lay.describe(statistics.median(times))
+                         + f"; median of {args.steps} timed layers"},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
+class Units:
+    """The launches of a workload on the device: one (layer state, step inputs, output) per layer
+    of a multi-layer workload, or per rotated copy of a one-layer workload. Step k launches
+    `per_step` consecutive units starting at unit k * per_step (mod the unit count)."""
+
+    def __init__(self, w, dev, T: int = 1, kv: str = "bf16", paged: int = 0):
+        from query_grouped_decode_kv_b300.layers import LayerState, StepInputs
+        self.w, self.T, self.kv, self.paged = w, T, kv, paged
+        self.eb = 1 if kv == "fp8" else 2
+        w2, pos, lens = step_shape(w, T)
+        self.w2, self.pos, self.lens = w2, pos, lens
+        self.pos_d, self.lens_d = pos.to(dev), lens.to(dev)
+        self.flush_each_step = needs_l2_flush(w, self.eb)
+        n_units = w.layers if w.layers > 1 else max(copies_for(w, self.eb), 1)
+        self.per_step = w.layers
+        self.layers, self.xs, self.outs = [], [], []
+        table_d = None
+        for li in range(n_units):
+            k, v = inputs.cache(w2, li, dev, tail="random")
+            if kv == "fp8":
+                ks, vs = inputs.amax_scale(k), inputs.amax_scale(v)
+                k, v = inputs.fp8_codes(k, ks), inputs.fp8_codes(v, vs)
+                self.layers.append(LayerState(k, v, fp8_scales=(ks, vs)))
+            elif paged:
+                k, v, table = inputs.page_pool(k, v, lens, paged, seed=PAGE_TABLE_SEED)
+                if table_d is None:
+                    table_d = table.to(dev)
+                self.layers.append(LayerState(k, v, table_d))
+            else:
+                self.layers.append(LayerState(k, v))
+            if T > 1:
+                self.xs.append(StepInputs(*inputs.multi_step_inputs(w2, T, li, dev)))
+                self.outs.append(torch.empty(w.b, T, w.h, w.d_h, dtype=torch.bfloat16,
+                                             device=dev))
+            else:
+                self.xs.append(StepInputs(*inputs.step_inputs(w2, li, dev)))
+                self.outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
+        self.bytes_per_launch = kv_bytes(w2, lens, self.eb, T)
+        self.flops_per_launch = attention_flops(w2, lens, T)
+
+    def launch(self, u: int, stream) -> None:
+        x = self.xs[u]
+        self.layers[u].step(x.q, x.k_new, x.v_new, self.pos_d, self.lens_d, self.outs[u],
+                            self.w2.scale, stream)
+
+    def step(self, k: int, stream) -> None:
+        n = len(self.layers)
+        for i in range(self.per_step):
+            self.launch((k * self.per_step + i) % n, stream)
+
+
+def timing_event():
+    return torch.cuda.Event(enable_timing=True, external=True)
+
+
+def time_steps(units: Units, stream, steps: int, flush, mqa, overlap: bool,
+               one_launch: bool = False) -> tuple[float, int]:
+    """Mean µs per step over `steps` steps recorded as one CUDA graph and replayed once (after
+    an untimed replay). With `flush`, every step is preceded by an L2 flush and bracketed by its
+    own event nodes (the flush untimed); else the graph runs between two events. `one_launch`:
+    every step is a single launch (unit k mod count). Returns (µs per step, launches per step)."""
+    mqa.set_launch_overlap(overlap, stream)
+    n = len(units.layers)
+    pairs = []
+    n0 = mqa.kernel_launch_count()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(steps):
+            if flush is not None:
+                flush.fill_(1)
+                pair = (timing_event(), timing_event())
+                pair[0].record(stream)
+            if one_launch:
+                units.launch(k % n, stream)
+            else:
+                units.step(k, stream)
+            if flush is not None:
+                pair[1].record(stream)
+                pairs.append(pair)
+    per_step = (mqa.kernel_launch_count() - n0) // steps
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0, "device status latched an error in a timed region"
+    ms = (sum(a.elapsed_time(b) for a, b in pairs) if flush is not None
+          else t0.elapsed_time(t1))
+    del g
+    return ms * 1000.0 / steps, per_step
+
+
+def measure_workload(w, dev, stream, args, mqa, flush_buf, T=1, kv="bf16", paged=0):
+    """One workload: warm-up, the overlapped step time and the isolated launch time. Returns
+    (summary dict, Units)."""
+    units = Units(w, dev, T, kv, paged)
+    with torch.cuda.stream(stream):
+        mqa.set_launch_overlap(True, stream)
+        for k in range(args.warmup):
+            units.step(k, stream)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
+    flush = flush_buf if units.flush_each_step else None
+    us_step, per_step = time_steps(units, stream, args.steps, flush, mqa, overlap=True)
+    us_iso, _ = time_steps(units, stream, min(args.steps, 20), flush_buf, mqa, overlap=False,
+                           one_launch=True)
+    mqa.set_launch_overlap(True, stream)
+    peak, _ = measured_peak_hbm()
+    us_launch = us_step / per_step
+    gbs = units.bytes_per_launch / (us_launch * 1e-6) / 1e9
+    summary = {
+        "us_per_step": us_step, "launches_per_step": per_step, "us_per_launch": us_launch,
+        "us_per_launch_isolated": us_iso,
+        "algorithmic_bytes_per_launch": units.bytes_per_launch,
+        "kv_gbs": gbs, "frac_of_hbm": gbs / peak,
+        "kv_gbs_isolated": units.bytes_per_launch / (us_iso * 1e-6) / 1e9,
+        "path": path_name(w, kv, T),
+        "kernel": "decode_attention_kernel (fused append + attention, mqa_decode_step"
+                  + ("_fp8" if kv == "fp8" else "_paged" if paged else "_multi" if T > 1 else "")
+                  + ")",
+        "l2": workload_config(w, paged, kv, T)["l2"],
+        "overlap": "consecutive launches overlap (mqa_set_launch_overlap)"
+                   + ("; the L2 flush between steps separates them" if flush is not None else ""),
+    }
+    return summary, units
+
+
+def e2e_host_driven(units: Units, dev, stream, steps: int, warmup: int, mqa):
+    """The step driven eagerly through the C ABI from pinned host buffers, every step: returns
+    (µs per step, h2d bytes, d2h bytes)."""
+    from query_grouped_decode_kv_b300.layers import HostStepBuffers, HostStepPipeline
+    w = units.w
+    n = units.per_step
+    lay = units.layers[:n]
+    buf = HostStepBuffers.allocate(n, w.b, w.h, w.g, w.d_h, dev, tokens=units.T)
+    for li in range(n):
+        x = units.xs[li]
+        buf.q_host[li].copy_(x.q.cpu())
+        buf.kn_host[li].copy_(x.k_new.cpu())
+        buf.vn_host[li].copy_(x.v_new.cpu())
+    buf.pos_host.copy_(units.pos)
+    buf.lens_host.copy_(units.lens)
+    pipeline = HostStepPipeline(lay, buf)
+    mqa.set_launch_overlap(True, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            pipeline.run(None, None, units.w2.scale, stream)
+    torch.cuda.synchronize()
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in events:
+            a.record(stream)
+            pipeline.run(None, None, units.w2.scale, stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0, "device status latched an error in the e2e region"
+    ms = sum(a.elapsed_time(b) for a, b in events)
+    return ms * 1000.0 / steps, buf.h2d_bytes, buf.d2h_bytes
+
+
 def run_ours(args, world, rank, local):
     import query_grouped_decode_kv_b300 as mqa
-    from query_grouped_decode_kv_b300.layers import (HostStepBuffers, HostStepPipeline,
-                                                     LayerState, StepInputs, decode_layers)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = inputs.WORKLOADS[args.workload]
-    T = args.tokens
-    w, pos, lens = step_shape(w, T)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-
-    pos_d, lens_d = pos.to(dev), lens.to(dev)
-    layers, xs, outs = [], [], []
-    table_d = None
-    for li in range(w.layers):
-        k, v = inputs.cache(w, li, dev, tail="random")
-        if args.kv == "fp8":
-            # codes of the same draws, one scale per tensor (largest magnitude -> 448)
-            ks, vs = inputs.amax_scale(k), inputs.amax_scale(v)
-            k, v = inputs.fp8_codes(k, ks), inputs.fp8_codes(v, vs)
-            layers.append(LayerState(k, v, fp8_scales=(ks, vs)))
-            xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
-            outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
-            continue
-        if args.paged:
-            # the same rows in page pools; one page table (a seeded shuffle of the pages that the
-            # attended rows need) shared by every layer
-            k, v, table = inputs.page_pool(k, v, lens, args.paged, seed=PAGE_TABLE_SEED)
-            if table_d is None:
-                table_d = table.to(dev)
-        layers.append(LayerState(k, v, table_d))
-        if T > 1:
-            xs.append(StepInputs(*inputs.multi_step_inputs(w, T, li, dev)))
-            outs.append(torch.empty(w.b, T, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
-            continue
-        xs.append(StepInputs(*inputs.step_inputs(w, li, dev)))
-        outs.append(torch.empty(w.b, w.h, w.d_h, dtype=torch.bfloat16, device=dev))
-    # small workloads fit in L2: flush it between steps by writing a buffer twice its size
-    eb = 1 if args.kv == "fp8" else 2
-    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if needs_l2_flush(w, eb)
-             else None)
+    T, kv, paged = args.tokens, args.kv, args.paged
+    headline = args.workload or HEADLINE
+    variant = T > 1 or kv != "bf16" or paged
+    others = [] if (args.workload or variant) else [n for n in ALL_WORKLOADS if n != headline]
     stream = torch.cuda.Stream(dev)
-    torch.cuda.synchronize()
-
-    def step(events=None, step_events=None):
-        if flush is not None:
-            flush.fill_(1)
-        if step_events is not None:
-            step_events[0].record(stream)
-        decode_layers(layers, xs, pos_d, lens_d, outs, w.scale, stream=stream, attn_events=events)
-        if step_events is not None:
-            step_events[1].record(stream)
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    def timing_event():
-        return torch.cuda.Event(enable_timing=True, external=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize()
-    assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
-
-    # ---- `value`: the step as CUDA-graph replays. Without an L2 flush, one graph replayed K
-    # times back to back between two events. With a flush, one graph per step whose event nodes
-    # bracket the step but not the flush before it, so the flush's time is not counted. ----
-    n0 = mqa.kernel_launch_count()
-    if flush is None:
-        step_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(step_graph, stream=stream):
-            step()
-        value_graphs, value_events = [step_graph] * args.steps, None
-    else:
-        value_graphs, value_events = [], []
-        for _ in range(args.steps):
-            pair = (timing_event(), timing_event())
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(step_events=pair)
-            value_graphs.append(g)
-            value_events.append(pair)
-    launches_per_step = (mqa.kernel_launch_count() - n0) // (1 if flush is None else args.steps)
-    # ---- per-launch attention durations: the same step with external event nodes around every
-    # attention launch, one graph per timed step so each launch keeps its own events ----
-    timed_graphs, ev = [], []
-    for _ in range(args.steps):
-        evs = [(timing_event(), timing_event()) for _ in range(w.layers)]
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(evs)
-        timed_graphs.append(g)
-        ev.append(evs)
-    with torch.cuda.stream(stream):
-        value_graphs[0].replay()
-        timed_graphs[0].replay()
-    torch.cuda.synchronize()
-
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    configs = {}
+    n_launch0 = mqa.kernel_launch_count()
     with ClockSampler(local) as clocks:
+        for name in others:
+            barrier()
+            summary, units = measure_workload(inputs.WORKLOADS[name], dev, stream, args, mqa,
+                                              flush_buf)
+            configs[name] = summary
+            del units
+            torch.cuda.empty_cache()
         barrier()
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            t_start.record(stream)
-            for g in value_graphs:
-                g.replay()
-            t_end.record(stream)
-        torch.cuda.synchronize()
+        summary, units = measure_workload(inputs.WORKLOADS[headline], dev, stream, args, mqa,
+                                          flush_buf, T, kv, paged)
+        configs[headline] = summary
         barrier()
-        # second timed region: kernel durations (event nodes add a little time between launches,
-        # so they stay out of the step time above)
-        with torch.cuda.stream(stream):
-            for g in timed_graphs:
-                g.replay()
-        torch.cuda.synchronize()
-        barrier()
-    launches = launches_per_step * args.steps
-    assert mqa.get_device_status() == 0, "device status latched an error in the timed region"
-    ms_total = (t_start.elapsed_time(t_end) if value_events is None
-                else sum(a.elapsed_time(b) for a, b in value_events))
-    attn_ms = [a.elapsed_time(b) for row in ev for (a, b) in row]
-    attn_avg_s = sum(attn_ms) / len(attn_ms) / 1000.0
-
-    # ---- end to end through host buffers: every step copies its inputs in from pinned host
-    # memory and its outputs out, overlapped with the kernels (layers.HostStepPipeline) ----
-    buf = HostStepBuffers.allocate(w.layers, w.b, w.h, w.g, w.d_h, dev, tokens=T)
-    for li, x in enumerate(xs):
-        buf.q_host[li].copy_(x.q.cpu())
-        buf.kn_host[li].copy_(x.k_new.cpu())
-        buf.vn_host[li].copy_(x.v_new.cpu())
-    pipeline = HostStepPipeline(layers, buf)
-    h2d, d2h = buf.h2d_bytes, buf.d2h_bytes
-
-    def e2e_step(step_graph_e2e, pair=None):
-        # an L2 flush (small workloads only) runs before the step's start event
-        if flush is not None:
-            flush.fill_(1)
-        if pair is not None:
-            pair[0].record(stream)
-        step_graph_e2e.replay()
-        if pair is not None:
-            pair[1].record(stream)
-
-    # the step through the public API once eagerly (it sizes the workspace), then as one graph
-    with torch.cuda.stream(stream):
-        pipeline.run(pos_d, lens_d, w.scale, stream)
-    torch.cuda.synchronize()
-    e2e_graph = pipeline.capture(pos_d, lens_d, w.scale, stream)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step(e2e_graph)
-    torch.cuda.synchronize()
-    e2e_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
+    launches_timed = summary["launches_per_step"] * args.steps
+    e2e_us, h2d, d2h = e2e_host_driven(units, dev, stream, args.steps, args.warmup, mqa)
     barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for pair in e2e_events:
-            e2e_step(e2e_graph, pair)
-    torch.cuda.synchronize()
-    barrier()
-    assert mqa.get_device_status() == 0, "device status latched an error in the e2e region"
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_events)
 
-    # ---- max over ranks ----
-    ms_per_step = ms_total / args.steps
-    e2e_per_step = e2e_ms / args.steps
+    us_step, us_launch, e2e_step = summary["us_per_step"], summary["us_per_launch"], e2e_us
     if world > 1:
-        ms_per_step, e2e_per_step, attn_avg_s = max_over_ranks(
-            [ms_per_step, e2e_per_step, attn_avg_s], dev)
+        us_step, us_launch, e2e_step = max_over_ranks([us_step, us_launch, e2e_step], dev)
 
     if rank == 0:
+        w = units.w
         peak, peak_kind = measured_peak_hbm()
-        nbytes = kv_bytes(w, lens, eb, T)
-        achieved = nbytes / attn_avg_s / 1e9
-        traffic = recorded_traffic(traffic_key(w, args.paged, args.kv, T))
-        value_us = whole_job_us_per_step(ms_per_step, world)
-        cb_us, cb_threads, cb_detail, _ = oracle_sample_timing(w, T=T)
+        nbytes = units.bytes_per_launch
+        achieved = nbytes / (us_launch * 1e-6) / 1e9
+        traffic = recorded_traffic(traffic_key(w, paged, kv, T))
+        value_us = whole_job_us_per_step(us_step / 1000.0, world)
+        lay = OracleLayer(w, T)
+        cb_s = lay.time_layer()
+        cb_us = cb_s * w.layers * 1e6
         line = {
             "metric": METRIC, "value": value_us, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_step / 1000.0,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16" if args.kv == "fp8" else "bf16",
-            "data": "synthetic", "config": dict(workload_config(w, args.paged, args.kv),
-                                                tokens_per_step=T),
+            "dtype": "f16" if kv == "fp8" else "bf16",
+            "data": "synthetic", "config": workload_config(w, paged, kv, T),
             "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
-            "attention_us_per_layer": attn_avg_s * 1e6,
+            "attention_us_per_layer": us_launch,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"{peak_kind} copy bandwidth",
-                         "kernel": "decode_attention_kernel (one fused append + attention launch per layer)",
+                         "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                         "kernel": summary["kernel"],
                          "algorithmic_bytes_per_launch": nbytes,
-                         "flops_per_launch": attention_flops(w, lens, T)},
-            "e2e": {"value": whole_job_us_per_step(e2e_per_step, world), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": int(launches),
+                         "us_per_launch": us_launch,
+                         "us_per_launch_from": "step time / launches per step "
+                                               "(launches x us_per_launch = ms_per_step)",
+                         "flops_per_launch": units.flops_per_launch},
+            "configs": configs,
+            "e2e": {"value": whole_job_us_per_step(e2e_step / 1000.0, world), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": f"eager: {units.per_step} C-ABI call(s) per step from the host, "
+                           "pinned-host copies in and out inside every step's timed region"},
+            "gpu_launches": int(launches_timed),
+            "gpu_launches_all_configs": int(mqa.kernel_launch_count() - n_launch0),
             "clocks": clocks.summary(),
-            "cpu_baseline": {"value": cb_us, "unit": UNIT, "cores": cb_threads, "kind": "oracle",
-                             "sample": cb_detail},
+            "cpu_baseline": {"value": cb_us, "unit": UNIT, "cores": lay.threads, "kind": "oracle",
+                             "sample": lay.describe(cb_s)},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -542,7 +612,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa_70b_80l", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(inputs.WORKLOADS),
+                    help="measure this workload alone (default: all five, the 80-layer step "
+                         "as the headline)")
     ap.add_argument("--paged", type=int, default=0, metavar="PAGE_SIZE",
                     help="keep the caches in page pools of this many rows (0: contiguous)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",

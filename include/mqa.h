@@ -308,6 +308,41 @@ MQA_API int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_ca
                                          mqa_bf16* out, int b, int h, int g, int d_h, int n_max,
                                          float scale, void* stream);
 
+/*
+ * mqa_set_launch_overlap -- let the decode-attention launches on `stream` overlap the kernel
+ * ahead of each of them on that stream (programmatic dependent launch). Off by default. The pages
+ * have no counterpart; this is a scheduling choice of the library.
+ *
+ * Why: a launch has a fixed part at both ends -- the pipeline fill before its first tile arrives
+ * and, after its last tile, the combine of the pieces of sequences split across CTAs -- during
+ * which HBM idles. With overlap on, a launch may start on SMs that the launch ahead of it has
+ * already left, so its fill (and its first tiles) run under the other launch's drain. This
+ * matters for back-to-back decode steps of many layers, where each launch is a few hundred
+ * microseconds at most.
+ *
+ * Contract (what the caller guarantees when it turns overlap on for a stream): the kernel that
+ * precedes a call on the stream writes none of that call's inputs -- q, k_new, v_new, pos,
+ * seq_lens, the page table, and every cache row the call reads other than the rows it appends.
+ * The consecutive layers of one decode step, whose inputs are all in place before the first
+ * layer is enqueued, satisfy it; so does a stream where only this library's decode launches
+ * follow one another on distinct caches. A stream that runs mqa_kv_append and then
+ * mqa_decode_attention does NOT (the append writes a row the attention reads): use the fused
+ * mqa_decode_step there, or leave overlap off.
+ *
+ * What the library guarantees in exchange: until the kernel ahead of it has finished and its
+ * writes are visible, a call only reads; it writes nothing -- no output, no appended cache row,
+ * no scratch -- before then. Results are bit for bit those of the same calls with overlap off.
+ * The setting applies to the attention, step, paged, fp8, multi-token and no-alloc calls on the
+ * mma.sync and CUDA-core paths (the forced tcgen05 path never overlaps), and to launches captured
+ * into a CUDA graph, where it becomes a programmatic edge.
+ *
+ *   stream   cudaStream_t, on the current device (NULL: the legacy default stream)
+ *   on       1 to allow overlap, 0 to forbid it
+ *
+ * Returns MQA_OK, MQA_ERR_INVALID_ARG (on not 0 or 1) or MQA_ERR_CUDA.
+ */
+MQA_API int mqa_set_launch_overlap(void* stream, int on);
+
 /* A static, human-readable name for a status code. Never returns NULL. */
 MQA_API const char* mqa_status_string(int status);
 
@@ -342,8 +377,11 @@ MQA_API int mqa_debug_timeout_site(int* site_out);
  *
  * mqa_debug_stall: with on = 1, the consumer warps of every following attention launch first wait
  * on a barrier that nothing completes, so that wait runs out after the wait limit and the launch
- * reports MQA_ERR_TIMEOUT at site 14 (a flag nothing sets; no fault and no hang). on = 0 turns it
- * off. Returns MQA_OK, or MQA_ERR_INVALID_ARG for another value.
+ * reports MQA_ERR_TIMEOUT at site 14 (a flag nothing sets; no fault and no hang). With on = 2 the
+ * mma.sync and CUDA-core kernels wait there instead right after a CTA has counted its arrival at a
+ * sequence split across CTAs, before any merge, so the launch gives up with arrival counters left
+ * non-zero (the tcgen05 kernel stalls at its start, as with 1). on = 0 turns it off. Returns
+ * MQA_OK, or MQA_ERR_INVALID_ARG for another value.
  */
 MQA_API int mqa_debug_set_wait_limit_ns(uint64_t ns);
 MQA_API int mqa_debug_stall(int on);

@@ -72,6 +72,8 @@ _lib.mqa_debug_set_wait_limit_ns.restype = _i32
 _lib.mqa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
 _lib.mqa_debug_override.restype = _i32
 _lib.mqa_debug_override.argtypes = [_i32, _i32]
+_lib.mqa_set_launch_overlap.restype = _i32
+_lib.mqa_set_launch_overlap.argtypes = [_vp, _i32]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_TIMEOUT = range(6)
 
@@ -122,10 +124,13 @@ def debug_set_wait_limit_ns(ns: int = 0) -> None:
         raise MqaError(st, "mqa_debug_set_wait_limit_ns")
 
 
-def debug_stall(on: bool) -> None:
+def debug_stall(on: bool | int) -> None:
     """Testing hook: make the consumer warps of following launches wait on a barrier nothing
-    completes, so each launch times out after the wait limit."""
-    st = _lib.mqa_debug_stall(1 if on else 0)
+    completes, so each launch times out after the wait limit: before their first tile (True or
+    1), or right after counting their first arrival at a split sequence (2), which leaves arrival
+    counters non-zero."""
+    mode = int(on) if not isinstance(on, bool) else (1 if on else 0)
+    st = _lib.mqa_debug_stall(mode)
     if st:
         raise MqaError(st, "mqa_debug_stall")
 
@@ -142,6 +147,17 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int) -> None:
     if not t.is_cuda or t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor with {ndim} dims, "
                          f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def set_launch_overlap(on: bool, stream=None) -> None:
+    """Allow (or forbid) the attention launches on ``stream`` to start before the kernel ahead
+    of them on it has finished (programmatic dependent launch). The caller guarantees that the
+    kernel preceding each call writes none of the call's inputs (q, new rows, positions,
+    lengths, page table, the cache rows it reads besides the ones it appends); see
+    ``mqa_set_launch_overlap`` in ``include/mqa.h``."""
+    st = _lib.mqa_set_launch_overlap(_vp(_stream_handle(stream)), 1 if on else 0)
+    if st:
+        raise MqaError(st, "mqa_set_launch_overlap")
 
 
 def get_device_status(stream=None) -> int:

@@ -78,7 +78,9 @@ struct DecodeParams {
   float scale_log2;           // scale * log2(e)
   unsigned long long timeout_ns;  // limit of every in-kernel wait
   unsigned long long drain_ns;    // limit of the waits for a CTA's own work in flight at exit
-  int debug_stall;                // testing: consumers first wait on a barrier nothing completes
+  int debug_stall;                // testing: consumers wait on a barrier nothing completes,
+                                  // 1: before their first tile; 2: right after counting their
+                                  // first arrival at a split segment (before any merge)
   // Fused append (mqa_decode_step): this step's K/V rows, token t written at row pos[bi] + t of
   // the caches before any tile holding that row is loaded. All null when the call only attends.
   const int32_t* pos;         // [b]
@@ -249,6 +251,7 @@ __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int
       if (c == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
+    pdl_wait();  // a cache row is written only once the kernel ahead on the stream has finished
     P.k_rows[dst + c] = new_row_chunk<EB>(P.k_new + src_row * CS, c, P.kq_scale);
     P.v_rows[dst + c] = new_row_chunk<EB>(P.v_new + src_row * CS, c, P.vq_scale);
   }
@@ -273,13 +276,17 @@ __device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int
 }
 
 // The new rows of segment (bi, j) that tile `tile` holds ([p0, p0 + T) meets the tile's rows),
-// written by the whole warp before the tile's copy; the caller fences and syncs the warp.
+// written by the whole warp before the tile's copy; the caller fences and syncs the warp. The
+// writes wait for the kernel ahead on the stream to finish (programmatic dependent launch): that
+// kernel may still be reading the rows being replaced.
 template <int D, int EB>
 __device__ __forceinline__ bool write_tile_rows(const DecodeParams& P, int bi, int j, int tile,
                                                 int p0, int lane) {
   const int lo = max(p0, tile * kTileKeys), hi = min(p0 + P.T, (tile + 1) * kTileKeys);
+  if (lo >= hi) return false;
+  pdl_wait();
   for (int p = lo; p < hi; ++p) write_new_row<D, EB>(P, bi, j, p - p0, p, lane);
-  return lo < hi;
+  return true;
 }
 
 // The tile count of every sequence as the CTAs see it: the exclusive prefix `cs` of the tile sums
@@ -571,6 +578,11 @@ __device__ __forceinline__ bool finish_split_segment(const DecodeParams& P, cons
     *sh.merge = (before + 1u == pc.count()) ? 1 : 0;
   }
   if (!consumer_sync(sh, cphase, P.timeout_ns)) return false;
+  if (P.debug_stall == 2 && !mbar_wait_bounded(sh.stall, 0, P.timeout_ns, sh.abort)) {
+    // testing: give up with this arrival counted and no merge done, leaving the counter dirty
+    if (!*sh.abort) give_up(sh, kSiteStall, 0);
+    return false;
+  }
   if (*sh.merge) {
     __threadfence();
     if (!merge_split_segment<D, NW, CR>(P, sh, cphase, bi, j, seg, pc)) return false;
@@ -633,6 +645,7 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
     const int L = __ldg(P.seq_lens + bi);
     if (L >= P.T && L <= P.n_max) continue;
     if (threadIdx.x == 0) latch_status(kStatusDeviceBounds);
+    pdl_wait();
     __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.T * P.h * D;
     for (int e = threadIdx.x; e < P.T * P.h * D; e += nthreads) ob[e] = __float2bfloat16_rn(0.f);
   }
@@ -1651,6 +1664,11 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   SharedLayout sh = carve_shared<D, EB, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // Programmatic dependent launch (when the host asked for it): the next launch on the stream may
+  // be scheduled now; its CTAs take SMs as this grid's CTAs exit. This kernel in turn reads its
+  // inputs at once but writes global memory (outputs, partial states, counters, appended cache
+  // rows) only after pdl_wait(), i.e. once the kernel ahead of it has finished.
+  pdl_launch_dependents();
 
   // ---- barriers, then the tiles of every sequence and their prefix ---------------------------
   __shared__ uint32_t chunk_tiles[kThreads + 1];
@@ -1710,7 +1728,8 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   cur.start(x0, sh.tix);
   int L = 0;
   bool began_at_zero = false;
-  if (P.debug_stall && !mbar_wait_bounded(sh.stall, 0, P.timeout_ns, sh.abort)) {
+  bool after_dep = false;  // pdl_wait() done: global writes allowed
+  if (P.debug_stall == 1 && !mbar_wait_bounded(sh.stall, 0, P.timeout_ns, sh.abort)) {
     if (!*sh.abort) give_up(sh, kSiteStall, 0);
     return;
   }
@@ -1786,6 +1805,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
       if (!consumer_sync(sh, cphase, P.timeout_ns)) {
         if (!*sh.abort) give_up(sh, kSiteConsumerSync, k);
         return;
+      }
+      if (!after_dep) {
+        pdl_wait();
+        after_dep = true;
       }
       combine_and_store<D, NW, CR>(P, sh, cur.bi, cur.j, complete,
                                    static_cast<int>(blockIdx.x) + seg, typename Consumer::Rows{});

@@ -159,8 +159,18 @@ int grow_buffer(DeviceBuffer& buf, size_t bytes, cudaStream_t stream, bool zero)
   return MQA_OK;
 }
 
+// The scratch a launch uses: the partial states, the arrival counters, and whether the whole
+// counter region (`counter_region_bytes`, all the counters any call may use there) must be zeroed
+// first.
+struct Scratch {
+  void* partials = nullptr;
+  unsigned int* counters = nullptr;
+  size_t counter_region_bytes = 0;
+  bool clear = false;
+};
+
 int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t counter_bytes,
-                  void** partials, unsigned int** counters, bool* clear) {
+                  Scratch* out) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   Workspace& ws = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
   if (int st = grow_buffer(ws.partials, partial_bytes, stream, false)) return st;
@@ -169,11 +179,25 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t cou
     if (int st = grow_buffer(ws.counters, counter_bytes, stream, true)) return st;
     ws.clean_epoch = epoch;
   }
-  *clear = ws.clean_epoch != epoch;
+  // After a timeout any counter of the region may be dirty, not only the ones this call uses, so
+  // the clear (and with it the clean mark) covers the whole region.
+  out->clear = ws.clean_epoch != epoch;
   ws.clean_epoch = epoch;
-  *partials = ws.partials.ptr;
-  *counters = static_cast<unsigned int*>(ws.counters.ptr);
+  out->partials = ws.partials.ptr;
+  out->counters = static_cast<unsigned int*>(ws.counters.ptr);
+  out->counter_region_bytes = ws.counters.bytes;
   return MQA_OK;
+}
+
+// Streams whose decode-attention launches may overlap the kernel ahead of them
+// (mqa_set_launch_overlap), keyed by (device, stream).
+std::mutex g_overlap_mutex;
+std::map<std::pair<int, uintptr_t>, bool> g_overlap;
+
+bool overlap_on(int dev, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_overlap_mutex);
+  auto it = g_overlap.find({dev, reinterpret_cast<uintptr_t>(stream)});
+  return it != g_overlap.end() && it->second;
 }
 
 struct DeviceInfo {
@@ -217,6 +241,7 @@ struct AttnKernelChoice {
   int threads = 0;
   size_t smem = 0;
   bool wide = false;  // eight consumer warps with a setmaxnreg split: check the register count
+  bool pdl = false;   // writes global memory only after griddepcontrol.wait (may overlap)
 };
 
 template <class Consumer, int D, int EB, bool TC, int WM>
@@ -226,6 +251,7 @@ AttnKernelChoice choice(int b) {
   c.threads = mqa::threads_of(Consumer::kWarps);
   c.smem = mqa::smem_bytes<D, EB>(Consumer::kWarps, Consumer::kCombRows);
   c.wide = Consumer::kWarps == 8;
+  c.pdl = true;
   return c;
 }
 
@@ -412,11 +438,12 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   return MQA_OK;
 }
 
-// `clear_counters`: zero the per-segment arrival counters first. They are zero whenever the
+// `sc.clear`: zero the scratch's whole counter region first. The counters are zero whenever the
 // scratch is fresh and every finished call leaves them at zero; only a call that gave up
-// (MQA_ERR_TIMEOUT) can leave them dirty.
-int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
-                  bool clear_counters) {
+// (MQA_ERR_TIMEOUT) can leave them dirty, and it may have used more of them than this call does.
+int launch_decode(const DecodePlan& p, const Scratch& sc) {
+  void* partials = sc.partials;
+  unsigned int* counters = sc.counters;
   CUtensorMap tmk, tmv;
   if (p.paged.table) {
     const long long pages_g = static_cast<long long>(p.paged.num_pages) * p.g;
@@ -436,8 +463,8 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   P.part_ml = partials ? reinterpret_cast<float2*>(static_cast<char*>(partials) + p.part_o_bytes)
                        : nullptr;
   P.seg_arrivals = counters;
-  if (counters && clear_counters &&
-      cudaMemsetAsync(counters, 0, p.counter_bytes, p.stream) != cudaSuccess)
+  if (counters && sc.clear &&
+      cudaMemsetAsync(counters, 0, sc.counter_region_bytes, p.stream) != cudaSuccess)
     return MQA_ERR_CUDA;
   P.b = p.b;
   P.h = p.h;
@@ -472,7 +499,22 @@ int launch_decode(const DecodePlan& p, void* partials, unsigned int* counters,
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;
   if (p.paged.table && p.path == kPathTcgen05) return MQA_ERR_UNSUPPORTED;
   if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
-  kc.fn<<<static_cast<unsigned>(p.ctas), kc.threads, kc.smem, p.stream>>>(tmk, tmv, P);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.ctas));
+  cfg.blockDim = dim3(static_cast<unsigned>(kc.threads));
+  cfg.dynamicSmemBytes = kc.smem;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  if (kc.pdl && overlap_on(p.dev, p.stream)) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, kc.fn, tmk, tmv, P) != cudaSuccess) {
+    cudaGetLastError();
+    return MQA_ERR_CUDA;
+  }
   g_launches.fetch_add(1);
   return launch_error();
 }
@@ -494,7 +536,7 @@ struct NoallocScratch {
 std::mutex g_noalloc_mutex;
 std::map<int, NoallocScratch> g_noalloc_addr;  // device ordinal -> its copy of the array
 
-int noalloc_scratch_address(int dev, void** out, bool* clear) {
+int noalloc_scratch_address(int dev, Scratch* out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   auto it = g_noalloc_addr.find(dev);
   if (it == g_noalloc_addr.end()) {
@@ -505,9 +547,13 @@ int noalloc_scratch_address(int dev, void** out, bool* clear) {
     it = g_noalloc_addr.emplace(dev, sc).first;
   }
   const uint64_t epoch = g_timeout_epoch.load();
-  *clear = it->second.clean_epoch != epoch;
+  // the counters keep a fixed leading region of the array, so no other call's partial states
+  // ever land on them; after a timeout that whole region is cleared
+  out->clear = it->second.clean_epoch != epoch;
   it->second.clean_epoch = epoch;
-  *out = it->second.ptr;
+  out->counters = static_cast<unsigned int*>(it->second.ptr);
+  out->partials = static_cast<char*>(it->second.ptr) + kNoallocCounterBytes;
+  out->counter_region_bytes = kNoallocCounterBytes;
   return MQA_OK;
 }
 
@@ -555,13 +601,22 @@ int mqa_get_device_status(void* stream, int* status_out) {
   return MQA_OK;
 }
 
+int mqa_set_launch_overlap(void* stream, int on) {
+  if (on != 0 && on != 1) return MQA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_overlap_mutex);
+  g_overlap[{dev, reinterpret_cast<uintptr_t>(stream)}] = on != 0;
+  return MQA_OK;
+}
+
 int mqa_debug_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns == 0 ? kWaitLimitNs : ns);
   return MQA_OK;
 }
 
 int mqa_debug_stall(int on) {
-  if (on != 0 && on != 1) return MQA_ERR_INVALID_ARG;
+  if (on < 0 || on > 2) return MQA_ERR_INVALID_ARG;
   g_debug_stall.store(on);
   return MQA_OK;
 }
@@ -612,15 +667,12 @@ int mqa_decode_attention(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_b
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan))
     return st;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
@@ -637,15 +689,12 @@ int mqa_decode_step(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_kv_append_paged(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_pool,
@@ -699,15 +748,12 @@ int mqa_decode_attention_paged(const mqa_bf16* q, const mqa_bf16* k_pool, const 
                            &plan))
     return st;
   plan.paged = pg;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
@@ -733,15 +779,12 @@ int mqa_decode_step_paged(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 // fp8 caches: the scales must be finite and positive; the kernels read d_h = 128 rows.
@@ -790,15 +833,12 @@ int mqa_decode_attention_fp8(const mqa_bf16* q, const uint8_t* k_cache, const ui
   plan.eb = 1;
   plan.k_scale = k_scale;
   plan.v_scale = v_scale;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
@@ -821,15 +861,12 @@ int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_kv_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
@@ -867,15 +904,12 @@ int mqa_decode_attention_multi(const mqa_bf16* q, const mqa_bf16* k_cache,
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan, T))
     return st;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
@@ -892,15 +926,12 @@ int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;
-  void* partials = nullptr;
-  unsigned int* counters = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes,
-                               &partials, &counters, &clear))
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
       return st;
   }
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
@@ -914,16 +945,11 @@ int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
   if (plan.counter_bytes > kNoallocCounterBytes ||
       plan.partial_bytes > MQA_NOALLOC_SCRATCH_BYTES - kNoallocCounterBytes)
     return MQA_ERR_UNSUPPORTED;
-  void* scratch = nullptr;
-  bool clear = false;
+  Scratch sc;
   if (plan.ctas > 1) {
-    if (int st = noalloc_scratch_address(plan.dev, &scratch, &clear)) return st;
+    if (int st = noalloc_scratch_address(plan.dev, &sc)) return st;
   }
-  // the counters keep a fixed leading region of the array, so no other call's partial states
-  // ever land on them
-  unsigned int* counters = static_cast<unsigned int*>(scratch);
-  void* partials = scratch ? static_cast<char*>(scratch) + kNoallocCounterBytes : nullptr;
-  return launch_decode(plan, partials, counters, clear);
+  return launch_decode(plan, sc);
 }
 
 }  // extern "C"

@@ -95,6 +95,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization may
+// start while the kernel ahead of it on the stream is still running; `griddepcontrol.wait`
+// blocks the calling thread until that kernel has completed and its memory writes are visible
+// (it returns at once when the launch has no such dependency). `launch_dependents` tells the
+// hardware that the next kernel on the stream may be scheduled as soon as every CTA of this grid
+// has signalled or exited; that kernel still takes an SM only once one is free.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------------------------
 // Warpgroup register reallocation (all 128 threads of a warpgroup execute the same one).
 // ---------------------------------------------------------------------------------------------
 // One thread of the (fully active) warp is elected, the lowest active lane. A bulk tensor copy

@@ -105,7 +105,8 @@ def decode_layers(layers: list[LayerState], step_in: list[StepInputs], pos: torc
 @dataclasses.dataclass
 class HostStepBuffers:
     """A whole step's per-layer inputs and outputs, packed layer-major so that a run of layers is
-    one contiguous block: pinned host copies and their device mirrors."""
+    one contiguous block, plus the step's append positions and attended lengths (shared by all
+    layers): pinned host copies and their device mirrors."""
     q_host: torch.Tensor      # [layers, b, h, d_h] bf16, pinned
     kn_host: torch.Tensor     # [layers, b, g, d_h]
     vn_host: torch.Tensor
@@ -114,6 +115,10 @@ class HostStepBuffers:
     kn_dev: torch.Tensor
     vn_dev: torch.Tensor
     out_dev: torch.Tensor
+    pos_host: torch.Tensor    # [b] int32, pinned
+    lens_host: torch.Tensor   # [b] int32, pinned
+    pos_dev: torch.Tensor
+    lens_dev: torch.Tensor
 
     @classmethod
     def allocate(cls, layers: int, b: int, h: int, g: int, d_h: int, device,
@@ -122,19 +127,23 @@ class HostStepBuffers:
         > 1, for T ([layers, b, T, h, d_h] ...)."""
         t = () if tokens == 1 else (tokens,)
 
-        def host(*shape):
-            return torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+        def host(*shape, dtype=torch.bfloat16):
+            return torch.empty(shape, dtype=dtype).pin_memory()
 
-        def dev(*shape):
-            return torch.empty(shape, dtype=torch.bfloat16, device=device)
+        def dev(*shape, dtype=torch.bfloat16):
+            return torch.empty(shape, dtype=dtype, device=device)
         return cls(host(layers, b, *t, h, d_h), host(layers, b, *t, g, d_h),
                    host(layers, b, *t, g, d_h), host(layers, b, *t, h, d_h),
                    dev(layers, b, *t, h, d_h), dev(layers, b, *t, g, d_h),
-                   dev(layers, b, *t, g, d_h), dev(layers, b, *t, h, d_h))
+                   dev(layers, b, *t, g, d_h), dev(layers, b, *t, h, d_h),
+                   host(b, dtype=torch.int32), host(b, dtype=torch.int32),
+                   dev(b, dtype=torch.int32), dev(b, dtype=torch.int32))
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.q_host, self.kn_host, self.vn_host))
+        return sum(t.numel() * t.element_size()
+                   for t in (self.q_host, self.kn_host, self.vn_host, self.pos_host,
+                             self.lens_host))
 
     @property
     def d2h_bytes(self) -> int:
@@ -160,8 +169,11 @@ class HostStepPipeline:
             self.ready = [torch.cuda.Event() for _ in self.runs]
             self.done = [torch.cuda.Event() for _ in self.runs]
 
-    def _copy_in(self, c0: int, c1: int) -> None:
+    def _copy_in(self, c0: int, c1: int, positions: bool = False) -> None:
         b = self.buf
+        if positions:
+            b.pos_dev.copy_(b.pos_host, non_blocking=True)
+            b.lens_dev.copy_(b.lens_host, non_blocking=True)
         b.q_dev[c0:c1].copy_(b.q_host[c0:c1], non_blocking=True)
         b.kn_dev[c0:c1].copy_(b.kn_host[c0:c1], non_blocking=True)
         b.vn_dev[c0:c1].copy_(b.vn_host[c0:c1], non_blocking=True)
@@ -172,23 +184,28 @@ class HostStepPipeline:
             self.layers[li].step(b.q_dev[li], b.kn_dev[li], b.vn_dev[li], pos, seq_lens,
                                  b.out_dev[li], scale, stream)
 
-    def run(self, pos: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+    def run(self, pos: torch.Tensor | None, seq_lens: torch.Tensor | None, scale: float,
             stream: torch.cuda.Stream) -> None:
         """Enqueue one step after the work already on `stream`; `stream` waits for the last copy
-        out before anything issued after this call."""
+        out before anything issued after this call. With `pos` and `seq_lens` None, the step's
+        positions and lengths are copied in from the pinned host buffers too (with the first run
+        of layers' inputs) and the device mirrors are used."""
         b = self.buf
+        from_host = pos is None
+        if from_host:
+            pos, seq_lens = b.pos_dev, b.lens_dev
         if len(self.runs) == 1:
             c0, c1 = self.runs[0]
             with torch.cuda.stream(stream):
-                self._copy_in(c0, c1)
+                self._copy_in(c0, c1, positions=from_host)
                 self._compute(c0, c1, pos, seq_lens, scale, stream)
                 b.out_host[c0:c1].copy_(b.out_dev[c0:c1], non_blocking=True)
             return
         self.start.record(stream)
         self.h2d.wait_event(self.start)
         with torch.cuda.stream(self.h2d):
-            for (c0, c1), ev in zip(self.runs, self.ready):
-                self._copy_in(c0, c1)
+            for ri, ((c0, c1), ev) in enumerate(zip(self.runs, self.ready)):
+                self._copy_in(c0, c1, positions=from_host and ri == 0)
                 ev.record(self.h2d)
         for (c0, c1), ready, done in zip(self.runs, self.ready, self.done):
             stream.wait_event(ready)

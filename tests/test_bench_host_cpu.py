@@ -88,11 +88,39 @@ def test_traffic_keys_name_the_variant():
     assert bench.traffic_key(w, paged=16, kv="fp8", T=4) == "gqa_70b_80l_paged16_fp8_T4"
 
 
-def test_l2_is_flushed_only_where_a_step_fits_twice_in_it():
-    assert bench.needs_l2_flush(inputs.WORKLOADS["gqa_8b"])
+def test_one_layer_workloads_rotate_through_copies_worth_four_l2_sizes():
+    for name in ("gqa_8b", "mqa_long", "mha_ref"):
+        w = inputs.WORKLOADS[name]
+        n = bench.copies_for(w)
+        assert 1 <= n <= bench.MAX_COPIES, name
+        # n copies hold at least four L2 sizes between two reads of one copy; n - 1 would not
+        assert n * bench.step_kv_bytes(w) >= bench.ROTATION_L2_MULTIPLE * bench.L2_BYTES
+        assert n == 1 or (n - 1) * bench.step_kv_bytes(w) < \
+            bench.ROTATION_L2_MULTIPLE * bench.L2_BYTES
+        assert not bench.needs_l2_flush(w)
+    assert bench.copies_for(inputs.WORKLOADS["mqa_long"]) == 2
+    assert bench.copies_for(inputs.WORKLOADS["gqa_70b_80l"]) == 1   # its 80 layers rotate
+
+
+def test_only_the_tiny_workload_is_flushed_between_steps():
     assert bench.needs_l2_flush(inputs.WORKLOADS["mqa_tiny"])
-    assert not bench.needs_l2_flush(inputs.WORKLOADS["gqa_70b_80l"])
-    assert not bench.needs_l2_flush(inputs.WORKLOADS["mha_ref"])
+    assert "flushed" in bench.workload_config(inputs.WORKLOADS["mqa_tiny"])["l2"]
+    for name in ("gqa_8b", "mqa_long", "mha_ref", "gqa_70b_80l"):
+        assert not bench.needs_l2_flush(inputs.WORKLOADS[name]), name
+
+
+def test_both_arms_describe_the_same_config():
+    # the reference arm and ours print workload_config of the same arguments
+    w = inputs.WORKLOADS["gqa_70b_80l"]
+    cfg = bench.workload_config(w)
+    assert cfg["tokens_per_step"] == 1 and cfg["workload"] == "gqa_70b_80l"
+    assert bench.workload_config(w, T=4)["tokens_per_step"] == 4
+
+
+def test_the_automatic_path_names_follow_the_group_size():
+    assert bench.path_name(inputs.WORKLOADS["mha_ref"]).startswith("CUDA cores")
+    assert bench.path_name(inputs.WORKLOADS["gqa_8b"]).startswith("CUDA cores")
+    assert bench.path_name(inputs.WORKLOADS["mqa_long"]).startswith("mma.sync")
 
 
 @pytest.mark.parametrize("T", [1, 2, 4])

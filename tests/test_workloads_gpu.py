@@ -1,7 +1,7 @@
 """GPU parity at the full sizes of the five decode workloads, in the launch configuration the
-benchmark times. The oracle checks every output of the small workloads and a sample of sequences
-(all their heads) of the large ones; the append is checked bit for bit on the sampled rows and,
-on the device, for "nothing else changed".
+benchmark times. The oracle checks every output of the four one-layer workloads (every sequence
+and head) and a sample of sequences of three layers of the 80-layer step; the append is checked
+bit for bit on the checked rows and, on the device, for "nothing else changed".
 """
 from __future__ import annotations
 
@@ -57,7 +57,7 @@ def _check_layer(mqa, w, q, kn, vn, k, v, pos, lens, sample, tag):
 
 
 @pytest.mark.parametrize("name,sample", [
-    ("mqa_tiny", None), ("gqa_8b", None), ("mqa_long", [0, 21, 63]), ("mha_ref", [0, 5]),
+    ("mqa_tiny", None), ("gqa_8b", None), ("mqa_long", None), ("mha_ref", None),
 ])
 def test_single_layer_workloads(mqa, name, sample):
     w = inputs.WORKLOADS[name]

@@ -74,3 +74,36 @@ def test_a_wait_that_runs_out_reports_a_timeout_and_the_next_call_is_right(mqa, 
     finally:
         mqa.debug_override(0, 0)
     P.assert_close(out, out_ref, f"after a timeout, path {path}")
+
+
+@pytest.mark.parametrize("h", [8, 32], ids=["cuda_cores_G4", "mma_sync_G16"])
+def test_a_timeout_with_arrivals_counted_is_cleared_for_a_larger_later_call(mqa, h):
+    """A launch over 600 (sequence, KV head) segments gives up after its CTAs have counted their
+    arrivals at split segments (testing stall 2), leaving those counters non-zero. A small call
+    follows on the same stream (4 segments), then the large shape again: both must match the
+    oracle, so the clear after the timeout has to cover every counter of the workspace, not just
+    the small call's."""
+    big = P.make_case(300, h, 2, 64, 500, 999, seed_id=830 + h)
+    small = P.make_case(2, h, 2, 64, 500, 999, seed_id=831 + h)
+    _, _, ref_big = P.oracle_step(big)
+    _, _, ref_small = P.oracle_step(small)
+    try:
+        mqa.debug_set_wait_limit_ns(20_000_000)
+        mqa.debug_stall(2)
+        P.gpu_step(big, mqa)
+        status = mqa.get_device_status()
+        site = mqa.debug_timeout_site()
+    finally:
+        mqa.debug_stall(False)
+        mqa.debug_set_wait_limit_ns(0)
+    assert status == TIMEOUT, f"expected MQA_ERR_TIMEOUT, got {status}"
+    assert site[0] in SITES_BEHIND_THE_STALL, f"unexpected wait site: {site}"
+    _, _, out_small = P.gpu_step(small, mqa)
+    torch.cuda.synchronize()
+    assert mqa.get_device_status() == 0
+    P.assert_close(out_small, ref_small, "small call after the timeout")
+    for rep in range(2):
+        _, _, out_big = P.gpu_step(big, mqa)
+        torch.cuda.synchronize()
+        assert mqa.get_device_status() == 0
+        P.assert_close(out_big, ref_big, f"large call after the timeout, run {rep}")

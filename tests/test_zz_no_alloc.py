@@ -4,10 +4,13 @@ latency-critical loop that cannot afford cudaMalloc's implicit synchronisation. 
 partial states in a fixed array inside the library instead of a cudaMalloc'd workspace.
 
 These tests call it through the C ABI (ctypes, raw pointers). They check its output against the
-allocating entry point, mqa_decode_attention, within the parity tolerance used everywhere else,
-on two calls in a row: the second call starts from the array contents the first call left
-behind. They also check that a problem too large for the array is refused without writing
-anything. The file name makes pytest collect it last.
+allocating entry point, mqa_decode_attention, and against the fp64 oracle, within the parity
+tolerance used everywhere else, on two calls in a row: the second call starts from the array
+contents the first call left behind. They also check that a problem too large for the array is
+refused without writing anything, that a call that gave up with arrival counters left non-zero
+does not spoil later calls of any size, and that consecutive calls allowed to overlap
+(mqa_set_launch_overlap) give the same bits as calls that do not. The file name makes pytest
+collect it last.
 """
 from __future__ import annotations
 
@@ -67,6 +70,8 @@ def test_noalloc_matches_the_allocating_entry_point_on_two_calls_in_a_row(api):
         torch.cuda.synchronize()
         assert B.get_device_status() == 0
         P.assert_close(out, P.widen(ref), f"noalloc vs allocating entry point, b{b} h{h} g{g}")
+        _, _, oracle_out = P.oracle_step(case)
+        P.assert_close(out, oracle_out, f"noalloc vs the fp64 oracle, b{b} h{h} g{g}")
 
 
 def test_noalloc_refuses_a_problem_larger_than_its_array(api):
@@ -86,3 +91,76 @@ def test_noalloc_refuses_a_problem_larger_than_its_array(api):
     assert _call_noalloc(lib, q, k, v, lens, out, 1.0 / math.sqrt(d_h)) == UNSUPPORTED
     torch.cuda.synchronize()
     assert np.all(P.bits(out) == P.bits(torch.full_like(q, 3.0)))
+
+
+TIMEOUT = 5
+
+
+def test_noalloc_after_a_timeout_that_left_arrival_counters_dirty(api):
+    """A no-alloc call over 600 segments gives up after its CTAs have counted arrivals at split
+    segments (testing stall 2). A small no-alloc call follows, then the large one again; both
+    must match the oracle, so the clear after the timeout must cover the array's whole counter
+    region."""
+    B, lib = api
+    dev = torch.device("cuda")
+    big = P.make_case(300, 32, 2, 64, 500, 999, seed_id=610)
+    small = P.make_case(2, 32, 2, 64, 500, 999, seed_id=611)
+
+    def run(case, stall=0):
+        q = case["q"].to(dev)
+        k, v = case["k"].to(dev), case["v"].to(dev)
+        lens = case["lens"].to(dev)
+        B.kv_append(case["k_new"].to(dev), case["v_new"].to(dev), k, v, case["pos"].to(dev))
+        out = torch.full_like(q, float("nan"))
+        assert _call_noalloc(lib, q, k, v, lens, out, case["scale"]) == 0
+        return out
+
+    try:
+        B.debug_set_wait_limit_ns(20_000_000)
+        B.debug_stall(2)
+        run(big)
+        status = B.get_device_status()
+        B.debug_timeout_site()
+    finally:
+        B.debug_stall(False)
+        B.debug_set_wait_limit_ns(0)
+    assert status == TIMEOUT, f"expected MQA_ERR_TIMEOUT, got {status}"
+    for case, tag in ((small, "small"), (big, "large"), (big, "large again")):
+        out = run(case)
+        torch.cuda.synchronize()
+        assert B.get_device_status() == 0
+        P.assert_close(out, P.oracle_step(case)[2], f"noalloc {tag} call after the timeout")
+
+
+def test_noalloc_calls_allowed_to_overlap_give_the_same_bits(api):
+    """Back-to-back no-alloc calls on distinct caches, with and without launch overlap on the
+    stream: the same outputs bit for bit (the array is written only after the call ahead has
+    finished)."""
+    B, lib = api
+    dev = torch.device("cuda")
+    cases = [P.make_case(4, 32, 4, 128, 300, 2000, seed_id=620 + i) for i in range(4)]
+    dev_cases = []
+    for c in cases:
+        k, v = c["k"].to(dev), c["v"].to(dev)
+        B.kv_append(c["k_new"].to(dev), c["v_new"].to(dev), k, v, c["pos"].to(dev))
+        dev_cases.append((c["q"].to(dev), k, v, c["lens"].to(dev), c["scale"]))
+    stream = torch.cuda.Stream()
+    results = {}
+    for on in (False, True):
+        B.set_launch_overlap(on, stream)
+        outs = [torch.full_like(q, float("nan")) for q, *_ in dev_cases]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for rep in range(3):
+                for (q, k, v, lens, scale), out in zip(dev_cases, outs):
+                    assert _call_noalloc(lib, q, k, v, lens, out, scale) == 0
+        stream.synchronize()
+        assert B.get_device_status() == 0
+        results[on] = [P.bits(o) for o in outs]
+    B.set_launch_overlap(False, stream)
+    for a, b in zip(results[False], results[True]):
+        assert np.array_equal(a, b)
+    for c, o in zip(cases, results[True]):
+        ref = P.oracle_step(c)[2]
+        out = torch.from_numpy(o.view(np.int16)).view(torch.bfloat16)
+        P.assert_close(out, ref, "overlapped noalloc call vs the oracle")
