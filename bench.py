@@ -228,12 +228,15 @@ def step_kv_bytes(w, eb: int = 2) -> int:
 
 
 def copies_for(w, eb: int = 2) -> int:
-    """Distinct copies of a workload's layers that consecutive steps rotate through, so that
-    ROTATION_L2_MULTIPLE L2 sizes of other data are read between two reads of the same copy (a
-    multi-layer workload's own layers count as one copy each); 0 when that would take more than
-    MAX_COPIES (the workload is then flushed from L2 before every step instead)."""
-    n = math.ceil(ROTATION_L2_MULTIPLE * L2_BYTES / step_kv_bytes(w, eb))
-    n = max(n, 1)
+    """Distinct copies of a one-layer workload that consecutive steps rotate through: enough that
+    ROTATION_L2_MULTIPLE L2 sizes of data are read between two reads of the same copy, and at
+    least two, so that no launch follows one on the same caches and output (the condition under
+    which consecutive launches may overlap). 1 for a multi-layer workload, whose own layers
+    rotate. 0 when it would take more than MAX_COPIES (the workload is then flushed from L2
+    before every step instead)."""
+    if w.layers > 1:
+        return 1
+    n = max(2, math.ceil(ROTATION_L2_MULTIPLE * L2_BYTES / step_kv_bytes(w, eb)))
     return n if n <= MAX_COPIES else 0
 
 
@@ -518,6 +521,26 @@ def e2e_host_driven(units: Units, dev, stream, steps: int, warmup: int, mqa):
     return ms * 1000.0 / steps, buf.h2d_bytes, buf.d2h_bytes
 
 
+def read_bandwidth_reference(dev, gib: int = 4, reps: int = 5) -> dict:
+    """Context for the roofline: what a plain library read stream reaches on this GPU (a torch
+    sum over `gib` GiB of bf16, best of `reps`). The roofline's peak stays the measured copy
+    bandwidth, whose bytes are half reads, half writes; a read-only stream such as the decode
+    kernel's can go past it."""
+    x = torch.ones(gib * 2**30 // 2, dtype=torch.bfloat16, device=dev)
+    best = float("inf")
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.sum(dtype=torch.float32)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del x
+    torch.cuda.empty_cache()
+    return {"gbs": gib * 2**30 / (best * 1e-3) / 1e9,
+            "how": f"torch bf16 sum over {gib} GiB (reads only), best of {reps}"}
+
+
 def run_ours(args, world, rank, local):
     import query_grouped_decode_kv_b300 as mqa
 
@@ -539,6 +562,7 @@ def run_ours(args, world, rank, local):
             dist.barrier()
 
     configs = {}
+    read_ref = read_bandwidth_reference(dev)
     n_launch0 = mqa.kernel_launch_count()
     with ClockSampler(local) as clocks:
         for name in others:
@@ -587,7 +611,9 @@ def run_ours(args, world, rank, local):
                          "us_per_launch": us_launch,
                          "us_per_launch_from": "step time / launches per step "
                                                "(launches x us_per_launch = ms_per_step)",
-                         "flops_per_launch": units.flops_per_launch},
+                         "flops_per_launch": units.flops_per_launch,
+                         "read_stream_reference": dict(read_ref,
+                                                       frac=achieved / read_ref["gbs"])},
             "configs": configs,
             "e2e": {"value": whole_job_us_per_step(e2e_step / 1000.0, world), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -310,31 +310,38 @@ MQA_API int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_ca
 
 /*
  * mqa_set_launch_overlap -- let the decode-attention launches on `stream` overlap the kernel
- * ahead of each of them on that stream (programmatic dependent launch). Off by default. The pages
- * have no counterpart; this is a scheduling choice of the library.
+ * immediately ahead of each of them on that stream (programmatic dependent launch). Off by
+ * default. The pages have no counterpart; this is a scheduling choice of the library.
  *
  * Why: a launch has a fixed part at both ends -- the pipeline fill before its first tile arrives
  * and, after its last tile, the combine of the pieces of sequences split across CTAs -- during
- * which HBM idles. With overlap on, a launch may start on SMs that the launch ahead of it has
- * already left, so its fill (and its first tiles) run under the other launch's drain. This
- * matters for back-to-back decode steps of many layers, where each launch is a few hundred
- * microseconds at most.
+ * which HBM idles, and its CTAs finish at different times. With overlap on, a launch starts on
+ * the SMs that the launch ahead of it has already left and streams its tiles under that launch's
+ * drain. This matters for back-to-back decode steps of many layers, where each launch lasts a
+ * few hundred microseconds at most.
  *
- * Contract (what the caller guarantees when it turns overlap on for a stream): the kernel that
- * precedes a call on the stream writes none of that call's inputs -- q, k_new, v_new, pos,
- * seq_lens, the page table, and every cache row the call reads other than the rows it appends.
- * The consecutive layers of one decode step, whose inputs are all in place before the first
- * layer is enqueued, satisfy it; so does a stream where only this library's decode launches
- * follow one another on distinct caches. A stream that runs mqa_kv_append and then
- * mqa_decode_attention does NOT (the append writes a row the attention reads): use the fused
- * mqa_decode_step there, or leave overlap off.
+ * Contract (what the caller guarantees when it turns overlap on for a stream), for every call on
+ * the stream and the kernel immediately ahead of it there:
+ *   1. that kernel writes none of the call's inputs: q, k_new, v_new, pos, seq_lens, the page
+ *      table, and every cache row the call reads other than the rows it appends;
+ *   2. that kernel neither reads nor writes the call's outputs: `out` and the cache rows the call
+ *      appends.
+ * The consecutive layers of one decode step satisfy it (each layer has its own caches and `out`,
+ * and all inputs are in place before the first layer is enqueued), and so does any sequence of
+ * this library's calls on distinct caches and outputs. A stream that runs mqa_kv_append and then
+ * mqa_decode_attention on the same cache does NOT (the append writes a row the attention reads):
+ * use the fused mqa_decode_step there. Neither does a call repeated back to back on the same
+ * caches and `out`.
  *
- * What the library guarantees in exchange: until the kernel ahead of it has finished and its
- * writes are visible, a call only reads; it writes nothing -- no output, no appended cache row,
- * no scratch -- before then. Results are bit for bit those of the same calls with overlap off.
- * The setting applies to the attention, step, paged, fp8, multi-token and no-alloc calls on the
- * mma.sync and CUDA-core paths (the forced tcgen05 path never overlaps), and to launches captured
- * into a CUDA graph, where it becomes a programmatic edge.
+ * What the library guarantees in exchange: results are bit for bit those of the same calls with
+ * overlap off. A call never shares its scratch with the launch ahead of it: the stream's
+ * workspace has two halves that consecutive launches take in turn, and a launch is allowed to
+ * start only once the launch two back has finished. mqa_decode_attention_noalloc has one scratch
+ * array, so with overlap on it reads early but writes nothing -- no output, no scratch -- before
+ * the kernel ahead has finished. The setting applies to the attention, step, paged, fp8,
+ * multi-token (h/g * T <= 64) and no-alloc calls on the mma.sync and CUDA-core paths (the forced
+ * tcgen05 path and the prefill path never overlap), and to launches captured into a CUDA graph,
+ * where it becomes a programmatic edge between consecutive kernel nodes.
  *
  *   stream   cudaStream_t, on the current device (NULL: the legacy default stream)
  *   on       1 to allow overlap, 0 to forbid it

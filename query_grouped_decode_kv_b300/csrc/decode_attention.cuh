@@ -43,12 +43,16 @@ constexpr int kSwizzleRowBytes = 128;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;  // two bf16 ones (the B fragment of P 1)
 constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 // NW (a template parameter below) is the number of consumer warps: 4 or 8.
-//  - NW = 4: one producer warp comes on top (160 threads, one warp per SM sub-partition each).
+//  - NW = 4: one producer warp and one launch-order warp come on top (192 threads).
 //  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
 //    every thread kLaunchRegsWide registers (the most 384 threads can have on one SM); the
 //    producer warpgroup then hands registers back (setmaxnreg.dec to kProducerRegs) and the
-//    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Only one producer lane works.
-__host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 1); }
+//    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Only one producer lane works;
+//    the next warp of the group is the launch-order warp.
+// The launch-order warp (warp NW + 1) only matters for launches that overlap the kernel ahead of
+// them on the stream with early writes (DecodeParams::early_writes): its lane 0 waits for that
+// kernel to finish and only then lets the next launch be scheduled.
+__host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 2); }
 constexpr int kLaunchRegsWide = 168;
 constexpr int kProducerRegs = 72;
 constexpr int kConsumerRegs = 216;
@@ -96,6 +100,15 @@ struct DecodeParams {
   // fp8 caches: the fused append stores e4m3(x / kq_scale) (and V with vq_scale); every final
   // output is multiplied by out_scale (the V scale; 1 for bf16 caches, where it changes nothing)
   float kq_scale, vq_scale, out_scale;
+  // Launch overlap (programmatic dependent launch), for launches that may start while the kernel
+  // ahead of them on the stream still runs. 0: the kernel signals its dependents at once and
+  // waits (griddepcontrol.wait) before its first global write. 1 (early writes): the host gave
+  // this launch scratch that the launch ahead does not use (the two halves of the workspace
+  // alternate) and the caller guarantees that the launch ahead neither reads nor writes this
+  // launch's outputs, so nothing waits; instead one thread per CTA waits and only then signals
+  // the dependents, so that the next launch -- which reuses the scratch of the launch ahead of
+  // this one -- cannot start before that launch has finished.
+  int early_writes;
 };
 
 // Stage geometry for head dimension D stored with EB bytes per element (2: bf16; 1: fp8 E4M3
@@ -251,7 +264,7 @@ __device__ __forceinline__ void append_uncovered_rows(const DecodeParams& P, int
       if (c == 0) latch_status(kStatusDeviceBounds);
       continue;
     }
-    pdl_wait();  // a cache row is written only once the kernel ahead on the stream has finished
+    if (!P.early_writes) pdl_wait();  // else the launch ahead does not touch this row
     P.k_rows[dst + c] = new_row_chunk<EB>(P.k_new + src_row * CS, c, P.kq_scale);
     P.v_rows[dst + c] = new_row_chunk<EB>(P.v_new + src_row * CS, c, P.vq_scale);
   }
@@ -276,15 +289,15 @@ __device__ __forceinline__ void write_new_row(const DecodeParams& P, int bi, int
 }
 
 // The new rows of segment (bi, j) that tile `tile` holds ([p0, p0 + T) meets the tile's rows),
-// written by the whole warp before the tile's copy; the caller fences and syncs the warp. The
-// writes wait for the kernel ahead on the stream to finish (programmatic dependent launch): that
-// kernel may still be reading the rows being replaced.
+// written by the whole warp before the tile's copy; the caller fences and syncs the warp. Unless
+// the launch has early writes, the writes wait for the kernel ahead on the stream to finish
+// (programmatic dependent launch): that kernel may still be reading the rows being replaced.
 template <int D, int EB>
 __device__ __forceinline__ bool write_tile_rows(const DecodeParams& P, int bi, int j, int tile,
                                                 int p0, int lane) {
   const int lo = max(p0, tile * kTileKeys), hi = min(p0 + P.T, (tile + 1) * kTileKeys);
   if (lo >= hi) return false;
-  pdl_wait();
+  if (!P.early_writes) pdl_wait();
   for (int p = lo; p < hi; ++p) write_new_row<D, EB>(P, bi, j, p - p0, p, lane);
   return true;
 }
@@ -645,7 +658,7 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
     const int L = __ldg(P.seq_lens + bi);
     if (L >= P.T && L <= P.n_max) continue;
     if (threadIdx.x == 0) latch_status(kStatusDeviceBounds);
-    pdl_wait();
+    if (!P.early_writes) pdl_wait();
     __nv_bfloat16* ob = P.out + static_cast<size_t>(bi) * P.T * P.h * D;
     for (int e = threadIdx.x; e < P.T * P.h * D; e += nthreads) ob[e] = __float2bfloat16_rn(0.f);
   }
@@ -1664,11 +1677,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   SharedLayout sh = carve_shared<D, EB, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Programmatic dependent launch (when the host asked for it): the next launch on the stream may
-  // be scheduled now; its CTAs take SMs as this grid's CTAs exit. This kernel in turn reads its
-  // inputs at once but writes global memory (outputs, partial states, counters, appended cache
-  // rows) only after pdl_wait(), i.e. once the kernel ahead of it has finished.
-  pdl_launch_dependents();
+  // Programmatic dependent launch (when the host asked for it). Without early writes, the next
+  // launch on the stream may be scheduled now (its CTAs take SMs as this grid's CTAs exit), and
+  // this kernel reads its inputs at once but writes global memory (outputs, partial states,
+  // counters, appended cache rows) only after pdl_wait(), once the kernel ahead has finished.
+  // With early writes, the launch-order warp below signals instead, after its own wait.
+  if (!P.early_writes) pdl_launch_dependents();
 
   // ---- barriers, then the tiles of every sequence and their prefix ---------------------------
   __shared__ uint32_t chunk_tiles[kThreads + 1];
@@ -1691,7 +1705,12 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   const unsigned long long W = sh.tix.total();
   const unsigned long long x0 = W * blockIdx.x / P.num_ctas;
   const unsigned long long x1 = W * (blockIdx.x + 1) / P.num_ctas;
-  if (x0 >= x1) return;
+  if (x0 >= x1) {
+    // a CTA with no tiles still waits for the kernel ahead before it exits, so that this grid
+    // never completes (nor lets the next launch start) before that kernel has
+    if (P.early_writes) pdl_wait();
+    return;
+  }
   const int ntiles = static_cast<int>(x1 - x0);
   const uint32_t stages_base = smem_addr(sh.stages);
   constexpr uint32_t kStageBytes = Geo::kStageBytes;
@@ -1708,6 +1727,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
       else
         produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+    } else if (warp == NW + 1 && lane == 0 && P.early_writes) {
+      // ============================ launch order ==============================================
+      pdl_wait();
+      pdl_launch_dependents();
     }
     return;
   }
@@ -1807,7 +1830,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         return;
       }
       if (!after_dep) {
-        pdl_wait();
+        if (!P.early_writes) pdl_wait();
         after_dep = true;
       }
       combine_and_store<D, NW, CR>(P, sh, cur.bi, cur.j, complete,

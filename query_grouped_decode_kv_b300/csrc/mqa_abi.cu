@@ -124,6 +124,11 @@ int check_paged(const PagedCache& pg, int g, int d_h, int* n_max) {
 // states (written before they are read in every call), and one arrival counter per segment. The
 // counters must read zero when a call starts: a new counter buffer is zeroed, every call that
 // finishes leaves its counters at zero, and nothing else ever writes there.
+//
+// Each buffer is two halves, and consecutive launches on the stream take alternate halves. A
+// launch that overlaps the one ahead of it (early writes) then never shares scratch with it; the
+// launch two back, which used the same half, has finished before it starts (its launch-order
+// warp sees to that).
 // ------------------------------------------------------------------------------------------------
 struct DeviceBuffer {
   void* ptr = nullptr;
@@ -132,6 +137,7 @@ struct DeviceBuffer {
 struct Workspace {
   DeviceBuffer partials, counters;
   uint64_t clean_epoch = 0;  // g_timeout_epoch when its counters were last known to be zero
+  uint32_t launches = 0;     // launches on this stream so far: the half the next one takes
 };
 std::mutex g_ws_mutex;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
@@ -159,33 +165,45 @@ int grow_buffer(DeviceBuffer& buf, size_t bytes, cudaStream_t stream, bool zero)
   return MQA_OK;
 }
 
-// The scratch a launch uses: the partial states, the arrival counters, and whether the whole
-// counter region (`counter_region_bytes`, all the counters any call may use there) must be zeroed
-// first.
+// The scratch a launch uses: the partial states, the arrival counters, whether the whole
+// counter region (`counter_region`, `counter_region_bytes`: all the counters any call may use
+// there, both halves of a workspace) must be zeroed first, and whether the scratch is not shared
+// with the launch ahead on the stream (a workspace half), so that the launch may write early.
 struct Scratch {
   void* partials = nullptr;
   unsigned int* counters = nullptr;
+  void* counter_region = nullptr;
   size_t counter_region_bytes = 0;
   bool clear = false;
+  bool alternating = false;
 };
 
 int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t counter_bytes,
                   Scratch* out) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
   Workspace& ws = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
-  if (int st = grow_buffer(ws.partials, partial_bytes, stream, false)) return st;
+  // two halves of each buffer, every half at least this call's need, 256-byte aligned
+  const size_t half_p = (partial_bytes + 255) & ~size_t{255};
+  const size_t half_c = (counter_bytes + 255) & ~size_t{255};
+  if (int st = grow_buffer(ws.partials, 2 * half_p, stream, false)) return st;
   const uint64_t epoch = g_timeout_epoch.load();
-  if (ws.counters.bytes < counter_bytes) {
-    if (int st = grow_buffer(ws.counters, counter_bytes, stream, true)) return st;
+  if (ws.counters.bytes < 2 * half_c) {
+    if (int st = grow_buffer(ws.counters, 2 * half_c, stream, true)) return st;
     ws.clean_epoch = epoch;
   }
   // After a timeout any counter of the region may be dirty, not only the ones this call uses, so
   // the clear (and with it the clean mark) covers the whole region.
   out->clear = ws.clean_epoch != epoch;
   ws.clean_epoch = epoch;
-  out->partials = ws.partials.ptr;
-  out->counters = static_cast<unsigned int*>(ws.counters.ptr);
+  const uint32_t half = ws.launches++ & 1u;
+  const size_t stride_p = (ws.partials.bytes / 2) & ~size_t{255};
+  const size_t stride_c = (ws.counters.bytes / 2) & ~size_t{255};
+  out->partials = static_cast<char*>(ws.partials.ptr) + half * stride_p;
+  out->counters = reinterpret_cast<unsigned int*>(static_cast<char*>(ws.counters.ptr) +
+                                                  half * stride_c);
+  out->counter_region = ws.counters.ptr;
   out->counter_region_bytes = ws.counters.bytes;
+  out->alternating = true;
   return MQA_OK;
 }
 
@@ -464,7 +482,7 @@ int launch_decode(const DecodePlan& p, const Scratch& sc) {
                        : nullptr;
   P.seg_arrivals = counters;
   if (counters && sc.clear &&
-      cudaMemsetAsync(counters, 0, sc.counter_region_bytes, p.stream) != cudaSuccess)
+      cudaMemsetAsync(sc.counter_region, 0, sc.counter_region_bytes, p.stream) != cudaSuccess)
     return MQA_ERR_CUDA;
   P.b = p.b;
   P.h = p.h;
@@ -505,12 +523,16 @@ int launch_decode(const DecodePlan& p, const Scratch& sc) {
   cfg.dynamicSmemBytes = kc.smem;
   cfg.stream = p.stream;
   cudaLaunchAttribute attr[1];
-  if (kc.pdl && overlap_on(p.dev, p.stream)) {
+  const bool overlap = kc.pdl && overlap_on(p.dev, p.stream);
+  if (overlap) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
+  // early writes need scratch the launch ahead does not share: a workspace half, or none at all
+  // (one CTA); the no-alloc array is a single region, so those launches wait before writing
+  P.early_writes = (overlap && (sc.alternating || p.ctas == 1)) ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, kc.fn, tmk, tmv, P) != cudaSuccess) {
     cudaGetLastError();
     return MQA_ERR_CUDA;
@@ -553,7 +575,9 @@ int noalloc_scratch_address(int dev, Scratch* out) {
   it->second.clean_epoch = epoch;
   out->counters = static_cast<unsigned int*>(it->second.ptr);
   out->partials = static_cast<char*>(it->second.ptr) + kNoallocCounterBytes;
+  out->counter_region = it->second.ptr;
   out->counter_region_bytes = kNoallocCounterBytes;
+  out->alternating = false;
   return MQA_OK;
 }
 

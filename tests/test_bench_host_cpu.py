@@ -93,12 +93,15 @@ def test_one_layer_workloads_rotate_through_copies_worth_four_l2_sizes():
         w = inputs.WORKLOADS[name]
         n = bench.copies_for(w)
         assert 1 <= n <= bench.MAX_COPIES, name
-        # n copies hold at least four L2 sizes between two reads of one copy; n - 1 would not
+        # n copies hold at least four L2 sizes between two reads of one copy; n - 1 would not,
+        # unless n is the floor of two (no launch follows one on the same caches)
         assert n * bench.step_kv_bytes(w) >= bench.ROTATION_L2_MULTIPLE * bench.L2_BYTES
-        assert n == 1 or (n - 1) * bench.step_kv_bytes(w) < \
+        assert n == 2 or (n - 1) * bench.step_kv_bytes(w) < \
             bench.ROTATION_L2_MULTIPLE * bench.L2_BYTES
+        assert n >= 2
         assert not bench.needs_l2_flush(w)
     assert bench.copies_for(inputs.WORKLOADS["mqa_long"]) == 2
+    assert bench.copies_for(inputs.WORKLOADS["mha_ref"]) == 2
     assert bench.copies_for(inputs.WORKLOADS["gqa_70b_80l"]) == 1   # its 80 layers rotate
 
 

@@ -5,8 +5,9 @@ running: it reads its inputs at once but writes nothing (outputs, appended rows,
 arrival counters) until that launch has finished. Results must therefore be bit for bit those of
 the same launches without overlap. These tests run sequences of launches both ways -- eager and
 captured in a CUDA graph, on every inner-product path, over contiguous, paged and fp8 caches, with
-one and several tokens, with a layer repeated back to back -- and compare every output and every
-cache byte, then check outputs against the fp64 oracle.
+one and several tokens, with layers revisited (their appends repeated) -- and compare every output
+and every cache byte, then check outputs against the fp64 oracle. No launch follows one on the same
+caches or output, which the overlap contract requires.
 """
 from __future__ import annotations
 
@@ -134,8 +135,9 @@ def _check_oracle(order, data, outs, pos, lens, scale, T=1, max_checks=3):
 def test_overlapped_fused_layers_equal_serial_ones_bit_for_bit(mqa, shape, graph):
     dev = torch.device("cuda")
     pos, lens, data = _layers(*shape, n=4, seed=700 + shape[1] + shape[2], dev=dev)
-    # distinct layers back to back, then one layer twice in a row (its own append repeated)
-    order = [0, 1, 2, 3, 3, 0, 1]
+    # distinct layers back to back, then layers again (their appends repeated); no launch
+    # follows one on the same caches, the condition for overlap
+    order = [0, 1, 2, 3, 0, 3, 1]
     scale = data[0][0].shape[-1] ** -0.5
     s = torch.cuda.Stream()
     args = (order, data, pos.to(dev), lens.to(dev), scale, s)
@@ -163,7 +165,7 @@ def test_overlapped_attention_calls_on_distinct_caches_equal_serial_ones(mqa):
 def test_overlapped_multi_token_layers_equal_serial_ones(mqa, T):
     dev = torch.device("cuda")
     pos, lens, data = _layers(3, 32, 4, 128, 200, 2500, n=3, seed=780 + T, dev=dev, T=T)
-    order = [0, 1, 2, 2, 0]
+    order = [0, 1, 2, 0, 2]
     s = torch.cuda.Stream()
     args = (order, data, pos.to(dev), lens.to(dev), 128 ** -0.5, s)
     serial = _run(mqa, *args, overlap=False, graph=False, step_fn=_fused(mqa))
