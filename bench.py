@@ -66,6 +66,7 @@ ALL_WORKLOADS = ["mqa_tiny", "gqa_8b", "mqa_long", "mha_ref", "gqa_70b_80l"]
 KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
                   "query_grouped_decode_kv_b300/csrc/decode_attention_tc.cuh",
                   "query_grouped_decode_kv_b300/csrc/kv_append.cuh",
+                  "query_grouped_decode_kv_b300/csrc/prefill_attention_tc.cuh",
                   "query_grouped_decode_kv_b300/csrc/ptx.cuh",
                   "query_grouped_decode_kv_b300/csrc/status.cuh",
                   "query_grouped_decode_kv_b300/csrc/mqa_abi.cu",
@@ -272,7 +273,7 @@ def path_name(w, kv: str = "bf16", T: int = 1) -> str:
     G = w.h // w.g
     if T > 1:
         return f"mma.sync tensor cores, {T} tokens x {G} heads = {T * G} rows per KV head"
-    if G < 8:
+    if G <= 2:
         return f"CUDA cores (fp32 FMA), G={G}" + (" over widened fp8 codes" if kv == "fp8" else "")
     return f"mma.sync tensor cores, G={G}" + (" (fp16 over widened fp8 codes)" if kv == "fp8"
                                               else " (bf16)")

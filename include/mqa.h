@@ -252,12 +252,20 @@ MQA_API int mqa_decode_step_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const 
  *                    0 <= pos[bi] and pos[bi] + T <= n_max, else that sequence is not written
  *   seq_lens         device, [b] int32, T <= seq_lens[bi] <= n_max (normally pos[bi] + T), else
  *                    zeros for that sequence
- *   T                tokens per sequence, >= 1, with T * (h / g) <= 64
+ *   T                tokens per sequence, >= 1, with T * (h / g) <= 2^22
  *   everything else  as for mqa_kv_append / mqa_decode_attention / mqa_decode_step
  *
- * The attention runs on the mma.sync tensor-core path whatever the group size (a forced CUDA-core
- * or tcgen05 path returns MQA_ERR_UNSUPPORTED when T > 1); both latched errors are
- * MQA_ERR_DEVICE_BOUNDS. The workspace is that of mqa_decode_attention.
+ * Two kernels serve these calls, by the rows a KV head's attention has, T * (h / g):
+ *   - up to 64 (speculative decoding): the mma.sync decode kernel, the rows of a KV head in one
+ *     tile of heads, K/V tiles split across CTAs and merged; the step is one launch;
+ *   - more (a prefill-sized T: a prompt chunk): the tcgen05 prefill kernel, 128 rows per
+ *     tensor-core tile with accumulators in tensor memory, each block of 128 rows finished by one
+ *     CTA; the step is two launches, the append and then the attention, since every block of a
+ *     sequence reads its new rows. Forcing the tcgen05 path (mqa_debug_override path 3) sends
+ *     every T > 1 call there.
+ * A forced CUDA-core path returns MQA_ERR_UNSUPPORTED when T > 1, and so does forced mma.sync past
+ * 64 rows. Both latched errors are MQA_ERR_DEVICE_BOUNDS. The decode kernel uses the workspace of
+ * mqa_decode_attention; the prefill kernel none.
  */
 MQA_API int mqa_kv_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
                                 mqa_bf16* v_cache, const int32_t* pos, int b, int T, int g,
@@ -398,7 +406,7 @@ MQA_API uint64_t mqa_kernel_launch_count(void);
 
 /*
  * Testing hook: force the number of CTAs that split the attention work (0 = automatic choice)
- * and the inner-product path: 0 = automatic (CUDA cores when h/g < 8, mma.sync tensor cores
+ * and the inner-product path: 0 = automatic (CUDA cores when h/g <= 2, mma.sync tensor cores
  * otherwise); 1 = CUDA cores (h/g <= 7 only); 2 = mma.sync tensor cores; 3 = tcgen05 tensor cores
  * with tensor-memory accumulators. Process-wide; returns
  * MQA_ERR_INVALID_ARG for a negative CTA count or an unknown path. Results must not depend on

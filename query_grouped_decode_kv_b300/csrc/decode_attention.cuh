@@ -21,9 +21,9 @@
 // sum l in fp32, log2 domain) for its slice of the tile's keys; at a segment's end the warps'
 // states are combined through shared memory.
 //
-// Inner products: for G >= 8 the grouped heads form a real dense contraction and run on tensor
-// cores (bf16 mma.sync m16n8k16, fp32 accumulate; S = Q K^T with the heads as M, then O += P V).
-// For G < 8 (MHA-like grouping) CUDA cores do fp32 FMAs.
+// Inner products: the grouped heads run on tensor cores as the M rows of bf16 mma.sync m16n8k16
+// products (fp32 accumulate; S = Q K^T, then O += P V). With one or two heads per K/V row
+// (MHA-like grouping) CUDA cores do fp32 FMAs instead; they serve up to seven heads when forced.
 //
 // Every wait is bounded in time: on expiry the kernel latches MQA_ERR_TIMEOUT and returns.
 #pragma once
@@ -922,7 +922,7 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
 }
 
 // ---------------------------------------------------------------------------------------------
-// Tensor-core consumer (G >= 8). WM warps (one per 16 heads) form a group; NW / WM groups split
+// Tensor-core consumer (the automatic path from G = 3). WM warps (one per 16 heads) form a group; NW / WM groups split
 // each tile's keys. kTokens: rows are (token, head) pairs of several new tokens, each masked by
 // its own causal limit (instances used only when T > 1, so the single-token kernels carry no
 // per-row state).
@@ -1096,7 +1096,7 @@ struct MmaConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// Tensor-core consumer for fp8 E4M3 caches (G >= 8): the same tile split, softmax and combine as
+// Tensor-core consumer for fp8 E4M3 caches (from G = 3): the same tile split, softmax and combine as
 // MmaConsumer, with fp16 MMAs (m16n8k16, fp32 accumulate). The codes are widened exactly to fp16
 // in registers (two codes per instruction); q is rounded to fp16 once per segment; the weights P
 // are rounded to fp16 once, and the running sum takes the same rounded values. The per-tensor
@@ -1304,7 +1304,7 @@ struct MmaConsumerF8 {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer (G < 8). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
+// CUDA-core consumer (G <= 7; fp8 caches, G <= 2 automatically). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
 // 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output. EB: the cache's
 // bytes per element (fp8 codes are widened exactly on load).
 // ---------------------------------------------------------------------------------------------
@@ -1469,7 +1469,7 @@ struct CcConsumer {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer for G < 8, lanes owning keys (bf16 caches). Eight warps form two tile groups
+// CUDA-core consumer for G <= 7 (automatically G <= 2), lanes owning keys (bf16 caches). Eight warps form two tile groups
 // of four; a group takes every other tile of the CTA's range, so each group has two of the four
 // stages (one being computed, one loading), and each warp 16 of a tile's 64 keys.
 // In S = Q K^T each key belongs to two lanes, l and l + 16, which form the dot product over the

@@ -14,6 +14,7 @@
 #include "decode_attention.cuh"
 #include "decode_attention_tc.cuh"
 #include "kv_append.cuh"
+#include "prefill_attention_tc.cuh"
 #include "status.cuh"
 
 namespace {
@@ -246,12 +247,16 @@ using AttnKernel = void (*)(const CUtensorMap, const CUtensorMap, const DecodePa
 // tcgen05 tensor cores with tensor-memory accumulators.
 enum Path { kPathAuto = 0, kPathCudaCores = 1, kPathMmaSync = 2, kPathTcgen05 = 3 };
 
-// Automatic choice. G < 8 (MHA-like grouping) has too few heads per K/V row for a real
-// contraction and runs on CUDA cores; from G = 8 the heads of a group form a dense matrix product
-// on the tensor cores (mma.sync: the tcgen05 kernel, 128-row MMA tiles with accumulators in
-// tensor memory, is not yet faster on any measured shape). Forcing mma.sync below 8 heads (path 2,
-// MMA rows mostly padding) is supported and tested.
-Path auto_path(int G) { return G < 8 ? kPathCudaCores : kPathMmaSync; }
+// Automatic choice, by measurement on B300. With one or two heads per K/V row (MHA-like
+// grouping) the heads are no contraction and CUDA cores stream the cache at the HBM rate. From
+// three heads on, the CUDA cores' fp32 FMAs (2 G d_h per key) fall behind HBM (at 32K rows:
+// 1.01x the copy bandwidth at G = 3, 0.87x at G = 4, 0.59x at G = 7, against 1.10x on mma.sync at
+// every G), so the group's heads go to the tensor cores as the M rows of m16n8k16 MMAs, padded
+// to 16 (mma.sync; the tcgen05 kernel, 128-row MMA tiles with accumulators in tensor memory, is
+// not faster on any measured decode shape). Forcing either path at any G up to 7 is supported
+// and tested.
+constexpr int kCudaCoreMaxGroup = 2;
+Path auto_path(int G) { return G <= kCudaCoreMaxGroup ? kPathCudaCores : kPathMmaSync; }
 
 // A kernel instance with the launch facts the host needs.
 struct AttnKernelChoice {
@@ -386,6 +391,7 @@ struct DecodePlan {
   int b, h, g, d_h, n_max, G;
   float scale;
   Path path;
+  bool prefill = false;  // several tokens with more than 64 rows per KV head: the prefill kernel
   cudaStream_t stream;
   int dev;
   long long bg, ctas;
@@ -408,22 +414,29 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   if (T <= 0) return MQA_ERR_INVALID_ARG;
   if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
   const int Gh = h / g;
-  // rows of a segment: the group's heads for each of the T tokens
-  if (static_cast<long long>(T) * Gh > mqa::kMaxGroup || b > mqa::kMaxBatch)
+  const int force_path = g_force_path.load();
+  // rows of a segment: the group's heads for each of the T tokens. Up to 64 of them run on the
+  // decode kernels; several tokens with more rows (or with the tcgen05 path forced) run on the
+  // prefill kernel, 128 rows per tensor-core tile.
+  const long long rows = static_cast<long long>(T) * Gh;
+  const bool prefill = T > 1 && (rows > mqa::kMaxGroup || force_path == kPathTcgen05);
+  if ((!prefill && rows > mqa::kMaxGroup) || b > mqa::kMaxBatch) return MQA_ERR_UNSUPPORTED;
+  if (prefill && (rows > mqa::kMaxPrefillRows ||
+                  (force_path != kPathAuto && force_path != kPathTcgen05)))
     return MQA_ERR_UNSUPPORTED;
-  const int G = T * Gh;
+  const int G = static_cast<int>(rows);
   const long long bg = static_cast<long long>(b) * g;
   const long long tiles_per_seg =
       (static_cast<long long>(n_max) + mqa::kTileKeys - 1) / mqa::kTileKeys;
   if (bg > (1ll << 24) || static_cast<long long>(b) * tiles_per_seg >= (1ll << 31) ||
       static_cast<double>(bg) * n_max * d_h > 9.0e18)
     return MQA_ERR_UNSUPPORTED;
-  const int force_path = g_force_path.load();
-  // several tokens: only the mma.sync consumer masks rows by token
-  const Path path = force_path == kPathAuto ? (T > 1 ? kPathMmaSync : auto_path(G))
-                                            : static_cast<Path>(force_path);
+  // several tokens on the decode kernels: only the mma.sync consumer masks rows by token
+  const Path path = prefill ? kPathTcgen05
+                            : (force_path == kPathAuto ? (T > 1 ? kPathMmaSync : auto_path(G))
+                                                       : static_cast<Path>(force_path));
   if (path == kPathCudaCores && G > 7) return MQA_ERR_UNSUPPORTED;
-  if (T > 1 && path != kPathMmaSync) return MQA_ERR_UNSUPPORTED;
+  if (T > 1 && !prefill && path != kPathMmaSync) return MQA_ERR_UNSUPPORTED;
 
   // ---- device facts ----
   int dev = 0;
@@ -432,9 +445,12 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   if (int st = device_info(dev, &info)) return st;
 
   // CTAs: one per SM, but no more than a quarter of the (upper bound on the) tile count, so that
-  // tiny problems are not scattered into many partial states.
+  // tiny problems are not scattered into many partial states. The prefill kernel: one per SM, at
+  // most one per unit (128 rows of one sequence and KV head); it keeps no partial states.
   const long long w_max = bg * tiles_per_seg;
-  long long ctas = (w_max + 3) / 4;
+  const long long units = bg * ((rows + mqa::kPfRows - 1) / mqa::kPfRows);
+  if (prefill && units >= (1ll << 31)) return MQA_ERR_UNSUPPORTED;
+  long long ctas = prefill ? units : (w_max + 3) / 4;
   if (ctas > info.sms) ctas = info.sms;
   if (ctas < 1) ctas = 1;
   if (const int f = g_force_ctas.load()) ctas = f;
@@ -450,10 +466,64 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   p.dev = dev;
   p.bg = bg;
   p.ctas = ctas;
-  p.part_o_bytes = static_cast<size_t>(slots) * G * d_h * sizeof(float);
-  p.partial_bytes = ctas > 1 ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
-  p.counter_bytes = ctas > 1 ? static_cast<size_t>(bg) * sizeof(unsigned int) : 0;
+  p.prefill = prefill;
+  const bool split = ctas > 1 && !prefill;
+  p.part_o_bytes = split ? static_cast<size_t>(slots) * G * d_h * sizeof(float) : 0;
+  p.partial_bytes = split ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
+  p.counter_bytes = split ? static_cast<size_t>(bg) * sizeof(unsigned int) : 0;
   return MQA_OK;
+}
+
+// The prefill kernel (several tokens, more than 64 rows per KV head): no scratch, no overlap.
+int launch_prefill(const DecodePlan& p) {
+  CUtensorMap tmk, tmv;
+  if (!make_cache_map(&tmk, p.k_cache, static_cast<int>(p.bg), p.n_max, p.d_h, 2) ||
+      !make_cache_map(&tmv, p.v_cache, static_cast<int>(p.bg), p.n_max, p.d_h, 2))
+    return MQA_ERR_CUDA;
+  DecodeParams P = {};
+  P.q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  P.seq_lens = p.seq_lens;
+  P.out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  P.b = p.b;
+  P.h = p.h;
+  P.g = p.g;
+  P.G = p.G;
+  P.T = p.T;
+  P.Gh = p.Gh;
+  P.n_max = p.n_max;
+  P.num_ctas = static_cast<int>(p.ctas);
+  P.scale_log2 = p.scale * 1.4426950408889634f;
+  P.kq_scale = P.vq_scale = P.out_scale = 1.f;
+  P.timeout_ns = g_wait_limit_ns.load();
+  P.drain_ns = kWaitLimitNs;
+  P.debug_stall = g_debug_stall.load();
+  P.early_writes = 0;
+  AttnKernelChoice kc;
+  kc.fn = p.d_h == 128 ? mqa::prefill_attention_tc_kernel<128> : mqa::prefill_attention_tc_kernel<64>;
+  kc.threads = mqa::kTcThreads;
+  kc.smem = mqa::tc_smem_bytes(p.d_h);
+  if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
+  kc.fn<<<static_cast<unsigned>(p.ctas), kc.threads, kc.smem, p.stream>>>(tmk, tmv, P);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+// T new rows per sequence into contiguous bf16 caches (one 16-byte chunk per thread).
+int launch_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_cache,
+                        mqa_bf16* v_cache, const int32_t* pos, int b, int T, int g, int d_h,
+                        int n_max, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(b) * T * g;
+  const int chunks = d_h / 8;
+  const long long total = rows * chunks;
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  mqa::kv_append_kernel<<<blocks, threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, T, g, chunks,
+      n_max);
+  g_launches.fetch_add(1);
+  return launch_error();
 }
 
 // `sc.clear`: zero the scratch's whole counter region first. The counters are zero whenever the
@@ -907,17 +977,8 @@ int mqa_kv_append_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* 
   if (rows > (1ll << 31) || static_cast<double>(b) * g * n_max * d_h > 9.0e18)
     return MQA_ERR_UNSUPPORTED;
 
-  const int chunks = d_h / 8;
-  const long long total = rows * chunks;
-  const int threads = 256;
-  const long long want = (total + threads - 1) / threads;
-  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
-  mqa::kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
-      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache), pos, b, T, g, chunks,
-      n_max);
-  g_launches.fetch_add(1);
-  return launch_error();
+  return launch_append_multi(k_new, v_new, k_cache, v_cache, pos, b, T, g, d_h, n_max,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int mqa_decode_attention_multi(const mqa_bf16* q, const mqa_bf16* k_cache,
@@ -928,6 +989,7 @@ int mqa_decode_attention_multi(const mqa_bf16* q, const mqa_bf16* k_cache,
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan, T))
     return st;
+  if (plan.prefill) return launch_prefill(plan);
   Scratch sc;
   if (plan.ctas > 1) {
     if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
@@ -947,6 +1009,13 @@ int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf
   if (int st = plan_decode(q, k_cache, v_cache, seq_lens, out, b, h, g, d_h, n_max, scale, stream,
                            &plan, T))
     return st;
+  if (plan.prefill) {
+    // every unit of a sequence reads its T new rows: append them first, then attend
+    if (int st = launch_append_multi(k_new, v_new, k_cache, v_cache, pos, b, T, g, d_h, n_max,
+                                     plan.stream))
+      return st;
+    return launch_prefill(plan);
+  }
   plan.k_new = k_new;
   plan.v_new = v_new;
   plan.pos = pos;

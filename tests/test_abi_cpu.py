@@ -304,8 +304,7 @@ def _append_multi(lib, kn=A, vn=A + 0x1000, kc=A + 0x2000, vc=A + 0x3000, pos=A 
 MULTI_CASES = [
     (dict(T=0), INVALID), (dict(T=-3), INVALID), (dict(q=0), INVALID), (dict(out=A + 4), INVALID),
     (dict(h=8, g=3), INVALID), (dict(d_h=96), UNSUPPORTED),
-    (dict(T=17, h=8, g=2), UNSUPPORTED),           # 17 tokens x 4 heads = 68 rows > 64
-    (dict(T=2, h=64, g=1), UNSUPPORTED),           # 2 x 64 rows
+    (dict(T=1 << 21, h=8, g=2), UNSUPPORTED),      # 2^21 tokens x 4 heads: past the prefill rows
 ]
 
 
@@ -329,10 +328,20 @@ def test_multi_append_host_checks(lib, kw, code):
     assert _append_multi(lib, **kw) == code
 
 
-def test_multi_rejects_forced_paths_other_than_mma_sync(lib):
-    for path in (1, 3):
+def test_multi_rejects_forced_cuda_cores_and_mma_sync_past_one_tile_of_rows(lib):
+    # several tokens: CUDA cores never; mma.sync up to 64 rows per KV head; more rows (17 tokens x
+    # 4 heads = 68) only on the tcgen05 prefill kernel, automatic or forced
+    for path, kw in ((1, dict(h=4, g=4)), (2, dict(T=17, h=8, g=2))):
         assert lib.mqa_debug_override(0, path) == OK
         try:
-            assert _attn_multi(lib, h=4, g=4) == UNSUPPORTED
+            assert _attn_multi(lib, **kw) == UNSUPPORTED
+        finally:
+            lib.mqa_debug_override(0, 0)
+    for path in (0, 3):
+        assert lib.mqa_debug_override(0, path) == OK
+        try:
+            # past the host checks (with no GPU here the launch itself then fails)
+            assert _attn_multi(lib, T=17, h=8, g=2) not in (INVALID, UNSUPPORTED)
+            assert _attn_multi(lib, T=2, h=64, g=1) not in (INVALID, UNSUPPORTED)
         finally:
             lib.mqa_debug_override(0, 0)

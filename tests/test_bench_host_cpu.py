@@ -122,7 +122,7 @@ def test_both_arms_describe_the_same_config():
 
 def test_the_automatic_path_names_follow_the_group_size():
     assert bench.path_name(inputs.WORKLOADS["mha_ref"]).startswith("CUDA cores")
-    assert bench.path_name(inputs.WORKLOADS["gqa_8b"]).startswith("CUDA cores")
+    assert bench.path_name(inputs.WORKLOADS["gqa_8b"]).startswith("mma.sync")   # G = 4
     assert bench.path_name(inputs.WORKLOADS["mqa_long"]).startswith("mma.sync")
 
 

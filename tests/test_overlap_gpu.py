@@ -127,11 +127,12 @@ def _check_oracle(order, data, outs, pos, lens, scale, T=1, max_checks=3):
 
 @pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
 @pytest.mark.parametrize("shape", [
-    (4, 32, 8, 128, 300, 3000),   # G = 4, CUDA cores (eight warps)
+    (4, 16, 8, 128, 300, 3000),   # G = 2, CUDA cores (eight warps)
+    (4, 32, 8, 128, 300, 3000),   # G = 4, mma.sync (four warps)
     (2, 16, 2, 64, 100, 2500),    # G = 8, mma.sync, d_h = 64
     (8, 64, 8, 128, 1000, 6000),  # G = 8, the 70B-class layer shape, shorter contexts
     (6, 32, 1, 128, 2000, 5000),  # G = 32, MQA (eight warps)
-], ids=["G4", "G8_d64", "G8", "G32"])
+], ids=["G2", "G4", "G8_d64", "G8", "G32"])
 def test_overlapped_fused_layers_equal_serial_ones_bit_for_bit(mqa, shape, graph):
     dev = torch.device("cuda")
     pos, lens, data = _layers(*shape, n=4, seed=700 + shape[1] + shape[2], dev=dev)

@@ -79,11 +79,12 @@ def gpu_paged(case, mqa, fused=True, stream=None):
 SHAPES = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 64, 128, 128),      # tiny MQA step, G = 8 (mma.sync)
-    (3, 8, 2, 64, 0, 300),        # G = 4, lengths from 1
+    (3, 8, 2, 64, 0, 300),        # G = 4 (mma.sync), lengths from 1
     (2, 16, 2, 128, 100, 700),    # G = 8, mma.sync
     (2, 32, 1, 128, 1, 1000),     # G = 32, eight consumer warps
     (4, 32, 8, 128, 0, 513),      # GQA 8B-class heads, short ragged contexts
     (2, 7, 1, 128, 60, 200),      # G = 7
+    (3, 4, 2, 128, 0, 300),       # G = 2, CUDA cores, lengths from 1
 ]
 PAGE_SIZES = [8, 16, 32, 64, 128]
 

@@ -76,7 +76,7 @@ def test_a_wait_that_runs_out_reports_a_timeout_and_the_next_call_is_right(mqa, 
     P.assert_close(out, out_ref, f"after a timeout, path {path}")
 
 
-@pytest.mark.parametrize("h", [8, 32], ids=["cuda_cores_G4", "mma_sync_G16"])
+@pytest.mark.parametrize("h", [4, 32], ids=["cuda_cores_G2", "mma_sync_G16"])
 def test_a_timeout_with_arrivals_counted_is_cleared_for_a_larger_later_call(mqa, h):
     """A launch over 600 (sequence, KV head) segments gives up after its CTAs have counted their
     arrivals at split segments (testing stall 2), leaving those counters non-zero. A small call
