@@ -103,6 +103,20 @@ def whole_job_us_per_step(ms_per_step: float, world: int) -> float:
     return ms_per_step * 1000.0 / world
 
 
+def measured_peak_bf16():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1800.0, "fallback"
+
+
+def is_prefill(w, T: int) -> bool:
+    """Several tokens with more than 64 rows per KV head run on the tcgen05 prefill kernel."""
+    return T > 1 and T * (w.h // w.g) > 64
+
+
 def measured_peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -271,6 +285,9 @@ def traffic_key(w, paged: int = 0, kv: str = "bf16", T: int = 1) -> str:
 def path_name(w, kv: str = "bf16", T: int = 1) -> str:
     """The inner-product path the library picks for this workload (its automatic rule)."""
     G = w.h // w.g
+    if is_prefill(w, T):
+        return (f"tcgen05 tensor cores (prefill kernel), {T} tokens x {G} heads = {T * G} rows "
+                "per KV head in 128-row tiles")
     if T > 1:
         return f"mma.sync tensor cores, {T} tokens x {G} heads = {T * G} rows per KV head"
     if G <= 2:
@@ -309,22 +326,53 @@ class OracleLayer:
         self.scale = w2.scale
         self.threads = oracle.num_threads()
 
+    # past this many attended (row, key) pairs a layer is timed on a sample of its tokens
+    MAX_PAIRS = 80_000_000   # about 40 GFLOP of fp64 at d_h = 128: some 20 s on 16 cores
+
+    def _sample(self):
+        """Tokens timed for T > 1: all when the layer is small, else an even sample, each token
+        run as the one-token attention it is (its own causal length)."""
+        T = self.T
+        pairs = self.w.h * sum(T * int(L) - T * (T - 1) // 2 for L in self.lens.tolist())
+        if T == 1 or pairs <= self.MAX_PAIRS:
+            return None
+        n = max(1, min(T, int(T * self.MAX_PAIRS / pairs)))
+        return sorted({int(round(i * (T - 1) / max(n - 1, 1))) for i in range(n)})
+
     def time_layer(self) -> float:
-        """Seconds of one whole-layer attention by the oracle (all sequences, all heads)."""
+        """Seconds of one whole-layer attention by the oracle (all sequences, all heads); with a
+        token sample, the sample's time scaled by the attended rows of the whole layer."""
+        import numpy as np
+
         import oracle
+        toks = self._sample()
         t0 = time.perf_counter()
-        if self.T > 1:
+        if self.T > 1 and toks is None:
             oracle.decode_attention_multi(self.q, self.k, self.v, self.lens, self.scale,
                                           threads=self.threads)
-        else:
+            return time.perf_counter() - t0
+        if self.T == 1:
             oracle.decode_attention(self.q, self.k, self.v, self.lens, self.scale,
                                     threads=self.threads)
-        return time.perf_counter() - t0
+            return time.perf_counter() - t0
+        T, rows_sampled = self.T, 0
+        for t in toks:
+            lim = (self.lens - T + 1 + t).astype(np.int32)
+            oracle.decode_attention(np.ascontiguousarray(self.q[:, t]), self.k, self.v, lim,
+                                    self.scale, threads=self.threads)
+            rows_sampled += int(lim.sum())
+        spent = time.perf_counter() - t0
+        rows_all = sum(T * int(L) - T * (T - 1) // 2 for L in self.lens.tolist())
+        return spent * rows_all / rows_sampled
 
     def describe(self, seconds: float) -> str:
         w = self.w
+        toks = self._sample()
+        part = ("" if toks is None else
+                f"; {len(toks)} of {self.T} tokens timed (each at its own causal length), scaled "
+                "by attended rows to the whole layer")
         return (f"one whole layer measured ({w.b} sequences, lengths {self.lens.tolist()}, all "
-                f"{w.h} heads" + (f", {self.T} tokens" if self.T > 1 else "")
+                f"{w.h} heads" + (f", {self.T} tokens" if self.T > 1 else "") + part
                 + f"): {seconds:.2f} s of oracle time, x {w.layers} identical layer(s)")
 
 
@@ -477,10 +525,14 @@ def measure_workload(w, dev, stream, args, mqa, flush_buf, T=1, kv="bf16", paged
         "algorithmic_bytes_per_launch": units.bytes_per_launch,
         "kv_gbs": gbs, "frac_of_hbm": gbs / peak,
         "kv_gbs_isolated": units.bytes_per_launch / (us_iso * 1e-6) / 1e9,
+        # one attention launch per layer (the prefill step adds an append launch per layer)
+        "tflops": units.flops_per_launch * w.layers / (us_step * 1e-6) / 1e12,
         "path": path_name(w, kv, T),
-        "kernel": "decode_attention_kernel (fused append + attention, mqa_decode_step"
-                  + ("_fp8" if kv == "fp8" else "_paged" if paged else "_multi" if T > 1 else "")
-                  + ")",
+        "kernel": ("prefill_attention_tc_kernel (mqa_decode_step_multi: an append launch, "
+                   "then this)" if is_prefill(w, T) else
+                   "decode_attention_kernel (fused append + attention, mqa_decode_step"
+                   + ("_fp8" if kv == "fp8" else "_paged" if paged else "_multi" if T > 1 else "")
+                   + ")"),
         "l2": workload_config(w, paged, kv, T)["l2"],
         "overlap": "consecutive launches overlap (mqa_set_launch_overlap)"
                    + ("; the L2 flush between steps separates them" if flush is not None else ""),
@@ -593,6 +645,27 @@ def run_ours(args, world, rank, local):
         achieved = nbytes / (us_launch * 1e-6) / 1e9
         traffic = recorded_traffic(traffic_key(w, paged, kv, T))
         value_us = whole_job_us_per_step(us_step / 1000.0, world)
+        common = {"kernel": summary["kernel"], "algorithmic_bytes_per_launch": nbytes,
+                  "flops_per_launch": units.flops_per_launch, "us_per_launch": us_launch,
+                  "us_per_launch_from": "step time / launches per step "
+                                        "(launches x us_per_launch = ms_per_step)"}
+        if is_prefill(w, T):
+            # the prefill kernel's score and value products are dense: tensor-bound
+            tpeak, tkind = measured_peak_bf16()
+            tflops = units.flops_per_launch * w.layers / (us_step * 1e-6) / 1e12
+            roofline = dict({"bound": "tensor", "achieved": tflops, "peak": tpeak,
+                             "unit": "TFLOP/s", "frac": tflops / tpeak, "traffic": traffic,
+                             "peak_kind": f"{tkind} cuBLAS bf16 (burst)",
+                             "note": "attention FLOPs of a step over the whole step time "
+                                     "(an append launch and an attention launch per layer)"},
+                            **common)
+        else:
+            roofline = dict({"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": traffic,
+                             "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                             "read_stream_reference": dict(read_ref,
+                                                           frac=achieved / read_ref["gbs"])},
+                            **common)
         lay = OracleLayer(w, T)
         cb_s = lay.time_layer()
         cb_us = cb_s * w.layers * 1e6
@@ -604,17 +677,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic", "config": workload_config(w, paged, kv, T),
             "kv_gbs": achieved, "kv_frac_of_peak": achieved / peak,
             "attention_us_per_layer": us_launch,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"{peak_kind} copy bandwidth (burst)",
-                         "kernel": summary["kernel"],
-                         "algorithmic_bytes_per_launch": nbytes,
-                         "us_per_launch": us_launch,
-                         "us_per_launch_from": "step time / launches per step "
-                                               "(launches x us_per_launch = ms_per_step)",
-                         "flops_per_launch": units.flops_per_launch,
-                         "read_stream_reference": dict(read_ref,
-                                                       frac=achieved / read_ref["gbs"])},
+            "roofline": roofline,
             "configs": configs,
             "e2e": {"value": whole_job_us_per_step(e2e_step / 1000.0, world), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
