@@ -392,16 +392,18 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
       if (!ok && !*b.abort) give_up(b, kSiteEpiloguePv, k);
       if (!__all_sync(0xffffffffu, ok)) return false;
       tc_fence_after_sync();
-      if (lim > 0) {
-        const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(
-            P.out + ((static_cast<size_t>(cur.bi) * P.T + t_row) * P.h +
-                     static_cast<size_t>(cur.j) * P.Gh + hh) * D);
+      // tcgen05.ld and tcgen05.wait are warp-collective (.sync.aligned): every lane runs them,
+      // padding rows included; only real rows (lim > 0) store
+      const float inv = lim > 0 ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(
+          P.out + ((static_cast<size_t>(cur.bi) * P.T + t_row) * P.h +
+                   static_cast<size_t>(cur.j) * P.Gh + hh) * D);
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + kTcOCol + c, o);
-          tmem_wait_ld();
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTcOCol + c, o);
+        tmem_wait_ld();
+        if (lim > 0) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
