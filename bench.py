@@ -290,8 +290,8 @@ def path_name(w, kv: str = "bf16", T: int = 1) -> str:
                 "per KV head in 128-row tiles")
     if T > 1:
         return f"mma.sync tensor cores, {T} tokens x {G} heads = {T * G} rows per KV head"
-    if G <= 2:
-        return f"CUDA cores (fp32 FMA), G={G}" + (" over widened fp8 codes" if kv == "fp8" else "")
+    if G <= 2 and kv != "fp8":
+        return f"CUDA cores (fp32 FMA), G={G}"
     return f"mma.sync tensor cores, G={G}" + (" (fp16 over widened fp8 codes)" if kv == "fp8"
                                               else " (bf16)")
 

@@ -406,8 +406,8 @@ MQA_API uint64_t mqa_kernel_launch_count(void);
 
 /*
  * Testing hook: force the number of CTAs that split the attention work (0 = automatic choice)
- * and the inner-product path: 0 = automatic (CUDA cores when h/g <= 2, mma.sync tensor cores
- * otherwise); 1 = CUDA cores (h/g <= 7 only); 2 = mma.sync tensor cores; 3 = tcgen05 tensor cores
+ * and the inner-product path: 0 = automatic (CUDA cores when h/g <= 2 over bf16 caches,
+ * mma.sync tensor cores otherwise, and for fp8 caches at every h/g); 1 = CUDA cores (h/g <= 7 only); 2 = mma.sync tensor cores; 3 = tcgen05 tensor cores
  * with tensor-memory accumulators. Process-wide; returns
  * MQA_ERR_INVALID_ARG for a negative CTA count or an unknown path. Results must not depend on
  * either setting beyond rounding.

@@ -392,6 +392,7 @@ struct DecodePlan {
   float scale;
   Path path;
   bool prefill = false;  // several tokens with more than 64 rows per KV head: the prefill kernel
+  bool path_forced = false;  // mqa_debug_override chose the inner-product path
   cudaStream_t stream;
   int dev;
   long long bg, ctas;
@@ -467,6 +468,7 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   p.bg = bg;
   p.ctas = ctas;
   p.prefill = prefill;
+  p.path_forced = force_path != kPathAuto;
   const bool split = ctas > 1 && !prefill;
   p.part_o_bytes = split ? static_cast<size_t>(slots) * G * d_h * sizeof(float) : 0;
   p.partial_bytes = split ? p.part_o_bytes + static_cast<size_t>(slots) * G * sizeof(float2) : 0;
@@ -581,7 +583,11 @@ int launch_decode(const DecodePlan& p, const Scratch& sc) {
   P.max_pages = p.paged.max_pages;
   P.num_pages = p.paged.num_pages;
 
-  const AttnKernelChoice kc = p.eb == 1       ? pick_kernel_fp8(p.path, p.G, p.b)
+  // fp8 caches: mma.sync at every group size unless forced. Measured on B300 (32K rows, launches
+  // back to back): the fp8 CUDA-core consumer reaches 0.37 (G = 1) to 0.21 (G = 7) of the copy
+  // bandwidth on fp8 bytes, the fp16 mma.sync consumer 0.72-0.73 at every G.
+  const Path fp8_path = p.path_forced ? p.path : kPathMmaSync;
+  const AttnKernelChoice kc = p.eb == 1       ? pick_kernel_fp8(fp8_path, p.G, p.b)
                               : p.d_h == 128 ? pick_kernel<128>(p.path, p.G, p.b, p.T)
                                              : pick_kernel<64>(p.path, p.G, p.b, p.T);
   if (!kc.fn) return MQA_ERR_UNSUPPORTED;

@@ -75,7 +75,7 @@ SHAPES = [
     # b, h, g, d_h, ctx_lo, ctx_hi
     (1, 8, 1, 128, 128, 128),     # G = 8, mma.sync (four consumer warps)
     (3, 8, 2, 128, 0, 300),       # G = 4
-    (3, 4, 2, 128, 0, 300),       # G = 2, CUDA cores
+    (3, 4, 2, 128, 0, 300),       # G = 2 (mma.sync: fp8 caches take it at every G)
     (2, 7, 1, 128, 60, 200),      # G = 7
     (2, 4, 4, 128, 60, 70),       # G = 1 (MHA) around the tile edge
     (2, 32, 2, 128, 100, 700),    # G = 16
