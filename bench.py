@@ -427,7 +427,11 @@ class Units:
             if kv == "fp8":
                 ks, vs = inputs.amax_scale(k), inputs.amax_scale(v)
                 k, v = inputs.fp8_codes(k, ks), inputs.fp8_codes(v, vs)
-                self.layers.append(LayerState(k, v, fp8_scales=(ks, vs)))
+                if paged:
+                    k, v, table = inputs.page_pool(k, v, lens, paged, seed=PAGE_TABLE_SEED)
+                    if table_d is None:
+                        table_d = table.to(dev)
+                self.layers.append(LayerState(k, v, table_d, fp8_scales=(ks, vs)))
             elif paged:
                 k, v, table = inputs.page_pool(k, v, lens, paged, seed=PAGE_TABLE_SEED)
                 if table_d is None:
@@ -712,10 +716,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=1, metavar="T",
                     help="new tokens per sequence per step (causal; T > 1: speculative decoding)")
     args = ap.parse_args(argv)
-    if args.kv == "fp8" and args.paged:
-        ap.error("--kv fp8 runs on contiguous caches")
-    if args.tokens < 1 or (args.tokens > 1 and (args.kv == "fp8" or args.paged)):
-        ap.error("--tokens T > 1 runs on contiguous bf16 caches")
+    if args.tokens < 1 or (args.tokens > 1 and args.kv == "fp8"):
+        ap.error("--tokens T > 1 runs on bf16 caches")
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()

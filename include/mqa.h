@@ -281,6 +281,64 @@ MQA_API int mqa_decode_step_multi(const mqa_bf16* q, const mqa_bf16* k_new,
                                   void* stream);
 
 /*
+ * Paged caches with fp8 codes or with several new tokens: mqa_kv_append_paged_fp8,
+ * mqa_decode_attention_paged_fp8, mqa_decode_step_paged_fp8 and mqa_kv_append_paged_multi,
+ * mqa_decode_attention_paged_multi, mqa_decode_step_paged_multi.
+ *
+ * A serving stack keeps its cache in pages and also quantizes it, or verifies several draft
+ * tokens at once: the nanhubrain.csdn.net MQA article §3.3 (vLLM's paged blocks) with §4.3
+ * question 3 (quantized K/V), and "GQA与MQA深度实战" (ybb.press) §十 items 7 and 12. These calls
+ * combine the page layout of the paged calls with the element type of the fp8 calls, or with the
+ * T tokens of the several-token calls; each is defined as the operation of the non-paged call on
+ * the rows the page table maps:
+ *   - pools, table, page_size, max_pages, num_pages: as for mqa_kv_append_paged (n_max of a
+ *     sequence is max_pages * page_size);
+ *   - the fp8 calls: pools [num_pages][g][page_size][d_h] of E4M3 codes (uint8), d_h = 128,
+ *     k_scale and v_scale as for mqa_kv_append_fp8; one new token per sequence;
+ *   - the several-token calls: q and out [b][T][h][d_h], k_new and v_new [b][T][g][d_h], token t
+ *     of sequence bi written at row pos[bi] + t through the table and attending the first
+ *     seq_lens[bi] - T + 1 + t rows; T * (h / g) <= 64 (the mma.sync decode kernel; a larger T
+ *     returns MQA_ERR_UNSUPPORTED here: the prefill kernel reads contiguous caches).
+ * A pos whose rows do not all fit the table skips that sequence's append, a used page index
+ * outside [0, num_pages) skips that row (its attention reads zeros there); both latch
+ * MQA_ERR_DEVICE_BOUNDS. The fused steps are one launch and use the workspace of
+ * mqa_decode_attention. Returns MQA_OK, MQA_ERR_INVALID_ARG, MQA_ERR_UNSUPPORTED or MQA_ERR_CUDA.
+ */
+MQA_API int mqa_kv_append_paged_fp8(const mqa_bf16* k_new, const mqa_bf16* v_new,
+                                    uint8_t* k_pool, uint8_t* v_pool, const int32_t* pos,
+                                    const int32_t* page_table, int b, int g, int d_h,
+                                    int page_size, int max_pages, int num_pages, float k_scale,
+                                    float v_scale, void* stream);
+MQA_API int mqa_decode_attention_paged_fp8(const mqa_bf16* q, const uint8_t* k_pool,
+                                           const uint8_t* v_pool, const int32_t* page_table,
+                                           const int32_t* seq_lens, mqa_bf16* out, int b, int h,
+                                           int g, int d_h, int page_size, int max_pages,
+                                           int num_pages, float scale, float k_scale,
+                                           float v_scale, void* stream);
+MQA_API int mqa_decode_step_paged_fp8(const mqa_bf16* q, const mqa_bf16* k_new,
+                                      const mqa_bf16* v_new, uint8_t* k_pool, uint8_t* v_pool,
+                                      const int32_t* pos, const int32_t* page_table,
+                                      const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g,
+                                      int d_h, int page_size, int max_pages, int num_pages,
+                                      float scale, float k_scale, float v_scale, void* stream);
+MQA_API int mqa_kv_append_paged_multi(const mqa_bf16* k_new, const mqa_bf16* v_new,
+                                      mqa_bf16* k_pool, mqa_bf16* v_pool, const int32_t* pos,
+                                      const int32_t* page_table, int b, int T, int g, int d_h,
+                                      int page_size, int max_pages, int num_pages, void* stream);
+MQA_API int mqa_decode_attention_paged_multi(const mqa_bf16* q, const mqa_bf16* k_pool,
+                                             const mqa_bf16* v_pool, const int32_t* page_table,
+                                             const int32_t* seq_lens, mqa_bf16* out, int b, int T,
+                                             int h, int g, int d_h, int page_size, int max_pages,
+                                             int num_pages, float scale, void* stream);
+MQA_API int mqa_decode_step_paged_multi(const mqa_bf16* q, const mqa_bf16* k_new,
+                                        const mqa_bf16* v_new, mqa_bf16* k_pool,
+                                        mqa_bf16* v_pool, const int32_t* pos,
+                                        const int32_t* page_table, const int32_t* seq_lens,
+                                        mqa_bf16* out, int b, int T, int h, int g, int d_h,
+                                        int page_size, int max_pages, int num_pages, float scale,
+                                        void* stream);
+
+/*
  * mqa_decode_attention_noalloc -- mqa_decode_attention for callers that cannot allocate device
  * memory. The source pages have no counterpart to this call; it exists for users of the library.
  *

@@ -88,6 +88,14 @@ def _configure(lib):
     lib.oracle_decode_attention_multi_bf16.restype = i32
     lib.oracle_decode_attention_multi_bf16.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                        i32, i32, dbl, i32]
+    lib.oracle_gather_pages_u8.restype = i32
+    lib.oracle_gather_pages_u8.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.oracle_kv_append_paged_multi.restype = i32
+    lib.oracle_kv_append_paged_multi.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                 i32, i32]
+    lib.oracle_kv_append_paged_fp8.restype = i32
+    lib.oracle_kv_append_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                               i32, ctypes.c_float, ctypes.c_float]
     lib.oracle_num_threads.restype = i32
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -258,6 +266,61 @@ def kv_append_paged(k_new, v_new, k_pool, v_pool, pos, table) -> int:
     b, max_pages = tb.shape
     return int(lib.oracle_kv_append_paged(_ptr(kn), _ptr(vn), _ptr(k_pool), _ptr(v_pool), _ptr(p),
                                           _ptr(tb), b, g, d_h, page_size, max_pages, num_pages))
+
+
+def gather_pages_u8(pool, table, page_size: int):
+    """gather_pages for a pool of one-byte codes [num_pages, g, page_size, d_h] (uint8): the
+    contiguous codes [b, g, max_pages * page_size, d_h]; rows of out-of-range pages are code 0 and
+    the status is 4. Returns (cache, status)."""
+    lib = _load()
+    pl = _c(pool, np.uint8)
+    tb = _c(table, np.int32)
+    num_pages, g, ps, d_h = pl.shape
+    if ps != page_size:
+        raise ValueError("page size mismatch")
+    b, max_pages = tb.shape
+    out = np.empty((b, g, max_pages * page_size, d_h), dtype=np.uint8)
+    st = int(lib.oracle_gather_pages_u8(_ptr(pl), _ptr(tb), b, g, d_h, page_size, max_pages,
+                                        num_pages, _ptr(out)))
+    if st == ERR_INVALID_ARG:
+        raise ValueError("oracle rejected the arguments")
+    return out, st
+
+
+def kv_append_paged_multi(k_new, v_new, k_pool, v_pool, pos, table) -> int:
+    """T new rows per sequence through the page table, in place (k_new [b, T, g, d_h]; pools
+    C-contiguous uint16 numpy arrays)."""
+    lib = _load()
+    for c in (k_pool, v_pool):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint16 and c.flags.c_contiguous):
+            raise TypeError("pools must be C-contiguous uint16 numpy arrays (updated in place)")
+    num_pages, g, page_size, d_h = k_pool.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    b, T = kn.shape[0], kn.shape[1]
+    p = _c(pos, np.int32)
+    tb = _c(table, np.int32)
+    max_pages = tb.shape[1]
+    return int(lib.oracle_kv_append_paged_multi(_ptr(kn), _ptr(vn), _ptr(k_pool), _ptr(v_pool),
+                                                _ptr(p), _ptr(tb), b, T, g, d_h, page_size,
+                                                max_pages, num_pages))
+
+
+def kv_append_paged_fp8(k_new, v_new, k_pool, v_pool, pos, table, k_scale: float,
+                        v_scale: float) -> int:
+    """The quantized append through the page table, in place (pools of codes: C-contiguous uint8
+    numpy arrays [num_pages, g, page_size, d_h])."""
+    lib = _load()
+    for c in (k_pool, v_pool):
+        if not (isinstance(c, np.ndarray) and c.dtype == np.uint8 and c.flags.c_contiguous):
+            raise TypeError("pools must be C-contiguous uint8 numpy arrays (updated in place)")
+    num_pages, g, page_size, d_h = k_pool.shape
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    p = _c(pos, np.int32)
+    tb = _c(table, np.int32)
+    b, max_pages = tb.shape
+    return int(lib.oracle_kv_append_paged_fp8(_ptr(kn), _ptr(vn), _ptr(k_pool), _ptr(v_pool),
+                                              _ptr(p), _ptr(tb), b, g, d_h, page_size, max_pages,
+                                              num_pages, float(k_scale), float(v_scale)))
 
 
 def e4m3_to_f64(codes) -> np.ndarray:

@@ -275,6 +275,104 @@ int oracle_kv_append_paged(const uint16_t* k_new, const uint16_t* v_new, uint16_
   return status;
 }
 
+/* The same gather for a pool of one-byte E4M3 codes (fp8 caches): rows of out-of-range pages   */
+/* come back as code 0 (the value 0) and the call reports ORACLE_ERR_BOUNDS.                    */
+int oracle_gather_pages_u8(const uint8_t* pool, const int32_t* table, int b, int g, int d_h,
+                           int page_size, int max_pages, int num_pages, uint8_t* cache) {
+  if (!pool || !table || !cache) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+    return ORACLE_ERR_INVALID_ARG;
+  const int n_max = max_pages * page_size;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi)
+    for (int j = 0; j < g; ++j)
+      for (int t = 0; t < n_max; ++t) {
+        uint8_t* dst = cache + (((size_t)bi * g + j) * (size_t)n_max + (size_t)t) * (size_t)d_h;
+        const int pg = table[(size_t)bi * max_pages + (t / page_size)];
+        if (pg < 0 || pg >= num_pages) {
+          status = ORACLE_ERR_BOUNDS;
+          memset(dst, 0, (size_t)d_h);
+          continue;
+        }
+        const size_t in_page = (size_t)(t % page_size);
+        memcpy(dst, pool + (((size_t)pg * g + j) * (size_t)page_size + in_page) * (size_t)d_h,
+               (size_t)d_h);
+      }
+  return status;
+}
+
+/* Several tokens through the table ([GQA-MQA] §八 with T new tokens; [MQA-CSDN] §3.3 paging):  */
+/* token t of sequence b goes to row pos[b] + t, i.e. row (pos[b] + t) % page_size of KV head j */
+/* in page table[b][(pos[b] + t) / page_size]. A sequence whose rows pos .. pos + T - 1 are not */
+/* all in [0, max_pages * page_size) is skipped; a row whose page index is out of range is      */
+/* skipped alone (the sequence's other rows are written); both report ORACLE_ERR_BOUNDS.       */
+int oracle_kv_append_paged_multi(const uint16_t* k_new, const uint16_t* v_new, uint16_t* k_pool,
+                                 uint16_t* v_pool, const int32_t* pos, const int32_t* table,
+                                 int b, int T, int g, int d_h, int page_size, int max_pages,
+                                 int num_pages) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !pos || !table) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || T <= 0 || g <= 0 || d_h <= 0 || page_size <= 0 || max_pages <= 0 ||
+      num_pages <= 0)
+    return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    const int p0 = pos[bi];
+    if (p0 < 0 || (long long)p0 + T > (long long)max_pages * page_size) {
+      status = ORACLE_ERR_BOUNDS;
+      continue;
+    }
+    for (int t = 0; t < T; ++t) {
+      const int p = p0 + t;
+      const int page = table[(size_t)bi * max_pages + p / page_size];
+      if (page < 0 || page >= num_pages) { status = ORACLE_ERR_BOUNDS; continue; }
+      const size_t row_in_page = (size_t)(p % page_size);
+      for (int j = 0; j < g; ++j) {
+        const size_t src = (((size_t)bi * T + t) * g + j) * (size_t)d_h;
+        const size_t dst = (((size_t)page * g + j) * (size_t)page_size + row_in_page) *
+                           (size_t)d_h;
+        memcpy(k_pool + dst, k_new + src, (size_t)d_h * sizeof(uint16_t));
+        memcpy(v_pool + dst, v_new + src, (size_t)d_h * sizeof(uint16_t));
+      }
+    }
+  }
+  return status;
+}
+
+/* The quantized append through the table: the codes of oracle_kv_append_fp8                   */
+/* (e4m3(float(x) / scale), the division once in binary32) at the row oracle_kv_append_paged    */
+/* writes. A bad position or page skips the sequence and reports ORACLE_ERR_BOUNDS.             */
+int oracle_kv_append_paged_fp8(const uint16_t* k_new, const uint16_t* v_new, uint8_t* k_pool,
+                               uint8_t* v_pool, const int32_t* pos, const int32_t* table, int b,
+                               int g, int d_h, int page_size, int max_pages, int num_pages,
+                               float k_scale, float v_scale) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !pos || !table) return ORACLE_ERR_INVALID_ARG;
+  if (b <= 0 || g <= 0 || d_h <= 0 || page_size <= 0 || max_pages <= 0 || num_pages <= 0)
+    return ORACLE_ERR_INVALID_ARG;
+  if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale))
+    return ORACLE_ERR_INVALID_ARG;
+  int status = ORACLE_OK;
+  for (int bi = 0; bi < b; ++bi) {
+    const int p = pos[bi];
+    if (p < 0 || p >= max_pages * page_size) { status = ORACLE_ERR_BOUNDS; continue; }
+    const int page = table[(size_t)bi * max_pages + p / page_size];
+    if (page < 0 || page >= num_pages) { status = ORACLE_ERR_BOUNDS; continue; }
+    const size_t prow = (size_t)(p % page_size);
+    for (int j = 0; j < g; ++j) {
+      const size_t src = ((size_t)bi * g + j) * (size_t)d_h;
+      const size_t dst = (((size_t)page * g + j) * (size_t)page_size + prow) * (size_t)d_h;
+      for (int d = 0; d < d_h; ++d) {
+        const float kx = (float)oracle_bf16_to_double(k_new[src + d]);
+        const float vx = (float)oracle_bf16_to_double(v_new[src + d]);
+        volatile float kq = kx / k_scale;
+        volatile float vq = vx / v_scale;
+        k_pool[dst + d] = oracle_double_to_e4m3((double)kq);
+        v_pool[dst + d] = oracle_double_to_e4m3((double)vq);
+      }
+    }
+  }
+  return status;
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Grouped decode attention: [GQA-MQA] §五.                                                   */
 /* ------------------------------------------------------------------------------------------ */

@@ -11,6 +11,8 @@ _BINDING_NAMES = {
     "kv_append", "decode_attention", "decode_step", "kv_append_paged", "decode_attention_paged",
     "decode_step_paged", "kv_append_fp8", "decode_attention_fp8", "decode_step_fp8",
     "kv_append_multi", "decode_attention_multi", "decode_step_multi",
+    "kv_append_paged_fp8", "decode_attention_paged_fp8", "decode_step_paged_fp8",
+    "kv_append_paged_multi", "decode_attention_paged_multi", "decode_step_paged_multi",
     "get_device_status", "status_string", "MqaError", "set_launch_overlap",
     "library_path", "kernel_launch_count", "debug_override", "debug_timeout_site", "debug_set_wait_limit_ns", "debug_stall", "raw",
 }

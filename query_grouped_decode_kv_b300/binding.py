@@ -58,6 +58,25 @@ _lib.mqa_decode_attention_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i32,
 _lib.mqa_decode_step_multi.restype = _i32
 _lib.mqa_decode_step_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                                        _i32, _i32, _i32, _f32, _vp]
+_lib.mqa_kv_append_paged_fp8.restype = _i32
+_lib.mqa_kv_append_paged_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                         _i32, _i32, _f32, _f32, _vp]
+_lib.mqa_decode_attention_paged_fp8.restype = _i32
+_lib.mqa_decode_attention_paged_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                                _i32, _i32, _i32, _i32, _f32, _f32, _f32, _vp]
+_lib.mqa_decode_step_paged_fp8.restype = _i32
+_lib.mqa_decode_step_paged_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                           _i32, _i32, _i32, _i32, _i32, _i32, _f32, _f32, _f32,
+                                           _vp]
+_lib.mqa_kv_append_paged_multi.restype = _i32
+_lib.mqa_kv_append_paged_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _i32, _vp]
+_lib.mqa_decode_attention_paged_multi.restype = _i32
+_lib.mqa_decode_attention_paged_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                                  _i32, _i32, _i32, _i32, _i32, _f32, _vp]
+_lib.mqa_decode_step_paged_multi.restype = _i32
+_lib.mqa_decode_step_paged_multi.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32,
+                                             _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp]
 _lib.mqa_status_string.restype = ctypes.c_char_p
 _lib.mqa_status_string.argtypes = [_i32]
 _lib.mqa_get_device_status.restype = _i32
@@ -529,4 +548,178 @@ def decode_step_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                     float(scale), _vp(_stream_handle(stream)))
     if st:
         raise MqaError(st, "mqa_decode_step_multi")
+    return out
+
+
+def _fp8_pool_shape(k_pool: torch.Tensor, v_pool: torch.Tensor, page_table: torch.Tensor, b: int,
+                    what: str) -> tuple[int, int, int, int, int]:
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _check_fp8_cache(t, n)
+    _check(page_table, "page_table", torch.int32, 2)
+    num_pages, g, page_size, d_h = k_pool.shape
+    if v_pool.shape != k_pool.shape or page_table.shape[0] != b:
+        raise ValueError(f"{what}: inconsistent shapes")
+    return num_pages, g, page_size, d_h, page_table.shape[1]
+
+
+def _out_like(q: torch.Tensor, out: torch.Tensor | None, ndim: int, what: str) -> torch.Tensor:
+    if out is None:
+        return torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, ndim)
+    if out.shape != q.shape:
+        raise ValueError(f"{what}: out must have q's shape")
+    return out
+
+
+def kv_append_paged_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor,
+                        v_pool: torch.Tensor, pos: torch.Tensor, page_table: torch.Tensor,
+                        k_scale: float, v_scale: float, stream=None) -> None:
+    """:func:`kv_append_fp8` into paged fp8 pools ``[num_pages, g, page_size, d_h]`` (uint8
+    codes) through ``page_table`` ``[b, max_pages]``."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(pos, "pos", torch.int32, 1)
+    b = pos.shape[0]
+    num_pages, g, page_size, d_h, max_pages = _fp8_pool_shape(k_pool, v_pool, page_table, b,
+                                                              "kv_append_paged_fp8")
+    if k_new.shape != (b, g, d_h) or v_new.shape != (b, g, d_h):
+        raise ValueError("kv_append_paged_fp8: inconsistent shapes")
+    st = _lib.mqa_kv_append_paged_fp8(k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                                      v_pool.data_ptr(), pos.data_ptr(), page_table.data_ptr(), b,
+                                      g, d_h, page_size, max_pages, num_pages, float(k_scale),
+                                      float(v_scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append_paged_fp8")
+
+
+def decode_attention_paged_fp8(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                               page_table: torch.Tensor, seq_lens: torch.Tensor, k_scale: float,
+                               v_scale: float, out: torch.Tensor | None = None,
+                               scale: float | None = None, stream=None) -> torch.Tensor:
+    """:func:`decode_attention_fp8` over paged fp8 pools."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _fp8_pool_shape(k_pool, v_pool, page_table, b,
+                                                             "decode_attention_paged_fp8")
+    if dk != d_h or seq_lens.shape != (b,):
+        raise ValueError("decode_attention_paged_fp8: inconsistent shapes")
+    out = _out_like(q, out, 3, "decode_attention_paged_fp8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention_paged_fp8(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                             page_table.data_ptr(), seq_lens.data_ptr(),
+                                             out.data_ptr(), b, h, g, d_h, page_size, max_pages,
+                                             num_pages, float(scale), float(k_scale),
+                                             float(v_scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention_paged_fp8")
+    return out
+
+
+def decode_step_paged_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          k_pool: torch.Tensor, v_pool: torch.Tensor, pos: torch.Tensor,
+                          page_table: torch.Tensor, seq_lens: torch.Tensor, k_scale: float,
+                          v_scale: float, out: torch.Tensor | None = None,
+                          scale: float | None = None, stream=None) -> torch.Tensor:
+    """:func:`decode_step_fp8` over paged fp8 pools: one launch that quantizes and appends the
+    new rows through the table and attends."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _fp8_pool_shape(k_pool, v_pool, page_table, b,
+                                                             "decode_step_paged_fp8")
+    if dk != d_h or seq_lens.shape != (b,) or pos.shape != (b,) or k_new.shape != (b, g, d_h) \
+            or v_new.shape != (b, g, d_h):
+        raise ValueError("decode_step_paged_fp8: inconsistent shapes")
+    out = _out_like(q, out, 3, "decode_step_paged_fp8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step_paged_fp8(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                        k_pool.data_ptr(), v_pool.data_ptr(), pos.data_ptr(),
+                                        page_table.data_ptr(), seq_lens.data_ptr(),
+                                        out.data_ptr(), b, h, g, d_h, page_size, max_pages,
+                                        num_pages, float(scale), float(k_scale), float(v_scale),
+                                        _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step_paged_fp8")
+    return out
+
+
+def kv_append_paged_multi(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor,
+                          v_pool: torch.Tensor, pos: torch.Tensor, page_table: torch.Tensor,
+                          stream=None) -> None:
+    """T rows per sequence (``k_new`` [b, T, g, d_h]) through the page table: token t goes to
+    row ``pos[b] + t``."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    b, T = k_new.shape[0], k_new.shape[1]
+    num_pages, g, page_size, d_h, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                          "kv_append_paged_multi")
+    if k_new.shape != (b, T, g, d_h) or v_new.shape != (b, T, g, d_h) or pos.shape != (b,):
+        raise ValueError("kv_append_paged_multi: inconsistent shapes")
+    st = _lib.mqa_kv_append_paged_multi(k_new.data_ptr(), v_new.data_ptr(), k_pool.data_ptr(),
+                                        v_pool.data_ptr(), pos.data_ptr(), page_table.data_ptr(),
+                                        b, T, g, d_h, page_size, max_pages, num_pages,
+                                        _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_kv_append_paged_multi")
+
+
+def decode_attention_paged_multi(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                 page_table: torch.Tensor, seq_lens: torch.Tensor,
+                                 out: torch.Tensor | None = None, scale: float | None = None,
+                                 stream=None) -> torch.Tensor:
+    """:func:`decode_attention_multi` over paged caches (q [b, T, h, d_h])."""
+    _check(q, "q", torch.bfloat16, 4)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, T, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                         "decode_attention_paged_multi")
+    if dk != d_h or seq_lens.shape != (b,):
+        raise ValueError("decode_attention_paged_multi: inconsistent shapes")
+    out = _out_like(q, out, 4, "decode_attention_paged_multi")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_attention_paged_multi(q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+                                               page_table.data_ptr(), seq_lens.data_ptr(),
+                                               out.data_ptr(), b, T, h, g, d_h, page_size,
+                                               max_pages, num_pages, float(scale),
+                                               _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_attention_paged_multi")
+    return out
+
+
+def decode_step_paged_multi(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                            k_pool: torch.Tensor, v_pool: torch.Tensor, pos: torch.Tensor,
+                            page_table: torch.Tensor, seq_lens: torch.Tensor,
+                            out: torch.Tensor | None = None, scale: float | None = None,
+                            stream=None) -> torch.Tensor:
+    """One launch doing :func:`kv_append_paged_multi` then :func:`decode_attention_paged_multi`."""
+    _check(q, "q", torch.bfloat16, 4)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(pos, "pos", torch.int32, 1)
+    _check(seq_lens, "seq_lens", torch.int32, 1)
+    b, T, h, d_h = q.shape
+    num_pages, g, page_size, dk, max_pages = _pool_shape(k_pool, v_pool, page_table, b,
+                                                         "decode_step_paged_multi")
+    if dk != d_h or seq_lens.shape != (b,) or pos.shape != (b,) \
+            or k_new.shape != (b, T, g, d_h) or v_new.shape != (b, T, g, d_h):
+        raise ValueError("decode_step_paged_multi: inconsistent shapes")
+    out = _out_like(q, out, 4, "decode_step_paged_multi")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_h)
+    st = _lib.mqa_decode_step_paged_multi(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                          k_pool.data_ptr(), v_pool.data_ptr(), pos.data_ptr(),
+                                          page_table.data_ptr(), seq_lens.data_ptr(),
+                                          out.data_ptr(), b, T, h, g, d_h, page_size, max_pages,
+                                          num_pages, float(scale), _vp(_stream_handle(stream)))
+    if st:
+        raise MqaError(st, "mqa_decode_step_paged_multi")
     return out

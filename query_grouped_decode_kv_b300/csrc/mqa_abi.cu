@@ -657,6 +657,90 @@ int noalloc_scratch_address(int dev, Scratch* out) {
   return MQA_OK;
 }
 
+// T rows per sequence through a page table, bf16 (eb = 2) or fp8 codes (eb = 1), after the
+// host checks of the paged calls.
+int launch_append_paged_rows(const mqa_bf16* k_new, const mqa_bf16* v_new, void* k_pool,
+                             void* v_pool, const int32_t* pos, const PagedCache& pg, int b, int T,
+                             int g, int d_h, int eb, float k_scale, float v_scale,
+                             cudaStream_t stream) {
+  const long long rows = static_cast<long long>(b) * T * g;
+  if (rows > (1ll << 31)) return MQA_ERR_UNSUPPORTED;
+  const long long total = rows * (d_h * eb / 16);
+  const int threads = 256;
+  const long long want = (total + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 65535 ? want : 65535);
+  auto kern = eb == 2 ? mqa::kv_append_paged_rows_kernel<2> : mqa::kv_append_paged_rows_kernel<1>;
+  kern<<<blocks, threads, 0, stream>>>(
+      reinterpret_cast<const uint4*>(k_new), reinterpret_cast<const uint4*>(v_new),
+      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), pos, pg.table, b, T, g, d_h,
+      pg.page_size, pg.max_pages, pg.num_pages, k_scale, v_scale);
+  g_launches.fetch_add(1);
+  return launch_error();
+}
+
+// Host checks shared by the paged appends: pointers, alignment, sizes, the pool geometry.
+int check_paged_append(const mqa_bf16* k_new, const mqa_bf16* v_new, const void* k_pool,
+                       const void* v_pool, const int32_t* pos, const PagedCache& pg, int b, int T,
+                       int g, int d_h) {
+  if (!k_new || !v_new || !k_pool || !v_pool || !pos) return MQA_ERR_INVALID_ARG;
+  if (b <= 0 || T <= 0 || g <= 0 || d_h <= 0) return MQA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return MQA_ERR_INVALID_ARG;
+  int n_max = 0;
+  if (int st = check_paged(pg, g, d_h, &n_max)) return st;
+  if (d_h != 64 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  return MQA_OK;
+}
+
+PagedCache paged_cache(const int32_t* table, int page_size, int max_pages, int num_pages) {
+  PagedCache pg;
+  pg.table = table;
+  pg.page_size = page_size;
+  pg.max_pages = max_pages;
+  pg.num_pages = num_pages;
+  return pg;
+}
+
+// Paged attention (and the fused step when k_new is given) after the host checks: fp8 codes
+// (eb = 1, with scales) or bf16 (eb = 2), T tokens per sequence on the decode kernels.
+int paged_decode(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                 const void* k_pool, const void* v_pool, const int32_t* pos,
+                 const PagedCache& pg, const int32_t* seq_lens, mqa_bf16* out, int b, int T,
+                 int h, int g, int d_h, float scale, int eb, float k_scale, float v_scale,
+                 void* stream) {
+  if (g <= 0) return MQA_ERR_INVALID_ARG;
+  if (k_new && (!v_new || !pos)) return MQA_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new) ||
+                (reinterpret_cast<uintptr_t>(pos) & 3u)))
+    return MQA_ERR_INVALID_ARG;
+  if (eb == 1 && !(std::isfinite(k_scale) && std::isfinite(v_scale) && k_scale > 0.f &&
+                   v_scale > 0.f))
+    return MQA_ERR_INVALID_ARG;
+  if (eb == 1 && d_h > 0 && d_h != 128) return MQA_ERR_UNSUPPORTED;
+  int n_max = 0;
+  if (int st = check_paged(pg, g, d_h, &n_max)) return st;
+  DecodePlan plan;
+  if (int st = plan_decode(q, static_cast<const mqa_bf16*>(k_pool),
+                           static_cast<const mqa_bf16*>(v_pool), seq_lens, out, b, h, g, d_h,
+                           n_max, scale, stream, &plan, T))
+    return st;
+  if (plan.prefill) return MQA_ERR_UNSUPPORTED;  // the prefill kernel reads contiguous caches
+  plan.paged = pg;
+  plan.eb = eb;
+  plan.k_scale = eb == 1 ? k_scale : 1.f;
+  plan.v_scale = eb == 1 ? v_scale : 1.f;
+  plan.k_new = k_new;
+  plan.v_new = v_new;
+  plan.pos = pos;
+  Scratch sc;
+  if (plan.ctas > 1) {
+    if (int st = get_workspace(plan.dev, plan.stream, plan.partial_bytes, plan.counter_bytes, &sc))
+      return st;
+  }
+  return launch_decode(plan, sc);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1049,6 +1133,71 @@ int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_cache,
     if (int st = noalloc_scratch_address(plan.dev, &sc)) return st;
   }
   return launch_decode(plan, sc);
+}
+
+int mqa_kv_append_paged_multi(const mqa_bf16* k_new, const mqa_bf16* v_new, mqa_bf16* k_pool,
+                              mqa_bf16* v_pool, const int32_t* pos, const int32_t* page_table,
+                              int b, int T, int g, int d_h, int page_size, int max_pages,
+                              int num_pages, void* stream) {
+  const PagedCache pg = paged_cache(page_table, page_size, max_pages, num_pages);
+  if (int st = check_paged_append(k_new, v_new, k_pool, v_pool, pos, pg, b, T, g, d_h)) return st;
+  return launch_append_paged_rows(k_new, v_new, k_pool, v_pool, pos, pg, b, T, g, d_h, 2, 1.f,
+                                  1.f, static_cast<cudaStream_t>(stream));
+}
+
+int mqa_decode_attention_paged_multi(const mqa_bf16* q, const mqa_bf16* k_pool,
+                                     const mqa_bf16* v_pool, const int32_t* page_table,
+                                     const int32_t* seq_lens, mqa_bf16* out, int b, int T, int h,
+                                     int g, int d_h, int page_size, int max_pages, int num_pages,
+                                     float scale, void* stream) {
+  return paged_decode(q, nullptr, nullptr, k_pool, v_pool, nullptr,
+                      paged_cache(page_table, page_size, max_pages, num_pages), seq_lens, out, b,
+                      T, h, g, d_h, scale, 2, 1.f, 1.f, stream);
+}
+
+int mqa_decode_step_paged_multi(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                                mqa_bf16* k_pool, mqa_bf16* v_pool, const int32_t* pos,
+                                const int32_t* page_table, const int32_t* seq_lens,
+                                mqa_bf16* out, int b, int T, int h, int g, int d_h, int page_size,
+                                int max_pages, int num_pages, float scale, void* stream) {
+  if (!k_new) return MQA_ERR_INVALID_ARG;
+  return paged_decode(q, k_new, v_new, k_pool, v_pool, pos,
+                      paged_cache(page_table, page_size, max_pages, num_pages), seq_lens, out, b,
+                      T, h, g, d_h, scale, 2, 1.f, 1.f, stream);
+}
+
+int mqa_kv_append_paged_fp8(const mqa_bf16* k_new, const mqa_bf16* v_new, uint8_t* k_pool,
+                            uint8_t* v_pool, const int32_t* pos, const int32_t* page_table, int b,
+                            int g, int d_h, int page_size, int max_pages, int num_pages,
+                            float k_scale, float v_scale, void* stream) {
+  const PagedCache pg = paged_cache(page_table, page_size, max_pages, num_pages);
+  if (int st = check_paged_append(k_new, v_new, k_pool, v_pool, pos, pg, b, 1, g, d_h)) return st;
+  if (!valid_fp8_scales(k_scale, v_scale)) return MQA_ERR_INVALID_ARG;
+  if (d_h != 128) return MQA_ERR_UNSUPPORTED;
+  return launch_append_paged_rows(k_new, v_new, k_pool, v_pool, pos, pg, b, 1, g, d_h, 1, k_scale,
+                                  v_scale, static_cast<cudaStream_t>(stream));
+}
+
+int mqa_decode_attention_paged_fp8(const mqa_bf16* q, const uint8_t* k_pool,
+                                   const uint8_t* v_pool, const int32_t* page_table,
+                                   const int32_t* seq_lens, mqa_bf16* out, int b, int h, int g,
+                                   int d_h, int page_size, int max_pages, int num_pages,
+                                   float scale, float k_scale, float v_scale, void* stream) {
+  return paged_decode(q, nullptr, nullptr, k_pool, v_pool, nullptr,
+                      paged_cache(page_table, page_size, max_pages, num_pages), seq_lens, out, b,
+                      1, h, g, d_h, scale, 1, k_scale, v_scale, stream);
+}
+
+int mqa_decode_step_paged_fp8(const mqa_bf16* q, const mqa_bf16* k_new, const mqa_bf16* v_new,
+                              uint8_t* k_pool, uint8_t* v_pool, const int32_t* pos,
+                              const int32_t* page_table, const int32_t* seq_lens, mqa_bf16* out,
+                              int b, int h, int g, int d_h, int page_size, int max_pages,
+                              int num_pages, float scale, float k_scale, float v_scale,
+                              void* stream) {
+  if (!k_new) return MQA_ERR_INVALID_ARG;
+  return paged_decode(q, k_new, v_new, k_pool, v_pool, pos,
+                      paged_cache(page_table, page_size, max_pages, num_pages), seq_lens, out, b,
+                      1, h, g, d_h, scale, 1, k_scale, v_scale, stream);
 }
 
 }  // extern "C"

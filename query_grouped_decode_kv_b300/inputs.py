@@ -151,7 +151,8 @@ def page_pool(k: torch.Tensor, v: torch.Tensor, rows: torch.Tensor, page_size: i
     order and holds -1 past them (``max_pages`` entries, by default enough for n_max rows).
     Returns (k_pool, v_pool, table): pools [num_pages, g, page_size, d_h] on the caches' device,
     table [b, max_pages] int32 on the CPU. Pool rows no sequence maps (spare pages, and rows of a
-    last page past n_max) hold ``fill``: NaN or zero.
+    last page past n_max) hold ``fill``: NaN or zero (for pools of uint8 E4M3 codes, the NaN code
+    0x7F or code 0).
     """
     b, g, n_max, d_h = k.shape
     need = [(int(r) + page_size - 1) // page_size for r in rows]
@@ -162,7 +163,10 @@ def page_pool(k: torch.Tensor, v: torch.Tensor, rows: torch.Tensor, page_size: i
     num_pages = sum(need) + spare_pages
     order = torch.randperm(num_pages, generator=_gen("cpu", seed)).to(torch.int32)
     table = torch.full((b, max_pages), -1, dtype=torch.int32)
-    value = 0.0 if fill == "zero" else float("nan")
+    if k.dtype == torch.uint8:   # E4M3 codes: 0x7F is a NaN code
+        value = 0 if fill == "zero" else 0x7F
+    else:
+        value = 0.0 if fill == "zero" else float("nan")
     k_pool = torch.full((num_pages, g, page_size, d_h), value, dtype=k.dtype, device=k.device)
     v_pool = torch.full_like(k_pool, value)
     used = 0

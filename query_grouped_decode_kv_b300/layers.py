@@ -19,24 +19,30 @@ class LayerState:
     """One layer's caches: contiguous [b, g, n_max, d_h] bf16, or, with a page table, page pools
     [num_pages, g, page_size, d_h] whose pages ``page_table`` [b, max_pages] int32 lists per
     sequence (the layers of a model normally share one table). With ``fp8_scales`` = (k_scale,
-    v_scale) the contiguous caches hold fp8 E4M3 codes (uint8) of value code * scale."""
+    v_scale) the caches (contiguous or pools) hold fp8 E4M3 codes (uint8) of value code * scale."""
     k_cache: torch.Tensor
     v_cache: torch.Tensor
     page_table: torch.Tensor | None = None
     fp8_scales: tuple[float, float] | None = None
 
-    def __post_init__(self):
-        if self.fp8_scales is not None and self.page_table is not None:
-            raise ValueError("fp8 caches are contiguous; paged caches are bf16")
-
     def step(self, q, k_new, v_new, pos, seq_lens, out, scale, stream) -> None:
-        """One fused append + attention launch on this layer (q of shape [b, T, h, d_h]: T new
-        tokens per sequence, causal)."""
+        """One fused append + attention on this layer (q of shape [b, T, h, d_h]: T new tokens
+        per sequence, causal; one launch, or two for a prefill-sized T on contiguous caches)."""
         if q.dim() == 4:
-            if self.fp8_scales is not None or self.page_table is not None:
-                raise ValueError("several tokens per step run on contiguous bf16 caches")
-            binding.decode_step_multi(q, k_new, v_new, self.k_cache, self.v_cache, pos,
-                                      seq_lens, out=out, scale=scale, stream=stream)
+            if self.fp8_scales is not None:
+                raise ValueError("several tokens per step run on bf16 caches")
+            if self.page_table is not None:
+                binding.decode_step_paged_multi(q, k_new, v_new, self.k_cache, self.v_cache, pos,
+                                                self.page_table, seq_lens, out=out, scale=scale,
+                                                stream=stream)
+            else:
+                binding.decode_step_multi(q, k_new, v_new, self.k_cache, self.v_cache, pos,
+                                          seq_lens, out=out, scale=scale, stream=stream)
+        elif self.fp8_scales is not None and self.page_table is not None:
+            ks, vs = self.fp8_scales
+            binding.decode_step_paged_fp8(q, k_new, v_new, self.k_cache, self.v_cache, pos,
+                                          self.page_table, seq_lens, ks, vs, out=out,
+                                          scale=scale, stream=stream)
         elif self.fp8_scales is not None:
             ks, vs = self.fp8_scales
             binding.decode_step_fp8(q, k_new, v_new, self.k_cache, self.v_cache, pos, seq_lens,
@@ -50,8 +56,14 @@ class LayerState:
                                       stream=stream)
 
     def append(self, k_new, v_new, pos, stream) -> None:
-        if k_new.dim() == 4:
+        if k_new.dim() == 4 and self.page_table is not None:
+            binding.kv_append_paged_multi(k_new, v_new, self.k_cache, self.v_cache, pos,
+                                          self.page_table, stream=stream)
+        elif k_new.dim() == 4:
             binding.kv_append_multi(k_new, v_new, self.k_cache, self.v_cache, pos, stream=stream)
+        elif self.fp8_scales is not None and self.page_table is not None:
+            binding.kv_append_paged_fp8(k_new, v_new, self.k_cache, self.v_cache, pos,
+                                        self.page_table, *self.fp8_scales, stream=stream)
         elif self.fp8_scales is not None:
             binding.kv_append_fp8(k_new, v_new, self.k_cache, self.v_cache, pos,
                                   *self.fp8_scales, stream=stream)
@@ -62,9 +74,16 @@ class LayerState:
                                     self.page_table, stream=stream)
 
     def attend(self, q, seq_lens, out, scale, stream) -> None:
-        if q.dim() == 4:
+        if q.dim() == 4 and self.page_table is not None:
+            binding.decode_attention_paged_multi(q, self.k_cache, self.v_cache, self.page_table,
+                                                 seq_lens, out=out, scale=scale, stream=stream)
+        elif q.dim() == 4:
             binding.decode_attention_multi(q, self.k_cache, self.v_cache, seq_lens, out=out,
                                            scale=scale, stream=stream)
+        elif self.fp8_scales is not None and self.page_table is not None:
+            binding.decode_attention_paged_fp8(q, self.k_cache, self.v_cache, self.page_table,
+                                               seq_lens, *self.fp8_scales, out=out, scale=scale,
+                                               stream=stream)
         elif self.fp8_scales is not None:
             binding.decode_attention_fp8(q, self.k_cache, self.v_cache, seq_lens,
                                          *self.fp8_scales, out=out, scale=scale, stream=stream)

@@ -54,6 +54,17 @@ MUTANTS = [
      "(size_t)n_max + (size_t)(p0 + T - 1 - t);"),
     ("fp8_append_without_scale", "(float)oracle_bf16_to_double(k_new[src + d]) / k_scale;",
      "(float)oracle_bf16_to_double(k_new[src + d]);"),
+    ("code_gather_wrong_page", "table[(size_t)bi * max_pages + (t / page_size)];",
+     "table[(size_t)bi * max_pages + (t / page_size + 1) % max_pages];"),
+    ("code_gather_wrong_row", "const size_t in_page = (size_t)(t % page_size);",
+     "const size_t in_page = (size_t)((t + 1) % page_size);"),
+    ("paged_multi_append_no_token_offset", "const int p = p0 + t;", "const int p = p0;"),
+    ("paged_multi_append_wrong_row", "const size_t row_in_page = (size_t)(p % page_size);",
+     "const size_t row_in_page = (size_t)((p + 1) % page_size);"),
+    ("paged_fp8_append_wrong_row", "const size_t prow = (size_t)(p % page_size);",
+     "const size_t prow = (size_t)((p + 1) % page_size);"),
+    ("paged_fp8_append_without_scale", "volatile float kq = kx / k_scale;",
+     "volatile float kq = kx;"),
 ]
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -475,6 +475,107 @@ def test_paged_append_rejects_a_bad_position_or_page_without_writing():
     assert np.array_equal(kp, kpool) and np.array_equal(vp, vpool)
 
 
+def _paged_u8_layout(b=2, g=2, max_pages=5, page_size=4, d_h=8, spare=3, seed=7):
+    """_paged_layout for one-byte codes: a contiguous C and the same rows cut into pages by
+    numpy reshapes alone, scattered over a pool by a random permutation."""
+    rng = np.random.default_rng(seed)
+    n = max_pages * page_size
+    C = rng.integers(0, 256, size=(b, g, n, d_h), dtype=np.uint8)
+    blocks = C.reshape(b, g, max_pages, page_size, d_h).transpose(0, 2, 1, 3, 4)
+    blocks = blocks.reshape(b * max_pages, g, page_size, d_h)
+    num_pages = b * max_pages + spare
+    slot = rng.permutation(num_pages)[:b * max_pages]
+    pool = rng.integers(0, 256, size=(num_pages, g, page_size, d_h), dtype=np.uint8)
+    pool[slot] = blocks
+    return C, pool, slot.reshape(b, max_pages).astype(np.int32)
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 16])
+def test_code_gather_undoes_an_independent_paging(page_size):
+    C, pool, table = _paged_u8_layout(page_size=page_size)
+    got, st = oracle.gather_pages_u8(pool, table, page_size)
+    assert st == oracle.OK and np.array_equal(got, C)
+    t2 = table.copy()
+    t2[0, 1] = -3                        # a page index out of range: code 0 there
+    got, st = oracle.gather_pages_u8(pool, t2, page_size)
+    assert st == oracle.ERR_BOUNDS
+    assert np.all(got[0, :, page_size:2 * page_size] == 0)
+    assert np.array_equal(got[1], C[1])
+
+
+def test_paged_append_of_several_tokens_matches_the_contiguous_one():
+    # T = 3 tokens from rows 6 and 11 of 4-row pages: the rows cross a page boundary
+    C, kpool, table = _paged_layout(seed=20)
+    _, vpool, _ = _paged_layout(seed=21)
+    rng = np.random.default_rng(22)
+    T = 3
+    kn = rng.integers(0, 1 << 16, size=(2, T, 2, 8), dtype=np.uint16)
+    vn = rng.integers(0, 1 << 16, size=(2, T, 2, 8), dtype=np.uint16)
+    pos = np.array([6, 11], dtype=np.int32)
+    kc, _ = oracle.gather_pages(kpool, table, 4)
+    vc, _ = oracle.gather_pages(vpool, table, 4)
+    assert oracle.kv_append_multi(kn, vn, kc, vc, pos) == oracle.OK
+    kp, vp = kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged_multi(kn, vn, kp, vp, pos, table) == oracle.OK
+    assert np.array_equal(oracle.gather_pages(kp, table, 4)[0], kc)
+    assert np.array_equal(oracle.gather_pages(vp, table, 4)[0], vc)
+    unused = sorted(set(range(kpool.shape[0])) - set(table.ravel().tolist()))
+    assert np.array_equal(kp[unused], kpool[unused])
+    # T = 1 is the one-token paged append
+    kp1, vp1, kp2, vp2 = kpool.copy(), vpool.copy(), kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged_multi(kn[:, :1], vn[:, :1], kp1, vp1, pos, table) == oracle.OK
+    assert oracle.kv_append_paged(kn[:, 0], vn[:, 0], kp2, vp2, pos, table) == oracle.OK
+    assert np.array_equal(kp1, kp2) and np.array_equal(vp1, vp2)
+
+
+def test_paged_append_of_several_tokens_skips_bad_rows_and_sequences():
+    _, kpool, table = _paged_layout(seed=23)
+    vpool = kpool.copy()
+    kn = np.full((2, 3, 2, 8), 7, dtype=np.uint16)
+    # sequence 1's rows 18 .. 20 run past max_pages * page_size = 20: skipped whole
+    kp, vp = kpool.copy(), vpool.copy()
+    st = oracle.kv_append_paged_multi(kn, kn, kp, vp, np.array([0, 18], dtype=np.int32), table)
+    assert st == oracle.ERR_BOUNDS
+    sel = table[1]
+    assert np.array_equal(kp[sel], kpool[sel])
+    assert np.all(kp[table[0, 0], :, 0:3] == 7)
+    # a bad page under row 4 (page 1) of sequence 0, rows 2 .. 4: rows 2, 3 written, row 4 not
+    t2 = table.copy()
+    t2[0, 1] = -1
+    kp, vp = kpool.copy(), vpool.copy()
+    st = oracle.kv_append_paged_multi(kn, kn, kp, vp, np.array([2, 0], dtype=np.int32), t2)
+    assert st == oracle.ERR_BOUNDS
+    assert np.all(kp[t2[0, 0], :, 2:4] == 7)
+    assert np.array_equal(kp[table[0, 1]], kpool[table[0, 1]])
+
+
+def test_paged_fp8_append_matches_the_contiguous_fp8_append():
+    rng = np.random.default_rng(24)
+    b, g, d_h, ps, mp = 2, 2, 16, 4, 5
+    num_pages = b * mp + 3
+    kpool = rng.integers(0, 256, size=(num_pages, g, ps, d_h), dtype=np.uint8)
+    vpool = rng.integers(0, 256, size=(num_pages, g, ps, d_h), dtype=np.uint8)
+    table = rng.permutation(num_pages)[:b * mp].reshape(b, mp).astype(np.int32)
+    kn = oracle.f64_to_bf16(rng.standard_normal((b, g, d_h)) * 3)
+    vn = oracle.f64_to_bf16(rng.standard_normal((b, g, d_h)))
+    pos = np.array([13, 6], dtype=np.int32)
+    ks, vs = 0.02, 0.005
+    kc, _ = oracle.gather_pages_u8(kpool, table, ps)
+    vc, _ = oracle.gather_pages_u8(vpool, table, ps)
+    assert oracle.kv_append_fp8(kn, vn, kc, vc, pos, ks, vs) == oracle.OK
+    kp, vp = kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged_fp8(kn, vn, kp, vp, pos, table, ks, vs) == oracle.OK
+    assert np.array_equal(oracle.gather_pages_u8(kp, table, ps)[0], kc)
+    assert np.array_equal(oracle.gather_pages_u8(vp, table, ps)[0], vc)
+    # a bad page or position writes nothing
+    t2 = table.copy()
+    t2[0, 3] = num_pages
+    kp, vp = kpool.copy(), vpool.copy()
+    assert oracle.kv_append_paged_fp8(kn, vn, kp, vp, np.array([13, 20], dtype=np.int32), t2,
+                                      ks, vs) == oracle.ERR_BOUNDS
+    assert np.array_equal(kp, kpool) and np.array_equal(vp, vpool)
+
+
 def test_paged_attention_brute_force_through_the_table():
     """Attention computed with pure-Python loops that fetch every row through the page table
     equals the oracle's attention over the gathered cache."""
