@@ -326,10 +326,13 @@ AttnKernelChoice pick_kernel_fp8(Path path, int G, int b) {
   constexpr int D = 128;
   if (path == kPathTcgen05) return {};
   if (path == kPathMmaSync) {
-    // up to 16 heads: two tile groups of four warps (an fp8 tile's HBM time is half a bf16
-    // tile's, so one group alone would wait on its own per-tile chain)
-    if (G <= 16) return choice<MmaConsumerF8<D, 1, 8, 2>, D, 1, true, 1>(b);
-    if (G <= 32) return choice<MmaConsumerF8<D, 2, 8>, D, 1, true, 2>(b);
+    // several tile groups: an fp8 tile's HBM time is half a bf16 tile's while a warp's per-tile
+    // chain is not shorter, so groups of warps take turns on the tiles. Measured on B300 (32K
+    // rows, launches back to back, fraction of the copy bandwidth on fp8 bytes): up to 16 heads
+    // four groups of two warps, 32 keys each, reach 0.77-0.79 against 0.71-0.73 for two groups of
+    // four; at 32 heads two groups of four edge out one of eight (0.456 against 0.449).
+    if (G <= 16) return choice<MmaConsumerF8<D, 1, 8, 4>, D, 1, true, 1>(b);
+    if (G <= 32) return choice<MmaConsumerF8<D, 2, 8, 2>, D, 1, true, 2>(b);
     return choice<MmaConsumerF8<D, 4, 8>, D, 1, true, 4>(b);
   }
   switch (G) {

@@ -296,9 +296,14 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
     if (!__all_sync(0xffffffffu, ok)) return false;
     tc_fence_after_sync();
 
-    // this row's 64 scores in log2 units; keys past the row's causal limit are -inf
+    // this row's 64 raw scores; the first nvis keys are visible to the row (its causal limit
+    // and the sequence's end), the rest are masked. Scaled scores are s * sc (log2 units); the
+    // row's largest scaled score comes from the largest raw score (or the smallest, for a
+    // negative scale), so the scale is applied once per key, inside the exponential's FFMA.
     const int key0 = cur.tile * kTileKeys;
     const int nvis = min(max(lim - key0, 0), kTileKeys);
+    const float sc = P.scale_log2;
+    const bool all_visible = __all_sync(0xffffffffu, nvis == kTileKeys);
     float s[kTileKeys];
     {
       uint32_t r0[32], r1[32];
@@ -308,13 +313,31 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        s[i] = i < nvis ? __uint_as_float(r0[i]) * P.scale_log2 : -INFINITY;
-        s[32 + i] = 32 + i < nvis ? __uint_as_float(r1[i]) * P.scale_log2 : -INFINITY;
+        s[i] = __uint_as_float(r0[i]);
+        s[32 + i] = __uint_as_float(r1[i]);
       }
     }
-    float mx = s[0];
+    float ext;
+    if (sc >= 0.f) {
+      ext = -INFINITY;
+      if (all_visible) {
 #pragma unroll
-    for (int i = 1; i < kTileKeys; ++i) mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < kTileKeys; ++i) ext = fmaxf(ext, s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTileKeys; ++i) ext = i < nvis ? fmaxf(ext, s[i]) : ext;
+      }
+    } else {
+      ext = INFINITY;
+      if (all_visible) {
+#pragma unroll
+        for (int i = 0; i < kTileKeys; ++i) ext = fminf(ext, s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTileKeys; ++i) ext = i < nvis ? fminf(ext, s[i]) : ext;
+      }
+    }
+    const float mx = nvis > 0 ? ext * sc : -INFINITY;  // the row's largest scaled score
     float alpha = 1.f;
     bool raise = false;
     if (cur.tile == 0) {
@@ -344,15 +367,28 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
       }
       tmem_wait_st();
     }
-    // probabilities, rounded to bf16 once: the same values feed P V and the running sum
+    // probabilities 2^(s sc - m), rounded to bf16 once: the same values feed P V and the running
+    // sum; masked keys weigh 0
     const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
     uint32_t pk[kTileKeys / 2];
     float ps = 0.f;
+    if (all_visible) {
 #pragma unroll
-    for (int i = 0; i < kTileKeys / 2; ++i) {
-      const uint32_t v = pack_bf16x2(fast_exp2(s[2 * i] - m_use), fast_exp2(s[2 * i + 1] - m_use));
-      ps += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
-      pk[i] = v;
+      for (int i = 0; i < kTileKeys / 2; ++i) {
+        const uint32_t v = pack_bf16x2(fast_exp2(fmaf(s[2 * i], sc, -m_use)),
+                                       fast_exp2(fmaf(s[2 * i + 1], sc, -m_use)));
+        ps += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+        pk[i] = v;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTileKeys / 2; ++i) {
+        const float p0 = 2 * i < nvis ? fast_exp2(fmaf(s[2 * i], sc, -m_use)) : 0.f;
+        const float p1 = 2 * i + 1 < nvis ? fast_exp2(fmaf(s[2 * i + 1], sc, -m_use)) : 0.f;
+        const uint32_t v = pack_bf16x2(p0, p1);
+        ps += __uint_as_float(v << 16) + __uint_as_float(v & 0xFFFF0000u);
+        pk[i] = v;
+      }
     }
     l += ps;
     tmem_st_32x32b_x32(tmem + lane_base + kTcPCol + bf * (kTileKeys / 2), pk);

@@ -151,3 +151,16 @@ def test_prefill_zeroes_a_sequence_whose_length_is_below_t(mqa):
         ref = oracle.decode_attention_multi(P.bits(c["q"][bi:bi + 1]), kb[bi:bi + 1],
                                             vb[bi:bi + 1], lens[bi:bi + 1], c["scale"])
         P.assert_close(out[bi:bi + 1], ref, f"valid sequence {bi}")
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.07, 0.5], ids=["zero", "negative", "large"])
+def test_prefill_any_finite_scale(mqa, scale):
+    """The scale enters once per key (inside the exponential) and the row's largest scaled score
+    is taken from the largest raw score, or the smallest for a negative scale; scale 0 gives the
+    mean of the visible V rows."""
+    c = _case(2, 16, 2, 128, 100, 600, 48, seed=1700)
+    c["scale"] = scale
+    kb, vb = _oracle_appended(c)
+    ref = oracle.decode_attention_multi(P.bits(c["q"]), kb, vb, c["lens"].numpy(), scale)
+    _, _, out = _gpu_attend(mqa, c, fused=True)
+    P.assert_close(out, ref, f"prefill scale {scale}")
