@@ -700,6 +700,42 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def line_problems(line: dict, rel: float = 1e-6) -> list[str]:
+    """Consistency checks of a printed JSON line (ours): each workload's launches times its time
+    per launch is its step time (so no launch takes longer than the step it is part of), the
+    roofline's achieved figure is the algorithmic bytes (or FLOPs) per launch over that time and
+    its fraction the achieved over the peak, and the end-to-end step is no faster than the
+    device-resident one. Returns the problems found (empty when consistent)."""
+    out = []
+
+    def close(a, b):
+        return abs(a - b) <= rel * max(abs(a), abs(b), 1e-30)
+
+    for name, c in line.get("configs", {}).items():
+        step, per, n = c["us_per_step"], c["us_per_launch"], c["launches_per_step"]
+        if n * per > step * (1 + rel):
+            out.append(f"{name}: {n} launches x {per} us > {step} us per step")
+        if not close(n * per, step):
+            out.append(f"{name}: launches x us_per_launch != us_per_step")
+        if not close(c["kv_gbs"], c["algorithmic_bytes_per_launch"] / (per * 1e-6) / 1e9):
+            out.append(f"{name}: kv_gbs is not bytes per launch over the time per launch")
+    r = line["roofline"]
+    head = line["configs"][line["config"]["workload"]]
+    if not close(r["us_per_launch"], head["us_per_launch"]):
+        out.append("roofline us_per_launch differs from the headline workload's")
+    if not close(line["value"], head["us_per_step"] * 1.0 / max(line.get("n_gpus", 1), 1)):
+        out.append("value is not the headline workload's step time (whole job)")
+    per_unit = (r["algorithmic_bytes_per_launch"] / 1e9 if r["bound"] == "hbm"
+                else r["flops_per_launch"] / 1e12)
+    if r["bound"] == "hbm" and not close(r["achieved"], per_unit / (r["us_per_launch"] * 1e-6)):
+        out.append("roofline achieved is not bytes per launch over us_per_launch")
+    if not close(r["frac"], r["achieved"] / r["peak"]):
+        out.append("roofline frac is not achieved / peak")
+    if line["e2e"]["value"] < line["value"] * (1 - 1e-3):
+        out.append("e2e step faster than the device-resident step")
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)

@@ -449,13 +449,15 @@ int plan_decode(const mqa_bf16* q, const mqa_bf16* k_cache, const mqa_bf16* v_ca
   if (int st = device_info(dev, &info)) return st;
 
   // CTAs: one per SM, but no more than a quarter of the (upper bound on the) tile count, so that
-  // tiny problems are not scattered into many partial states. The prefill kernel: one per SM, at
+  // tiny problems are not scattered into many partial states. The prefill kernel: two per SM, at
   // most one per unit (128 rows of one sequence and KV head); it keeps no partial states.
   const long long w_max = bg * tiles_per_seg;
   const long long units = bg * ((rows + mqa::kPfRows - 1) / mqa::kPfRows);
   if (prefill && units >= (1ll << 31)) return MQA_ERR_UNSUPPORTED;
   long long ctas = prefill ? units : (w_max + 3) / 4;
-  if (ctas > info.sms) ctas = info.sms;
+  const long long max_ctas = prefill ? static_cast<long long>(mqa::kPfCtasPerSm) * info.sms
+                                     : info.sms;
+  if (ctas > max_ctas) ctas = max_ctas;
   if (ctas < 1) ctas = 1;
   if (const int f = g_force_ctas.load()) ctas = f;
 
@@ -506,7 +508,7 @@ int launch_prefill(const DecodePlan& p) {
   AttnKernelChoice kc;
   kc.fn = p.d_h == 128 ? mqa::prefill_attention_tc_kernel<128> : mqa::prefill_attention_tc_kernel<64>;
   kc.threads = mqa::kTcThreads;
-  kc.smem = mqa::tc_smem_bytes(p.d_h);
+  kc.smem = mqa::pf_smem_bytes(p.d_h);
   if (int st = prepare_kernel(p.dev, kc, kc.smem)) return st;
   kc.fn<<<static_cast<unsigned>(p.ctas), kc.threads, kc.smem, p.stream>>>(tmk, tmv, P);
   g_launches.fetch_add(1);

@@ -18,16 +18,16 @@
 // inside its CTA, so there are no partial states. The units of one segment are consecutive, so
 // the CTAs that read a segment's K and V run at about the same time and share them through L2.
 //
-// Inside a CTA (192 threads, the roles of the decode tcgen05 kernel): warps 0-3 own one row each
-// per thread (thread t = row t of the block = tensor-memory lane t): they write the unit's Q into
-// shared memory, run the online softmax with the row's own causal limit, and write the output
-// row; warp 4 streams the K and V tiles with bulk tensor copies into separate rings; one lane of
-// warp 5 issues the MMAs from an event loop and warp 5 owns the tensor memory.
+// Inside a CTA (192 threads, the roles of the decode tcgen05 kernel; two CTAs per SM): warps 0-3
+// own one row each per thread (thread t = row t of the block = tensor-memory lane t): they write
+// the unit's Q into shared memory, run the online softmax with the row's own causal limit, and
+// write the output row; warp 4 streams the K and V tiles with bulk tensor copies into separate
+// rings; one lane of warp 5 issues the MMAs from an event loop and warp 5 owns the tensor memory.
 //
 //   S = Q K^T      M = 128 rows, N = 64 keys, K = d_h; A = Q, B = the K tile (shared memory,
-//                  128-byte swizzle); S in tensor memory, fp32, kTcBufs buffers
+//                  128-byte swizzle); S in tensor memory, fp32, kPfBufs buffers
 //   softmax        thread r loads its 64 scores, masks the keys past its limit, and writes its
-//                  bf16 probabilities into its row of a P buffer in tensor memory
+//                  bf16 probabilities over the first 32 columns of its row of that S buffer
 //   O += P V       M = 128, N = d_h, K = 64 keys; A = P (tensor memory), B = the V tile
 //                  (N-major); O in tensor memory, fp32
 //
@@ -47,6 +47,93 @@ namespace mqa {
 
 constexpr int kPfRows = kTcRows;  // rows per unit (MMA M)
 constexpr int kMaxPrefillRows = 1 << 22;  // largest T * h / g served
+
+// Two CTAs per SM, so that every SM sub-partition runs two softmax warps whose per-tile chains
+// hide each other's latency: each CTA takes half the tensor memory and under half the shared
+// memory. Tensor memory (256 columns per CTA): kPfBufs S buffers of 64 columns, and O; the bf16
+// probabilities P of a tile go back into the first 32 columns of its own S buffer once the
+// scores are in registers (an S buffer is reused only after the P V that read its P finished).
+constexpr int kPfCtasPerSm = 2;
+constexpr int kPfBufs = 2;
+constexpr int kPfTmemCols = 256;
+constexpr int kPfSCol = 0;                       // S (then P) buffers: kPfBufs x 64 columns
+constexpr int kPfOCol = kPfBufs * kTileKeys;     // O: d_h columns
+static_assert(kPfOCol + 128 <= kPfTmemCols, "tensor-memory columns");
+__host__ __device__ constexpr int pf_k_stages(int D) { return D == 128 ? 2 : 4; }
+__host__ __device__ constexpr int pf_v_stages(int D) { return D == 128 ? 2 : 4; }
+__host__ __device__ constexpr int pf_barrier_count(int D) {
+  return 2 * pf_k_stages(D) + 2 * pf_v_stages(D) + 1 + 3 * kPfBufs + 4;
+}
+__host__ __device__ constexpr size_t pf_smem_bytes(int D) {
+  return 1024 + static_cast<size_t>((pf_k_stages(D) + pf_v_stages(D)) * tc_tile_bytes(D) +
+                                    tc_q_bytes(D) + pf_barrier_count(D) * 8 + 32);
+}
+static_assert(pf_smem_bytes(128) <= 110 * 1024 && pf_smem_bytes(64) <= 110 * 1024,
+              "two CTAs per SM");
+
+// The prefill kernel's shared memory, in the decode tcgen05 kernel's struct (the bounded waits
+// and give_up use its fields): the K ring, the V ring, Q, and the barriers.
+template <int D>
+__device__ __forceinline__ TcShared carve_pf_shared(uint8_t* raw) {
+  TcShared t = {};
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  constexpr int NK = pf_k_stages(D), NV = pf_v_stages(D);
+  t.base.stages = p;  // K ring
+  t.vring = p + NK * tc_tile_bytes(D);
+  p += (NK + NV) * tc_tile_bytes(D);
+  t.q = p;
+  p += tc_q_bytes(D);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p);
+  t.base.full = bars;
+  t.base.empty = bars + NK;
+  t.v_full = bars + 2 * NK;
+  t.v_empty = bars + 2 * NK + NV;
+  t.s_full = bars + 2 * NK + 2 * NV;
+  t.p_full = t.s_full + kPfBufs;
+  t.pv_done = t.p_full + kPfBufs;
+  t.q_full = t.pv_done + kPfBufs;
+  t.tmem_done = t.q_full + 1;
+  t.drain = t.tmem_done + 1;
+  t.base.stall = t.drain + 1;
+  t.base.cbar = t.base.stall + 1;  // unused
+  p += pf_barrier_count(D) * 8;
+  t.base.abort = reinterpret_cast<volatile int*>(p);
+  t.base.merge = t.base.abort + 1;
+  t.tmem_base = reinterpret_cast<uint32_t*>(p + 8);
+  return t;
+}
+
+// MMA issue for tile k: S into buffer k % kPfBufs; O += P V with P from the first 32 columns of
+// that buffer. The descriptors are those of the decode tcgen05 kernel's scores and values.
+template <int D>
+struct PfMma {
+  static constexpr uint32_t kIdescS = umma_idesc_bf16_f32(kTcRows, kTileKeys, false);
+  static constexpr uint32_t kIdescO = umma_idesc_bf16_f32(kTcRows, D, true);
+  uint32_t kring, vring, q, tmem;
+  __device__ __forceinline__ void scores(int k) const {
+    const uint32_t kst = kring + (k % pf_k_stages(D)) * tc_tile_bytes(D);
+    const uint32_t d_tmem = tmem + kPfSCol + (k % kPfBufs) * kTileKeys;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk & 3) * 32;
+      const uint64_t a = sw128_desc(q + (kk >> 2) * (kTcRows * kSwizzleRowBytes) + off, 0, 1024);
+      const uint64_t bd = sw128_desc(kst + (kk >> 2) * (kTileKeys * kSwizzleRowBytes) + off, 0,
+                                     1024);
+      umma_ss(d_tmem, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+    }
+  }
+  __device__ __forceinline__ void values(int k, bool overwrite) const {
+    const uint32_t vst = vring + (k % pf_v_stages(D)) * tc_tile_bytes(D);
+    const uint32_t p_tmem = tmem + kPfSCol + (k % kPfBufs) * kTileKeys;
+#pragma unroll
+    for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+      const uint64_t bd = sw128_desc(vst + kk * 16 * kSwizzleRowBytes,
+                                     kTileKeys * kSwizzleRowBytes, 1024);
+      umma_ts(tmem + kPfOCol, p_tmem + kk * 8, bd, kIdescO, (overwrite && kk == 0) ? 0u : 1u);
+    }
+  }
+};
 
 // Units of the launch: NB blocks of 128 rows per segment, b * g segments.
 __device__ __forceinline__ long long pf_blocks(const DecodeParams& P) {
@@ -125,16 +212,16 @@ __device__ __forceinline__ void pf_write_q(const DecodeParams& P, const TcShared
 // ---------------------------------------------------------------------------------------------
 // MMA issue (one lane of warp 5): the event loop of the decode tcgen05 kernel over the units'
 // tiles. Tile k (counted over the CTA's units) uses K stage k % NK, V stage k % NV and the
-// tensor-memory buffers k % kTcBufs at phase k / kTcBufs; the S MMAs of a unit's first tile wait
+// tensor-memory buffers k % kPfBufs at phase k / kPfBufs; the S MMAs of a unit's first tile wait
 // for its Q (q_full, one phase per unit).
 // ---------------------------------------------------------------------------------------------
 // Returns the number of tiles whose score MMAs it issued.
 template <int D>
 __device__ __forceinline__ int pf_issue_loop(const DecodeParams& P, const TcShared& sh,
                                              uint32_t tmem, long long U) {
-  constexpr int NK = tc_k_stages(D), NV = tc_v_stages(D);
+  constexpr int NK = pf_k_stages(D), NV = pf_v_stages(D);
   const SharedLayout& b = sh.base;
-  TcMma<D> mma{smem_addr(b.stages), smem_addr(sh.vring), smem_addr(sh.q), tmem};
+  PfMma<D> mma{smem_addr(b.stages), smem_addr(sh.vring), smem_addr(sh.q), tmem};
   PfCursor cur, cs;  // cur: the tile whose P V comes next (k); cs: the next to score (ks)
   cur.start(P, U);
   cs = cur;
@@ -143,27 +230,27 @@ __device__ __forceinline__ int pf_issue_loop(const DecodeParams& P, const TcShar
   uint64_t last = global_timer_ns();
   for (uint32_t polls = 1; !cur.done(U); ++polls) {
     bool progressed = false;
-    if (!cs.done(U) && ks < k + kTcBufs) {
+    if (!cs.done(U) && ks < k + kPfBufs) {
       const bool need_q = (cs.tile == 0);
-      if ((ks < kTcBufs ||
-           mbar_test(&sh.pv_done[ks % kTcBufs], ((ks - kTcBufs) / kTcBufs) & 1)) &&
+      if ((ks < kPfBufs ||
+           mbar_test(&sh.pv_done[ks % kPfBufs], ((ks - kPfBufs) / kPfBufs) & 1)) &&
           mbar_test(&b.full[ks % NK], (ks / NK) & 1) &&
           (!need_q || mbar_test(sh.q_full, qnext & 1))) {
         if (need_q) ++qnext;
         tc_fence_after_sync();
         mma.scores(ks);
-        umma_commit(&sh.s_full[ks % kTcBufs]);
+        umma_commit(&sh.s_full[ks % kPfBufs]);
         umma_commit(&b.empty[ks % NK]);
         cs.advance(P, U);
         ++ks;
         progressed = true;
       }
     }
-    if (k < ks && mbar_test(&sh.p_full[k % kTcBufs], (k / kTcBufs) & 1) &&
+    if (k < ks && mbar_test(&sh.p_full[k % kPfBufs], (k / kPfBufs) & 1) &&
         mbar_test(&sh.v_full[k % NV], (k / NV) & 1)) {
       tc_fence_after_sync();
       mma.values(k, cur.tile == 0);
-      umma_commit(&sh.pv_done[k % kTcBufs]);
+      umma_commit(&sh.pv_done[k % kPfBufs]);
       umma_commit(&sh.v_empty[k % NV]);
       cur.advance(P, U);
       ++k;
@@ -176,7 +263,7 @@ __device__ __forceinline__ int pf_issue_loop(const DecodeParams& P, const TcShar
     if ((polls & 63u) == 0u) {
       if (*b.abort) return ks;
       if (global_timer_ns() - last > P.timeout_ns) {
-        const bool scoring = !cs.done(U) && ks < k + kTcBufs;
+        const bool scoring = !cs.done(U) && ks < k + kPfBufs;
         give_up(b, scoring ? kSiteMmaFull : kSiteMmaP, scoring ? ks : k);
         return ks;
       }
@@ -195,7 +282,7 @@ __device__ __forceinline__ void pf_produce_tiles(const CUtensorMap* tm_k, const 
                                                  const DecodeParams& P, const TcShared& sh,
                                                  long long U) {
   constexpr uint32_t kTile = tc_tile_bytes(D);
-  constexpr int NK = tc_k_stages(D), NV = tc_v_stages(D);
+  constexpr int NK = pf_k_stages(D), NV = pf_v_stages(D);
   const SharedLayout& b = sh.base;
   prefetch_tensor_map(tm_k);
   prefetch_tensor_map(tm_v);
@@ -257,7 +344,7 @@ __device__ __forceinline__ void pf_produce_tiles(const CUtensorMap* tm_k, const 
 template <int D>
 __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcShared& sh,
                                                 uint32_t tmem, long long U) {
-  constexpr int NV = tc_v_stages(D);
+  constexpr int NV = pf_v_stages(D);
   const SharedLayout& b = sh.base;
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
@@ -290,8 +377,8 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
       m_ref = -INFINITY;
       l = 0.f;
     }
-    const int bf = k % kTcBufs;
-    bool ok = mbar_wait_bounded(&sh.s_full[bf], (k / kTcBufs) & 1, P.timeout_ns, b.abort);
+    const int bf = k % kPfBufs;
+    bool ok = mbar_wait_bounded(&sh.s_full[bf], (k / kPfBufs) & 1, P.timeout_ns, b.abort);
     if (!ok && !*b.abort) give_up(b, kSiteSoftmaxS, k);
     if (!__all_sync(0xffffffffu, ok)) return false;
     tc_fence_after_sync();
@@ -307,7 +394,7 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
     float s[kTileKeys];
     {
       uint32_t r0[32], r1[32];
-      const uint32_t taddr = tmem + lane_base + kTcSCol + bf * kTileKeys;
+      const uint32_t taddr = tmem + lane_base + kPfSCol + bf * kTileKeys;
       tmem_ld_32x32b_x32(taddr, r0);
       tmem_ld_32x32b_x32(taddr + 32, r1);
       tmem_wait_ld();
@@ -351,7 +438,7 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
     if (__any_sync(0xffffffffu, raise)) {
       // O must hold P V of the previous tile before its rows are rescaled
       const int kp = k - 1;
-      ok = mbar_wait_bounded(&sh.pv_done[kp % kTcBufs], (kp / kTcBufs) & 1, P.timeout_ns,
+      ok = mbar_wait_bounded(&sh.pv_done[kp % kPfBufs], (kp / kPfBufs) & 1, P.timeout_ns,
                              b.abort);
       if (!ok && !*b.abort) give_up(b, kSiteSoftmaxPv, k);
       if (!__all_sync(0xffffffffu, ok)) return false;
@@ -359,11 +446,11 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTcOCol + c, o);
+        tmem_ld_32x32b_x32(tmem + lane_base + kPfOCol + c, o);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st_32x32b_x32(tmem + lane_base + kTcOCol + c, o);
+        tmem_st_32x32b_x32(tmem + lane_base + kPfOCol + c, o);
       }
       tmem_wait_st();
     }
@@ -391,7 +478,8 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
       }
     }
     l += ps;
-    tmem_st_32x32b_x32(tmem + lane_base + kTcPCol + bf * (kTileKeys / 2), pk);
+    // P over the first 32 columns of this tile's S buffer (the scores are in registers)
+    tmem_st_32x32b_x32(tmem + lane_base + kPfSCol + bf * kTileKeys, pk);
     tmem_wait_st();
 
     const int valid = cur.L - key0;  // rows of the tile below the sequence's length
@@ -424,7 +512,7 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
         fence_proxy_async_smem();
         mbar_arrive(sh.q_full);
       }
-      ok = mbar_wait_bounded(&sh.pv_done[bf], (k / kTcBufs) & 1, P.timeout_ns, b.abort);
+      ok = mbar_wait_bounded(&sh.pv_done[bf], (k / kPfBufs) & 1, P.timeout_ns, b.abort);
       if (!ok && !*b.abort) give_up(b, kSiteEpiloguePv, k);
       if (!__all_sync(0xffffffffu, ok)) return false;
       tc_fence_after_sync();
@@ -437,7 +525,7 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTcOCol + c, o);
+        tmem_ld_32x32b_x32(tmem + lane_base + kPfOCol + c, o);
         tmem_wait_ld();
         if (lim > 0) {
 #pragma unroll
@@ -462,32 +550,31 @@ __device__ __forceinline__ bool pf_softmax_loop(const DecodeParams& P, const TcS
 // The kernel. P.G = T * Gh rows per segment (T >= 2), contiguous bf16 caches, no fused append.
 // ---------------------------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, kPfCtasPerSm)
     prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                 const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  TcShared sh = carve_tc_shared<D>(smem_raw);
+  TcShared sh = carve_pf_shared<D>(smem_raw);
   SharedLayout& b = sh.base;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
   if (warp == 5) {
-    tmem_alloc(sh.tmem_base, kTcTmemCols);
+    tmem_alloc(sh.tmem_base, kPfTmemCols);
     tmem_relinquish_alloc_permit();
   }
   if (tid == 0) {
     *b.abort = 0;
     *b.merge = 0;
-    for (int st = 0; st < tc_k_stages(D); ++st) {
+    for (int st = 0; st < pf_k_stages(D); ++st) {
       mbar_init(&b.full[st], 1);
       mbar_init(&b.empty[st], 1);
     }
-    for (int st = 0; st < tc_v_stages(D); ++st) {
+    for (int st = 0; st < pf_v_stages(D); ++st) {
       mbar_init(&sh.v_full[st], 1);
       mbar_init(&sh.v_empty[st], 1);
     }
-    mbar_init(b.cbar, 128);
-    for (int i = 0; i < kTcBufs; ++i) {
+    for (int i = 0; i < kPfBufs; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], 128);
       mbar_init(&sh.pv_done[i], 1);
@@ -524,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTcTmemCols);
+    tmem_dealloc(tmem, kPfTmemCols);
     return;
   }
   // warps 0-3

@@ -142,3 +142,31 @@ def test_step_shape_attends_every_new_row(T):
     assert w.n_max == w0.n_max + T - 1
     assert torch.equal(lens, pos + T) and lens.dtype == torch.int32
     assert int(lens.max()) <= w.n_max
+
+
+RECORDED_LINE = bench.os.path.join(bench.ROOT, "profiles", "bench_default_line.json")
+
+
+def test_the_recorded_default_line_is_self_consistent():
+    """The JSON line of a default run on B300 (profiles/bench_default_line.json): every
+    workload's launches x time per launch equals its step time, the roofline follows from the
+    bytes and that time, and the end-to-end step is no faster than the device step."""
+    with open(RECORDED_LINE) as fh:
+        line = json.load(fh)
+    assert bench.line_problems(line) == []
+    head = line["configs"][line["config"]["workload"]]
+    assert head["launches_per_step"] * line["roofline"]["us_per_launch"] <= \
+        line["ms_per_step"] * 1000.0 * (1 + 1e-9)
+    assert set(line["configs"]) == set(bench.ALL_WORKLOADS)
+
+
+def test_the_line_checks_catch_a_launch_longer_than_its_step():
+    with open(RECORDED_LINE) as fh:
+        line = json.load(fh)
+    bad = json.loads(json.dumps(line))
+    head = bad["config"]["workload"]
+    bad["configs"][head]["us_per_launch"] *= 1.04      # as an event-decorated launch time would
+    assert any("launches" in p for p in bench.line_problems(bad))
+    bad = json.loads(json.dumps(line))
+    bad["roofline"]["frac"] *= 1.1
+    assert any("frac" in p for p in bench.line_problems(bad))
