@@ -1,9 +1,11 @@
 """Launch overlap (programmatic dependent launch, mqa_set_launch_overlap) on the GPU.
 
 With overlap on, a decode launch may start while the launch ahead of it on the stream is still
-running: it reads its inputs at once but writes nothing (outputs, appended rows, partial states,
-arrival counters) until that launch has finished. Results must therefore be bit for bit those of
-the same launches without overlap. These tests run sequences of launches both ways -- eager and
+running. Over caches of up to 768 MiB it writes at once, into scratch the launch ahead does not
+use, and holds the launch after it back until the launch ahead has finished; over larger caches
+it reads at once but writes nothing (outputs, appended rows, partial states, arrival counters)
+until that launch has finished. Results must be bit for bit those of the same launches without
+overlap. These tests run sequences of launches both ways -- eager and
 captured in a CUDA graph, on every inner-product path, over contiguous, paged and fp8 caches, with
 one and several tokens, with layers revisited (their appends repeated) -- and compare every output
 and every cache byte, then check outputs against the fp64 oracle. No launch follows one on the same
@@ -222,3 +224,37 @@ def test_overlap_setting_is_per_stream_and_validated(mqa):
     lib = mqa.raw()
     assert lib.mqa_set_launch_overlap(s1.cuda_stream, 2) == 1   # MQA_ERR_INVALID_ARG
     assert lib.mqa_set_launch_overlap(s1.cuda_stream, -1) == 1
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+@pytest.mark.parametrize("shape", [
+    (4, 16, 8, 128, 300, 3000),   # G = 2, CUDA cores
+    (4, 64, 8, 128, 300, 3000),   # G = 8, mma.sync
+], ids=["G2", "G8"])
+def test_overlapped_layers_over_large_caches_equal_serial_ones(mqa, shape, graph):
+    """Caches of more than 768 MiB (here about 870 MB per layer, most of it rows past the
+    contexts): overlapped launches then read early but wait for the launch ahead before their
+    first write. Same bits as without overlap, and the oracle's result."""
+    import dataclasses
+    dev = torch.device("cuda")
+    b, h, g, d_h, lo, hi = shape
+    extra = 50_000
+    assert 2 * b * g * (hi + 1 + extra) * d_h * 2 > 768 * 2 ** 20
+    w = dataclasses.replace(inputs.custom("big", b, h, g, d_h, lo, hi, wid=820 + h),
+                            extra_rows=extra)
+    pos, lens = inputs.positions_and_lengths(w)
+    data = []
+    for li in range(3):
+        lw = dataclasses.replace(inputs.custom("big", b, h, g, d_h, lo, hi, wid=821 + h + li),
+                                 extra_rows=extra)
+        q, kn, vn = inputs.step_inputs(lw, 0, dev)
+        k, v = inputs.cache(lw, 0, dev, tail="nan", lengths=pos)
+        data.append((q, kn, vn, k, v))
+    order = [0, 1, 2, 0, 2]
+    scale = d_h ** -0.5
+    s = torch.cuda.Stream()
+    args = (order, data, pos.to(dev), lens.to(dev), scale, s)
+    serial = _run(mqa, *args, overlap=False, graph=graph, step_fn=_fused(mqa))
+    overl = _run(mqa, *args, overlap=True, graph=graph, step_fn=_fused(mqa))
+    _same_bits(*serial, *overl)
+    _check_oracle(order, data, overl[0], pos, lens, scale, max_checks=1)
