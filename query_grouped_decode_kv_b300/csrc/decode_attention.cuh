@@ -1304,9 +1304,192 @@ struct MmaConsumerF8 {
 };
 
 // ---------------------------------------------------------------------------------------------
-// CUDA-core consumer (G <= 7; fp8 caches, G <= 2 automatically). Warp w takes keys [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW,
-// 16 or 8); lane owns DPL = D/32 consecutive columns of q, K, V and the output. EB: the cache's
-// bytes per element (fp8 codes are widened exactly on load).
+// Consumer over fp8 E4M3 caches for groups of at most 8 heads: the products of MmaConsumerF8,
+// transposed. S^T = K q^T and O^T = V^T P^T put keys (then output columns) on the 16 rows of
+// each m16n8k16 MMA and the group's heads on its 8 columns, so no MMA carries padding rows: half
+// the MMAs, exponentials and accumulators of the head-row form, whose 16 rows hold 8 heads.
+//
+// S^T: one ldmatrix.x4 over the K stage gives a lane four consecutive codes (columns 4c .. 4c+3
+// of a 16-column block, c = lane % 4) of key r and of key r + 8 (r = lane / 4) for two column
+// blocks; widened, they are the A fragments of two k16 steps in the k order 2c, 2c+1 -> 4c, 4c+1
+// and 2c+8, 2c+9 -> 4c+2, 4c+3, which the B fragments of q^T (head r of the group, zero past G)
+// repeat.
+// P^T: the accumulator of S^T holds keys r and r + 8 by heads 2c, 2c+1; rounded to fp16 and
+// transposed with movmatrix it is the B fragment of P^T (head r by keys 2c, 2c+1 and 2c+8, 2c+9).
+// O^T: ldmatrix.trans over the V stage gives a lane keys 2c, 2c+1 of columns 2r, 2r+1 of a
+// 16-column block; one byte permute and two widenings make the A fragment whose rows r and r + 8
+// are the block's columns 2r and 2r + 1. The accumulator of block b then holds columns 16b + 2r
+// (c0, c1) and 16b + 2r + 1 (c2, c3) of heads 2c (c0, c2) and 2c + 1 (c1, c3).
+// Tile groups and key groups as in MmaConsumerF8: the NW warps form TG groups that take turns on
+// the tiles, and the NW / TG warps of a group split each tile's keys.
+// ---------------------------------------------------------------------------------------------
+template <int D, int NW, int TG>
+struct MmaConsumerF8T {
+  static constexpr int kWarps = NW;
+  static constexpr int kTileGroups = TG;
+  static constexpr bool kSharedQ = false;
+  static constexpr int kCombRows = 8;            // heads per warp
+  static constexpr int NGRP = NW / TG;           // key groups per tile group
+  static constexpr int KPW = kTileKeys / NGRP;   // keys per warp per tile
+  static constexpr int MT_S = KPW / 16;          // m-tiles of S^T (16 keys each)
+  static constexpr int KS_QK = D / 16;           // k-steps over the head dimension
+  static constexpr int MT_O = D / 16;            // m-tiles of O^T (16 output columns each)
+  static_assert(D == 128 && MT_S >= 1 && KS_QK % 2 == 0 && MT_O % 2 == 0, "tile split");
+
+  uint32_t qb[KS_QK][2];  // B fragments of q^T for head lane / 4 of the group
+  float o[MT_O][4];
+  float ol[4];  // P^T summed over keys by an all-ones A: c0 head 2c, c1 head 2c + 1
+  float m[2];   // softmax references of heads 2c and 2c + 1 (log2 units)
+
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
+                                                int lane) {
+    const int r = lane >> 2;
+    const bool valid = r < P.G;
+    const uint2* qr = reinterpret_cast<const uint2*>(P.q + (valid ? row_offset(P, bi, j, r, D) : 0));
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ++ks) {
+      // columns 16 ks + 4c .. + 3 of head r (one 8-byte load)
+      const uint2 x = valid ? __ldg(qr + ks * 4 + (lane & 3)) : make_uint2(0u, 0u);
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&x.x);
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&x.y);
+      qb[ks][0] = pack_f16x2(__low2float(a), __high2float(a));
+      qb[ks][1] = pack_f16x2(__low2float(b), __high2float(b));
+    }
+#pragma unroll
+    for (int n = 0; n < MT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    ol[0] = ol[1] = ol[2] = ol[3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+  }
+
+  // One tile: this warp's KPW keys from grp * KPW. `valid` = rows of the sequence from the tile's
+  // first row on (at least 1; may exceed the tile).
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
+                                       int valid, float scale_log2) {
+    const int mat = lane >> 3, rr = lane & 7;
+    const int r = lane >> 2;
+    // S^T, column blocks ks into s and ks + 1 into s2 (two independent chains per m-tile)
+    float s[MT_S][4], s2[MT_S][4];
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+      s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ks += 2) {
+#pragma unroll
+      for (int t = 0; t < MT_S; ++t) {
+        // matrices: keys 0-7 / 8-15 of the m-tile x column blocks ks / ks + 1
+        const int key = grp * KPW + t * 16 + rr + ((mat & 1) ? 8 : 0);
+        uint32_t w0, w1, w2, w3;
+        ldsm_x4(swz_bytes(kbase, key, (ks + (mat >> 1)) * 16), w0, w1, w2, w3);
+        uint32_t a[4], a2[4];
+        e4m3x4_to_f16x2x2(w0, a[0], a[2]);    // key r,     block ks
+        e4m3x4_to_f16x2x2(w1, a[1], a[3]);    // key r + 8, block ks
+        e4m3x4_to_f16x2x2(w2, a2[0], a2[2]);  // key r,     block ks + 1
+        e4m3x4_to_f16x2x2(w3, a2[1], a2[3]);  // key r + 8, block ks + 1
+        mma_16816_f16(s[t], a, qb[ks][0], qb[ks][1]);
+        mma_16816_f16(s2[t], a2, qb[ks + 1][0], qb[ks + 1][1]);
+      }
+    }
+    // scale (log2 domain), mask keys at or beyond the length, running max per head
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      const int key = grp * KPW + t * 16 + r;
+      const bool in0 = key < valid, in1 = key + 8 < valid;
+      s[t][0] = in0 ? (s[t][0] + s2[t][0]) * scale_log2 : -INFINITY;  // key r,     head 2c
+      s[t][1] = in0 ? (s[t][1] + s2[t][1]) * scale_log2 : -INFINITY;  // key r,     head 2c + 1
+      s[t][2] = in1 ? (s[t][2] + s2[t][2]) * scale_log2 : -INFINITY;  // key r + 8, head 2c
+      s[t][3] = in1 ? (s[t][3] + s2[t][3]) * scale_log2 : -INFINITY;  // key r + 8, head 2c + 1
+      mx0 = fmaxf(mx0, fmaxf(s[t][0], s[t][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[t][1], s[t][3]));
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    // lazy reference, as in MmaConsumer::tile (weights stay below 2^kLazyLog2, well inside fp16)
+    const bool up0 = mx0 > m[0] + kLazyLog2, up1 = mx1 > m[1] + kLazyLog2;
+    float al0 = 1.f, al1 = 1.f;
+    if (up0) { al0 = fast_exp2(m[0] - mx0); m[0] = mx0; }
+    if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
+    const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
+    const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      s[t][0] = fast_exp2(s[t][0] - ref0);
+      s[t][1] = fast_exp2(s[t][1] - ref1);
+      s[t][2] = fast_exp2(s[t][2] - ref0);
+      s[t][3] = fast_exp2(s[t][3] - ref1);
+    }
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+#pragma unroll
+      for (int n = 0; n < MT_O; ++n) {
+        o[n][0] *= al0; o[n][1] *= al1;
+        o[n][2] *= al0; o[n][3] *= al1;
+      }
+      ol[0] *= al0; ol[1] *= al1; ol[2] *= al0; ol[3] *= al1;
+    }
+    // O^T += V^T P^T with the weights rounded to fp16 once; the all-ones A sums those weights
+    const uint32_t ones[4] = {kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2};
+#pragma unroll
+    for (int kk = 0; kk < MT_S; ++kk) {
+      const uint32_t b0 = movmatrix_trans(pack_f16x2(s[kk][0], s[kk][1]));  // keys 2c, 2c+1
+      const uint32_t b1 = movmatrix_trans(pack_f16x2(s[kk][2], s[kk][3]));  // keys 2c+8, 2c+9
+      mma_16816_f16(ol, ones, b0, b1);
+#pragma unroll
+      for (int cb = 0; cb < MT_O; cb += 2) {
+        // matrices: keys 0-7 / 8-15 of this k-step x column blocks cb / cb + 1
+        const int key = grp * KPW + kk * 16 + rr + ((mat & 1) ? 8 : 0);
+        uint32_t w0, w1, w2, w3;
+        ldsm_x4_trans(swz_bytes(vbase, key, (cb + (mat >> 1)) * 16), w0, w1, w2, w3);
+        // bytes (0, 2) of a permuted word are column 2r of keys 2c, 2c+1; bytes (1, 3) column
+        // 2r + 1
+        uint32_t a[4], a2[4];
+        e4m3x4_to_f16x2x2(__byte_perm(w0, 0u, 0x3120), a[0], a[1]);
+        e4m3x4_to_f16x2x2(__byte_perm(w1, 0u, 0x3120), a[2], a[3]);
+        e4m3x4_to_f16x2x2(__byte_perm(w2, 0u, 0x3120), a2[0], a2[1]);
+        e4m3x4_to_f16x2x2(__byte_perm(w3, 0u, 0x3120), a2[2], a2[3]);
+        mma_16816_f16(o[cb], a, b0, b1);
+        mma_16816_f16(o[cb + 1], a2, b0, b1);
+      }
+    }
+  }
+
+  // Publish this warp's state (the group's heads 0..7) to the combine scratch.
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+    const int r = lane >> 2, h0 = (lane & 3) * 2;
+    float* row0 = sh.comb_o + (warp * kCombRows + h0) * comb_row_floats(D);
+    float* row1 = row0 + comb_row_floats(D);
+#pragma unroll
+    for (int b = 0; b < MT_O; ++b) {
+      *reinterpret_cast<float2*>(row0 + b * 16 + 2 * r) = make_float2(o[b][0], o[b][2]);
+      *reinterpret_cast<float2*>(row1 + b * 16 + 2 * r) = make_float2(o[b][1], o[b][3]);
+    }
+    if (r == 0) {
+      sh.comb_ml[warp * kCombRows + h0] = make_float2(m[0], ol[0]);
+      sh.comb_ml[warp * kCombRows + h0 + 1] = make_float2(m[1], ol[1]);
+    }
+  }
+
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        ws[w] = w;
+        rs[w] = hr;
+      }
+      return NW;
+    }
+  };
+};
+
+// ---------------------------------------------------------------------------------------------
+// CUDA-core consumer (G <= 7; over fp8 codes only when that path is forced). Warp w takes keys
+// [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW, 16 or 8); lane owns DPL = D/32 consecutive
+// columns of q, K, V and the output. EB: the cache's bytes per element (fp8 codes are widened
+// exactly on load).
 // ---------------------------------------------------------------------------------------------
 template <int D, int G, int NW, int EB = 2>
 struct CcConsumer {

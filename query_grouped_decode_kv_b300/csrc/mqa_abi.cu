@@ -332,14 +332,20 @@ AttnKernelChoice pick_kernel(Path path, int G, int b, int T) {
 AttnKernelChoice pick_kernel_fp8(Path path, int G, int b) {
   using mqa::CcConsumer;
   using mqa::MmaConsumerF8;
+  using mqa::MmaConsumerF8T;
   constexpr int D = 128;
   if (path == kPathTcgen05) return {};
   if (path == kPathMmaSync) {
     // several tile groups: an fp8 tile's HBM time is half a bf16 tile's while a warp's per-tile
-    // chain is not shorter, so groups of warps take turns on the tiles. Measured on B300 (32K
-    // rows, launches back to back, fraction of the copy bandwidth on fp8 bytes): up to 16 heads
-    // four groups of two warps, 32 keys each, reach 0.77-0.79 against 0.71-0.73 for two groups of
-    // four; at 32 heads two groups of four edge out one of eight (0.456 against 0.449).
+    // chain is not shorter, so groups of warps take turns on the tiles. Up to 8 heads the
+    // products run transposed (heads on the MMA's 8 columns, no padding rows). Measured on B300
+    // (32K rows, launches back to back, fraction of the copy bandwidth on fp8 bytes): at G = 1-8
+    // the transposed form reaches 0.90-0.91 with four groups of two warps (0.90-0.91 with eight
+    // single warps, 0.82-0.83 with two groups of four) against 0.78-0.79 for the head-row form;
+    // up to 16 heads four groups of two warps of the head-row form reach 0.77-0.79 against
+    // 0.71-0.73 for two groups of four; at 32 heads two groups of four edge out one of eight
+    // (0.456 against 0.449).
+    if (G <= 8) return choice<MmaConsumerF8T<D, 8, 4>, D, 1, true, 1>(b);
     if (G <= 16) return choice<MmaConsumerF8<D, 1, 8, 4>, D, 1, true, 1>(b);
     if (G <= 32) return choice<MmaConsumerF8<D, 2, 8, 2>, D, 1, true, 2>(b);
     return choice<MmaConsumerF8<D, 4, 8>, D, 1, true, 4>(b);

@@ -204,6 +204,14 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements spread over the warp as an MMA accumulator row
+// pair: lane l holds row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1, before and after.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // Four E4M3 codes (bytes 0..3 of w) -> two packed f16x2: bytes 0, 1 -> lo (byte 0 in the low
 // half), bytes 2, 3 -> hi. Exact: every E4M3 value is an fp16 value.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
