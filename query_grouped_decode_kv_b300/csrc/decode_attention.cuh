@@ -43,16 +43,18 @@ constexpr int kSwizzleRowBytes = 128;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;  // two bf16 ones (the B fragment of P 1)
 constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 // NW (a template parameter below) is the number of consumer warps: 4 or 8.
-//  - NW = 4: one producer warp and one launch-order warp come on top (192 threads).
+//  - NW = 4: a producer warp, a launch-order warp and a second producer warp (used over paged
+//    caches only) come on top (224 threads).
 //  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
 //    every thread kLaunchRegsWide registers (the most 384 threads can have on one SM); the
 //    producer warpgroup then hands registers back (setmaxnreg.dec to kProducerRegs) and the
-//    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Only one producer lane works;
-//    the next warp of the group is the launch-order warp.
+//    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Warp NW is the producer,
+//    warp NW + 1 the launch-order warp, warp NW + 2 the second producer over paged caches.
 // The launch-order warp (warp NW + 1) only matters for launches that overlap the kernel ahead of
 // them on the stream with early writes (DecodeParams::early_writes): its lane 0 waits for that
 // kernel to finish and only then lets the next launch be scheduled.
-__host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 2); }
+__host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 3); }
+constexpr int kPagedProducers = 2;  // producer warps over paged caches (warps NW and NW + 2)
 constexpr int kLaunchRegsWide = 168;
 constexpr int kProducerRegs = 72;
 constexpr int kConsumerRegs = 216;
@@ -143,7 +145,7 @@ __host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
   using Geo = Geometry<D, EB>;
   return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
-         32 * 4 +                           // the paged producer's looked-up pages
+         kPagedProducers * 32 * 4 +         // the paged producers' looked-up pages
          kMaxCcHeads * cc_q_row_floats(D) * 4 +  // q of the segment in fp32 (CUDA-core consumer)
          NW * kMaxCcHeads * kCcWarpKeys * 4;     // its key weights, per warp
 }
@@ -371,7 +373,7 @@ struct SharedLayout {
   uint64_t* stall;      // testing: a barrier nothing completes (DecodeParams::debug_stall)
   volatile int* abort;  // set when any warp gives up
   volatile int* merge;  // this CTA is the last to arrive at the segment being finished
-  int* pages;           // [32] paged caches: the pages of the tiles being issued (producer warp)
+  int* pages;           // [2][32] paged caches: the pages of the tiles being issued (per producer)
   float* q_f32;         // the segment's q in fp32 (CcConsumer2), laid out by cc_q_index
   float* p_cc;          // [NW][kMaxCcHeads][kCcWarpKeys] key weights of a tile (CcConsumer2)
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
@@ -402,7 +404,7 @@ __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
   s.merge = s.abort + 1;
   p += 16;
   s.pages = reinterpret_cast<int*>(p);  // 16-byte aligned: every region before it is a multiple
-  p += 32 * 4;                           // of 16 bytes
+  p += kPagedProducers * 32 * 4;         // of 16 bytes
   s.q_f32 = reinterpret_cast<float*>(p);
   p += kMaxCcHeads * cc_q_row_floats(D) * 4;
   s.p_cc = reinterpret_cast<float*>(p);
@@ -795,11 +797,14 @@ __device__ __forceinline__ void load_tile_pages(const int* slots, int kt, int (&
   }
 }
 
+// Several producer warps share a CTA's tiles over paged caches (np of them; this one is number
+// pi): warp pi issues tiles pi, pi + np, ... with its own page lookups and its own 32 slots.
 template <int D, int EB, int NB>
 __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
                                                     const CUtensorMap* tm_v,
                                                     const DecodeParams& P, const SharedLayout& sh,
-                                                    unsigned long long x0, int ntiles, int lane) {
+                                                    unsigned long long x0, int ntiles, int lane,
+                                                    int np, int pi) {
   using Geo = Geometry<D, EB>;
   constexpr int kStages = Geo::kStages;
   constexpr uint32_t kStageBytes = Geo::kStageBytes;
@@ -817,32 +822,41 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
   }
   const uint64_t policy = l2_policy_evict_first();
   const int my_tile = lane / NB;  // this lane's tile within a lookup batch
+  int* slots = sh.pages + pi * 32;
+  // this warp's tiles: k = pi + i * np for i < nmine
+  const int nmine = ntiles > pi ? (ntiles - pi + np - 1) / np : 0;
+  if (nmine == 0) return;
   TileCursor cur;
-  cur.start(x0, sh.tix);
+  cur.start(x0 + static_cast<unsigned long long>(pi), sh.tix);
   // `pages_next`: this lane's page of the next batch; `ahead`: the cursor of that batch's first tile
   TileCursor ahead = cur;
   int pages_next = 0;
-  if (my_tile < ntiles)
-    pages_next = lookup_page<NB>(P, cursor_ahead(cur, my_tile, x0 + my_tile, sh.tix), lane,
-                                 page_shift);
+  if (my_tile < nmine)
+    pages_next = lookup_page<NB>(
+        P, cursor_ahead(cur, my_tile * np, x0 + static_cast<unsigned long long>(pi + my_tile * np),
+                        sh.tix),
+        lane, page_shift);
   int issued = 0;
   int seq = -1, L = 0, row_p = -1;  // the sequence of the last tile, its length and append row
-  for (int k = 0; k < ntiles; ++k) {
-    const int kt = k % T;
+  for (int i = 0; i < nmine; ++i) {
+    const int k = pi + i * np;
+    const int kt = i % T;
     if (kt == 0) {
-      // batch k / T starts: publish its pages (looked up a batch ago) to lane 0 and look up the
-      // next batch
+      // batch i / T starts: publish its pages (looked up a batch ago) to the slots and look up
+      // the next batch
       __syncwarp();
-      sh.pages[lane] = pages_next;
+      slots[lane] = pages_next;
       __syncwarp();
-      const int k1 = k + T;
-      if (k1 < ntiles) {
-        ahead = cursor_ahead(ahead, T, x0 + static_cast<unsigned long long>(k1), sh.tix);
-        if (k1 + my_tile < ntiles)
-          pages_next = lookup_page<NB>(P, cursor_ahead(ahead, my_tile,
-                                                       x0 + static_cast<unsigned long long>(
-                                                                k1 + my_tile), sh.tix),
-                                       lane, page_shift);
+      const int i1 = i + T;
+      if (i1 < nmine) {
+        ahead = cursor_ahead(ahead, T * np, x0 + static_cast<unsigned long long>(pi + i1 * np),
+                             sh.tix);
+        if (i1 + my_tile < nmine)
+          pages_next = lookup_page<NB>(
+              P,
+              cursor_ahead(ahead, my_tile * np,
+                           x0 + static_cast<unsigned long long>(pi + (i1 + my_tile) * np), sh.tix),
+              lane, page_shift);
       }
     }
     if (cur.bi != seq) {
@@ -875,7 +889,7 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
       uint8_t* kdst = sh.stages + st * kStageBytes;
       uint8_t* vdst = kdst + kKvBytes;
       int pg[NB];
-      load_tile_pages<NB>(sh.pages, kt, pg);
+      load_tile_pages<NB>(slots, kt, pg);
       bool any_bad = false;
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
@@ -897,12 +911,20 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
     }
     __syncwarp();
     ++issued;
-    cur.advance(sh.tix);
+    for (int a = 0; a < np; ++a) cur.advance(sh.tix);
   }
-  if (lane != 0) return;
+  if (lane != 0 || issued == 0) return;
+  // let this warp's copies still in flight land before the CTA may exit (bounded). With np
+  // dividing the stage count, stage k % kStages only ever holds this warp's tiles, so a tile is
+  // known to have landed once this warp has refilled its stage: the ones still to wait for are
+  // those within kStages of the last tile it issued.
   const volatile int never = 0;
-  for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+  const int k_last = pi + (issued - 1) * np;
+  for (int i = 0; i < issued; ++i) {
+    const int k = pi + i * np;
+    if (k > k_last - kStages)
+      mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+  }
 }
 
 // Boxes per tile from the page size (8, 16, 32 rows; 64 or more: one box).
@@ -912,12 +934,12 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
                                                         const DecodeParams& P,
                                                         const SharedLayout& sh,
                                                         unsigned long long x0, int ntiles,
-                                                        int lane) {
+                                                        int lane, int np, int pi) {
   switch (P.page_size) {
-    case 8: produce_tiles_paged<D, EB, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    case 16: produce_tiles_paged<D, EB, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    case 32: produce_tiles_paged<D, EB, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
-    default: produce_tiles_paged<D, EB, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane); break;
+    case 8: produce_tiles_paged<D, EB, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    case 16: produce_tiles_paged<D, EB, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    case 32: produce_tiles_paged<D, EB, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    default: produce_tiles_paged<D, EB, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
   }
 }
 
@@ -1905,11 +1927,14 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   if (warp >= NW) {
     // ================================ producer ================================================
-    if (warp == NW) {
-      if (P.page_table != nullptr)
-        produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
-      else
-        produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+    // contiguous caches: warp NW issues every tile (two or four copies each); paged caches take
+    // up to 2 * 64 / page_size copies per tile, and warps NW and NW + 2 issue alternate tiles
+    const bool paged = P.page_table != nullptr;
+    if (warp == NW && !paged) {
+      produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
+    } else if (paged && (warp == NW || warp == NW + 2)) {
+      produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, kPagedProducers,
+                                     warp == NW ? 0 : 1);
     } else if (warp == NW + 1 && lane == 0 && P.early_writes) {
       // ============================ launch order ==============================================
       pdl_wait();
@@ -1924,6 +1949,11 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   constexpr int TG = Consumer::kTileGroups;
   constexpr int WPG = NW / TG;  // warps per tile group
   static_assert(TG == 1 || kTensorCores || Consumer::kSharedQ, "tile groups of this consumer");
+  // Each stage must always serve the same tile group, which takes its uses in order: a group
+  // that could wait on a stage two uses ahead would see the parity of the use before it.
+  static_assert(kStages % TG == 0, "stages per tile group");
+  // and each stage to one paged producer warp (its drain relies on it)
+  static_assert(kStages % kPagedProducers == 0, "stages per producer");
   const int tg = warp / WPG;
   const int gw = warp % WPG;
   const int grp = kTensorCores ? gw / WM : warp;

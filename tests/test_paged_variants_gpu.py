@@ -90,6 +90,39 @@ def test_paged_fp8_step_matches_the_oracle(mqa, shape, page_size, fused):
     assert torch.equal(out.view(torch.int16), out_c.view(torch.int16))
 
 
+@pytest.mark.parametrize("ctas", [1, 3, 148, 1000])
+@pytest.mark.parametrize("page_size", [8, 16])
+def test_paged_fp8_any_cta_split_equals_contiguous(mqa, page_size, ctas):
+    """Two producer warps share a CTA's tiles over paged caches (alternate tiles, each with its
+    own page lookups): one CTA walks every tile, 1000 CTAs leave most with one tile or none.
+    The same split over the same codes laid out contiguously gives the same bits."""
+    case = fp8_case((3, 16, 2, 128, 1, 1500), seed_id=1740 + page_size)
+    rows = torch.maximum(case["lens"], case["pos"] + 1)
+    _page(case, case["k8"], case["v8"], rows, page_size, seed=1741 + page_size)
+    dev = torch.device("cuda")
+    q, kn, vn = case["q"].to(dev), case["k_new"].to(dev), case["v_new"].to(dev)
+    pos, lens, table = case["pos"].to(dev), case["lens"].to(dev), case["table"].to(dev)
+    ks, vs = case["k_scale"], case["v_scale"]
+    mqa.debug_override(ctas, 0)
+    try:
+        kpd, vpd = case["k_pool"].to(dev), case["v_pool"].to(dev)
+        out = mqa.decode_step_paged_fp8(q, kn, vn, kpd, vpd, pos, table, lens, ks, vs,
+                                        scale=case["scale"])
+        kc8, vc8 = case["k8"].to(dev), case["v8"].to(dev)
+        out_c = mqa.decode_step_fp8(q, kn, vn, kc8, vc8, pos, lens, ks, vs, scale=case["scale"])
+        torch.cuda.synchronize()
+    finally:
+        mqa.debug_override(0, 0)
+    assert mqa.get_device_status() == 0
+    assert torch.equal(out.view(torch.int16), out_c.view(torch.int16))
+    # the appended rows landed in the pools where the table maps them
+    kp, vp = case["k_pool"].numpy().copy(), case["v_pool"].numpy().copy()
+    assert oracle.kv_append_paged_fp8(P.bits(case["k_new"]), P.bits(case["v_new"]), kp, vp,
+                                      case["pos"].numpy(), case["table"].numpy(), ks,
+                                      vs) == oracle.OK
+    assert np.array_equal(kpd.cpu().numpy(), kp) and np.array_equal(vpd.cpu().numpy(), vp)
+
+
 def test_paged_fp8_bad_page_latches_and_skips_the_append(mqa):
     case = fp8_case((3, 16, 2, 128, 100, 400), seed_id=1720)
     rows = torch.maximum(case["lens"], case["pos"] + 1)
