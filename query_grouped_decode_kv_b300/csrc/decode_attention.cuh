@@ -43,18 +43,23 @@ constexpr int kSwizzleRowBytes = 128;
 constexpr uint32_t kOnesBf16x2 = 0x3F803F80u;  // two bf16 ones (the B fragment of P 1)
 constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 // NW (a template parameter below) is the number of consumer warps: 4 or 8.
-//  - NW = 4: a producer warp, a launch-order warp and a second producer warp (used over paged
-//    caches only) come on top (224 threads).
+//  - NW = 4: a producer warp, a launch-order warp and a second producer warp come on top
+//    (224 threads).
 //  - NW = 8: two consumer warpgroups and one producer warpgroup (384 threads). The launch gives
 //    every thread kLaunchRegsWide registers (the most 384 threads can have on one SM); the
 //    producer warpgroup then hands registers back (setmaxnreg.dec to kProducerRegs) and the
 //    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Warp NW is the producer,
-//    warp NW + 1 the launch-order warp, warp NW + 2 the second producer over paged caches.
+//    warp NW + 1 the launch-order warp, warp NW + 2 the second producer.
 // The launch-order warp (warp NW + 1) only matters for launches that overlap the kernel ahead of
 // them on the stream with early writes (DecodeParams::early_writes): its lane 0 waits for that
 // kernel to finish and only then lets the next launch be scheduled.
 __host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 3); }
-constexpr int kPagedProducers = 2;  // producer warps over paged caches (warps NW and NW + 2)
+// Producer warps (warps NW and NW + 2, alternate tiles). Measured on B300 against one producer
+// warp, launches back to back: the 70B-class layer over fp8 codes 62.1-62.7 us against 68.7 us
+// contiguous, 8-row fp8 pages 0.69 of the copy bandwidth against 0.42; the 80-layer bf16 step
+// 7,835 against 7,913 us; mha_ref 152.5 against 157.7 us.
+constexpr int kPagedProducers = 2;       // over paged caches
+constexpr int kContiguousProducers = 2;  // over contiguous caches
 constexpr int kLaunchRegsWide = 168;
 constexpr int kProducerRegs = 72;
 constexpr int kConsumerRegs = 216;
@@ -667,15 +672,17 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
 }
 
 // ---------------------------------------------------------------------------------------------
-// Producer warp: stream the CTA's tiles [x0, x0 + ntiles) into the stage ring with bulk tensor
-// copies (one elected lane), after writing the fused append's new row into the cache when the
-// tile holds it (whole warp, one 16-byte chunk per lane). Stage st is refilled once its `empty`
-// barrier has completed the phase of its previous use.
+// Producer warps: stream the CTA's tiles [x0, x0 + ntiles) into the stage ring with bulk tensor
+// copies (one elected lane per warp), after writing the fused append's new row into the cache
+// when the tile holds it (whole warp, one 16-byte chunk per lane). With np producer warps, warp
+// pi issues tiles pi, pi + np, ...; np divides the stage count, so every stage is refilled by one
+// warp, once its `empty` barrier has completed the phase of its previous use.
 // ---------------------------------------------------------------------------------------------
 template <int D, int EB>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                               const DecodeParams& P, const SharedLayout& sh,
-                                              unsigned long long x0, int ntiles, int lane) {
+                                              unsigned long long x0, int ntiles, int lane,
+                                              int np, int pi) {
   using Geo = Geometry<D, EB>;
   constexpr int kStages = Geo::kStages;
   constexpr uint32_t kStageBytes = Geo::kStageBytes;
@@ -686,11 +693,14 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
     prefetch_tensor_map(tm_v);
   }
   const uint64_t policy = l2_policy_evict_first();
+  const int nmine = ntiles > pi ? (ntiles - pi + np - 1) / np : 0;
+  if (nmine == 0) return;
   TileCursor cur;
-  cur.start(x0, sh.tix);
+  cur.start(x0 + static_cast<unsigned long long>(pi), sh.tix);
   int issued = 0;
   int row_bi = -1, row_p = -1;  // the first append row of sequence row_bi (-1: none to write)
-  for (int k = 0; k < ntiles; ++k) {
+  for (int i = 0; i < nmine; ++i) {
+    const int k = pi + i * np;
     const int st = k % kStages;
     const uint32_t par = ((k / kStages) & 1) ^ 1;
     // the whole warp waits (no branch on the lane); a vote keeps the outcome warp-uniform
@@ -728,13 +738,18 @@ __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUt
     }
     __syncwarp();
     ++issued;
-    cur.advance(sh.tix);
+    for (int a = 0; a < np; ++a) cur.advance(sh.tix);
   }
-  if (lane != 0) return;
-  // let the copies still in flight land before the CTA may exit (bounded; no-op normally)
+  if (lane != 0 || issued == 0) return;
+  // let this warp's copies still in flight land before the CTA may exit (bounded; no-op
+  // normally): with np dividing the stage count, the tiles within kStages of its last one
   const volatile int never = 0;
-  for (int k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-    mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+  const int k_last = pi + (issued - 1) * np;
+  for (int i = 0; i < issued; ++i) {
+    const int k = pi + i * np;
+    if (k > k_last - kStages)
+      mbar_wait_bounded(&sh.full[k % kStages], (k / kStages) & 1, P.drain_ns, &never);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1927,14 +1942,17 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   }
   if (warp >= NW) {
     // ================================ producer ================================================
-    // contiguous caches: warp NW issues every tile (two or four copies each); paged caches take
-    // up to 2 * 64 / page_size copies per tile, and warps NW and NW + 2 issue alternate tiles
+    // warps NW and NW + 2 issue alternate tiles (a tile takes two or four copies from contiguous
+    // caches, up to 2 * 64 / page_size from paged ones), so one warp's issue rate does not bound
+    // the CTA
     const bool paged = P.page_table != nullptr;
-    if (warp == NW && !paged) {
-      produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane);
-    } else if (paged && (warp == NW || warp == NW + 2)) {
-      produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, kPagedProducers,
-                                     warp == NW ? 0 : 1);
+    const int np = paged ? kPagedProducers : kContiguousProducers;
+    if (warp == NW || (np == 2 && warp == NW + 2)) {
+      const int pi = warp == NW ? 0 : 1;
+      if (paged)
+        produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
+      else
+        produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
     } else if (warp == NW + 1 && lane == 0 && P.early_writes) {
       // ============================ launch order ==============================================
       pdl_wait();
@@ -1953,7 +1971,8 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   // that could wait on a stage two uses ahead would see the parity of the use before it.
   static_assert(kStages % TG == 0, "stages per tile group");
   // and each stage to one paged producer warp (its drain relies on it)
-  static_assert(kStages % kPagedProducers == 0, "stages per producer");
+  static_assert(kStages % kPagedProducers == 0 && kStages % kContiguousProducers == 0,
+                "stages per producer");
   const int tg = warp / WPG;
   const int gw = warp % WPG;
   const int grp = kTensorCores ? gw / WM : warp;
