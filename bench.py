@@ -63,14 +63,19 @@ UNIT = "us/step"
 FALLBACK_HBM_GBS = 6400.0
 HEADLINE = "gqa_70b_80l"
 ALL_WORKLOADS = ["mqa_tiny", "gqa_8b", "mqa_long", "mha_ref", "gqa_70b_80l"]
-KERNEL_SOURCES = ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
-                  "query_grouped_decode_kv_b300/csrc/decode_attention_tc.cuh",
-                  "query_grouped_decode_kv_b300/csrc/kv_append.cuh",
-                  "query_grouped_decode_kv_b300/csrc/prefill_attention_tc.cuh",
-                  "query_grouped_decode_kv_b300/csrc/ptx.cuh",
-                  "query_grouped_decode_kv_b300/csrc/status.cuh",
-                  "query_grouped_decode_kv_b300/csrc/mqa_abi.cu",
-                  "include/mqa.h"]
+# The sources each kernel family is built from: a stored DRAM capture of a family's kernel holds
+# while they are unchanged.
+KERNEL_SOURCES = {
+    "decode": ["query_grouped_decode_kv_b300/csrc/decode_attention.cuh",
+               "query_grouped_decode_kv_b300/csrc/kv_append.cuh",
+               "query_grouped_decode_kv_b300/csrc/ptx.cuh",
+               "query_grouped_decode_kv_b300/csrc/status.cuh",
+               "query_grouped_decode_kv_b300/csrc/mqa_abi.cu",
+               "include/mqa.h"],
+}
+KERNEL_SOURCES["prefill"] = KERNEL_SOURCES["decode"] + [
+    "query_grouped_decode_kv_b300/csrc/decode_attention_tc.cuh",
+    "query_grouped_decode_kv_b300/csrc/prefill_attention_tc.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
 L2_BYTES = 126 * 1024 * 1024
 ROTATION_L2_MULTIPLE = 4   # bytes read between two reads of the same copy, in L2 sizes
@@ -126,26 +131,29 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(family: str = "decode") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch from a committed ncu summary, if it was taken on the
-    current kernel sources; else None."""
+    """DRAM bytes per launch of the step's dominant kernel from a committed ncu summary, if it
+    was taken on the current sources of that kernel's family; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except Exception:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
-        return None
     per = rec.get("per_workload", {}).get(workload)
-    return None if per is None else per.get("dram_bytes_per_launch")
+    if per is None:
+        return None
+    family = per.get("family", "decode")
+    if family not in KERNEL_SOURCES or per.get("source_hash") != kernel_source_hash(family):
+        return None
+    return per.get("dram_bytes_per_launch")
 
 
 class ClockSampler:

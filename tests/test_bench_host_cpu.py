@@ -7,6 +7,7 @@ keys, the L2-flush rule and the causal FLOP count. The benchmark's timing rules 
 from __future__ import annotations
 
 import json
+import os
 import re
 
 import pytest
@@ -49,17 +50,30 @@ def test_clock_summary_without_samples_says_unavailable(tmp_path):
 
 def test_stored_traffic_is_used_only_on_the_sources_it_was_taken_on(tmp_path, monkeypatch):
     f = tmp_path / "traffic.json"
-    rec = {"source_hash": bench.kernel_source_hash(),
-           "per_workload": {"w": {"dram_bytes_per_launch": 123}}}
+    rec = {"per_workload": {
+        "w": {"dram_bytes_per_launch": 123, "family": "decode",
+              "source_hash": bench.kernel_source_hash("decode")},
+        "w_T512": {"dram_bytes_per_launch": 456, "family": "prefill",
+                   "source_hash": bench.kernel_source_hash("prefill")}}}
     f.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.recorded_traffic("w") == 123
+    assert bench.recorded_traffic("w_T512") == 456
     assert bench.recorded_traffic("another") is None
-    rec["source_hash"] = "0" * 16              # taken on other kernel sources
+    rec["per_workload"]["w"]["source_hash"] = "0" * 16    # taken on other kernel sources
+    rec["per_workload"]["w_T512"]["family"] = "decode"    # hashed over the wrong family
     f.write_text(json.dumps(rec))
     assert bench.recorded_traffic("w") is None
+    assert bench.recorded_traffic("w_T512") is None
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "absent.json"))
     assert bench.recorded_traffic("w") is None
+
+
+def test_the_prefill_family_covers_the_decode_sources():
+    assert set(bench.KERNEL_SOURCES["decode"]) < set(bench.KERNEL_SOURCES["prefill"])
+    for fam in bench.KERNEL_SOURCES.values():
+        for rel in fam:
+            assert os.path.exists(os.path.join(bench.ROOT, rel)), rel
 
 
 _KEY = re.compile(r"^(?P<wl>[a-z0-9_]+?)(?:_paged(?P<p>\d+))?(?P<f8>_fp8)?(?:_T(?P<T>\d+))?$")
