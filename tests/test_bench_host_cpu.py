@@ -92,7 +92,11 @@ def test_committed_traffic_is_close_above_the_algorithmic_bytes():
         w, _, lens = bench.step_shape(inputs.WORKLOADS[m.group("wl")], T)
         algorithmic = bench.kv_bytes(w, lens, 1 if m.group("f8") else 2, T)
         ratio = entry["dram_bytes_per_launch"] / algorithmic
-        assert 0.999 <= ratio <= 1.04, (key, ratio)
+        # a decode launch reads each K/V row once; the prefill kernel's 128-row blocks of one
+        # segment read its K/V through L2, and the rows that miss come from DRAM again
+        hi = 1.15 if entry.get("family") == "prefill" else 1.04
+        assert 0.999 <= ratio <= hi, (key, ratio)
+        assert entry["family"] in bench.KERNEL_SOURCES, key
 
 
 def test_traffic_keys_name_the_variant():
