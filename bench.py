@@ -347,27 +347,29 @@ class OracleLayer:
         n = max(1, min(T, int(T * self.MAX_PAIRS / pairs)))
         return sorted({int(round(i * (T - 1) / max(n - 1, 1))) for i in range(n)})
 
-    def time_layer(self) -> float:
+    def time_layer(self, threads: int | None = None) -> float:
         """Seconds of one whole-layer attention by the oracle (all sequences, all heads); with a
-        token sample, the sample's time scaled by the attended rows of the whole layer."""
+        token sample, the sample's time scaled by the attended rows of the whole layer.
+        `threads`: the oracle's thread count (default: every host core)."""
         import numpy as np
 
         import oracle
+        nthr = self.threads if threads is None else threads
         toks = self._sample()
         t0 = time.perf_counter()
         if self.T > 1 and toks is None:
             oracle.decode_attention_multi(self.q, self.k, self.v, self.lens, self.scale,
-                                          threads=self.threads)
+                                          threads=nthr)
             return time.perf_counter() - t0
         if self.T == 1:
             oracle.decode_attention(self.q, self.k, self.v, self.lens, self.scale,
-                                    threads=self.threads)
+                                    threads=nthr)
             return time.perf_counter() - t0
         T, rows_sampled = self.T, 0
         for t in toks:
             lim = (self.lens - T + 1 + t).astype(np.int32)
             oracle.decode_attention(np.ascontiguousarray(self.q[:, t]), self.k, self.v, lim,
-                                    self.scale, threads=self.threads)
+                                    self.scale, threads=nthr)
             rows_sampled += int(lim.sum())
         spent = time.perf_counter() - t0
         rows_all = sum(T * int(L) - T * (T - 1) // 2 for L in self.lens.tolist())
@@ -472,12 +474,24 @@ def timing_event():
     return torch.cuda.Event(enable_timing=True, external=True)
 
 
+REPLAYS = 5  # timed replays after the one the step time is taken from, for the spread
+
+
+def spread(samples) -> dict:
+    """p10, median and p90 of a list of µs-per-step samples (nearest rank)."""
+    xs = sorted(samples)
+    pick = lambda q: xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]  # noqa: E731
+    return {"n": len(xs), "p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9)}
+
+
 def time_steps(units: Units, stream, steps: int, flush, mqa, overlap: bool,
-               one_launch: bool = False) -> tuple[float, int]:
+               one_launch: bool = False) -> tuple[float, int, dict]:
     """Mean µs per step over `steps` steps recorded as one CUDA graph and replayed once (after
     an untimed replay). With `flush`, every step is preceded by an L2 flush and bracketed by its
     own event nodes (the flush untimed); else the graph runs between two events. `one_launch`:
-    every step is a single launch (unit k mod count). Returns (µs per step, launches per step)."""
+    every step is a single launch (unit k mod count). Returns (µs per step, launches per step,
+    spread): the spread is over the single steps of that replay when each step has its own
+    events, else over REPLAYS more timed replays of the whole graph."""
     mqa.set_launch_overlap(overlap, stream)
     n = len(units.layers)
     pairs = []
@@ -507,10 +521,25 @@ def time_steps(units: Units, stream, steps: int, flush, mqa, overlap: bool,
         t1.record(stream)
     torch.cuda.synchronize()
     assert mqa.get_device_status() == 0, "device status latched an error in a timed region"
-    ms = (sum(a.elapsed_time(b) for a, b in pairs) if flush is not None
-          else t0.elapsed_time(t1))
+    if flush is not None:
+        per = [a.elapsed_time(b) * 1000.0 for a, b in pairs]
+        ms = sum(per) / 1000.0
+        dist = spread(per)
+    else:
+        ms = t0.elapsed_time(t1)
+        more = []
+        for _ in range(REPLAYS):
+            a, b = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            more.append(a.elapsed_time(b) * 1000.0 / steps)
+        assert mqa.get_device_status() == 0, "device status latched an error in a timed region"
+        dist = spread(more)
     del g
-    return ms * 1000.0 / steps, per_step
+    return ms * 1000.0 / steps, per_step, dist
 
 
 def measure_workload(w, dev, stream, args, mqa, flush_buf, T=1, kv="bf16", paged=0):
@@ -524,16 +553,19 @@ def measure_workload(w, dev, stream, args, mqa, flush_buf, T=1, kv="bf16", paged
     torch.cuda.synchronize()
     assert mqa.get_device_status() == 0, "device status latched an error during warm-up"
     flush = flush_buf if units.flush_each_step else None
-    us_step, per_step = time_steps(units, stream, args.steps, flush, mqa, overlap=True)
-    us_iso, _ = time_steps(units, stream, min(args.steps, 20), flush_buf, mqa, overlap=False,
-                           one_launch=True)
+    us_step, per_step, dist = time_steps(units, stream, args.steps, flush, mqa, overlap=True)
+    us_iso, _, dist_iso = time_steps(units, stream, min(args.steps, 20), flush_buf, mqa,
+                                     overlap=False, one_launch=True)
     mqa.set_launch_overlap(True, stream)
     peak, _ = measured_peak_hbm()
     us_launch = us_step / per_step
     gbs = units.bytes_per_launch / (us_launch * 1e-6) / 1e9
     summary = {
         "us_per_step": us_step, "launches_per_step": per_step, "us_per_launch": us_launch,
+        "us_per_step_spread": dict(dist, over=("single steps of the timed replay" if flush is not None
+                                               else f"{REPLAYS} more timed replays of the K steps")),
         "us_per_launch_isolated": us_iso,
+        "us_per_launch_isolated_spread": dict(dist_iso, over="single isolated launches"),
         "algorithmic_bytes_per_launch": units.bytes_per_launch,
         "kv_gbs": gbs, "frac_of_hbm": gbs / peak,
         "kv_gbs_isolated": units.bytes_per_launch / (us_iso * 1e-6) / 1e9,
@@ -701,6 +733,11 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": {"value": cb_us, "unit": UNIT, "cores": lay.threads, "kind": "oracle",
                              "sample": lay.describe(cb_s)},
         }
+        if others:
+            # the two smallest workloads' oracle on one host thread (one whole layer each)
+            line["cpu_baseline"]["single_thread_us_per_step"] = {
+                name: OracleLayer(inputs.WORKLOADS[name]).time_layer(threads=1) * 1e6
+                for name in ("mqa_tiny", "gqa_8b")}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -727,6 +764,10 @@ def line_problems(line: dict, rel: float = 1e-6) -> list[str]:
             out.append(f"{name}: launches x us_per_launch != us_per_step")
         if not close(c["kv_gbs"], c["algorithmic_bytes_per_launch"] / (per * 1e-6) / 1e9):
             out.append(f"{name}: kv_gbs is not bytes per launch over the time per launch")
+        for key in ("us_per_step_spread", "us_per_launch_isolated_spread"):
+            d = c.get(key)
+            if d is not None and not d["p10"] <= d["median"] <= d["p90"]:
+                out.append(f"{name}: {key} is not ordered")
     r = line["roofline"]
     head = line["configs"][line["config"]["workload"]]
     if not close(r["us_per_launch"], head["us_per_launch"]):

@@ -188,3 +188,20 @@ def test_the_line_checks_catch_a_launch_longer_than_its_step():
     bad = json.loads(json.dumps(line))
     bad["roofline"]["frac"] *= 1.1
     assert any("frac" in p for p in bench.line_problems(bad))
+
+
+def test_spread_is_nearest_rank_percentiles():
+    d = bench.spread([5.0, 1.0, 4.0, 2.0, 3.0])
+    assert d == {"n": 5, "p10": 1.0, "median": 3.0, "p90": 5.0}
+    one = bench.spread([7.0])
+    assert one["p10"] == one["median"] == one["p90"] == 7.0
+    many = bench.spread(list(range(101)))
+    assert (many["p10"], many["median"], many["p90"]) == (10, 50, 90)
+
+
+def test_line_checker_flags_an_unordered_spread():
+    line = json.loads(open(os.path.join(bench.ROOT, "profiles", "bench_default_line.json")).read())
+    assert bench.line_problems(line) == []
+    name = line["config"]["workload"]
+    line["configs"][name]["us_per_step_spread"] = {"n": 5, "p10": 3.0, "median": 2.0, "p90": 4.0}
+    assert any("not ordered" in p for p in bench.line_problems(line))
