@@ -258,3 +258,48 @@ def test_overlapped_layers_over_large_caches_equal_serial_ones(mqa, shape, graph
     overl = _run(mqa, *args, overlap=True, graph=graph, step_fn=_fused(mqa))
     _same_bits(*serial, *overl)
     _check_oracle(order, data, overl[0], pos, lens, scale, max_checks=1)
+
+
+def test_overlapped_paged_fp8_and_paged_multi_layers_equal_serial_ones(mqa):
+    """Pages combined with fp8 codes, and with several new tokens, under overlap: the two paged
+    producer warps of every launch write their tiles' new rows early or after the wait."""
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    order = [0, 1, 2, 0, 2]
+    # fp8 codes in 16-row pages
+    pos, lens, data = _layers(4, 32, 4, 128, 300, 3000, n=3, seed=800, dev=dev)
+    f8, scales, table = [], [], None
+    for (q, kn, vn, k, v) in data:
+        ks, vs = inputs.amax_scale(k), inputs.amax_scale(v)
+        kp, vp, tbl = inputs.page_pool(inputs.fp8_codes(k, ks), inputs.fp8_codes(v, vs), lens, 16,
+                                       seed=801)
+        table = tbl.to(dev)
+        f8.append((q, kn, vn, kp, vp))
+        scales.append((ks, vs))
+
+    def paged_fp8(li, q, kn, vn, k, v, pos_d, lens_d, o, scale, stream):
+        mqa.decode_step_paged_fp8(q, kn, vn, k, v, pos_d, table, lens_d, *scales[li], out=o,
+                                  scale=scale, stream=stream)
+    args = (order, f8, pos.to(dev), lens.to(dev), 128 ** -0.5, s)
+    serial = _run(mqa, *args, overlap=False, graph=False, step_fn=paged_fp8)
+    overl = _run(mqa, *args, overlap=True, graph=True, step_fn=paged_fp8)
+    for x, y in zip(serial[0], overl[0]):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    for (k0, v0), (k1, v1) in zip(serial[1], overl[1]):
+        assert torch.equal(k0, k1) and torch.equal(v0, v1)
+    # four tokens per sequence in 8-row pages
+    T = 4
+    pos, lens, data = _layers(3, 32, 4, 128, 200, 2500, n=3, seed=810, dev=dev, T=T)
+    paged = []
+    for (q, kn, vn, k, v) in data:
+        kp, vp, tbl = inputs.page_pool(k, v, lens, 8, seed=811)
+        table = tbl.to(dev)
+        paged.append((q, kn, vn, kp, vp))
+
+    def paged_multi(li, q, kn, vn, k, v, pos_d, lens_d, o, scale, stream):
+        mqa.decode_step_paged_multi(q, kn, vn, k, v, pos_d, table, lens_d, out=o, scale=scale,
+                                    stream=stream)
+    args = (order, paged, pos.to(dev), lens.to(dev), 128 ** -0.5, s)
+    serial = _run(mqa, *args, overlap=False, graph=False, step_fn=paged_multi)
+    overl = _run(mqa, *args, overlap=True, graph=True, step_fn=paged_multi)
+    _same_bits(*serial, *overl)
