@@ -403,13 +403,14 @@ MQA_API int mqa_decode_attention_noalloc(const mqa_bf16* q, const mqa_bf16* k_ca
  * overlap off. A call whose K and V caches together span at most 768 MiB (b*g*n_max rows of
  * d_h elements, counted for both caches) writes early: it never shares its scratch with the
  * launch ahead of it (the stream's workspace has two halves that consecutive launches take in
- * turn), and the launch after it may start only once the launch ahead has finished. A call over
- * larger caches, and every mqa_decode_attention_noalloc call (one scratch array), reads early but
- * writes nothing -- no output, no scratch, no appended row -- before the kernel ahead has
- * finished. The setting applies to the attention, step, paged, fp8,
- * multi-token (h/g * T <= 64) and no-alloc calls on the mma.sync and CUDA-core paths (the forced
- * tcgen05 path and the prefill path never overlap), and to launches captured into a CUDA graph,
- * where it becomes a programmatic edge between consecutive kernel nodes.
+ * turn). A call over larger caches, and every mqa_decode_attention_noalloc call (one scratch
+ * array), reads early but writes nothing -- no output, no scratch, no appended row -- before the
+ * kernel ahead has finished. In both cases the launch after a call may start only once the
+ * kernel ahead of the call has finished, so no launch runs beside the one two back. The setting
+ * applies to the attention, step, paged, fp8, multi-token (h/g * T <= 64) and no-alloc calls on
+ * the mma.sync and CUDA-core paths (the forced tcgen05 path and the prefill path never overlap),
+ * and to launches captured into a CUDA graph, where it becomes a programmatic edge between
+ * consecutive kernel nodes.
  *
  *   stream   cudaStream_t, on the current device (NULL: the legacy default stream)
  *   on       1 to allow overlap, 0 to forbid it

@@ -50,9 +50,9 @@ constexpr uint32_t kOnesF16x2 = 0x3C003C00u;   // two fp16 ones
 //    producer warpgroup then hands registers back (setmaxnreg.dec to kProducerRegs) and the
 //    consumer warpgroups take them (setmaxnreg.inc to kConsumerRegs). Warp NW is the producer,
 //    warp NW + 1 the launch-order warp, warp NW + 2 the second producer.
-// The launch-order warp (warp NW + 1) only matters for launches that overlap the kernel ahead of
-// them on the stream with early writes (DecodeParams::early_writes): its lane 0 waits for that
-// kernel to finish and only then lets the next launch be scheduled.
+// The launch-order warp (warp NW + 1) matters for launches that overlap the kernel ahead of them
+// on the stream: its lane 0 waits for that kernel to finish and only then lets the next launch be
+// scheduled, so that a launch never starts before the one two back has finished.
 __host__ __device__ constexpr int threads_of(int NW) { return NW == 8 ? 384 : 32 * (NW + 3); }
 // Producer warps (warps NW and NW + 2, alternate tiles). Measured on B300 against one producer
 // warp, launches back to back: the 70B-class layer over fp8 codes 62.1-62.7 us against 68.7 us
@@ -108,13 +108,14 @@ struct DecodeParams {
   // output is multiplied by out_scale (the V scale; 1 for bf16 caches, where it changes nothing)
   float kq_scale, vq_scale, out_scale;
   // Launch overlap (programmatic dependent launch), for launches that may start while the kernel
-  // ahead of them on the stream still runs. 0: the kernel signals its dependents at once and
-  // waits (griddepcontrol.wait) before its first global write. 1 (early writes): the host gave
-  // this launch scratch that the launch ahead does not use (the two halves of the workspace
-  // alternate) and the caller guarantees that the launch ahead neither reads nor writes this
-  // launch's outputs, so nothing waits; instead one thread per CTA waits and only then signals
-  // the dependents, so that the next launch -- which reuses the scratch of the launch ahead of
-  // this one -- cannot start before that launch has finished.
+  // ahead of them on the stream still runs. In both modes one thread per CTA waits
+  // (griddepcontrol.wait) for that kernel and only then signals the dependents, so the next
+  // launch starts only once the kernel ahead has finished: a launch never runs beside the one two
+  // back, which may write its inputs and shares its half of the workspace. 0: the kernel also
+  // waits before its first global write. 1 (early writes): the host gave this launch scratch that
+  // the launch ahead does not use (the two halves of the workspace alternate) and the caller
+  // guarantees that the launch ahead neither reads nor writes this launch's outputs, so the
+  // writes do not wait.
   int early_writes;
 };
 
@@ -1897,12 +1898,10 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   SharedLayout sh = carve_shared<D, EB, NW, CR>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Programmatic dependent launch (when the host asked for it). Without early writes, the next
-  // launch on the stream may be scheduled now (its CTAs take SMs as this grid's CTAs exit), and
-  // this kernel reads its inputs at once but writes global memory (outputs, partial states,
-  // counters, appended cache rows) only after pdl_wait(), once the kernel ahead has finished.
-  // With early writes, the launch-order warp below signals instead, after its own wait.
-  if (!P.early_writes) pdl_launch_dependents();
+  // Programmatic dependent launch (when the host asked for it): this kernel reads its inputs at
+  // once. Without early writes it writes global memory (outputs, partial states, counters,
+  // appended cache rows) only after pdl_wait(), once the kernel ahead has finished. In both
+  // modes the launch-order warp below lets the next launch be scheduled after its own wait.
 
   // ---- barriers, then the tiles of every sequence and their prefix ---------------------------
   __shared__ uint32_t chunk_tiles[kThreads + 1];
@@ -1928,7 +1927,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
   if (x0 >= x1) {
     // a CTA with no tiles still waits for the kernel ahead before it exits, so that this grid
     // never completes (nor lets the next launch start) before that kernel has
-    if (P.early_writes) pdl_wait();
+    pdl_wait();
     return;
   }
   const int ntiles = static_cast<int>(x1 - x0);
@@ -1953,7 +1952,7 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
         produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
       else
         produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
-    } else if (warp == NW + 1 && lane == 0 && P.early_writes) {
+    } else if (warp == NW + 1 && lane == 0) {
       // ============================ launch order ==============================================
       pdl_wait();
       pdl_launch_dependents();

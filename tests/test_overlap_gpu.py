@@ -303,3 +303,59 @@ def test_overlapped_paged_fp8_and_paged_multi_layers_equal_serial_ones(mqa):
     serial = _run(mqa, *args, overlap=False, graph=False, step_fn=paged_multi)
     overl = _run(mqa, *args, overlap=True, graph=True, step_fn=paged_multi)
     _same_bits(*serial, *overl)
+
+
+def test_a_launch_never_runs_beside_the_one_two_back(mqa):
+    """Three fused steps over large caches (the wait-before-writing mode): A (layer 0, a long
+    context, one CTA), B (layer 1, one CTA) and C (layer 0 again, the next token, four CTAs).
+    A appends row p of layer 0 near its end; C attends over row p, and its last CTA reaches it
+    early. The overlap contract only covers adjacent launches (A and C are two apart), so C must
+    not start before A has finished: the launch-order warp of B releases C only after B's own wait
+    on A. Same bits as without overlap. (On B300 a build that let B release C at its start passed
+    this test as well: the hardware did not start C early. The release after the wait makes the
+    order hold by construction.)"""
+    import dataclasses
+    dev = torch.device("cuda")
+    b, h, g, d_h = 1, 64, 8, 128
+    ctx = 150_000
+    extra = 60_000  # caches of 2 * 8 * 210,002 * 128 * 2 B = 860 MB per layer: above 768 MiB
+    w0 = dataclasses.replace(inputs.custom("far", b, h, g, d_h, ctx, ctx, wid=830), extra_rows=extra)
+    w1 = dataclasses.replace(inputs.custom("far", b, h, g, d_h, 10, 10, wid=831), extra_rows=extra)
+    assert 2 * b * g * w0.n_max * d_h * 2 > 768 * 2 ** 20
+    pos0, lens0 = inputs.positions_and_lengths(w0)
+    pos1, lens1 = inputs.positions_and_lengths(w1)
+    k0, v0 = inputs.cache(w0, 0, dev, tail="nan")
+    k1, v1 = inputs.cache(w1, 0, dev, tail="nan")
+    qa, kna, vna = inputs.step_inputs(w0, 0, dev)
+    qb, knb, vnb = inputs.step_inputs(w1, 0, dev)
+    qc, knc, vnc = inputs.step_inputs(w0, 1, dev)
+    pos_c, lens_c = (pos0 + 1).to(dev), (lens0 + 1).to(dev)
+    scale = d_h ** -0.5
+
+    def run(overlap):
+        ks = [(k0.clone(), v0.clone()), (k1.clone(), v1.clone())]
+        outs = [torch.empty_like(qa), torch.empty_like(qb), torch.empty_like(qc)]
+        s = torch.cuda.Stream()
+        mqa.set_launch_overlap(overlap, s)
+        torch.cuda.synchronize()
+        try:
+            with torch.cuda.stream(s):
+                mqa.debug_override(1, 0)
+                mqa.decode_step(qa, kna, vna, *ks[0], pos0.to(dev), lens0.to(dev), out=outs[0],
+                                scale=scale, stream=s)
+                mqa.decode_step(qb, knb, vnb, *ks[1], pos1.to(dev), lens1.to(dev), out=outs[1],
+                                scale=scale, stream=s)
+                mqa.debug_override(4, 0)
+                mqa.decode_step(qc, knc, vnc, *ks[0], pos_c, lens_c, out=outs[2], scale=scale,
+                                stream=s)
+            s.synchronize()
+        finally:
+            mqa.debug_override(0, 0)
+            mqa.set_launch_overlap(False, s)
+        assert mqa.get_device_status() == 0
+        return outs, ks
+
+    serial = run(False)
+    overl = run(True)
+    assert torch.isfinite(overl[0][2].float()).all(), "C read a row A had not written yet"
+    _same_bits(*serial, *overl)
