@@ -171,15 +171,24 @@ class HostStepBuffers:
 
 class HostStepPipeline:
     """Drives whole decode steps from pinned host inputs to pinned host outputs with the transfers
-    overlapped with the kernels: the inputs of each run of `chunk` layers are copied in on one
-    stream, that run's fused launches wait only for them, and its outputs are copied out on
-    another stream while the next run computes. A step of one run stays on the caller's stream.
-    Streams and events are created once, so a step costs only the enqueues."""
+    overlapped with the kernels: the inputs of each run of layers are copied in on one stream,
+    that run's fused launches wait only for them, and its outputs are copied out on another
+    stream while the next run computes. A step of one run stays on the caller's stream.
+    Streams and events are created once, so a step costs only the enqueues.
+
+    The runs are the first `chunk` layers, the layers between, and the last `chunk` layers. Only
+    the first run's inputs and the last run's outputs are exposed; the middle run's copies hide
+    under the first and last runs' kernels. Every boundary between runs is an event wait and
+    record on the launch stream, and there consecutive launches cannot overlap, so the runs are
+    as few as that allows."""
 
     def __init__(self, layers: list[LayerState], buf: HostStepBuffers, chunk: int = 8):
         self.layers, self.buf = layers, buf
         n = len(layers)
-        self.runs = [(c0, min(n, c0 + chunk)) for c0 in range(0, n, chunk)]
+        if n <= 2 * chunk:
+            self.runs = [(c0, min(n, c0 + chunk)) for c0 in range(0, n, chunk)]
+        else:
+            self.runs = [(0, chunk), (chunk, n - chunk), (n - chunk, n)]
         if len(self.runs) > 1:
             dev = buf.q_dev.device
             self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

@@ -101,7 +101,7 @@ def test_80_layer_step_sampled(mqa):
 
 
 @pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
-@pytest.mark.parametrize("chunk", [3, 8], ids=["runs_of_3", "one_run"])
+@pytest.mark.parametrize("chunk", [2, 3, 8], ids=["runs_2_3_2", "runs_3_1_3", "one_run"])
 def test_host_driven_step_matches_the_device_step(mqa, chunk, graph):
     """layers.HostStepPipeline (inputs copied in and outputs out, overlapped in runs of layers)
     gives, bit for bit, the outputs and caches of the device-resident multi-layer step."""
