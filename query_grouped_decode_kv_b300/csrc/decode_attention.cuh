@@ -123,14 +123,14 @@ struct DecodeParams {
 // codes). A cache row is D * EB bytes, split into 128-byte swizzle rows ("halves"), one TMA box
 // column range each; a stage holds one tile's K rows then its V rows; the ring holds kRingBytes,
 // so the narrower rows get twice the stages (and twice the tiles in flight).
-template <int D, int EB>
+template <int D, int EB, int RB = kRingBytes>
 struct Geometry {
   static constexpr int kRowBytes = D * EB;
   static constexpr int kHalves = kRowBytes / kSwizzleRowBytes;
   static constexpr int kBoxCols = kSwizzleRowBytes / EB;   // elements per 128-byte box row
   static constexpr int kKvBytes = kTileKeys * kRowBytes;   // one tile of K (or of V)
   static constexpr int kStageBytes = 2 * kKvBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes;  // 4 (32 KB stages) or 8 (16 KB)
+  static constexpr int kStages = RB / kStageBytes;  // in a 128 KB ring: 4 (32 KB stages) or 8
   static_assert(kRowBytes % kSwizzleRowBytes == 0 && kStages >= 2 && kStages <= 8, "geometry");
 };
 
@@ -146,18 +146,18 @@ __host__ __device__ constexpr int cc_q_index(int D, int hh, int d) {
 
 // Dynamic shared memory: [align pad][stages][comb_o][comb_ml][barriers][abort, merge flags]
 // [page slots]. CR = rows per warp in the combine scratch (the head rows one consumer warp holds).
-template <int D, int EB>
+template <int D, int EB, int RB = kRingBytes>
 __host__ __device__ constexpr int smem_fixed_bytes(int NW, int CR) {
-  using Geo = Geometry<D, EB>;
+  using Geo = Geometry<D, EB, RB>;
   return Geo::kStages * Geo::kStageBytes + NW * CR * comb_row_floats(D) * 4 + NW * CR * 8 +
          (2 * Geo::kStages + 2) * 8 + 16 +  // full, empty, cbar, stall; abort, merge flags
          kPagedProducers * 32 * 4 +         // the paged producers' looked-up pages
          kMaxCcHeads * cc_q_row_floats(D) * 4 +  // q of the segment in fp32 (CUDA-core consumer)
          NW * kMaxCcHeads * kCcWarpKeys * 4;     // its key weights, per warp
 }
-template <int D, int EB>
+template <int D, int EB, int RB = kRingBytes>
 __host__ __device__ constexpr size_t smem_bytes(int NW, int CR) {
-  return 1024 + static_cast<size_t>(smem_fixed_bytes<D, EB>(NW, CR));
+  return 1024 + static_cast<size_t>(smem_fixed_bytes<D, EB, RB>(NW, CR));
 }
 
 // Element offset of row r (= t * Gh + hh) of segment (bi, j) in q or out ([b][T][h][D]).
@@ -385,9 +385,9 @@ struct SharedLayout {
   TileIndex tix;        // tiles per sequence (its cs lives in static shared memory)
 };
 
-template <int D, int EB, int NW, int CR>
+template <int D, int EB, int NW, int CR, int RB = kRingBytes>
 __device__ __forceinline__ SharedLayout carve_shared(uint8_t* raw) {
-  using Geo = Geometry<D, EB>;
+  using Geo = Geometry<D, EB, RB>;
   constexpr int kStages = Geo::kStages;
   static_assert((NW * CR * comb_row_floats(D) * 4) % 16 == 0 && (NW * CR * 8) % 16 == 0 &&
                     ((2 * kStages + 2) * 8) % 16 == 0,
@@ -679,12 +679,12 @@ __device__ __forceinline__ void zero_invalid_sequences(const DecodeParams& P, in
 // pi issues tiles pi, pi + np, ...; np divides the stage count, so every stage is refilled by one
 // warp, once its `empty` barrier has completed the phase of its previous use.
 // ---------------------------------------------------------------------------------------------
-template <int D, int EB>
+template <int D, int EB, int RB = kRingBytes>
 __device__ __forceinline__ void produce_tiles(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                               const DecodeParams& P, const SharedLayout& sh,
                                               unsigned long long x0, int ntiles, int lane,
                                               int np, int pi) {
-  using Geo = Geometry<D, EB>;
+  using Geo = Geometry<D, EB, RB>;
   constexpr int kStages = Geo::kStages;
   constexpr uint32_t kStageBytes = Geo::kStageBytes;
   constexpr uint32_t kKvBytes = Geo::kKvBytes;
@@ -815,13 +815,13 @@ __device__ __forceinline__ void load_tile_pages(const int* slots, int kt, int (&
 
 // Several producer warps share a CTA's tiles over paged caches (np of them; this one is number
 // pi): warp pi issues tiles pi, pi + np, ... with its own page lookups and its own 32 slots.
-template <int D, int EB, int NB>
+template <int D, int EB, int NB, int RB = kRingBytes>
 __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
                                                     const CUtensorMap* tm_v,
                                                     const DecodeParams& P, const SharedLayout& sh,
                                                     unsigned long long x0, int ntiles, int lane,
                                                     int np, int pi) {
-  using Geo = Geometry<D, EB>;
+  using Geo = Geometry<D, EB, RB>;
   constexpr int kStages = Geo::kStages;
   constexpr uint32_t kStageBytes = Geo::kStageBytes;
   constexpr uint32_t kKvBytes = Geo::kKvBytes;
@@ -944,7 +944,7 @@ __device__ __forceinline__ void produce_tiles_paged(const CUtensorMap* tm_k,
 }
 
 // Boxes per tile from the page size (8, 16, 32 rows; 64 or more: one box).
-template <int D, int EB>
+template <int D, int EB, int RB = kRingBytes>
 __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
                                                         const CUtensorMap* tm_v,
                                                         const DecodeParams& P,
@@ -952,10 +952,10 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
                                                         unsigned long long x0, int ntiles,
                                                         int lane, int np, int pi) {
   switch (P.page_size) {
-    case 8: produce_tiles_paged<D, EB, 8>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
-    case 16: produce_tiles_paged<D, EB, 4>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
-    case 32: produce_tiles_paged<D, EB, 2>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
-    default: produce_tiles_paged<D, EB, 1>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    case 8: produce_tiles_paged<D, EB, 8, RB>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    case 16: produce_tiles_paged<D, EB, 4, RB>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    case 32: produce_tiles_paged<D, EB, 2, RB>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
+    default: produce_tiles_paged<D, EB, 1, RB>(tm_k, tm_v, P, sh, x0, ntiles, lane, np, pi); break;
   }
 }
 
@@ -968,6 +968,8 @@ __device__ __forceinline__ void produce_tiles_paged_any(const CUtensorMap* tm_k,
 template <int D, int WM, int NW, bool kTokens = false>
 struct MmaConsumer {
   static constexpr int kWarps = NW;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
   static constexpr int kTileGroups = 1;
   static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 16;  // head rows per warp
@@ -1160,6 +1162,8 @@ struct MmaConsumer {
 template <int D, int WM, int NW, int TG = 1>
 struct MmaConsumerF8 {
   static constexpr int kWarps = NW;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
   static constexpr int kTileGroups = TG;
   static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 16;  // head rows per warp
@@ -1364,6 +1368,8 @@ struct MmaConsumerF8 {
 template <int D, int NW, int TG>
 struct MmaConsumerF8T {
   static constexpr int kWarps = NW;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
   static constexpr int kTileGroups = TG;
   static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 8;            // heads per warp
@@ -1524,6 +1530,168 @@ struct MmaConsumerF8T {
 };
 
 // ---------------------------------------------------------------------------------------------
+// Consumer over bf16 caches for groups of at most 8 heads: the products transposed as in
+// MmaConsumerF8T (S^T = K q^T, O^T = V^T P^T; keys, then output columns, on the 16 MMA rows and
+// the group's heads on the 8 columns), with the tiles' bf16 rows taken by ldmatrix as they are.
+// S^T: ldmatrix.x4 gives the A fragment of 16 keys by 16 columns directly; the B fragment of q^T
+// is head r's columns (2c, 2c+1) and (2c+8, 2c+9) of the k-step, loaded once per segment.
+// O^T: ldmatrix.x4.trans over the V stage gives the A fragment of 16 columns by 16 keys. P^T and
+// the row sums as in MmaConsumerF8T. With four warps, each takes 16 keys of every tile.
+// ---------------------------------------------------------------------------------------------
+template <int D, int NW>
+struct MmaConsumerT {
+  static constexpr int kWarps = NW;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
+  static constexpr int kTileGroups = 1;
+  static constexpr bool kSharedQ = false;
+  static constexpr int kCombRows = 8;            // heads per warp
+  static constexpr int KPW = kTileKeys / NW;     // keys per warp per tile
+  static constexpr int MT_S = KPW / 16;          // m-tiles of S^T (16 keys each)
+  static constexpr int KS_QK = D / 16;           // k-steps over the head dimension
+  static constexpr int MT_O = D / 16;            // m-tiles of O^T (16 output columns each)
+  static_assert(MT_S >= 1 && KS_QK % 2 == 0, "tile split");
+
+  uint32_t qb[KS_QK][2];  // B fragments of q^T for head lane / 4 of the group
+  float o[MT_O][4];
+  float ol[4];  // P^T summed over keys by an all-ones A: c0 head 2c, c1 head 2c + 1
+  float m[2];   // softmax references of heads 2c and 2c + 1 (log2 units)
+
+  __device__ __forceinline__ void begin_segment(const DecodeParams& P, int bi, int j, int mi,
+                                                int lane) {
+    const int r = lane >> 2, c = lane & 3;
+    const bool valid = r < P.G;
+    const uint32_t* qr =
+        reinterpret_cast<const uint32_t*>(P.q + (valid ? row_offset(P, bi, j, r, D) : 0));
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ++ks) {
+      // columns 16 ks + 2c, + 1 and 16 ks + 8 + 2c, + 1 of head r
+      qb[ks][0] = valid ? __ldg(qr + ks * 8 + c) : 0u;
+      qb[ks][1] = valid ? __ldg(qr + ks * 8 + 4 + c) : 0u;
+    }
+#pragma unroll
+    for (int n = 0; n < MT_O; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    ol[0] = ol[1] = ol[2] = ol[3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+  }
+
+  // One tile: this warp's KPW keys from grp * KPW. `valid` = rows of the sequence from the tile's
+  // first row on (at least 1; may exceed the tile).
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, int grp, int lane,
+                                       int valid, float scale_log2) {
+    const int mat = lane >> 3, rr = lane & 7;
+    const int r = lane >> 2;
+    // S^T, k-steps ks into s and ks + 1 into s2 (two independent chains per m-tile)
+    float s[MT_S][4], s2[MT_S][4];
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+      s2[t][0] = s2[t][1] = s2[t][2] = s2[t][3] = 0.f;
+    }
+#pragma unroll
+    for (int ks = 0; ks < KS_QK; ks += 2) {
+#pragma unroll
+      for (int t = 0; t < MT_S; ++t) {
+        // matrices: keys 0-7 / 8-15 of the m-tile (mat & 1) x columns + 0-7 / + 8-15 (mat >> 1)
+        const int key = grp * KPW + t * 16 + rr + ((mat & 1) ? 8 : 0);
+        uint32_t a[4], a2[4];
+        ldsm_x4(swz_bytes(kbase, key, ks * 32 + (mat >> 1) * 16), a[0], a[1], a[2], a[3]);
+        ldsm_x4(swz_bytes(kbase, key, (ks + 1) * 32 + (mat >> 1) * 16), a2[0], a2[1], a2[2],
+                a2[3]);
+        mma_16816(s[t], a, qb[ks][0], qb[ks][1]);
+        mma_16816(s2[t], a2, qb[ks + 1][0], qb[ks + 1][1]);
+      }
+    }
+    // scale (log2 domain), mask keys at or beyond the length, running max per head
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      const int key = grp * KPW + t * 16 + r;
+      const bool in0 = key < valid, in1 = key + 8 < valid;
+      s[t][0] = in0 ? (s[t][0] + s2[t][0]) * scale_log2 : -INFINITY;  // key r,     head 2c
+      s[t][1] = in0 ? (s[t][1] + s2[t][1]) * scale_log2 : -INFINITY;  // key r,     head 2c + 1
+      s[t][2] = in1 ? (s[t][2] + s2[t][2]) * scale_log2 : -INFINITY;  // key r + 8, head 2c
+      s[t][3] = in1 ? (s[t][3] + s2[t][3]) * scale_log2 : -INFINITY;  // key r + 8, head 2c + 1
+      mx0 = fmaxf(mx0, fmaxf(s[t][0], s[t][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[t][1], s[t][3]));
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    // lazy reference, as in MmaConsumer::tile
+    const bool up0 = mx0 > m[0] + kLazyLog2, up1 = mx1 > m[1] + kLazyLog2;
+    float al0 = 1.f, al1 = 1.f;
+    if (up0) { al0 = fast_exp2(m[0] - mx0); m[0] = mx0; }
+    if (up1) { al1 = fast_exp2(m[1] - mx1); m[1] = mx1; }
+    const float ref0 = (m[0] == -INFINITY) ? 0.f : m[0];
+    const float ref1 = (m[1] == -INFINITY) ? 0.f : m[1];
+#pragma unroll
+    for (int t = 0; t < MT_S; ++t) {
+      s[t][0] = fast_exp2(s[t][0] - ref0);
+      s[t][1] = fast_exp2(s[t][1] - ref1);
+      s[t][2] = fast_exp2(s[t][2] - ref0);
+      s[t][3] = fast_exp2(s[t][3] - ref1);
+    }
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+#pragma unroll
+      for (int n = 0; n < MT_O; ++n) {
+        o[n][0] *= al0; o[n][1] *= al1;
+        o[n][2] *= al0; o[n][3] *= al1;
+      }
+      ol[0] *= al0; ol[1] *= al1; ol[2] *= al0; ol[3] *= al1;
+    }
+    // O^T += V^T P^T with the weights rounded to bf16 once; the all-ones A sums those weights
+    const uint32_t ones[4] = {kOnesBf16x2, kOnesBf16x2, kOnesBf16x2, kOnesBf16x2};
+#pragma unroll
+    for (int kk = 0; kk < MT_S; ++kk) {
+      const uint32_t b0 = movmatrix_trans(pack_bf16x2(s[kk][0], s[kk][1]));  // keys 2c, 2c+1
+      const uint32_t b1 = movmatrix_trans(pack_bf16x2(s[kk][2], s[kk][3]));  // keys 2c+8, 2c+9
+      mma_16816(ol, ones, b0, b1);
+#pragma unroll
+      for (int cb = 0; cb < MT_O; ++cb) {
+        // matrices: keys 0-7 / 8-15 of this k-step (mat >> 1) x columns + 0-7 / + 8-15 (mat & 1)
+        const int key = grp * KPW + kk * 16 + rr + ((mat >> 1) ? 8 : 0);
+        uint32_t a[4];
+        ldsm_x4_trans(swz_bytes(vbase, key, cb * 32 + (mat & 1) * 16), a[0], a[1], a[2], a[3]);
+        mma_16816(o[cb], a, b0, b1);
+      }
+    }
+  }
+
+  // Publish this warp's state (the group's heads 0..7) to the combine scratch: output column
+  // 16 b + r holds c0 / c1, column 16 b + r + 8 holds c2 / c3.
+  __device__ __forceinline__ void publish(const SharedLayout& sh, int warp, int lane) {
+    const int r = lane >> 2, h0 = (lane & 3) * 2;
+    float* row0 = sh.comb_o + (warp * kCombRows + h0) * comb_row_floats(D);
+    float* row1 = row0 + comb_row_floats(D);
+#pragma unroll
+    for (int b = 0; b < MT_O; ++b) {
+      row0[b * 16 + r] = o[b][0];
+      row0[b * 16 + r + 8] = o[b][2];
+      row1[b * 16 + r] = o[b][1];
+      row1[b * 16 + r + 8] = o[b][3];
+    }
+    if (r == 0) {
+      sh.comb_ml[warp * kCombRows + h0] = make_float2(m[0], ol[0]);
+      sh.comb_ml[warp * kCombRows + h0 + 1] = make_float2(m[1], ol[1]);
+    }
+  }
+
+  struct Rows {
+    __device__ __forceinline__ int operator()(int hr, int* ws, int* rs) const {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        ws[w] = w;
+        rs[w] = hr;
+      }
+      return NW;
+    }
+  };
+};
+
+// ---------------------------------------------------------------------------------------------
 // CUDA-core consumer (G <= 7; over fp8 codes only when that path is forced). Warp w takes keys
 // [KPW w, KPW (w + 1)) of every tile (KPW = 64 / NW, 16 or 8); lane owns DPL = D/32 consecutive
 // columns of q, K, V and the output. EB: the cache's bytes per element (fp8 codes are widened
@@ -1532,6 +1700,8 @@ struct MmaConsumerF8T {
 template <int D, int G, int NW, int EB = 2>
 struct CcConsumer {
   static constexpr int kWarps = NW;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
   static constexpr int kTileGroups = 1;
   static constexpr bool kSharedQ = false;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
@@ -1707,6 +1877,8 @@ struct CcConsumer {
 template <int D, int G>
 struct CcConsumer2 {
   static constexpr int kWarps = 8;
+  static constexpr int kRingBytes = mqa::kRingBytes;  // the stage ring
+  static constexpr int kCtasPerSm = 1;
   static constexpr int kTileGroups = 2;
   static constexpr bool kSharedQ = true;
   static constexpr int kCombRows = 8;   // head rows per warp (G <= 7)
@@ -1886,16 +2058,17 @@ struct CcConsumer2 {
 // CcConsumer2<D, G> or CcConsumer<D, G, NW, EB>; EB: the cache's bytes per element (2 bf16, 1 fp8).
 // ---------------------------------------------------------------------------------------------
 template <int D, int EB, class Consumer, bool kTensorCores, int WM>
-__global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
+__global__ void __launch_bounds__(threads_of(Consumer::kWarps), Consumer::kCtasPerSm)
     decode_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
-  using Geo = Geometry<D, EB>;
+  constexpr int RB = Consumer::kRingBytes;
+  using Geo = Geometry<D, EB, RB>;
   constexpr int kStages = Geo::kStages;
   constexpr int NW = Consumer::kWarps;
   constexpr int CR = Consumer::kCombRows;
   constexpr int kThreads = threads_of(NW);
   extern __shared__ uint8_t smem_raw[];
-  SharedLayout sh = carve_shared<D, EB, NW, CR>(smem_raw);
+  SharedLayout sh = carve_shared<D, EB, NW, CR, RB>(smem_raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   // Programmatic dependent launch (when the host asked for it): this kernel reads its inputs at
@@ -1949,9 +2122,9 @@ __global__ void __launch_bounds__(threads_of(Consumer::kWarps), 1)
     if (warp == NW || (np == 2 && warp == NW + 2)) {
       const int pi = warp == NW ? 0 : 1;
       if (paged)
-        produce_tiles_paged_any<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
+        produce_tiles_paged_any<D, EB, RB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
       else
-        produce_tiles<D, EB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
+        produce_tiles<D, EB, RB>(&tm_k, &tm_v, P, sh, x0, ntiles, lane, np, pi);
     } else if (warp == NW + 1 && lane == 0) {
       // ============================ launch order ==============================================
       pdl_wait();

@@ -260,12 +260,13 @@ enum Path { kPathAuto = 0, kPathCudaCores = 1, kPathMmaSync = 2, kPathTcgen05 = 
 // grouping) the heads are no contraction and CUDA cores stream the cache at the HBM rate. From
 // three heads on, the CUDA cores' fp32 FMAs (2 G d_h per key) fall behind HBM (at 32K rows:
 // 1.01x the copy bandwidth at G = 3, 0.87x at G = 4, 0.59x at G = 7, against 1.10x on mma.sync at
-// every G), so the group's heads go to the tensor cores as the M rows of m16n8k16 MMAs, padded
-// to 16 (mma.sync; the tcgen05 kernel, 128-row MMA tiles with accumulators in tensor memory, is
-// not faster on any measured decode shape). Forcing either path at any G up to 7 is supported
-// and tested.
+// every G), so the group's heads go to the tensor cores (mma.sync m16n8k16: up to 8 heads as the
+// N columns of transposed products, beyond that as M rows padded to 16; the tcgen05 kernel,
+// 128-row MMA tiles with accumulators in tensor memory, is not faster on any measured decode
+// shape). Forcing either path at any G up to 7 is supported and tested.
 constexpr int kCudaCoreMaxGroup = 2;
 Path auto_path(int G) { return G <= kCudaCoreMaxGroup ? kPathCudaCores : kPathMmaSync; }
+
 
 // A kernel instance with the launch facts the host needs.
 struct AttnKernelChoice {
@@ -281,7 +282,7 @@ AttnKernelChoice choice(int b) {
   AttnKernelChoice c;
   c.fn = mqa::decode_attention_kernel<D, EB, Consumer, TC, WM>;
   c.threads = mqa::threads_of(Consumer::kWarps);
-  c.smem = mqa::smem_bytes<D, EB>(Consumer::kWarps, Consumer::kCombRows);
+  c.smem = mqa::smem_bytes<D, EB, Consumer::kRingBytes>(Consumer::kWarps, Consumer::kCombRows);
   c.wide = Consumer::kWarps == 8;
   c.pdl = true;
   return c;
@@ -311,6 +312,11 @@ AttnKernelChoice pick_kernel(Path path, int G, int b, int T) {
     return choice<MmaConsumer<D, 4, 8, true>, D, 2, true, 4>(b);
   }
   if (path == kPathMmaSync) {
+    // up to 8 heads, one token: the products transposed (heads on the MMA's 8 columns, no
+    // padding rows). Measured on B300 against the head-row consumer, launches back to back:
+    // gqa_8b 17.15 against 18.15 us, one 70B-class layer 99.9 against 100.9 us, the 80-layer
+    // step in a graph 7,805 against 7,830 us.
+    if (G <= 8) return choice<mqa::MmaConsumerT<D, 4>, D, 2, true, 1>(b);
     if (G <= 16) return choice<MmaConsumer<D, 1, 4>, D, 2, true, 1>(b);
     if (G <= 32) return choice<MmaConsumer<D, 2, 8>, D, 2, true, 2>(b);
     return choice<MmaConsumer<D, 4, 8>, D, 2, true, 4>(b);
