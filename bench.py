@@ -131,11 +131,21 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed: what the compiler
+    sees, so that a change to the comments keeps a stored capture valid. (String literals in
+    these sources hold no comment markers.)"""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(family: str = "decode") -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[family]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -2054,8 +2054,10 @@ struct CcConsumer2 {
 };
 
 // ---------------------------------------------------------------------------------------------
-// The kernel. `Consumer` is MmaConsumer<D, WM, NW>, MmaConsumerF8<D, WM, NW>,
-// CcConsumer2<D, G> or CcConsumer<D, G, NW, EB>; EB: the cache's bytes per element (2 bf16, 1 fp8).
+// The kernel. `Consumer` is MmaConsumerT<D, NW>, MmaConsumer<D, WM, NW>, MmaConsumerF8T<D, NW, TG>,
+// MmaConsumerF8<D, WM, NW, TG>, CcConsumer2<D, G> or CcConsumer<D, G, NW, EB>; EB: the cache's
+// bytes per element (2 bf16, 1 fp8). The consumer also sets the stage ring's size and the CTAs
+// per SM the kernel is built for.
 // ---------------------------------------------------------------------------------------------
 template <int D, int EB, class Consumer, bool kTensorCores, int WM>
 __global__ void __launch_bounds__(threads_of(Consumer::kWarps), Consumer::kCtasPerSm)

@@ -205,3 +205,11 @@ def test_line_checker_flags_an_unordered_spread():
     name = line["config"]["workload"]
     line["configs"][name]["us_per_step_spread"] = {"n": 5, "p10": 3.0, "median": 2.0, "p90": 4.0}
     assert any("not ordered" in p for p in bench.line_problems(line))
+
+
+def test_the_source_hash_ignores_comments_and_whitespace():
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n/* note\n   on two lines */\n"
+    assert bench.code_tokens(code) == "int f(int x) { return x + 1; }"
+    assert bench.code_tokens(code.replace("// one more", "// another note")) == \
+        bench.code_tokens(code)
+    assert bench.code_tokens(code.replace("x + 1", "x + 2")) != bench.code_tokens(code)
