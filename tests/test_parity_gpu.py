@@ -288,3 +288,21 @@ def test_two_streams_do_not_share_a_workspace(mqa):
     torch.cuda.synchronize()
     for o, r in zip(outs, refs):
         P.assert_close(o, r, "concurrent streams")
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 7])
+@pytest.mark.parametrize("d_h", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 7, 8])
+def test_transposed_consumer_at_every_small_group(mqa, G, d_h, ctas):
+    """Up to 8 heads per KV head, the mma.sync path runs the transposed products (heads on the
+    MMA's 8 columns, padding columns past G): every G on both head sizes, with the default CTA
+    count, one CTA walking every segment, and 7 CTAs splitting segments at tile boundaries."""
+    case = P.make_case(3, 2 * G, 2, d_h, 1, 700, seed_id=500 + 10 * G + d_h // 64)
+    _, _, out_ref = P.oracle_step(case)
+    mqa.debug_override(ctas, 2)
+    try:
+        _, _, out = P.gpu_step(case, mqa)
+        assert mqa.get_device_status() == 0
+    finally:
+        mqa.debug_override(0, 0)
+    P.assert_close(out, out_ref, f"G={G} d_h={d_h} ctas={ctas}")
