@@ -14,16 +14,18 @@
 // c + segment and counts its arrival on the segment's counter, and the last CTA to arrive merges
 // the slots with the log-sum-exp identity (then resets the counter to zero for the next call).
 //
-// Inside a CTA: one producer warp streams each tile's K and V rows from HBM into a ring of
-// shared-memory stages with bulk tensor copies (TMA, 128-byte swizzle); four consumer warps read
-// every stage once, so the K/V bytes of a KV head are fetched exactly once and reused by all G
-// query heads that share them. Each consumer warp keeps an online softmax (running max m and
-// sum l in fp32, log2 domain) for its slice of the tile's keys; at a segment's end the warps'
+// Inside a CTA: two producer warps stream alternate tiles' K and V rows from HBM into a ring of
+// shared-memory stages with bulk tensor copies (TMA, 128-byte swizzle); four or eight consumer
+// warps read every stage once, so the K/V bytes of a KV head are fetched exactly once and reused
+// by all G query heads that share them. Each consumer warp keeps an online softmax (running max m
+// and sum l in fp32, log2 domain) for its slice of the tile's keys; at a segment's end the warps'
 // states are combined through shared memory.
 //
-// Inner products: the grouped heads run on tensor cores as the M rows of bf16 mma.sync m16n8k16
-// products (fp32 accumulate; S = Q K^T, then O += P V). With one or two heads per K/V row
-// (MHA-like grouping) CUDA cores do fp32 FMAs instead; they serve up to seven heads when forced.
+// Inner products: the grouped heads run on tensor cores in mma.sync m16n8k16 products (fp32
+// accumulate): up to 8 heads as the N columns of transposed products (S^T = K q^T, then
+// O^T += V^T P^T), beyond that as the M rows (S = Q K^T, then O += P V). With one or two heads per
+// K/V row (MHA-like grouping) CUDA cores do fp32 FMAs instead; they serve up to seven heads when
+// forced.
 //
 // Every wait is bounded in time: on expiry the kernel latches MQA_ERR_TIMEOUT and returns.
 #pragma once
